@@ -1,0 +1,339 @@
+/*
+ * trit_oracle.c -- reference CPU implementation of the ternary bit-plane
+ * select-accumulate path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
+ * CPU-baseline leg call this code; the product library never does, and this
+ * file shares no code, header, table or constant with it.
+ *
+ * It is deliberately plain and slow: every weight is decoded bit by bit into
+ * one int8, products are accumulated in int64, and nothing is blocked, fused,
+ * vectorised or reordered.  Single-threaded.
+ *
+ * Sources (page title -- section):
+ *   [FMT] "The .trit format, version 1" -- 2.3 Ternary payload; 4 Validation
+ *   [TRI] "Tritium: One Weight Format for Ternary Inference on Commodity CPUs
+ *          and Multiplier-Free Hardware" -- The .trit v1 layout; Invariants;
+ *          On popcount; The hardware core; Numerics; Why exactness, concretely
+ *
+ * Readings where the pages are silent (the activation quantiser formula, the
+ * zero row, the dequantisation order) are stated at each function.
+ *
+ * Return codes are bit masks:
+ *   1  both planes set in one weight position (P1)
+ *   2  padding bit set past the last column (P2)
+ *   4  value outside {-1, 0, +1} handed to the packer
+ *   8  non-finite activation handed to the quantiser
+ *   32 accumulator outside the int32 range
+ *   64 bad argument
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define OR_P1          1
+#define OR_P2          2
+#define OR_NOT_TERNARY 4
+#define OR_NONFINITE   8
+#define OR_OVERFLOW    32
+#define OR_ARG         64
+
+/* [FMT] 2.3: beats_per_row = ceil(cols / 64). */
+int64_t oracle_beats_per_row(int64_t cols) { return (cols + 63) / 64; }
+
+/* [FMT] 2.3: byte_len = rows * beats_per_row * 16. */
+int64_t oracle_payload_bytes(int64_t rows, int64_t cols)
+{
+    return rows * oracle_beats_per_row(cols) * 16;
+}
+
+/* [FMT] 2.3: beat b of row r is the 16 bytes at (r * beats_per_row + b) * 16. */
+static const uint8_t *beat_at(const uint8_t *payload, int64_t cols, int64_t r, int64_t b)
+{
+    return payload + (r * oracle_beats_per_row(cols) + b) * 16;
+}
+
+/* [FMT] 2.3: bytes 0..8 hold pos, bytes 8..16 hold neg, each a little-endian
+ * u64 whose bit k is the k-th least significant bit.  Bit k of a little-endian
+ * u64 is bit (k % 8) of byte (k / 8). */
+static int pos_bit(const uint8_t *beat, int k) { return (beat[k / 8] >> (k % 8)) & 1; }
+static int neg_bit(const uint8_t *beat, int k) { return (beat[8 + k / 8] >> (k % 8)) & 1; }
+
+/*
+ * Pack an int8 ternary matrix (rows x cols, row-major) into the .trit v1
+ * ternary payload.  [FMT] 2.3: bit k of pos set <=> W[r][b*64+k] = +1, bit k
+ * of neg set <=> W[r][b*64+k] = -1, neither set <=> 0; padding bits past cols
+ * stay clear (P2).  A value outside {-1, 0, +1} is rejected, with its linear
+ * index in *bad.
+ */
+int oracle_pack(const int8_t *w, int64_t rows, int64_t cols, uint8_t *payload, int64_t *bad)
+{
+    if (rows < 0 || cols < 0) return OR_ARG;
+    memset(payload, 0, (size_t)oracle_payload_bytes(rows, cols));
+    int64_t bpr = oracle_beats_per_row(cols);
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t c = 0; c < cols; c++) {
+            int8_t v = w[r * cols + c];
+            int64_t b = c / 64;
+            int k = (int)(c % 64);
+            uint8_t *beat = payload + (r * bpr + b) * 16;
+            if (v == 1) {
+                beat[k / 8] |= (uint8_t)(1u << (k % 8));
+            } else if (v == -1) {
+                beat[8 + k / 8] |= (uint8_t)(1u << (k % 8));
+            } else if (v != 0) {
+                if (bad) *bad = r * cols + c;
+                return OR_NOT_TERNARY;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Check both payload invariants.  [TRI] Invariants / [FMT] 2.3:
+ *   P1: pos AND neg = 0 in every beat, padding included;
+ *   P2: on every row's last beat, (pos OR neg) AND NOT tail = 0, where tail is
+ *       all ones when cols % 64 = 0 and (1 << (cols % 64)) - 1 otherwise, the
+ *       shift done in 64 bits.
+ * Written here bit by bit: a padding bit is one whose column b*64+k >= cols.
+ * Returns the OR of the kinds found (0 = clean) and, in *first, the smallest
+ * offending bit position (r * beats_per_row + b) * 64 + k over both kinds.
+ */
+int oracle_verify(const uint8_t *payload, int64_t rows, int64_t cols, int64_t *first)
+{
+    int64_t bpr = oracle_beats_per_row(cols);
+    int kinds = 0;
+    int64_t best = -1;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < bpr; b++) {
+            const uint8_t *beat = beat_at(payload, cols, r, b);
+            for (int k = 0; k < 64; k++) {
+                int p = pos_bit(beat, k), n = neg_bit(beat, k);
+                int here = 0;
+                if (p && n) here |= OR_P1;
+                if ((p || n) && b * 64 + k >= cols) here |= OR_P2;
+                if (here) {
+                    kinds |= here;
+                    if (best < 0) best = (r * bpr + b) * 64 + k;
+                }
+            }
+        }
+    }
+    if (first) *first = best;
+    return kinds;
+}
+
+/*
+ * Inverse of oracle_pack.  A weight position with both bits set is rejected
+ * ([FMT] 2.3, P1: every consumer must treat it as an error), with its bit
+ * position (as in oracle_verify) in *bad.  Padding bits are not columns and
+ * are not read.
+ */
+int oracle_unpack(const uint8_t *payload, int64_t rows, int64_t cols, int8_t *w, int64_t *bad)
+{
+    int64_t bpr = oracle_beats_per_row(cols);
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < bpr; b++) {
+            const uint8_t *beat = beat_at(payload, cols, r, b);
+            for (int k = 0; k < 64; k++) {
+                int p = pos_bit(beat, k), n = neg_bit(beat, k);
+                if (p && n) {
+                    if (bad) *bad = (r * bpr + b) * 64 + k;
+                    return OR_P1;
+                }
+                int64_t c = b * 64 + k;
+                if (c < cols) w[r * cols + c] = (int8_t)(p ? 1 : (n ? -1 : 0));
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Per-token absmax activation quantiser.  [TRI] Numerics names the recipe
+ * (per-token absmax int8, codes invariant under a uniform positive scale) but
+ * prints no formula; the reading used here, for each row of x (M x K, fp32):
+ *   a     = max_c |x_c|                      (exact in fp32)
+ *   inv   = 127.0f / a                       (IEEE fp32 division)
+ *   q_c   = clamp(rint(x_c * inv), -127, 127) (fp32 product, ties to even)
+ *   scale = a
+ * Special cases:
+ *   - any non-finite x_c: the row is rejected (row_err = 8), q = 0, scale = 0;
+ *   - a = 0: q = 0 and scale = 0;
+ *   - a < 2^-96, where 127/a could overflow: x and a are first multiplied by
+ *     2^96, which is exact, so the codes are those of the row scaled into the
+ *     normal range (the uniform-scale invariance above).
+ * q is written with row stride ldq >= K; columns K..ldq-1 are zero
+ * ([FMT] 2.3: activation buffers are sized beats_per_row * 64 with a zero tail).
+ * Returns the OR of the row errors.
+ */
+int oracle_quant(const float *x, int64_t M, int64_t K, int64_t ldq, int8_t *q, float *scale,
+                 uint8_t *row_err)
+{
+    int any = 0;
+    for (int64_t m = 0; m < M; m++) {
+        const float *xr = x + m * K;
+        int8_t *qr = q + m * ldq;
+        memset(qr, 0, (size_t)ldq);
+        row_err[m] = 0;
+        scale[m] = 0.0f;
+        int finite = 1;
+        float a = 0.0f;
+        for (int64_t c = 0; c < K; c++) {
+            if (!isfinite(xr[c])) finite = 0;
+            else if (fabsf(xr[c]) > a) a = fabsf(xr[c]);
+        }
+        if (!finite) {
+            row_err[m] = OR_NONFINITE;
+            any |= OR_NONFINITE;
+            continue;
+        }
+        if (a == 0.0f) continue;
+        float pre = 1.0f;
+        if (a < 0x1p-96f) pre = 0x1p96f;
+        float inv = 127.0f / (a * pre);
+        for (int64_t c = 0; c < K; c++) {
+            float v = rintf((xr[c] * pre) * inv);
+            if (v > 127.0f) v = 127.0f;
+            if (v < -127.0f) v = -127.0f;
+            qr[c] = (int8_t)v;
+        }
+        scale[m] = a;
+    }
+    return any;
+}
+
+/*
+ * Decode one payload row to one int8 per column, bit by bit ([TRI]
+ * Verification: the oracle expands bit planes to one i8 per weight).  Every
+ * bit of every beat of the row, padding included, is checked for P1.
+ * Returns 0 or OR_P1 with the first offending bit position in *bad.
+ */
+static int decode_row(const uint8_t *payload, int64_t cols, int64_t r, int8_t *wrow, int64_t *bad)
+{
+    int64_t bpr = oracle_beats_per_row(cols);
+    for (int64_t b = 0; b < bpr; b++) {
+        const uint8_t *beat = beat_at(payload, cols, r, b);
+        for (int k = 0; k < 64; k++) {
+            int p = pos_bit(beat, k), n = neg_bit(beat, k);
+            if (p && n) {
+                if (bad) *bad = (r * bpr + b) * 64 + k;
+                return OR_P1;
+            }
+            int64_t c = b * 64 + k;
+            if (c < cols) wrow[c] = (int8_t)(p ? 1 : (n ? -1 : 0));
+        }
+    }
+    return 0;
+}
+
+/*
+ * y = W x for the selected payload rows, plus its fp32 dequantisation.
+ *   payload : rows N x cols K as in [FMT] 2.3
+ *   x       : M activation rows of int8 with row stride ldx (>= K); only
+ *             columns < K are read -- padding columns do not exist
+ *   x_scale : M per-row scales (the absmax of each quantised row)
+ *   sel     : indices of the payload rows to evaluate (NULL = all N, in order)
+ *   y_i32, y_f32 : M x nsel, row-major
+ * For each selected row the weights are decoded to int8 and
+ *   acc = sum_c W[r][c] * x[m][c]   in int64,
+ * which must lie in the int32 range ([TRI] The hardware core: a 32-bit
+ * accumulator, with -128 activations widened before they are negated).
+ * Dequantisation, in the order the configuration states it, one fp32
+ * round-to-nearest step at a time, without contraction ([TRI] Why exactness:
+ * scale by each factor in turn):
+ *   y_f32 = (((float)acc * w_scale) * x_scale[m]) / 127.0f
+ * A row containing a both-bits-set position is rejected (row_err = 1, its
+ * outputs 0); the return value is the OR of the row errors.
+ */
+int oracle_gemm(const uint8_t *payload, float w_scale, const int8_t *x, int64_t ldx,
+                const float *x_scale, int64_t M, int64_t N, int64_t K, const int64_t *sel,
+                int64_t nsel, int32_t *y_i32, float *y_f32, uint8_t *row_err, int8_t *scratch)
+{
+    int any = 0;
+    if (sel == NULL) nsel = N;
+    for (int64_t i = 0; i < nsel; i++) {
+        int64_t r = sel ? sel[i] : i;
+        if (r < 0 || r >= N) return OR_ARG;
+        row_err[i] = (uint8_t)decode_row(payload, K, r, scratch, NULL);
+        for (int64_t m = 0; m < M; m++) {
+            y_i32[m * nsel + i] = 0;
+            y_f32[m * nsel + i] = 0.0f;
+        }
+        if (row_err[i]) {
+            any |= row_err[i];
+            continue;
+        }
+        for (int64_t m = 0; m < M; m++) {
+            const int8_t *xr = x + m * ldx;
+            int64_t acc = 0;
+            for (int64_t c = 0; c < K; c++) acc += (int64_t)scratch[c] * (int64_t)xr[c];
+            if (acc > INT32_MAX || acc < INT32_MIN) {
+                row_err[i] |= OR_OVERFLOW;
+                any |= OR_OVERFLOW;
+                continue;
+            }
+            float f = (float)(int32_t)acc;
+            f = f * w_scale;
+            f = f * x_scale[m];
+            f = f / 127.0f;
+            y_i32[m * nsel + i] = (int32_t)acc;
+            y_f32[m * nsel + i] = f;
+        }
+    }
+    return any;
+}
+
+/*
+ * The bit-serial popcount formulation ([TRI] On popcount), kept as a second,
+ * independent evaluation of the integer result.  Writing each int8 activation
+ * in two's complement, x = -128*b7 + sum_{j<7} 2^j * b_j, gives
+ *   y = sum_{j<7} 2^j (popc(pos & X_j) - popc(neg & X_j))
+ *       - 128 (popc(pos & X_7) - popc(neg & X_7))
+ * where X_j is the 64-bit mask of bit j of the activations of one beat.  The
+ * masks are built per beat with columns >= K cleared.  Only the int32 result
+ * is produced; a both-bits-set position makes the row's result unspecified
+ * here (oracle_gemm is the one that rejects).
+ */
+static int popcount64(uint64_t v)
+{
+    int n = 0;
+    while (v) {
+        n += (int)(v & 1u);
+        v >>= 1;
+    }
+    return n;
+}
+
+int oracle_gemm_popcount(const uint8_t *payload, const int8_t *x, int64_t ldx, int64_t M,
+                         int64_t N, int64_t K, int32_t *y_i32)
+{
+    int64_t bpr = oracle_beats_per_row(K);
+    for (int64_t r = 0; r < N; r++) {
+        for (int64_t m = 0; m < M; m++) {
+            const int8_t *xr = x + m * ldx;
+            int64_t acc = 0;
+            for (int64_t b = 0; b < bpr; b++) {
+                const uint8_t *beat = beat_at(payload, K, r, b);
+                uint64_t pos = 0, neg = 0;
+                for (int i = 0; i < 8; i++) {
+                    pos |= (uint64_t)beat[i] << (8 * i);
+                    neg |= (uint64_t)beat[8 + i] << (8 * i);
+                }
+                for (int j = 0; j < 8; j++) {
+                    uint64_t xj = 0;
+                    for (int k = 0; k < 64; k++) {
+                        int64_t c = b * 64 + k;
+                        if (c < K && (((uint8_t)xr[c] >> j) & 1u)) xj |= (uint64_t)1 << k;
+                    }
+                    int64_t d = (int64_t)popcount64(pos & xj) - (int64_t)popcount64(neg & xj);
+                    acc += (j == 7) ? -128 * d : ((int64_t)1 << j) * d;
+                }
+            }
+            if (acc > INT32_MAX || acc < INT32_MIN) return OR_OVERFLOW;
+            y_i32[m * N + r] = (int32_t)acc;
+        }
+    }
+    return 0;
+}
