@@ -217,3 +217,19 @@ def test_quant_rejects_non_finite_rows(orc):
     assert e.tolist() == [0, orc.NONFINITE, 0, orc.NONFINITE]
     assert (q[1] == 0).all() and (q[3] == 0).all() and s[1] == 0 and s[3] == 0
     assert (q[0, :65] == 127).all() and (q[2, :65] == 127).all()
+
+
+def test_quant_denormal_row_matches_unscaled(orc):
+    """A row of small integers times 2^-140 is denormal but exact; 127/absmax
+    would overflow fp32 there, and the codes must still equal those of the
+    unscaled integers (uniform-scale invariance)."""
+    rng = synth.rng_for(920)
+    n = rng.integers(-127, 128, size=(3, 200)).astype(np.float32)
+    n[:, 0] = 127
+    tiny = (n.astype(np.float64) * 2.0 ** -140).astype(np.float32)
+    assert np.array_equal(tiny.astype(np.float64) * 2.0 ** 140, n.astype(np.float64))
+    q0, s0, _ = orc.quant(n)
+    qt, st, e = orc.quant(tiny)
+    assert not e.any()
+    np.testing.assert_array_equal(qt, q0)
+    np.testing.assert_array_equal(st, tiny[:, 0])
