@@ -1,0 +1,424 @@
+"""Benchmark: batch-1 ternary decode over the 30-layer BitNet-b1.58-2B4T-shaped
+stack (210 projections, 2.08e9 weights, 521 MB of .trit v1 planes).
+
+One step = one decode token: quantise the 210 fresh fp32 activation vectors
+(one launch) and compute the 210 ternary products (one persistent launch),
+inputs resident in HBM.  Weights are synthetic, seeded, drawn with per-layer
+zero fractions uniform in [0.385, 0.508]; the 521 MB of planes exceed the
+129 MB L2, so every step streams them from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("batch-1 ternary GEMV HBM GB/s (% of GB300 peak) and tok/s over 30-layer stack")
+WORKLOAD = "bitnet-2b4t-30layer-ternary-decode-batch1"
+SEED = 2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---- clocks -----------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- workload -----------------------------------------------------------------
+
+def build_stack(device, layers: int):
+    import numpy as np
+    import torch
+
+    import synth
+    from bit_plane_select_gb300.stack import TernaryStack
+
+    st = TernaryStack(device)
+    for layer, idx, name, N, K in synth.stack_items(layers):
+        w = synth.stack_weights(SEED, layer, idx)
+        st.add(torch.from_numpy(w), float(synth.w_scale(w)), M=1, name=f"L{layer}.{name}")
+    st.finalize()
+    for i, (layer, idx, name, N, K) in enumerate(synth.stack_items(layers)):
+        st.x[i].copy_(torch.from_numpy(synth.projection_acts(SEED, layer, idx, 1)))
+    torch.cuda.synchronize()
+    return st
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+GEMV_SOURCES = ["bit_plane_select_gb300/csrc/trit_gemv.cu",
+                "bit_plane_select_gb300/csrc/trit_internal.cuh"]
+
+
+def committed_traffic(bytes_per_launch_expected):
+    """DRAM bytes per launch of the product kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "select_accumulate_stack30.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != source_hash(GEMV_SOURCES):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+
+    st = build_stack(dev, args.layers)
+    stream = torch.cuda.current_stream(dev)
+
+    # warm-up
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    st.err.zero_()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            st.quantize()
+            ev[i][1].record(stream)
+            st.products()
+            ev[i][2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    quant_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    prod_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    err = int(st.err.item())
+
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    ms_per_step = total_ms / K
+    step_bytes = st.product_bytes()
+    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9        # GB/s, whole job
+    tok_s = world * K / (total_ms * 1e-3)
+    peak, peak_kind = peaks()
+
+    # dominant kernel: the product launch
+    prod_avg_ms = sum(prod_ms) / K
+    achieved = step_bytes / (prod_avg_ms * 1e-3) / 1e9
+    traffic = committed_traffic(step_bytes)
+
+    # e2e: host fp32 activations in, host y_i32 + y_f32 out, every step
+    x_host = st.x_arena.cpu().pin_memory()
+    y_host = torch.empty_like(st.y_arena, device="cpu").pin_memory()
+    f_host = torch.empty_like(st.f_arena, device="cpu").pin_memory()
+    E = max(1, min(K, args.e2e_steps))
+    for _ in range(3):
+        st.x_arena.copy_(x_host, non_blocking=True)
+        st.step()
+        y_host.copy_(st.y_arena, non_blocking=True)
+        f_host.copy_(st.f_arena, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        st.x_arena.copy_(x_host, non_blocking=True)
+        st.step()
+        y_host.copy_(st.y_arena, non_blocking=True)
+        f_host.copy_(st.f_arena, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    if world > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = st.x_arena.numel() * 4
+    d2h = st.y_arena.numel() * 4 + st.f_arena.numel() * 4
+
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "tok_per_s": round(tok_s, 1),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "layers": args.layers,
+            "projections": len(st.specs),
+            "batch": 1,
+            "weights": st.weights,
+            "plane_bytes": st.plane_bytes,
+            "algorithmic_bytes_per_step": step_bytes,
+            "l2": "inputs larger than L2: 521 MB of planes streamed per step (L2 129 MB)",
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+        },
+        "roofline": {
+            "kernel": "select_accumulate_kernel<1> (trit_gemm_many, one launch per token)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "avg_launch_us": round(prod_avg_ms * 1e3, 3),
+            "quant_avg_us": round(sum(quant_ms) / K * 1e3, 3),
+        },
+        "e2e": {
+            "value": round(step_bytes / (e2e_ms * 1e-3) / 1e9 * world, 1),
+            "unit": "GB/s",
+            "tok_per_s": round(world / (e2e_ms * 1e-3), 1),
+            "ms_per_step": round(e2e_ms, 5),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "steps": E,
+        },
+        "gpu_launches": 2 * K,
+        "err_flag": err,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_layers)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---- the CPU oracle ---------------------------------------------------------
+
+def oracle_sample(layers, rows_frac=1.0):
+    """Pack (untimed) the sampled projections with the oracle; returns a list of
+    (payload, w_scale, x fp32, K, rows) items."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    items = []
+    for layer, idx, name, N, K in synth.stack_items(layers):
+        w = synth.stack_weights(SEED, layer, idx)
+        n = max(1, int(round(N * rows_frac)))
+        items.append((oracle.pack(w[:n]), float(synth.w_scale(w)),
+                      synth.projection_acts(SEED, layer, idx, 1), K, n))
+    return items
+
+
+def oracle_step(items):
+    import oracle
+    for payload, ws, x, K, n in items:
+        q, s, _ = oracle.quant(x)
+        oracle.gemm(payload, ws, q, s, K)
+
+
+def cpu_baseline(layers):
+    """The oracle as it stands, single-threaded, on the first `layers` layers of
+    the same stack; scaled to the full 30-layer token."""
+    import synth
+    items = oracle_sample(layers)
+    weights = sum(N * K for _, _, _, N, K in synth.stack_items(layers))
+    t = time.perf_counter()
+    oracle_step(items)
+    dt = time.perf_counter() - t
+    full = sum(N * K for _, _, _, N, K in synth.stack_items(synth.LAYERS))
+    token_s = dt * full / weights
+    plane_b = weights / 4
+    return {"value": round(plane_b / dt / 1e9, 3), "unit": "GB/s",
+            "tok_per_s": round(1.0 / token_s, 4), "cores": 1, "kind": "oracle",
+            "sample": f"layers 0..{layers - 1} of the 30-layer stack ({len(items)} projections, "
+                      f"{weights} weights), quantise + product, one pass, {dt:.2f} s"}
+
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores, each step a bounded sample of the
+    token: a fixed fraction of every projection's rows."""
+    import synth
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    budget_s = args.reference_budget
+    steps = args.steps + args.warmup
+    full = sum(N * K for _, _, _, N, K in synth.stack_items(synth.LAYERS))
+    # calibrate: one projection
+    cal = oracle_sample(1, rows_frac=0.05)
+    t = time.perf_counter()
+    oracle_step(cal)
+    cal_s = (time.perf_counter() - t) / sum(n * K for _, _, _, K, n in cal)
+    frac = min(1.0, budget_s / steps / (cal_s * full))
+    frac = max(frac, 1.0 / 2560)
+    items = oracle_sample(synth.LAYERS, rows_frac=frac)
+    w_sample = sum(n * K for _, _, _, K, n in items)
+    b_sample = sum(n * ((K + 63) // 64) * 16 + K + 4 + 8 * n for _, _, _, K, n in items)
+    for _ in range(args.warmup):
+        oracle_step(items)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(items)
+    dt = (time.perf_counter() - t) / args.steps
+    value = b_sample / dt / 1e9
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "tok_per_s": round(w_sample / full / dt, 6),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": synth.LAYERS, "batch": 1},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{frac:.5f} of the rows of each of the 210 projections "
+                                   f"({w_sample} weights) per step, quantise + product"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-layers", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

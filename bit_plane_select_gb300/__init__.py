@@ -1,0 +1,274 @@
+"""bit_plane_select_gb300 -- ternary select-accumulate GEMV/GEMM over .trit v1
+bit planes on GB300 (sm_103a).
+
+This module is a thin ctypes binding of ``libtrit.so`` (declared in
+``include/trit.h``): it checks tensor dtypes/devices and passes raw device
+pointers and the current torch stream.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU fallback -- if the library is not
+built, or the device is not an sm_103 GPU, the calls raise.
+
+Functions carry the C names:
+  trit_pack, trit_unpack, trit_verify, trit_quant_act, trit_quant_act_many,
+  trit_gemv, trit_gemm, trit_gemm_many
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "TritError", "ERR_P1", "ERR_P2", "ERR_NOT_TERNARY", "ERR_NONFINITE", "ERR_TIMEOUT",
+    "library_path", "lib", "payload_bytes", "k_pad", "trit_pack", "trit_unpack", "trit_verify",
+    "trit_quant_act", "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
+    "ProjList", "ActList", "TritProj", "TritAct",
+]
+
+ERR_P1 = 1
+ERR_P2 = 2
+ERR_NOT_TERNARY = 4
+ERR_NONFINITE = 8
+ERR_TIMEOUT = 16
+
+_STATUS = {0: "TRIT_OK", 1: "TRIT_E_ARG", 2: "TRIT_E_SHAPE", 4: "TRIT_E_SCALE",
+           6: "TRIT_E_CUDA", 7: "TRIT_E_DEVICE"}
+
+
+class TritError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        super().__init__(f"{where}: {_STATUS.get(status, status)} {detail}".strip())
+        self.status = status
+
+
+class TritProj(ctypes.Structure):
+    _fields_ = [("planes", ctypes.c_void_p), ("x_i8", ctypes.c_void_p),
+                ("x_scale", ctypes.c_void_p), ("y_i32", ctypes.c_void_p),
+                ("y_f32", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+
+
+class TritAct(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("x_i8", ctypes.c_void_p), ("x_scale", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libtrit.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with bit_plane_select_gb300.build.build() "
+                "(needs nvcc); there is no fallback implementation")
+        L = ctypes.CDLL(path)
+        p, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        L.trit_status_string.restype = ctypes.c_char_p
+        L.trit_status_string.argtypes = [ctypes.c_int]
+        L.trit_last_cuda_error.restype = ctypes.c_char_p
+        L.trit_last_cuda_error.argtypes = []
+        L.trit_abi_version.restype = i32
+        L.trit_payload_bytes.restype = i64
+        L.trit_payload_bytes.argtypes = [i64, i64]
+        L.trit_pack.argtypes = [p, i64, i64, f32, p, p, p, p]
+        L.trit_unpack.argtypes = [p, i64, i64, p, p, p]
+        L.trit_verify.argtypes = [p, i64, i64, p, p, p]
+        L.trit_quant_act.argtypes = [p, i64, i64, p, p, p, p]
+        L.trit_quant_act_many.argtypes = [p, i32, p, p]
+        L.trit_gemv.argtypes = [p, f32, p, p, i64, i64, p, p, p, p]
+        L.trit_gemm.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
+        L.trit_gemm_many.argtypes = [p, i32, p, p]
+        for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
+                     "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        detail = lib().trit_last_cuda_error().decode() if status == 6 else ""
+        raise TritError(status, where, detail)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor | None, dtype, name: str, optional: bool = False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def payload_bytes(N: int, K: int) -> int:
+    return int(lib().trit_payload_bytes(N, K))
+
+
+def k_pad(K: int) -> int:
+    """Row stride of the int8 activations: 64 * ceil(K / 64)."""
+    return ((K + 63) // 64) * 64
+
+
+def _err(err_flag, device):
+    if err_flag is None:
+        err_flag = torch.zeros(1, dtype=torch.int32, device=device)
+    return err_flag
+
+
+def trit_pack(w: torch.Tensor, w_scale: float, planes=None, scale_out=None, err_flag=None,
+              stream=None):
+    """int8 [N, K] ternary -> planes uint8 [N, ceil(K/64), 16].  Returns (planes, err_flag)."""
+    N, K = w.shape
+    if planes is None:
+        planes = torch.empty((N, (K + 63) // 64, 16), dtype=torch.uint8, device=w.device)
+    err_flag = _err(err_flag, w.device)
+    _check(lib().trit_pack(_dev(w, torch.int8, "w"), N, K, float(w_scale),
+                           _dev(planes, torch.uint8, "planes"),
+                           _dev(scale_out, torch.float32, "scale_out", True),
+                           _dev(err_flag, torch.int32, "err_flag"), _stream(stream)), "trit_pack")
+    return planes, err_flag
+
+
+def trit_unpack(planes: torch.Tensor, K: int, w=None, err_flag=None, stream=None):
+    N = planes.shape[0]
+    if w is None:
+        w = torch.empty((N, K), dtype=torch.int8, device=planes.device)
+    err_flag = _err(err_flag, planes.device)
+    _check(lib().trit_unpack(_dev(planes, torch.uint8, "planes"), N, K, _dev(w, torch.int8, "w"),
+                             _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_unpack")
+    return w, err_flag
+
+
+def trit_verify(planes: torch.Tensor, K: int, err_flag=None, first_bad=None, stream=None):
+    """Returns (err_flag, first_bad); first_bad is an int64 tensor initialised to -1
+    (UINT64_MAX) when not given."""
+    N = planes.shape[0]
+    err_flag = _err(err_flag, planes.device)
+    if first_bad is None:
+        first_bad = torch.full((1,), -1, dtype=torch.int64, device=planes.device)
+    _check(lib().trit_verify(_dev(planes, torch.uint8, "planes"), N, K,
+                             _dev(err_flag, torch.int32, "err_flag"),
+                             _dev(first_bad, torch.int64, "first_bad"), _stream(stream)),
+           "trit_verify")
+    return err_flag, first_bad
+
+
+def trit_quant_act(x: torch.Tensor, x_i8=None, x_scale=None, err_flag=None, stream=None):
+    """fp32 [M, K] -> (x_i8 [M, K_pad], x_scale [M], err_flag)."""
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    M, K = x.shape
+    if x_i8 is None:
+        x_i8 = torch.empty((M, k_pad(K)), dtype=torch.int8, device=x.device)
+    if x_scale is None:
+        x_scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    err_flag = _err(err_flag, x.device)
+    _check(lib().trit_quant_act(_dev(x, torch.float32, "x"), M, K, _dev(x_i8, torch.int8, "x_i8"),
+                                _dev(x_scale, torch.float32, "x_scale"),
+                                _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_quant_act")
+    return x_i8, x_scale, err_flag
+
+
+def trit_gemm(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale: torch.Tensor,
+              K: int, y_i32=None, y_f32=None, err_flag=None, stream=None, want=("i32", "f32")):
+    """y = W x for M = x_i8.shape[0] rows.  Returns (y_i32, y_f32, err_flag)."""
+    N = planes.shape[0]
+    M = x_i8.shape[0] if x_i8.dim() == 2 else 1
+    if y_i32 is None and "i32" in want:
+        y_i32 = torch.empty((M, N), dtype=torch.int32, device=planes.device)
+    if y_f32 is None and "f32" in want:
+        y_f32 = torch.empty((M, N), dtype=torch.float32, device=planes.device)
+    err_flag = _err(err_flag, planes.device)
+    _check(lib().trit_gemm(_dev(planes, torch.uint8, "planes"), float(w_scale),
+                           _dev(x_i8, torch.int8, "x_i8"), _dev(x_scale, torch.float32, "x_scale"),
+                           M, N, K, _dev(y_i32, torch.int32, "y_i32", True),
+                           _dev(y_f32, torch.float32, "y_f32", True),
+                           _dev(err_flag, torch.int32, "err_flag"), _stream(stream)), "trit_gemm")
+    return y_i32, y_f32, err_flag
+
+
+def trit_gemv(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale: torch.Tensor,
+              K: int, y_i32=None, y_f32=None, err_flag=None, stream=None):
+    N = planes.shape[0]
+    if y_i32 is None:
+        y_i32 = torch.empty(N, dtype=torch.int32, device=planes.device)
+    if y_f32 is None:
+        y_f32 = torch.empty(N, dtype=torch.float32, device=planes.device)
+    err_flag = _err(err_flag, planes.device)
+    _check(lib().trit_gemv(_dev(planes, torch.uint8, "planes"), float(w_scale),
+                           _dev(x_i8, torch.int8, "x_i8"), _dev(x_scale, torch.float32, "x_scale"),
+                           N, K, _dev(y_i32, torch.int32, "y_i32", True),
+                           _dev(y_f32, torch.float32, "y_f32", True),
+                           _dev(err_flag, torch.int32, "err_flag"), _stream(stream)), "trit_gemv")
+    return y_i32, y_f32, err_flag
+
+
+class ProjList:
+    """A prepared host array of trit_proj entries (tensors are kept alive).
+
+    entries: iterables of (planes, w_scale, x_i8, x_scale, K, y_i32, y_f32);
+    M is x_i8's row count, N the planes' row count.
+    """
+
+    def __init__(self, entries):
+        self._keep = []
+        items = []
+        for planes, w_scale, x_i8, x_scale, K, y_i32, y_f32 in entries:
+            M = x_i8.shape[0] if x_i8.dim() == 2 else 1
+            items.append(TritProj(
+                _dev(planes, torch.uint8, "planes"), _dev(x_i8, torch.int8, "x_i8"),
+                _dev(x_scale, torch.float32, "x_scale"),
+                _dev(y_i32, torch.int32, "y_i32", True), _dev(y_f32, torch.float32, "y_f32", True),
+                M, planes.shape[0], K, float(w_scale), 0))
+            self._keep.append((planes, x_i8, x_scale, y_i32, y_f32))
+        self.count = len(items)
+        self.array = (TritProj * self.count)(*items)
+
+
+class ActList:
+    """A prepared host array of trit_act entries: (x fp32 [M, K], x_i8, x_scale)."""
+
+    def __init__(self, entries):
+        self._keep = []
+        items = []
+        for x, x_i8, x_scale in entries:
+            M, K = x.shape
+            items.append(TritAct(_dev(x, torch.float32, "x"), _dev(x_i8, torch.int8, "x_i8"),
+                                 _dev(x_scale, torch.float32, "x_scale"), M, K))
+            self._keep.append((x, x_i8, x_scale))
+        self.count = len(items)
+        self.array = (TritAct * self.count)(*items)
+
+
+def trit_gemm_many(plist: ProjList, err_flag: torch.Tensor, stream=None):
+    _check(lib().trit_gemm_many(ctypes.cast(plist.array, ctypes.c_void_p), plist.count,
+                                _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_gemm_many")
+
+
+def trit_quant_act_many(alist: ActList, err_flag: torch.Tensor, stream=None):
+    _check(lib().trit_quant_act_many(ctypes.cast(alist.array, ctypes.c_void_p), alist.count,
+                                     _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_quant_act_many")

@@ -1,0 +1,252 @@
+// The extern "C" boundary of libtrit: argument validation on the host, then
+// dispatch to the launchers.  Nothing is enqueued when validation fails.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "trit_internal.cuh"
+
+namespace trit {
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+int g_dev_ok[kMaxDevices] = {0};   // 0 unknown, 1 sm_103, -1 other
+std::mutex g_dev_mutex;
+
+trit_status cuda_fail(cudaError_t e) {
+    snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return TRIT_E_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool rows_ok(int64_t n) { return n >= 1 && n <= kMaxRows; }
+bool cols_ok(int64_t k) { return k >= 1 && k <= kMaxK; }
+
+// The library carries sm_103a code only.
+trit_status check_device() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return TRIT_E_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_dev_ok[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = sms;
+        g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_dev_ok[dev] == 1 ? TRIT_OK : TRIT_E_DEVICE;
+}
+
+trit_status check_proj(const trit_proj &p) {
+    if (!p.planes || !p.x_i8 || !p.x_scale || (!p.y_i32 && !p.y_f32) || p.reserved != 0)
+        return TRIT_E_ARG;
+    if (!aligned(p.planes, 16) || !aligned(p.x_i8, 16) || !aligned(p.x_scale, 4) ||
+        !aligned(p.y_i32, 4) || !aligned(p.y_f32, 4))
+        return TRIT_E_ARG;
+    if (!rows_ok(p.M) || !rows_ok(p.N) || !cols_ok(p.K)) return TRIT_E_SHAPE;
+    if (!isfinite(p.w_scale) || !(p.w_scale > 0.0f)) return TRIT_E_SCALE;
+    return TRIT_OK;
+}
+
+ProjDev to_dev(const trit_proj &p) {
+    ProjDev d;
+    d.planes = reinterpret_cast<const uint4 *>(p.planes);
+    d.x = p.x_i8;
+    d.x_scale = p.x_scale;
+    d.y_i32 = p.y_i32;
+    d.y_f32 = p.y_f32;
+    d.M = p.M;
+    d.N = p.N;
+    d.K = int32_t(p.K);
+    d.B = int32_t(beats_per_row(p.K));
+    d.w_scale = p.w_scale;
+    d.pad_ = 0;
+    return d;
+}
+
+trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, cudaStream_t s) {
+    if (!list || count <= 0 || !err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        trit_status st = check_proj(list[i]);
+        if (st != TRIT_OK) return st;
+    }
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    static thread_local ProjDev one[TRIT_MAX_LIST_PER_LAUNCH];
+    static thread_local ProjDev many[TRIT_MAX_LIST_PER_LAUNCH];
+    int n1 = 0, nm = 0;
+    auto flush1 = [&]() -> cudaError_t {
+        cudaError_t e = n1 ? launch_gemv_many(one, n1, err_flag, s) : cudaSuccess;
+        n1 = 0;
+        return e;
+    };
+    auto flushm = [&]() -> cudaError_t {
+        cudaError_t e = nm ? launch_gemm_dp4a_many(many, nm, err_flag, s) : cudaSuccess;
+        nm = 0;
+        return e;
+    };
+    for (int32_t i = 0; i < count; ++i) {
+        cudaError_t e = cudaSuccess;
+        if (list[i].M == 1) {
+            one[n1++] = to_dev(list[i]);
+            if (n1 == TRIT_MAX_LIST_PER_LAUNCH) e = flush1();
+        } else {
+            many[nm++] = to_dev(list[i]);
+            if (nm == TRIT_MAX_LIST_PER_LAUNCH) e = flushm();
+        }
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    cudaError_t e = flush1();
+    if (e == cudaSuccess) e = flushm();
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+}  // namespace trit
+
+using namespace trit;
+
+extern "C" {
+
+TRIT_API const char *trit_status_string(trit_status s) {
+    switch (s) {
+        case TRIT_OK: return "TRIT_OK";
+        case TRIT_E_ARG: return "TRIT_E_ARG: bad pointer, count or alignment";
+        case TRIT_E_SHAPE: return "TRIT_E_SHAPE: size outside the supported range";
+        case TRIT_E_SCALE: return "TRIT_E_SCALE: w_scale must be finite and > 0";
+        case TRIT_E_CUDA: return "TRIT_E_CUDA: a CUDA call failed";
+        case TRIT_E_DEVICE: return "TRIT_E_DEVICE: the current device is not sm_103";
+    }
+    return "unknown trit_status";
+}
+
+TRIT_API const char *trit_last_cuda_error(void) { return g_last_cuda_error; }
+
+TRIT_API int32_t trit_abi_version(void) { return 1; }
+
+TRIT_API int64_t trit_payload_bytes(int64_t N, int64_t K) {
+    if (!rows_ok(N) || !cols_ok(K)) return -1;
+    return N * beats_per_row(K) * 16;
+}
+
+TRIT_API trit_status trit_pack(const int8_t *w, int64_t N, int64_t K, float w_scale,
+                               uint8_t *planes, float *scale_out, uint32_t *err_flag,
+                               trit_stream_t stream) {
+    if (!w || !planes || !err_flag || !aligned(planes, 16) || !aligned(scale_out, 4) ||
+        !aligned(err_flag, 4))
+        return TRIT_E_ARG;
+    if (!rows_ok(N) || !cols_ok(K)) return TRIT_E_SHAPE;
+    if (!isfinite(w_scale) || !(w_scale > 0.0f)) return TRIT_E_SCALE;
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_pack(w, N, K, w_scale, planes, scale_out, err_flag,
+                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+TRIT_API trit_status trit_unpack(const uint8_t *planes, int64_t N, int64_t K, int8_t *w,
+                                 uint32_t *err_flag, trit_stream_t stream) {
+    if (!w || !planes || !err_flag || !aligned(planes, 16) || !aligned(err_flag, 4))
+        return TRIT_E_ARG;
+    if (!rows_ok(N) || !cols_ok(K)) return TRIT_E_SHAPE;
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_unpack(planes, N, K, w, err_flag, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+TRIT_API trit_status trit_verify(const uint8_t *planes, int64_t N, int64_t K, uint32_t *err_flag,
+                                 uint64_t *first_bad, trit_stream_t stream) {
+    if (!planes || !err_flag || !aligned(planes, 16) || !aligned(err_flag, 4) ||
+        !aligned(first_bad, 8))
+        return TRIT_E_ARG;
+    if (!rows_ok(N) || !cols_ok(K)) return TRIT_E_SHAPE;
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_verify(planes, N, K, err_flag,
+                                  reinterpret_cast<unsigned long long *>(first_bad),
+                                  reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+TRIT_API trit_status trit_quant_act_many(const trit_act *list, int32_t count, uint32_t *err_flag,
+                                         trit_stream_t stream) {
+    if (!list || count <= 0 || !err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
+    int64_t rows = 0;
+    for (int32_t i = 0; i < count; ++i) {
+        const trit_act &a = list[i];
+        if (!a.x || !a.x_i8 || !a.x_scale || !aligned(a.x, 4) || !aligned(a.x_i8, 16) ||
+            !aligned(a.x_scale, 4))
+            return TRIT_E_ARG;
+        if (!rows_ok(a.M) || !cols_ok(a.K)) return TRIT_E_SHAPE;
+        rows += a.M;
+        if (rows > kMaxRows) return TRIT_E_SHAPE;
+    }
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_quant_many(list, count, err_flag, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+TRIT_API trit_status trit_quant_act(const float *x, int64_t M, int64_t K, int8_t *x_i8,
+                                    float *x_scale, uint32_t *err_flag, trit_stream_t stream) {
+    trit_act a;
+    a.x = x;
+    a.x_i8 = x_i8;
+    a.x_scale = x_scale;
+    a.M = M;
+    a.K = K;
+    return trit_quant_act_many(&a, 1, err_flag, stream);
+}
+
+TRIT_API trit_status trit_gemm_many(const trit_proj *list, int32_t count, uint32_t *err_flag,
+                                    trit_stream_t stream) {
+    return run_many(list, count, err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+TRIT_API trit_status trit_gemm(const uint8_t *planes, float w_scale, const int8_t *x_i8,
+                               const float *x_scale, int64_t M, int64_t N, int64_t K,
+                               int32_t *y_i32, float *y_f32, uint32_t *err_flag,
+                               trit_stream_t stream) {
+    trit_proj p;
+    p.planes = planes;
+    p.x_i8 = x_i8;
+    p.x_scale = x_scale;
+    p.y_i32 = y_i32;
+    p.y_f32 = y_f32;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.w_scale = w_scale;
+    p.reserved = 0;
+    return run_many(&p, 1, err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_t *x_i8,
+                               const float *x_scale, int64_t N, int64_t K, int32_t *y_i32,
+                               float *y_f32, uint32_t *err_flag, trit_stream_t stream) {
+    return trit_gemm(planes, w_scale, x_i8, x_scale, 1, N, K, y_i32, y_f32, err_flag, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,437 @@
+// Select-accumulate kernels for decode: y = W x over .trit v1 bit planes,
+// exact int32 accumulation with dp4a, one persistent launch per product list.
+//
+// What is computed ("Tritium: One Weight Format for Ternary Inference ..." --
+// Introduction, Eq. 3; "The .trit format, version 1" -- 1 and 2.3):
+//   y_r = sum_{c : pos bit set} x_c - sum_{c : neg bit set} x_c
+// over beats of 64 columns (pos, neg = two 64-bit masks).  Any beat with
+// pos & neg != 0 sets TRIT_ERR_P1.
+//
+// Work split.  A warp handles 4 rows x 8 beats per step: lane = 8*rs + bs
+// reads beat (8t + bs) of row (4g + rs) with one 16-byte load, so one warp
+// load covers 4 x 128 contiguous bytes.  A "group" is 4 rows; it takes
+// ceil(B/8) steps.  The launch is persistent: every CTA gets an equal share of
+// the total steps of the list (groups never split), and each warp a contiguous
+// run of the CTA's groups.  The CTA keeps the activation row(s) of the
+// current product in shared memory in the permuted layout of trit_internal.cuh.
+//
+// M = 1 (2^j-weighted masks).  For plane word P (32 columns) and j = 0..7,
+// P & (0x01010101 << j) has byte i equal to 2^j exactly when column 8i+j is
+// selected, so dp4a(X_j, P & mask_j) adds 2^j * (sum of the selected x in
+// {j, 8+j, 16+j, 24+j}).  Eight accumulators per plane, one per j, are
+// divided by 2^j (exact: each is a multiple of 2^j) only when a row ends.
+// Cost per beat: 32 AND + 32 dp4a -- no shifts, no byte-mask expansion.
+//
+// Long rows.  The staged activations must fit in shared memory, so a product
+// whose rows exceed kSegBeats(MT) beats is split into column segments.  Each
+// segment adds its exact int32 partial into the output with an integer
+// atomic (exact and order-independent, so the result is bit-identical to a
+// single pass); the caller's int32 output, or else the fp32 output buffer
+// reinterpreted as int32, is zeroed first and a final pass applies the fp32
+// dequantisation.  No scratch memory is used.
+//
+// M > 1 (+-1 bytes).  Each beat is expanded once into sixteen words of bytes
+// in {+1, 0, -1} (shift + sign-replicating byte permute + one LOP3 per word)
+// and reused for every activation row held by the CTA: 16 dp4a per row.
+#include "trit_internal.cuh"
+
+namespace trit {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kLanesPerRow = 8;
+constexpr int kRowsPerGroup = 32 / kLanesPerRow;
+constexpr int kDepth = 4;                   // 16-byte loads in flight per lane
+constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
+
+// Beats per column segment for MT staged rows: MT * kSegBeats * 80 bytes of
+// shared memory stay under 92 KB.  A segment takes at most 144 steps per row,
+// so the 2^j-weighted accumulators (at most 2^17 per step) stay below 2^25.
+__host__ __device__ constexpr int seg_beats(int mt) { return 1152 / mt; }
+
+struct Entry {
+    const uint4 *planes;
+    const int8_t *x;        // first activation row of this entry, stride xld
+    const float *x_scale;   // first scale of this entry
+    int32_t *y_i32;         // first output row of this entry, stride N
+    float *y_f32;
+    int64_t N;
+    int64_t groups;         // ceil(N / 4)
+    int64_t cost_begin;     // prefix sum of groups * iters over the list
+    int64_t xld;            // activation row stride (K_pad)
+    int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / 8)
+    int32_t bstride;        // beats per full row of the planes
+    int32_t mrows;          // activation rows of this entry (<= MT)
+    float w_scale;
+    int32_t *acc;           // non-NULL: atomically add the int32 partial here (stride N)
+};
+
+struct List {
+    int32_t count;
+    int32_t xs_words;       // shared words per staged activation row
+    int64_t total_cost;
+    uint32_t *err;
+    Entry e[kMaxList];
+};
+
+// Stage activation rows 0..mrows-1 of entry E into shared memory, permuted,
+// zero past column K, covering iters*8 beats.
+template <int MT>
+__device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_words) {
+    const int halves = E.iters * 8 * 2;
+    for (int idx = threadIdx.x; idx < halves * MT; idx += kThreads) {
+        const int m = idx / halves;
+        const int hb = idx - m * halves;
+        uint32_t out[8];
+        if (m < E.mrows) {
+            const int c0 = hb * 32;
+            const int8_t *xr = E.x + int64_t(m) * E.xld;
+            uint32_t in[8];
+            if (c0 + 32 <= E.K) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(xr + c0);
+                const uint4 u0 = p[0], u1 = p[1];
+                in[0] = u0.x; in[1] = u0.y; in[2] = u0.z; in[3] = u0.w;
+                in[4] = u1.x; in[5] = u1.y; in[6] = u1.z; in[7] = u1.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int c = c0 + 4 * k + b;
+                        const uint32_t v = c < E.K ? (uint32_t)(uint8_t)xr[c] : 0u;
+                        w |= v << (8 * b);
+                    }
+                    in[k] = w;
+                }
+            }
+            permute_block(in, out);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) out[j] = 0;
+        }
+        uint32_t *dst = xs + m * xs_words + (hb >> 1) * kXBeatWords + (hb & 1) * 8;
+        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+}
+
+__device__ __forceinline__ int32_t row_sum8(int32_t v) {
+    v += __shfl_xor_sync(~0u, v, 1);
+    v += __shfl_xor_sync(~0u, v, 2);
+    v += __shfl_xor_sync(~0u, v, 4);
+    return v;
+}
+
+// Process groups [gb, ge) of entry E with one warp.  Returns the OR of pos & neg.
+template <int MT>
+__device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *xs, int xs_words,
+                                               int64_t gb, int64_t ge, int rs, int bs) {
+    const int it = E.iters;
+    const int ngroups = int(ge - gb);
+    const int steps = ngroups * it;
+    uint32_t viol = 0;
+
+    // load cursor: group lg (relative to gb), step lt; lrow points at beat bs of
+    // this lane's row of group lg
+    int lg = 0, lt = 0;
+    int64_t lrow_idx = gb * kRowsPerGroup + rs;
+    const uint4 *lrow = E.planes + lrow_idx * E.bstride + bs;
+    auto next_load = [&]() -> uint4 {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (lg < ngroups && lrow_idx < E.N && lt * kLanesPerRow + bs < E.B)
+            v = ldg_stream(lrow + lt * kLanesPerRow);
+        if (++lt == it) {
+            lt = 0;
+            ++lg;
+            lrow_idx += kRowsPerGroup;
+            lrow += int64_t(kRowsPerGroup) * E.bstride;
+        }
+        return v;
+    };
+
+    uint4 ring[kDepth];
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) ring[d] = next_load();
+
+    int acc[MT == 1 ? 16 : MT];
+#pragma unroll
+    for (int i = 0; i < (MT == 1 ? 16 : MT); ++i) acc[i] = 0;
+    int64_t row = gb * kRowsPerGroup + rs;   // compute cursor: this lane's row
+    int ct = 0;
+
+    for (int s = 0; s < steps; s += kDepth) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+            if (s + d < steps) {
+                const uint4 v = ring[d];
+                ring[d] = next_load();
+                viol |= (v.x & v.z) | (v.y & v.w);
+                const int beat = ct * kLanesPerRow + bs;
+
+                if constexpr (MT == 1) {
+                    const uint4 *X = reinterpret_cast<const uint4 *>(xs + beat * kXBeatWords);
+                    const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
+                    const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t msk = 0x01010101u << j;
+                        acc[j] = dp4a_su(xl[j], v.x & msk, acc[j]);
+                        acc[j] = dp4a_su(xh[j], v.y & msk, acc[j]);
+                        acc[8 + j] = dp4a_su(xl[j], v.z & msk, acc[8 + j]);
+                        acc[8 + j] = dp4a_su(xh[j], v.w & msk, acc[8 + j]);
+                    }
+                } else {
+                    // bytes of w: +1 where pos, -1 (0xFF) where neg, 0 elsewhere
+                    uint32_t wl[8], wh[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t nl = prmt(v.z << (7 - j), 0u, 0xBA98u);
+                        const uint32_t nh = prmt(v.w << (7 - j), 0u, 0xBA98u);
+                        wl[j] = ((v.x >> j) & 0x01010101u) | nl;
+                        wh[j] = ((v.y >> j) & 0x01010101u) | nh;
+                    }
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const uint4 *X =
+                            reinterpret_cast<const uint4 *>(xs + m * xs_words + beat * kXBeatWords);
+                        const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
+                        int a = acc[m];
+                        a = dp4a_ss(a0.x, wl[0], a); a = dp4a_ss(a0.y, wl[1], a);
+                        a = dp4a_ss(a0.z, wl[2], a); a = dp4a_ss(a0.w, wl[3], a);
+                        a = dp4a_ss(a1.x, wl[4], a); a = dp4a_ss(a1.y, wl[5], a);
+                        a = dp4a_ss(a1.z, wl[6], a); a = dp4a_ss(a1.w, wl[7], a);
+                        a = dp4a_ss(a2.x, wh[0], a); a = dp4a_ss(a2.y, wh[1], a);
+                        a = dp4a_ss(a2.z, wh[2], a); a = dp4a_ss(a2.w, wh[3], a);
+                        a = dp4a_ss(a3.x, wh[4], a); a = dp4a_ss(a3.y, wh[5], a);
+                        a = dp4a_ss(a3.z, wh[6], a); a = dp4a_ss(a3.w, wh[7], a);
+                        acc[m] = a;
+                    }
+                }
+
+                if (++ct == it) {
+                    if constexpr (MT == 1) {
+                        int32_t y = 0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) y += (acc[j] - acc[8 + j]) >> j;
+                        y = row_sum8(y);
+                        if (bs == 0 && row < E.N) {
+                            if (E.acc) {
+                                atomicAdd(E.acc + row, y);
+                            } else {
+                                if (E.y_i32) E.y_i32[row] = y;
+                                if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, E.x_scale[0]);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] = 0;
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            const int32_t y = row_sum8(acc[m]);
+                            acc[m] = 0;
+                            if (bs == 0 && row < E.N && m < E.mrows) {
+                                const int64_t o = int64_t(m) * E.N + row;
+                                if (E.acc) {
+                                    atomicAdd(E.acc + o, y);
+                                } else {
+                                    if (E.y_i32) E.y_i32[o] = y;
+                                    if (E.y_f32) E.y_f32[o] = dequant(y, E.w_scale, E.x_scale[m]);
+                                }
+                            }
+                        }
+                    }
+                    ct = 0;
+                    row += kRowsPerGroup;
+                }
+            }
+        }
+    }
+    return viol;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
+    select_accumulate_kernel(const __grid_constant__ List L) {
+    extern __shared__ __align__(16) uint32_t xs[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rs = lane / kLanesPerRow, bs = lane % kLanesPerRow;
+    const int64_t lo = int64_t(blockIdx.x) * L.total_cost / gridDim.x;
+    const int64_t hi = (int64_t(blockIdx.x) + 1) * L.total_cost / gridDim.x;
+    uint32_t viol = 0;
+
+    int e = 0;
+    while (e + 1 < L.count && L.e[e + 1].cost_begin <= lo) ++e;
+    for (; e < L.count && L.e[e].cost_begin < hi; ++e) {
+        const Entry &E = L.e[e];
+        const int64_t it = E.iters;
+        // groups whose first step lies in [lo, hi)
+        const int64_t dlo = lo - E.cost_begin, dhi = hi - E.cost_begin;
+        const int64_t g0 = dlo <= 0 ? 0 : (dlo + it - 1) / it;
+        int64_t g1 = (dhi + it - 1) / it;
+        if (g1 > E.groups) g1 = E.groups;
+        if (g0 >= g1) continue;
+        __syncthreads();   // the previous entry's readers are done with xs
+        stage_x<MT>(E, xs, L.xs_words);
+        __syncthreads();
+        const int64_t n = g1 - g0;
+        const int64_t wb = g0 + n * warp / kWarps, we = g0 + n * (warp + 1) / kWarps;
+        if (wb < we) viol |= run_groups<MT>(E, xs, L.xs_words, wb, we, rs, bs);
+    }
+    if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
+}
+
+template <int MT>
+int occupancy(size_t smem) {
+    int dev = 0, occ = 0;
+    cudaGetDevice(&dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_accumulate_kernel<MT>, kThreads,
+                                                  smem);
+    return occ < 1 ? 1 : occ;
+}
+
+template <int MT>
+cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t s) {
+    static thread_local List L;   // host staging for the by-value parameter block
+    L.count = n;
+    L.err = err;
+    int64_t cost = 0, groups = 0;
+    int max_iters = 1;
+    for (int i = 0; i < n; ++i) {
+        L.e[i] = entries[i];
+        L.e[i].cost_begin = cost;
+        cost += entries[i].groups * entries[i].iters;
+        groups += entries[i].groups;
+        if (entries[i].iters > max_iters) max_iters = entries[i].iters;
+    }
+    L.total_cost = cost;
+    L.xs_words = max_iters * kLanesPerRow * kXBeatWords;
+    const size_t smem = size_t(L.xs_words) * 4 * MT;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(select_accumulate_kernel<MT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t per_sm = occupancy<MT>(smem);
+    const int64_t cap = per_sm * device_sm_count();
+    const int64_t want = (groups + kWarps - 1) / kWarps;
+    const int grid = int(want < cap ? (want < 1 ? 1 : want) : cap);
+    select_accumulate_kernel<MT><<<grid, kThreads, smem, s>>>(L);
+    return cudaGetLastError();
+}
+
+// The fp32 pass of segmented products: y_f32 = dequant(acc) where acc is the
+// product's int32 sums (y_i32, or the y_f32 buffer itself read as int32).
+__global__ void __launch_bounds__(256) segment_epilogue_kernel(const int32_t *acc, float *y_f32,
+                                                               int64_t M, int64_t N, float w_scale,
+                                                               const float *x_scale) {
+    const int64_t total = M * N;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t m = i / N;
+        y_f32[i] = dequant(acc[i], w_scale, x_scale[m]);
+    }
+}
+
+// One list entry: activation rows [m0, m0 + mrows) and beats [b0, b0 + nb) of p.
+Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb, int32_t *acc) {
+    Entry E;
+    const int64_t Kp = int64_t(p.B) * 64;
+    E.planes = p.planes + b0;
+    E.x = p.x + m0 * Kp + b0 * 64;
+    E.x_scale = p.x_scale + m0;
+    E.y_i32 = p.y_i32 ? p.y_i32 + m0 * p.N : nullptr;
+    E.y_f32 = p.y_f32 ? p.y_f32 + m0 * p.N : nullptr;
+    E.acc = acc ? acc + m0 * p.N : nullptr;
+    E.N = p.N;
+    E.groups = (p.N + kRowsPerGroup - 1) / kRowsPerGroup;
+    E.cost_begin = 0;
+    E.xld = Kp;
+    const int64_t kseg = int64_t(p.K) - b0 * 64;
+    E.K = int32_t(kseg < nb * 64 ? kseg : nb * 64);
+    E.B = int32_t(nb);
+    E.iters = int32_t((nb + kLanesPerRow - 1) / kLanesPerRow);
+    E.bstride = p.B;
+    E.mrows = mrows;
+    E.w_scale = p.w_scale;
+    return E;
+}
+
+template <int MT>
+cudaError_t launch_entries(const Entry *all, int count, uint32_t *err, cudaStream_t s) {
+    for (int base = 0; base < count; base += kMaxList) {
+        const int n = count - base < kMaxList ? count - base : kMaxList;
+        cudaError_t e = launch_list<MT>(all + base, n, err, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// Expand the products into list entries -- activation rows MT at a time, and
+// column segments for rows longer than seg_beats(MT) -- and launch them.
+template <int MT>
+cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {
+    static thread_local Entry buf[kMaxList];
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+    // zero the accumulation targets of segmented products first
+    for (int i = 0; i < count && e == cudaSuccess; ++i) {
+        const ProjDev &p = list[i];
+        if (p.B > seg_beats(MT)) {
+            int32_t *acc = p.y_i32 ? p.y_i32 : reinterpret_cast<int32_t *>(p.y_f32);
+            e = cudaMemsetAsync(acc, 0, size_t(p.M * p.N) * sizeof(int32_t), s);
+        }
+    }
+    for (int i = 0; i < count && e == cudaSuccess; ++i) {
+        const ProjDev &p = list[i];
+        const bool seg = p.B > seg_beats(MT);
+        int32_t *acc = !seg ? nullptr : (p.y_i32 ? p.y_i32 : reinterpret_cast<int32_t *>(p.y_f32));
+        for (int64_t m0 = 0; m0 < p.M && e == cudaSuccess; m0 += MT) {
+            const int rows = int(p.M - m0 < MT ? p.M - m0 : MT);
+            for (int64_t b0 = 0; b0 < p.B && e == cudaSuccess; b0 += seg_beats(MT)) {
+                const int64_t nb = p.B - b0 < seg_beats(MT) ? p.B - b0 : seg_beats(MT);
+                buf[n++] = make_entry(p, m0, rows, b0, nb, acc);
+                if (n == kMaxList) {
+                    e = launch_entries<MT>(buf, n, err, s);
+                    n = 0;
+                }
+            }
+        }
+    }
+    if (e == cudaSuccess && n) e = launch_entries<MT>(buf, n, err, s);
+    for (int i = 0; i < count && e == cudaSuccess; ++i) {
+        const ProjDev &p = list[i];
+        if (p.B > seg_beats(MT) && p.y_f32) {
+            const int32_t *acc = p.y_i32 ? p.y_i32 : reinterpret_cast<const int32_t *>(p.y_f32);
+            const int64_t total = p.M * p.N;
+            int64_t blocks = (total + 255) / 256;
+            const int64_t cap = int64_t(device_sm_count()) * 8;
+            blocks = blocks < cap ? blocks : cap;
+            segment_epilogue_kernel<<<int(blocks), 256, 0, s>>>(acc, p.y_f32, p.M, p.N, p.w_scale,
+                                                                p.x_scale);
+            e = cudaGetLastError();
+        }
+    }
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {
+    return launch_products<1>(list, count, err, s);
+}
+
+// Activation rows are taken 8 at a time (4 or 2 when every product of the list
+// has fewer); each chunk re-reads the planes.
+cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {
+    int64_t maxM = 1;
+    for (int i = 0; i < count; ++i) maxM = list[i].M > maxM ? list[i].M : maxM;
+    if (maxM >= 8) return launch_products<8>(list, count, err, s);
+    if (maxM >= 4) return launch_products<4>(list, count, err, s);
+    return launch_products<2>(list, count, err, s);
+}
+
+}  // namespace trit

@@ -1,0 +1,111 @@
+// Internal declarations shared by the libtrit translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "trit.h"
+
+namespace trit {
+
+// ---- sizes -----------------------------------------------------------------
+
+constexpr int64_t kMaxK = (int64_t(1) << 24) - 1;     // 128*K < 2^31
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+__host__ __device__ inline int64_t beats_per_row(int64_t K) { return (K + 63) / 64; }
+
+// ---- device helpers ---------------------------------------------------------
+
+// d = c + sum_i a.s8[i] * b.u8[i]: signed activation bytes against unsigned
+// mask bytes (mask bytes hold 0 or 2^j, up to 128).
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// d = c + sum_i a.s8[i] * b.s8[i].
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Byte permute: result byte i is byte sel.nibble[i] of {b:a} (8 bytes); a
+// nibble with bit 3 set replicates the sign bit of the selected byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// 16-byte streaming load of read-once data: not kept in L1.
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// The fp32 dequantisation of one output, one rounding per step, never contracted.
+__device__ __forceinline__ float dequant(int32_t y, float w_scale, float x_scale) {
+    float f = __int2float_rn(y);
+    f = __fmul_rn(f, w_scale);
+    f = __fmul_rn(f, x_scale);
+    return __fdiv_rn(f, 127.0f);
+}
+
+// Permuted activation layout used by the select-accumulate kernels.  For each
+// 32-column half of a beat (h = 0: columns 0..31, h = 1: 32..63) word j (0..7)
+// holds the bytes of columns 8i + j, i = 0..3, so that the four bits j, 8+j,
+// 16+j, 24+j of a 32-bit plane word line up with its four bytes.  A beat takes
+// 16 words; the shared-memory copy pads each beat to kXBeatWords words so that
+// eight consecutive beats fall on distinct banks.
+constexpr int kXBeatWords = 20;
+
+// Transpose of one 32-column block: in[k] = natural words (bytes 4k..4k+3),
+// out[j] = bytes (j, 8+j, 16+j, 24+j).
+__device__ __forceinline__ void permute_block(const uint32_t in[8], uint32_t out[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int w = j >> 2;                  // word holding byte j within each 8-byte group
+        const uint32_t s = (uint32_t)(j & 3);  // byte within that word
+        // bytes: column j (word w), 8+j (word 2+w), 16+j (word 4+w), 24+j (word 6+w)
+        uint32_t lo = prmt(in[w], in[2 + w], s | ((s + 4) << 4));
+        uint32_t hi = prmt(in[4 + w], in[6 + w], s | ((s + 4) << 4));
+        out[j] = prmt(lo, hi, 0x5410);
+    }
+}
+
+// ---- launchers (host) ---------------------------------------------------------
+
+struct ProjDev {            // one product as a kernel sees it
+    const uint4 *planes;
+    const int8_t *x;
+    const float *x_scale;
+    int32_t *y_i32;
+    float *y_f32;
+    int64_t M, N;
+    int32_t K, B;
+    float w_scale;
+    int32_t pad_;
+};
+
+cudaError_t launch_pack(const int8_t *w, int64_t N, int64_t K, float w_scale, uint8_t *planes,
+                        float *scale_out, uint32_t *err, cudaStream_t s);
+cudaError_t launch_unpack(const uint8_t *planes, int64_t N, int64_t K, int8_t *w, uint32_t *err,
+                          cudaStream_t s);
+cudaError_t launch_verify(const uint8_t *planes, int64_t N, int64_t K, uint32_t *err,
+                          unsigned long long *first_bad, cudaStream_t s);
+cudaError_t launch_quant_many(const trit_act *list, int count, uint32_t *err, cudaStream_t s);
+
+// M = 1 products.
+cudaError_t launch_gemv_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
+// 2 <= M products, dp4a with beats reused across rows held in registers.
+cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace trit

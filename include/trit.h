@@ -1,0 +1,210 @@
+/*
+ * trit.h -- C ABI of libtrit: ternary select-accumulate matrix-vector and
+ * matrix-matrix products over .trit v1 bit planes, on NVIDIA GB300 (sm_103a).
+ *
+ * For an output row r the product is
+ *     y_r = sum_{c : W[r][c] = +1} x_c  -  sum_{c : W[r][c] = -1} x_c,
+ * with no multiplications ("Tritium: One Weight Format for Ternary Inference
+ * on Commodity CPUs and Multiplier-Free Hardware" -- Introduction, Eq. 3;
+ * "The .trit format, version 1" -- 1 Why bit planes).
+ *
+ * Layouts
+ *   planes   The .trit v1 ternary payload ("The .trit format, version 1" --
+ *            2.3): N rows x B = ceil(K/64) beats x 16 bytes, row-major.  Beat b
+ *            of row r is at byte (r*B + b)*16: bytes 0..8 a little-endian u64
+ *            `pos` (bit k set <=> W[r][64b+k] = +1), bytes 8..16 `neg`
+ *            (bit k set <=> W[r][64b+k] = -1).  Both bits set is illegal (P1);
+ *            padding bits past column K must be clear (P2).
+ *   x_i8     M activation rows of int8, row stride K_pad = 64*B bytes; only
+ *            columns < K are read (the library zero-fills the tail itself).
+ *   x_scale  M fp32 per-row scales, the absmax of each quantised row.
+ *   y_i32    M x N int32, row-major: the exact integer products.
+ *   y_f32    M x N fp32, row-major:
+ *            (((float)y_i32 * w_scale) * x_scale[m]) / 127, each step rounded
+ *            to nearest in fp32 ("Tritium ..." -- Why exactness, concretely:
+ *            scale by each factor in turn).
+ *
+ * Conventions for every entry point
+ *   - Data pointers are DEVICE pointers to caller-owned memory.  The library
+ *     keeps no pointer after the call returns and allocates no device memory.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *     call returns without synchronising; results are valid once the stream
+ *     has synchronised.
+ *   - Argument errors found on the host return a nonzero trit_status and
+ *     enqueue nothing.  A failed CUDA launch returns TRIT_E_CUDA
+ *     (trit_last_cuda_error() names it).
+ *   - Errors in the data are OR-ed by the kernels into *err_flag, a device
+ *     uint32 (TRIT_ERR_* bits).  Kernels only set bits: the caller zeroes the
+ *     flag before the call and reads it after the stream has synchronised.
+ *   - Supported sizes: 1 <= K < 2^24 (so |y| <= 128*K fits int32),
+ *     1 <= N, M <= 2^31 - 1.  No size is silently skipped; anything outside
+ *     returns TRIT_E_SHAPE.
+ *   - Alignment: planes and x_i8 16-byte aligned; fp32/int32 arrays 4-byte
+ *     aligned.
+ */
+#ifndef TRIT_H
+#define TRIT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define TRIT_API __declspec(dllexport)
+#else
+#define TRIT_API __attribute__((visibility("default")))
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no CUDA include. */
+typedef struct CUstream_st *trit_stream_t;
+
+typedef enum trit_status {
+    TRIT_OK = 0,
+    TRIT_E_ARG = 1,         /* NULL where a pointer is required, count <= 0, misalignment */
+    TRIT_E_SHAPE = 2,       /* a size outside the supported range */
+    TRIT_E_SCALE = 4,       /* w_scale not finite or <= 0 ("The .trit format, version 1" -- 2.2) */
+    TRIT_E_CUDA = 6,        /* a CUDA runtime call or launch failed */
+    TRIT_E_DEVICE = 7       /* the current device is not an sm_103 GPU */
+} trit_status;
+
+/* Bits of *err_flag. */
+#define TRIT_ERR_P1 1u            /* a beat with pos & neg != 0 (both bits set) */
+#define TRIT_ERR_P2 2u            /* a padding bit past column K is set (trit_verify only) */
+#define TRIT_ERR_NOT_TERNARY 4u   /* trit_pack saw a value outside {-1, 0, +1} */
+#define TRIT_ERR_NONFINITE 8u     /* trit_quant_act saw a NaN or infinity */
+#define TRIT_ERR_TIMEOUT 16u      /* a bounded wait inside a kernel gave up */
+
+/* Most list entries one launch of the *_many calls accepts; longer lists are
+ * split into consecutive launches on the same stream. */
+#define TRIT_MAX_LIST_PER_LAUNCH 256
+
+/* Human-readable name of a status code (static storage). */
+TRIT_API const char *trit_status_string(trit_status s);
+
+/* Text of the last CUDA error this thread saw inside the library, or "". */
+TRIT_API const char *trit_last_cuda_error(void);
+
+/* ABI version; bumped on any change of a signature or a layout. */
+TRIT_API int32_t trit_abi_version(void);
+
+/* Bytes of the ternary payload of an N x K matrix: N * ceil(K/64) * 16
+ * ("The .trit format, version 1" -- 2.3, byte_len).  Returns -1 if N or K is
+ * outside the supported range. */
+TRIT_API int64_t trit_payload_bytes(int64_t N, int64_t K);
+
+/*
+ * trit_pack -- int8 ternary weights to bit planes ("The .trit format,
+ * version 1" -- 2.3; "Tritium ..." -- The .trit v1 layout).
+ *   w          [N][K] int8, row-major, values in {-1, 0, +1}
+ *   w_scale    per-tensor dequantisation factor; must be finite and > 0
+ *   planes     out: N * ceil(K/64) * 16 bytes; padding bits are written clear
+ *   scale_out  out, may be NULL: receives w_scale (one fp32), the scale that
+ *              travels with the planes
+ *   err_flag   TRIT_ERR_NOT_TERNARY if any value is outside {-1, 0, +1}; such a
+ *              weight is stored as 0
+ */
+TRIT_API trit_status trit_pack(const int8_t *w, int64_t N, int64_t K, float w_scale,
+                               uint8_t *planes, float *scale_out, uint32_t *err_flag,
+                               trit_stream_t stream);
+
+/*
+ * trit_unpack -- bit planes back to int8 ternary weights [N][K] (inverse of
+ * trit_pack).  A both-bits-set position sets TRIT_ERR_P1 and is written as 0
+ * ("The .trit format, version 1" -- 2.3, P1: every consumer treats it as an
+ * error).
+ */
+TRIT_API trit_status trit_unpack(const uint8_t *planes, int64_t N, int64_t K, int8_t *w,
+                                 uint32_t *err_flag, trit_stream_t stream);
+
+/*
+ * trit_verify -- check P1 on every beat and P2 on every row's last beat
+ * ("The .trit format, version 1" -- 2.3 and 4, checks 17 and 18; "Tritium
+ * ..." -- Invariants).  P2 uses the 64-bit tail mask
+ *     tail = (K % 64 == 0) ? ~0 : (1 << (K % 64)) - 1.
+ *   err_flag   TRIT_ERR_P1 and/or TRIT_ERR_P2
+ *   first_bad  may be NULL; else the caller initialises it to UINT64_MAX and it
+ *              receives the smallest offending bit position
+ *              (r*B + b)*64 + k over both kinds -- row r, beat b, bit k.
+ */
+TRIT_API trit_status trit_verify(const uint8_t *planes, int64_t N, int64_t K,
+                                 uint32_t *err_flag, uint64_t *first_bad,
+                                 trit_stream_t stream);
+
+/*
+ * trit_quant_act -- per-token absmax int8 activation quantiser ("Tritium ..."
+ * -- Numerics; the pages give no formula, this is the reading used):
+ *   a = max_c |x[m][c]|;  inv = 127.0f / a (IEEE fp32 division);
+ *   q = clamp(round_half_even(x * inv), -127, 127);  x_scale[m] = a.
+ * a = 0 gives q = 0 and x_scale = 0.  When a < 2^-96 both x and a are first
+ * multiplied by 2^96 (exact) so that 127/a stays finite.  A row holding a NaN
+ * or an infinity sets TRIT_ERR_NONFINITE and is written as q = 0, x_scale = 0.
+ *   x        [M][K] fp32, row-major
+ *   x_i8     out: [M][K_pad], K_pad = 64*ceil(K/64); columns K..K_pad-1 = 0
+ *   x_scale  out: [M] fp32
+ */
+TRIT_API trit_status trit_quant_act(const float *x, int64_t M, int64_t K, int8_t *x_i8,
+                                    float *x_scale, uint32_t *err_flag, trit_stream_t stream);
+
+/*
+ * trit_gemm -- y = W x for M activation rows (layouts above).  Integer
+ * accumulation is exact (int32; every kernel gives identical bits, "Tritium
+ * ..." -- CPU kernels, Verification).  The kernel is chosen by M: one row per
+ * pass for M = 1, beats reused across up to 8 rows held in registers for small
+ * M, and tensor cores with planes expanded to +-1 in shared memory for large M.
+ *   w_scale   finite, > 0
+ *   y_i32, y_f32  outputs, either may be NULL (not both)
+ *   err_flag  TRIT_ERR_P1 if any beat has both bits set; the outputs of a row
+ *             holding such a beat are unspecified, all other rows are exact.
+ */
+TRIT_API trit_status trit_gemm(const uint8_t *planes, float w_scale, const int8_t *x_i8,
+                               const float *x_scale, int64_t M, int64_t N, int64_t K,
+                               int32_t *y_i32, float *y_f32, uint32_t *err_flag,
+                               trit_stream_t stream);
+
+/* trit_gemv -- trit_gemm with M = 1. */
+TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_t *x_i8,
+                               const float *x_scale, int64_t N, int64_t K, int32_t *y_i32,
+                               float *y_f32, uint32_t *err_flag, trit_stream_t stream);
+
+/* One product of a list: the arguments of trit_gemm, all device pointers. */
+typedef struct trit_proj {
+    const uint8_t *planes;
+    const int8_t *x_i8;
+    const float *x_scale;
+    int32_t *y_i32;      /* may be NULL */
+    float *y_f32;        /* may be NULL (not both) */
+    int64_t M, N, K;
+    float w_scale;
+    uint32_t reserved;   /* must be 0 */
+} trit_proj;
+
+/*
+ * trit_gemm_many -- a list of independent products (e.g. the 210 ternary
+ * projections of one decode token, "Tritium ..." -- Why it does not scale)
+ * computed by one persistent launch per kernel kind, so that the cost of a
+ * launch is paid once per list, not once per product.  `list` is a HOST array
+ * of `count` entries (read before the call returns); entries must not write
+ * overlapping outputs.  Results are those of calling trit_gemm on each entry.
+ */
+TRIT_API trit_status trit_gemm_many(const trit_proj *list, int32_t count, uint32_t *err_flag,
+                                    trit_stream_t stream);
+
+/* One quantisation of a list: the arguments of trit_quant_act. */
+typedef struct trit_act {
+    const float *x;
+    int8_t *x_i8;
+    float *x_scale;
+    int64_t M, K;
+} trit_act;
+
+/* trit_quant_act_many -- a host list of independent quantisations, one launch. */
+TRIT_API trit_status trit_quant_act_many(const trit_act *list, int32_t count,
+                                         uint32_t *err_flag, trit_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRIT_H */

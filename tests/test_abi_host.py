@@ -1,0 +1,96 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every entry point include/trit.h declares; the ctypes structs match
+the header's layout; argument errors are rejected before anything touches a
+device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "trit.h")
+
+
+@pytest.fixture(scope="module")
+def trit():
+    from bit_plane_select_gb300 import build
+    build.build()
+    import bit_plane_select_gb300 as t
+    return t
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"TRIT_API\s+[\w\s\*]+?\b(trit_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act", "trit_gemv",
+                     "trit_gemm", "trit_gemm_many", "trit_quant_act_many"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(trit):
+    lib = ctypes.CDLL(trit.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert trit.lib().trit_abi_version() == 1
+
+
+def test_struct_layouts(trit):
+    assert ctypes.sizeof(trit.TritProj) == 72
+    assert trit.TritProj.w_scale.offset == 64
+    assert ctypes.sizeof(trit.TritAct) == 40
+
+
+def test_payload_bytes(trit):
+    assert trit.payload_bytes(2560, 2560) == 1638400
+    assert trit.payload_bytes(2, 3) == 32
+    assert trit.payload_bytes(0, 3) == -1
+    assert trit.payload_bytes(1, 1 << 24) == -1
+
+
+def test_status_strings(trit):
+    L = trit.lib()
+    assert L.trit_status_string(0) == b"TRIT_OK"
+    assert L.trit_status_string(2).startswith(b"TRIT_E_SHAPE")
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="uses fake pointers; only run where no GPU can be reached")
+def test_argument_errors_are_rejected_on_the_host(trit):
+    """Every case here is invalid by construction, so the library must return
+    before any CUDA call; nothing is enqueued."""
+    L = trit.lib()
+    p = ctypes.c_void_p(0x10000)       # a 16-byte-aligned fake address, never dereferenced
+    odd = ctypes.c_void_p(0x10001)
+    null = ctypes.c_void_p(0)
+    s = null
+    # trit_pack(w, N, K, w_scale, planes, scale_out, err, stream)
+    assert L.trit_pack(null, 4, 64, 1.0, p, null, p, s) == 1
+    assert L.trit_pack(p, 4, 64, 1.0, odd, null, p, s) == 1
+    assert L.trit_pack(p, 0, 64, 1.0, p, null, p, s) == 2
+    assert L.trit_pack(p, 4, 1 << 24, 1.0, p, null, p, s) == 2
+    assert L.trit_pack(p, 4, 64, float("nan"), p, null, p, s) == 4
+    assert L.trit_pack(p, 4, 64, 0.0, p, null, p, s) == 4
+    assert L.trit_pack(p, 4, 64, -1.0, p, null, p, s) == 4
+    # trit_gemm(planes, w_scale, x, x_scale, M, N, K, y_i32, y_f32, err, stream)
+    assert L.trit_gemm(p, 1.0, p, p, 1, 8, 64, null, null, p, s) == 1
+    assert L.trit_gemm(p, 1.0, p, p, 0, 8, 64, p, p, p, s) == 2
+    assert L.trit_gemm(p, 1.0, p, p, 1, 8, 0, p, p, p, s) == 2
+    assert L.trit_gemm(p, float("inf"), p, p, 1, 8, 64, p, p, p, s) == 4
+    assert L.trit_gemm(p, 1.0, odd, p, 1, 8, 64, p, p, p, s) == 1
+    assert L.trit_gemm(p, 1.0, p, p, 1, 8, 64, p, p, null, s) == 1
+    assert L.trit_gemm_many(null, 1, p, s) == 1
+    lst = (trit.TritProj * 2)(trit.TritProj(p, p, p, p, p, 1, 8, 64, 1.0, 0),
+                              trit.TritProj(p, p, p, p, p, 1, 8, 64, 1.0, 7))
+    assert L.trit_gemm_many(ctypes.cast(lst, ctypes.c_void_p), 2, p, s) == 1   # reserved != 0
+    assert L.trit_gemm_many(ctypes.cast(lst, ctypes.c_void_p), 0, p, s) == 1
+    # trit_quant_act(x, M, K, x_i8, x_scale, err, stream)
+    assert L.trit_quant_act(p, 2, 0, p, p, p, s) == 2
+    assert L.trit_quant_act(p, 2, 10, odd, p, p, s) == 1
+    # trit_verify(planes, N, K, err, first_bad, stream)
+    assert L.trit_verify(p, 2, 10, null, null, s) == 1
+    assert L.trit_verify(p, 2, 10, p, ctypes.c_void_p(0x10004), s) == 1

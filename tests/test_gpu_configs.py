@@ -1,0 +1,207 @@
+"""Full-size parity on the five workloads, through the same calls the benchmark
+times (one quantise launch and one product launch over the whole list).
+
+Outputs the oracle can afford are compared one by one: every row for the
+single GEMV and the single layer, sampled rows (first, last and seeded random
+ones) for the 30-layer stack, the batch sweep and the prefill GEMMs.  Every
+output row is also covered at full size by an invariant that holds at any
+size: sum_r y[m, r] = sum_c x[m, c] * (sum_r W[r, c]), the column sums taken
+from the drawn int8 weights in numpy int64."""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+SAMPLE_ROWS = 12
+
+
+@pytest.fixture(scope="module")
+def t():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_plane_select_gb300 import build
+    build.build()
+    import bit_plane_select_gb300 as t
+    torch.cuda.set_device(0)
+    return t
+
+
+def host(x):
+    torch.cuda.synchronize()
+    return x.cpu().numpy()
+
+
+def assert_f32_close(got, ref, tol=1e-6):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30)
+    assert float(rel.max(initial=0.0)) <= tol
+
+
+def sample_rows(N, key):
+    rng = synth.rng_for(500, *key)
+    rows = {0, N - 1} | set(rng.integers(0, N, SAMPLE_ROWS - 2).tolist())
+    return np.array(sorted(rows), np.int64)
+
+
+def check_projection(orc, w, x_host, q_dev, s_dev, y_dev, f_dev, ws, K, rows=None, mrows=None):
+    """x_host fp32 [M, K]: the GPU's codes must equal the oracle's; then the
+    outputs of `rows` (all when None) for activation rows `mrows` (all when
+    None) are compared one by one, and the column-sum invariant over all rows."""
+    q_ref, s_ref, e_ref = orc.quant(x_host)
+    assert not e_ref.any()
+    q_gpu, s_gpu = host(q_dev), host(s_dev)
+    np.testing.assert_array_equal(q_gpu, q_ref)
+    np.testing.assert_array_equal(s_gpu, s_ref)
+    y, f = host(y_dev), host(f_dev)
+    if mrows is not None:
+        q_ref, s_ref, y, f = q_ref[mrows], s_ref[mrows], y[mrows], f[mrows]
+    sub = w if rows is None else w[rows]
+    ry, rf, rerr = orc.gemm(orc.pack(sub), ws, q_ref, s_ref, K)
+    assert not rerr.any()
+    ys = y if rows is None else y[:, rows]
+    fs = f if rows is None else f[:, rows]
+    np.testing.assert_array_equal(ys, ry)
+    assert_f32_close(fs, rf)
+    colsum = w.astype(np.int64).sum(axis=0)
+    np.testing.assert_array_equal(y.astype(np.int64).sum(axis=1),
+                                  q_ref[:, :K].astype(np.int64) @ colsum)
+
+
+def test_config0_single_gemv(t, orc):
+    w, x = synth.config0()
+    ws = float(synth.w_scale(w))
+    planes, err = t.trit_pack(torch.from_numpy(w).cuda(), ws)
+    q, s, err = t.trit_quant_act(torch.from_numpy(x).cuda(), err_flag=err)
+    y, f, err = t.trit_gemv(planes, ws, q, s, 2560, err_flag=err)
+    assert int(host(err)[0]) == 0
+    check_projection(orc, w, x, q, s, y[None, :], f[None, :], ws, 2560)
+
+
+def build_stack(t, layers, seed, M, p0_per_layer=True, items=None):
+    from bit_plane_select_gb300.stack import TernaryStack
+    st = TernaryStack("cuda")
+    ws_list = []
+    items = list(items if items is not None else synth.stack_items(layers))
+    for layer, idx, name, N, K in items:
+        w = synth.stack_weights(seed, layer, idx) if p0_per_layer else \
+            synth.projection_weights(seed, layer, idx)
+        ws = float(synth.w_scale(w))
+        ws_list.append(ws)
+        st.add(torch.from_numpy(w), ws, M=M, name=f"L{layer}.{name}")
+    st.finalize()
+    for i, (layer, idx, name, N, K) in enumerate(items):
+        st.x[i].copy_(torch.from_numpy(synth.projection_acts(seed, layer, idx, M)))
+    return st, items, ws_list
+
+
+def test_config1_one_layer(t, orc):
+    st, items, wss = build_stack(t, 1, 1, 1, p0_per_layer=False)
+    st.step()
+    assert int(host(st.err)[0]) == 0
+    for i, (layer, idx, name, N, K) in enumerate(items):
+        w = synth.projection_weights(1, layer, idx)
+        x = synth.projection_acts(1, layer, idx, 1)
+        check_projection(orc, w, x, st.q[i], st.s[i], st.y[i], st.f[i], wss[i], K)
+
+
+def test_config2_stack_sampled(t, orc):
+    st, items, wss = build_stack(t, synth.LAYERS, 2, 1)
+    for _ in range(2):     # the benchmark's warm-up and timed steps repeat the same calls
+        st.step()
+    assert int(host(st.err)[0]) == 0
+    assert st.plane_bytes == 521011200
+    for i, (layer, idx, name, N, K) in enumerate(items):
+        w = synth.stack_weights(2, layer, idx)
+        x = synth.projection_acts(2, layer, idx, 1)
+        check_projection(orc, w, x, st.q[i], st.s[i], st.y[i], st.f[i], wss[i], K,
+                         rows=sample_rows(N, (2, layer, idx)))
+
+
+def test_config3_batch_sweep_and_corruption(t, orc):
+    Mmax = max(synth.BATCH_SWEEP)
+    st, items, wss = build_stack(t, synth.LAYERS, 3, Mmax)
+    st.quantize()
+    for M in synth.BATCH_SWEEP:
+        plist = t.ProjList([(st.planes[i], wss[i], st.q[i][:M], st.s[i][:M], items[i][4],
+                             st.y[i][:M], st.f[i][:M]) for i in range(len(items))])
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t.trit_gemm_many(plist, err)
+        assert int(host(err)[0]) == 0, M
+        mrows = np.arange(M)
+        for i in range(0, len(items), 1 if M in (1, 64) else 13):
+            layer, idx, name, N, K = items[i]
+            w = synth.stack_weights(3, layer, idx)
+            x = synth.projection_acts(3, layer, idx, Mmax)
+            check_projection(orc, w, x, st.q[i], st.s[i], st.y[i][:M], st.f[i][:M], wss[i], K,
+                             rows=sample_rows(N, (3, layer, idx, M)), mrows=mrows)
+
+    # 0.1% of the beats of every projection get both bits set at one position
+    corrupted_rows = {}
+    for i, (layer, idx, name, N, K) in enumerate(items):
+        B = (K + 63) // 64
+        beats, bits = synth.corrupt_positions(3, layer, idx, N * B)
+        flat = st.planes[i].view(-1, 16)
+        bi = torch.from_numpy(beats).cuda()
+        byte = torch.from_numpy(bits // 8).cuda()
+        val = torch.from_numpy((1 << (bits % 8)).astype(np.uint8)).cuda()
+        flat[bi, byte] |= val
+        flat[bi, byte + 8] |= val
+        corrupted_rows[i] = (beats // B, beats, bits)
+    for M in (1, 4):
+        plist = t.ProjList([(st.planes[i], wss[i], st.q[i][:M], st.s[i][:M], items[i][4],
+                             st.y[i][:M], st.f[i][:M]) for i in range(len(items))])
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t.trit_gemm_many(plist, err)
+        assert int(host(err)[0]) == t.ERR_P1
+        for i in range(0, len(items), 29):
+            layer, idx, name, N, K = items[i]
+            rows_bad = corrupted_rows[i][0]
+            rows = np.unique(np.concatenate([rows_bad[:4], sample_rows(N, (4, layer, idx))]))
+            payload = host(st.planes[i][torch.from_numpy(rows).cuda()])
+            q_ref, s_ref, _ = orc.quant(synth.projection_acts(3, layer, idx, Mmax))
+            ry, rf, rerr = orc.gemm(payload, wss[i], q_ref[:M], s_ref[:M], K)
+            bad = np.isin(rows, rows_bad)
+            np.testing.assert_array_equal(rerr != 0, bad)   # the oracle rejects exactly those rows
+            y = host(st.y[i][:M])[:, rows]
+            np.testing.assert_array_equal(y[:, ~bad], ry[:, ~bad])
+
+
+def test_config4_prefill_sampled(t, orc):
+    layers = synth.LAYERS
+    items = list(synth.prefill_items(layers))
+    planes, wss = [], []
+    for layer, idx, name, N, K in items:
+        w = synth.projection_weights(4, layer, idx)
+        ws = float(synth.w_scale(w))
+        p, _ = t.trit_pack(torch.from_numpy(w).cuda(), ws)
+        planes.append(p)
+        wss.append(ws)
+    for M in synth.PREFILL_M:
+        xs_host, entries = {}, []
+        for i, (layer, idx, name, N, K) in enumerate(items):
+            x = synth.projection_acts(4, layer, idx, M)
+            q, s, _ = t.trit_quant_act(torch.from_numpy(x).cuda())
+            y = torch.empty((M, N), dtype=torch.int32, device="cuda")
+            f = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            entries.append((planes[i], wss[i], q, s, K, y, f))
+            if i % 7 == 0 or i == len(items) - 1:
+                xs_host[i] = x
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        t.trit_gemm_many(t.ProjList(entries), err)
+        assert int(host(err)[0]) == 0
+        rng = synth.rng_for(501, M)
+        for i, (layer, idx, name, N, K) in enumerate(items):
+            if i % 7 and i != len(items) - 1:
+                continue
+            w = synth.projection_weights(4, layer, idx)
+            rows = sample_rows(N, (5, layer, idx, M))
+            mrows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, 10)]))
+            _, _, q, s, _, y, f = entries[i]
+            check_projection(orc, w, xs_host[i], q, s, y, f, wss[i], K, rows=rows, mrows=mrows)
+        del entries
+        torch.cuda.empty_cache()
