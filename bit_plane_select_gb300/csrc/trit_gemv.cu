@@ -7,13 +7,16 @@
 // over beats of 64 columns (pos, neg = two 64-bit masks).  Any beat with
 // pos & neg != 0 sets TRIT_ERR_P1.
 //
-// Work split.  A warp handles 4 rows x 8 beats per step: lane = 8*rs + bs
-// reads beat (8t + bs) of row (4g + rs) with one 16-byte load, so one warp
-// load covers 4 x 128 contiguous bytes.  A "group" is 4 rows; it takes
-// ceil(B/8) steps.  The launch is persistent: every CTA gets an equal share of
-// the total steps of the list (groups never split), and each warp a contiguous
-// run of the CTA's groups.  The CTA keeps the activation row(s) of the
-// current product in shared memory in the permuted layout of trit_internal.cuh.
+// Work split.  A warp handles 8 rows x 4 beats per step: lane = 4*rs + bs reads
+// beat (4t + bs) of row (8g + rs) with one 16-byte load, so one warp load covers
+// 8 x 64 contiguous bytes (whole 32-byte sectors).  A "group" is 8 rows; it
+// takes ceil(B/4) steps.  The launch is persistent: every CTA gets an equal
+// share of the total steps of the list (groups never split) and each warp a
+// contiguous run of the CTA's groups.  The CTA keeps the activation row(s) of
+// the current product in shared memory in the permuted layout of
+// trit_internal.cuh.  Loads past the end of a warp's rows or of a row's beats
+// are clamped to the last valid address (their data meets zero activations or
+// an unwritten row), so the hot loop carries no predicates.
 //
 // M = 1 (2^j-weighted masks).  For plane word P (32 columns) and j = 0..7,
 // P & (0x01010101 << j) has byte i equal to 2^j exactly when column 8i+j is
@@ -23,16 +26,16 @@
 // Cost per beat: 32 AND + 32 dp4a -- no shifts, no byte-mask expansion.
 //
 // Long rows.  The staged activations must fit in shared memory, so a product
-// whose rows exceed kSegBeats(MT) beats is split into column segments.  Each
-// segment adds its exact int32 partial into the output with an integer
-// atomic (exact and order-independent, so the result is bit-identical to a
-// single pass); the caller's int32 output, or else the fp32 output buffer
-// reinterpreted as int32, is zeroed first and a final pass applies the fp32
-// dequantisation.  No scratch memory is used.
+// whose rows exceed seg_beats(MT) beats is split into column segments.  Each
+// segment adds its exact int32 partial into the output with an integer atomic
+// (exact and order-independent, so the result is bit-identical to a single
+// pass); the caller's int32 output, or else the fp32 output buffer read as
+// int32, is zeroed first and a final pass applies the fp32 dequantisation.
+// No scratch memory is used.
 //
-// M > 1 (+-1 bytes).  Each beat is expanded once into sixteen words of bytes
-// in {+1, 0, -1} (shift + sign-replicating byte permute + one LOP3 per word)
-// and reused for every activation row held by the CTA: 16 dp4a per row.
+// M > 1 (+-1 bytes).  Each beat is expanded once into sixteen words of bytes in
+// {+1, 0, -1} (shift + sign-replicating byte permute + one LOP3 per word) and
+// reused for every activation row held by the CTA: 16 dp4a per row.
 #include "trit_internal.cuh"
 
 namespace trit {
@@ -40,14 +43,15 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kLanesPerRow = 8;
+constexpr int kLanesPerRow = 4;
 constexpr int kRowsPerGroup = 32 / kLanesPerRow;
 constexpr int kDepth = 4;                   // 16-byte loads in flight per lane
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
+constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 
-// Beats per column segment for MT staged rows: MT * kSegBeats * 80 bytes of
-// shared memory stay under 92 KB.  A segment takes at most 144 steps per row,
-// so the 2^j-weighted accumulators (at most 2^17 per step) stay below 2^25.
+// Beats per column segment for MT staged rows: MT * seg_beats * 80 bytes of
+// shared memory stay at 90 KB.  A segment takes at most 288 steps per row, so
+// the 2^j-weighted accumulators (at most 2^17 per step) stay below 2^26.
 __host__ __device__ constexpr int seg_beats(int mt) { return 1152 / mt; }
 
 struct Entry {
@@ -56,15 +60,15 @@ struct Entry {
     const float *x_scale;   // first scale of this entry
     int32_t *y_i32;         // first output row of this entry, stride N
     float *y_f32;
+    int32_t *acc;           // non-NULL: atomically add the int32 partial here (stride N)
     int64_t N;
-    int64_t groups;         // ceil(N / 4)
+    int64_t groups;         // ceil(N / 8)
     int64_t cost_begin;     // prefix sum of groups * iters over the list
     int64_t xld;            // activation row stride (K_pad)
-    int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / 8)
+    int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / 4)
     int32_t bstride;        // beats per full row of the planes
     int32_t mrows;          // activation rows of this entry (<= MT)
     float w_scale;
-    int32_t *acc;           // non-NULL: atomically add the int32 partial here (stride N)
 };
 
 struct List {
@@ -75,11 +79,11 @@ struct List {
     Entry e[kMaxList];
 };
 
-// Stage activation rows 0..mrows-1 of entry E into shared memory, permuted,
-// zero past column K, covering iters*8 beats.
+// Stage activation rows 0..MT-1 of entry E into shared memory, permuted, zero
+// past column K and for rows >= mrows, covering iters*4 beats.
 template <int MT>
 __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_words) {
-    const int halves = E.iters * 8 * 2;
+    const int halves = E.iters * kLanesPerRow * 2;
     for (int idx = threadIdx.x; idx < halves * MT; idx += kThreads) {
         const int m = idx / halves;
         const int hb = idx - m * halves;
@@ -117,10 +121,9 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
     }
 }
 
-__device__ __forceinline__ int32_t row_sum8(int32_t v) {
+__device__ __forceinline__ int32_t row_sum4(int32_t v) {
     v += __shfl_xor_sync(~0u, v, 1);
     v += __shfl_xor_sync(~0u, v, 2);
-    v += __shfl_xor_sync(~0u, v, 4);
     return v;
 }
 
@@ -129,24 +132,26 @@ template <int MT>
 __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *xs, int xs_words,
                                                int64_t gb, int64_t ge, int rs, int bs) {
     const int it = E.iters;
-    const int ngroups = int(ge - gb);
-    const int steps = ngroups * it;
+    const int steps = int(ge - gb) * it;
+    const int64_t N = E.N;
     uint32_t viol = 0;
 
-    // load cursor: group lg (relative to gb), step lt; lrow points at beat bs of
-    // this lane's row of group lg
-    int lg = 0, lt = 0;
+    // ---- load cursor: beat loff of the (clamped) row at lrow; loff runs
+    // bs, bs+4, ... and is clamped to the row's last beat, rows past the warp's
+    // last valid row read that row -- every load stays inside the planes
+    const int last_beat = E.B - 1;
+    const int64_t last_row = (ge * kRowsPerGroup < N ? ge * kRowsPerGroup : N) - 1;
     int64_t lrow_idx = gb * kRowsPerGroup + rs;
-    const uint4 *lrow = E.planes + lrow_idx * E.bstride + bs;
+    const uint4 *lrow = E.planes + (lrow_idx < last_row ? lrow_idx : last_row) * E.bstride;
+    int lt = 0, loff = bs;
     auto next_load = [&]() -> uint4 {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (lg < ngroups && lrow_idx < E.N && lt * kLanesPerRow + bs < E.B)
-            v = ldg_stream(lrow + lt * kLanesPerRow);
+        const uint4 v = ldg_stream(lrow + (loff < last_beat ? loff : last_beat));
+        loff += kLanesPerRow;
         if (++lt == it) {
             lt = 0;
-            ++lg;
+            loff = bs;
             lrow_idx += kRowsPerGroup;
-            lrow += int64_t(kRowsPerGroup) * E.bstride;
+            lrow = E.planes + (lrow_idx < last_row ? lrow_idx : last_row) * E.bstride;
         }
         return v;
     };
@@ -155,100 +160,106 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
 #pragma unroll
     for (int d = 0; d < kDepth; ++d) ring[d] = next_load();
 
+    // ---- compute cursor
     int acc[MT == 1 ? 16 : MT];
 #pragma unroll
     for (int i = 0; i < (MT == 1 ? 16 : MT); ++i) acc[i] = 0;
-    int64_t row = gb * kRowsPerGroup + rs;   // compute cursor: this lane's row
+    int64_t row = gb * kRowsPerGroup + rs;
     int ct = 0;
+    const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
+    const int xbase = bs * kXBeatVec;
+    int xoff = xbase;
 
-    for (int s = 0; s < steps; s += kDepth) {
+    auto body = [&](uint4 &slot) {
+        const uint4 v = slot;
+        slot = next_load();
+        viol |= (v.x & v.z) | (v.y & v.w);
+        if constexpr (MT == 1) {
+            const uint4 a0 = xs4[xoff], a1 = xs4[xoff + 1], a2 = xs4[xoff + 2], a3 = xs4[xoff + 3];
+            const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
 #pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
-            if (s + d < steps) {
-                const uint4 v = ring[d];
-                ring[d] = next_load();
-                viol |= (v.x & v.z) | (v.y & v.w);
-                const int beat = ct * kLanesPerRow + bs;
-
-                if constexpr (MT == 1) {
-                    const uint4 *X = reinterpret_cast<const uint4 *>(xs + beat * kXBeatWords);
-                    const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
-                    const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                    const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t msk = 0x01010101u << j;
+                acc[j] = dp4a_su(xl[j], v.x & msk, acc[j]);
+                acc[j] = dp4a_su(xh[j], v.y & msk, acc[j]);
+                acc[8 + j] = dp4a_su(xl[j], v.z & msk, acc[8 + j]);
+                acc[8 + j] = dp4a_su(xh[j], v.w & msk, acc[8 + j]);
+            }
+        } else {
+            // bytes of w: +1 where pos, -1 (0xFF) where neg, 0 elsewhere
+            uint32_t wl[8], wh[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t msk = 0x01010101u << j;
-                        acc[j] = dp4a_su(xl[j], v.x & msk, acc[j]);
-                        acc[j] = dp4a_su(xh[j], v.y & msk, acc[j]);
-                        acc[8 + j] = dp4a_su(xl[j], v.z & msk, acc[8 + j]);
-                        acc[8 + j] = dp4a_su(xh[j], v.w & msk, acc[8 + j]);
-                    }
-                } else {
-                    // bytes of w: +1 where pos, -1 (0xFF) where neg, 0 elsewhere
-                    uint32_t wl[8], wh[8];
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t nl = prmt(v.z << (7 - j), 0u, 0xBA98u);
+                const uint32_t nh = prmt(v.w << (7 - j), 0u, 0xBA98u);
+                wl[j] = ((v.x >> j) & 0x01010101u) | nl;
+                wh[j] = ((v.y >> j) & 0x01010101u) | nh;
+            }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t nl = prmt(v.z << (7 - j), 0u, 0xBA98u);
-                        const uint32_t nh = prmt(v.w << (7 - j), 0u, 0xBA98u);
-                        wl[j] = ((v.x >> j) & 0x01010101u) | nl;
-                        wh[j] = ((v.y >> j) & 0x01010101u) | nh;
-                    }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        const uint4 *X =
-                            reinterpret_cast<const uint4 *>(xs + m * xs_words + beat * kXBeatWords);
-                        const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
-                        int a = acc[m];
-                        a = dp4a_ss(a0.x, wl[0], a); a = dp4a_ss(a0.y, wl[1], a);
-                        a = dp4a_ss(a0.z, wl[2], a); a = dp4a_ss(a0.w, wl[3], a);
-                        a = dp4a_ss(a1.x, wl[4], a); a = dp4a_ss(a1.y, wl[5], a);
-                        a = dp4a_ss(a1.z, wl[6], a); a = dp4a_ss(a1.w, wl[7], a);
-                        a = dp4a_ss(a2.x, wh[0], a); a = dp4a_ss(a2.y, wh[1], a);
-                        a = dp4a_ss(a2.z, wh[2], a); a = dp4a_ss(a2.w, wh[3], a);
-                        a = dp4a_ss(a3.x, wh[4], a); a = dp4a_ss(a3.y, wh[5], a);
-                        a = dp4a_ss(a3.z, wh[6], a); a = dp4a_ss(a3.w, wh[7], a);
-                        acc[m] = a;
-                    }
-                }
-
-                if (++ct == it) {
-                    if constexpr (MT == 1) {
-                        int32_t y = 0;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) y += (acc[j] - acc[8 + j]) >> j;
-                        y = row_sum8(y);
-                        if (bs == 0 && row < E.N) {
-                            if (E.acc) {
-                                atomicAdd(E.acc + row, y);
-                            } else {
-                                if (E.y_i32) E.y_i32[row] = y;
-                                if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, E.x_scale[0]);
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = 0;
-                    } else {
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            const int32_t y = row_sum8(acc[m]);
-                            acc[m] = 0;
-                            if (bs == 0 && row < E.N && m < E.mrows) {
-                                const int64_t o = int64_t(m) * E.N + row;
-                                if (E.acc) {
-                                    atomicAdd(E.acc + o, y);
-                                } else {
-                                    if (E.y_i32) E.y_i32[o] = y;
-                                    if (E.y_f32) E.y_f32[o] = dequant(y, E.w_scale, E.x_scale[m]);
-                                }
-                            }
-                        }
-                    }
-                    ct = 0;
-                    row += kRowsPerGroup;
-                }
+            for (int m = 0; m < MT; ++m) {
+                const uint4 *X = xs4 + m * (xs_words / 4) + xoff;
+                const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
+                int a = acc[m];
+                a = dp4a_ss(a0.x, wl[0], a); a = dp4a_ss(a0.y, wl[1], a);
+                a = dp4a_ss(a0.z, wl[2], a); a = dp4a_ss(a0.w, wl[3], a);
+                a = dp4a_ss(a1.x, wl[4], a); a = dp4a_ss(a1.y, wl[5], a);
+                a = dp4a_ss(a1.z, wl[6], a); a = dp4a_ss(a1.w, wl[7], a);
+                a = dp4a_ss(a2.x, wh[0], a); a = dp4a_ss(a2.y, wh[1], a);
+                a = dp4a_ss(a2.z, wh[2], a); a = dp4a_ss(a2.w, wh[3], a);
+                a = dp4a_ss(a3.x, wh[4], a); a = dp4a_ss(a3.y, wh[5], a);
+                a = dp4a_ss(a3.z, wh[6], a); a = dp4a_ss(a3.w, wh[7], a);
+                acc[m] = a;
             }
         }
+        xoff += kLanesPerRow * kXBeatVec;
+        if (++ct == it) {
+            if constexpr (MT == 1) {
+                const int32_t y = row_sum4(
+                    (acc[0] - acc[8]) + ((acc[1] - acc[9]) >> 1) + ((acc[2] - acc[10]) >> 2) +
+                    ((acc[3] - acc[11]) >> 3) + ((acc[4] - acc[12]) >> 4) +
+                    ((acc[5] - acc[13]) >> 5) + ((acc[6] - acc[14]) >> 6) +
+                    ((acc[7] - acc[15]) >> 7));
+                if (bs == 0 && row < N) {
+                    if (E.acc) {
+                        atomicAdd(E.acc + row, y);
+                    } else {
+                        if (E.y_i32) E.y_i32[row] = y;
+                        if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, E.x_scale[0]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = 0;
+            } else {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const int32_t y = row_sum4(acc[m]);
+                    acc[m] = 0;
+                    if (bs == 0 && row < N && m < E.mrows) {
+                        const int64_t o = int64_t(m) * N + row;
+                        if (E.acc) {
+                            atomicAdd(E.acc + o, y);
+                        } else {
+                            if (E.y_i32) E.y_i32[o] = y;
+                            if (E.y_f32) E.y_f32[o] = dequant(y, E.w_scale, E.x_scale[m]);
+                        }
+                    }
+                }
+            }
+            ct = 0;
+            xoff = xbase;
+            row += kRowsPerGroup;
+        }
+    };
+
+    int s = 0;
+    for (; s + kDepth <= steps; s += kDepth) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) body(ring[d]);
     }
+#pragma unroll
+    for (int d = 0; d < kDepth - 1; ++d)
+        if (s + d < steps) body(ring[d]);
     return viol;
 }
 
@@ -262,8 +273,16 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
     const int64_t hi = (int64_t(blockIdx.x) + 1) * L.total_cost / gridDim.x;
     uint32_t viol = 0;
 
-    int e = 0;
-    while (e + 1 < L.count && L.e[e + 1].cost_begin <= lo) ++e;
+    int e = 0;   // last entry whose cost range starts at or before lo
+    {
+        int a = 0, b = L.count - 1;
+        while (a < b) {
+            const int mid = (a + b + 1) >> 1;
+            if (L.e[mid].cost_begin <= lo) a = mid;
+            else b = mid - 1;
+        }
+        e = a;
+    }
     for (; e < L.count && L.e[e].cost_begin < hi; ++e) {
         const Entry &E = L.e[e];
         const int64_t it = E.iters;
@@ -285,11 +304,20 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
 
 template <int MT>
 int occupancy(size_t smem) {
-    int dev = 0, occ = 0;
+    // cached per (shared-memory size, device); sizes repeat from call to call
+    static thread_local size_t last_smem = ~size_t(0);
+    static thread_local int last_dev = -1, last_occ = 1;
+    int dev = 0;
     cudaGetDevice(&dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_accumulate_kernel<MT>, kThreads,
-                                                  smem);
-    return occ < 1 ? 1 : occ;
+    if (smem != last_smem || dev != last_dev) {
+        int occ = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_accumulate_kernel<MT>, kThreads,
+                                                      smem);
+        last_occ = occ < 1 ? 1 : occ;
+        last_smem = smem;
+        last_dev = dev;
+    }
+    return last_occ;
 }
 
 template <int MT>
@@ -315,8 +343,7 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
                                              int(smem));
         if (e != cudaSuccess) return e;
     }
-    const int64_t per_sm = occupancy<MT>(smem);
-    const int64_t cap = per_sm * device_sm_count();
+    const int64_t cap = int64_t(occupancy<MT>(smem)) * device_sm_count();
     const int64_t want = (groups + kWarps - 1) / kWarps;
     const int grid = int(want < cap ? (want < 1 ? 1 : want) : cap);
     select_accumulate_kernel<MT><<<grid, kThreads, smem, s>>>(L);
