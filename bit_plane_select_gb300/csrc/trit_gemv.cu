@@ -263,6 +263,79 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
     return viol;
 }
 
+// M = 1 with rows of exactly 4*IT beats: the group loop is unrolled step by
+// step, so every load, shared-memory read and accumulator index is static.
+// The ring depth D divides IT, so step t of every group uses ring slot t % D;
+// the last D loads of a group already fetch the next group's first beats.
+template <int IT, int D>
+__device__ __forceinline__ uint32_t run_fixed(const Entry &E, const uint32_t *xs, int64_t gb,
+                                              int64_t ge, int rs, int bs) {
+    static_assert(IT % D == 0, "ring depth must divide the steps of a row");
+    const uint4 *const planes = E.planes;
+    const int64_t bstride = E.bstride;
+    const int64_t N = E.N;
+    int32_t *const y_i32 = E.y_i32;
+    float *const y_f32 = E.y_f32;
+    int32_t *const acc_out = E.acc;
+    const float w_scale = E.w_scale;
+    const float x_scale = E.x_scale[0];
+    const int64_t last_row = (ge * kRowsPerGroup < N ? ge * kRowsPerGroup : N) - 1;
+    auto row_ptr = [&](int64_t g) -> const uint4 * {
+        const int64_t r = g * kRowsPerGroup + rs;
+        return planes + (r < last_row ? r : last_row) * bstride + bs;
+    };
+    const uint4 *xb = reinterpret_cast<const uint4 *>(xs) + bs * kXBeatVec;
+
+    uint32_t viol = 0;
+    const uint4 *rp = row_ptr(gb);
+    const uint4 *rpn = row_ptr(gb + 1);
+    uint4 ring[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) ring[d] = ldg_stream(rp + d * kLanesPerRow);
+
+    int64_t row = gb * kRowsPerGroup + rs;
+    for (int64_t g = gb; g < ge; ++g) {
+        int acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0;
+#pragma unroll
+        for (int t = 0; t < IT; ++t) {
+            const uint4 v = ring[t % D];
+            ring[t % D] = (t + D < IT) ? ldg_stream(rp + (t + D) * kLanesPerRow)
+                                       : ldg_stream(rpn + (t + D - IT) * kLanesPerRow);
+            viol |= (v.x & v.z) | (v.y & v.w);
+            const uint4 *X = xb + t * (kLanesPerRow * kXBeatVec);
+            const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
+            const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t msk = 0x01010101u << j;
+                acc[j] = dp4a_su(xl[j], v.x & msk, acc[j]);
+                acc[j] = dp4a_su(xh[j], v.y & msk, acc[j]);
+                acc[8 + j] = dp4a_su(xl[j], v.z & msk, acc[8 + j]);
+                acc[8 + j] = dp4a_su(xh[j], v.w & msk, acc[8 + j]);
+            }
+        }
+        const int32_t y = row_sum4(
+            (acc[0] - acc[8]) + ((acc[1] - acc[9]) >> 1) + ((acc[2] - acc[10]) >> 2) +
+            ((acc[3] - acc[11]) >> 3) + ((acc[4] - acc[12]) >> 4) + ((acc[5] - acc[13]) >> 5) +
+            ((acc[6] - acc[14]) >> 6) + ((acc[7] - acc[15]) >> 7));
+        if (bs == 0 && row < N) {
+            if (acc_out) {
+                atomicAdd(acc_out + row, y);
+            } else {
+                if (y_i32) y_i32[row] = y;
+                if (y_f32) y_f32[row] = dequant(y, w_scale, x_scale);
+            }
+        }
+        row += kRowsPerGroup;
+        rp = rpn;
+        rpn = row_ptr(g + 2);
+    }
+    return viol;
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
     select_accumulate_kernel(const __grid_constant__ List L) {
@@ -297,7 +370,19 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
         __syncthreads();
         const int64_t n = g1 - g0;
         const int64_t wb = g0 + n * warp / kWarps, we = g0 + n * (warp + 1) / kWarps;
-        if (wb < we) viol |= run_groups<MT>(E, xs, L.xs_words, wb, we, rs, bs);
+        if (wb < we) {
+            if constexpr (MT == 1) {
+                if (E.B == 40 && E.iters == 10) {
+                    viol |= run_fixed<10, 5>(E, xs, wb, we, rs, bs);
+                    continue;
+                }
+                if (E.B == 108 && E.iters == 27) {
+                    viol |= run_fixed<27, 3>(E, xs, wb, we, rs, bs);
+                    continue;
+                }
+            }
+            viol |= run_groups<MT>(E, xs, L.xs_words, wb, we, rs, bs);
+        }
     }
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
 }
