@@ -9,7 +9,7 @@ built, or the device is not an sm_103 GPU, the calls raise.
 
 Functions carry the C names:
   trit_pack, trit_unpack, trit_verify, trit_quant_act, trit_quant_act_many,
-  trit_gemv, trit_gemm, trit_gemm_many
+  trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many
 """
 from __future__ import annotations
 
@@ -24,7 +24,8 @@ __all__ = [
     "TritError", "ERR_P1", "ERR_P2", "ERR_NOT_TERNARY", "ERR_NONFINITE", "ERR_TIMEOUT",
     "library_path", "lib", "payload_bytes", "k_pad", "trit_pack", "trit_unpack", "trit_verify",
     "trit_quant_act", "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
-    "ProjList", "ActList", "TritProj", "TritAct",
+    "trit_quant_gemv_many", "ProjList", "ActList", "QProjList", "TritProj", "TritAct",
+    "TritQProj", "MAX_FUSED_K",
 ]
 
 ERR_P1 = 1
@@ -32,6 +33,7 @@ ERR_P2 = 2
 ERR_NOT_TERNARY = 4
 ERR_NONFINITE = 8
 ERR_TIMEOUT = 16
+MAX_FUSED_K = 73728
 
 _STATUS = {0: "TRIT_OK", 1: "TRIT_E_ARG", 2: "TRIT_E_SHAPE", 4: "TRIT_E_SCALE",
            6: "TRIT_E_CUDA", 7: "TRIT_E_DEVICE"}
@@ -48,6 +50,13 @@ class TritProj(ctypes.Structure):
                 ("x_scale", ctypes.c_void_p), ("y_i32", ctypes.c_void_p),
                 ("y_f32", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+
+
+class TritQProj(ctypes.Structure):
+    _fields_ = [("planes", ctypes.c_void_p), ("x", ctypes.c_void_p), ("x_i8", ctypes.c_void_p),
+                ("x_scale", ctypes.c_void_p), ("y_i32", ctypes.c_void_p),
+                ("y_f32", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
 
 
 class TritAct(ctypes.Structure):
@@ -88,8 +97,10 @@ def lib():
         L.trit_gemv.argtypes = [p, f32, p, p, i64, i64, p, p, p, p]
         L.trit_gemm.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         L.trit_gemm_many.argtypes = [p, i32, p, p]
+        L.trit_quant_gemv_many.argtypes = [p, i32, p, p]
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
-                     "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many"):
+                     "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
+                     "trit_quant_gemv_many"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -247,6 +258,26 @@ class ProjList:
         self.array = (TritProj * self.count)(*items)
 
 
+class QProjList:
+    """A prepared host array of trit_qproj entries (fused quantise-and-multiply,
+    M = 1): (planes, w_scale, x fp32 [K] or [1, K], x_i8 out or None,
+    x_scale out or None, y_i32, y_f32)."""
+
+    def __init__(self, entries):
+        self._keep = []
+        items = []
+        for planes, w_scale, x, x_i8, x_scale, y_i32, y_f32 in entries:
+            K = x.shape[-1]
+            items.append(TritQProj(
+                _dev(planes, torch.uint8, "planes"), _dev(x, torch.float32, "x"),
+                _dev(x_i8, torch.int8, "x_i8", True), _dev(x_scale, torch.float32, "x_scale", True),
+                _dev(y_i32, torch.int32, "y_i32", True), _dev(y_f32, torch.float32, "y_f32", True),
+                planes.shape[0], K, float(w_scale), 0))
+            self._keep.append((planes, x, x_i8, x_scale, y_i32, y_f32))
+        self.count = len(items)
+        self.array = (TritQProj * self.count)(*items)
+
+
 class ActList:
     """A prepared host array of trit_act entries: (x fp32 [M, K], x_i8, x_scale)."""
 
@@ -266,6 +297,12 @@ def trit_gemm_many(plist: ProjList, err_flag: torch.Tensor, stream=None):
     _check(lib().trit_gemm_many(ctypes.cast(plist.array, ctypes.c_void_p), plist.count,
                                 _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
            "trit_gemm_many")
+
+
+def trit_quant_gemv_many(qlist: QProjList, err_flag: torch.Tensor, stream=None):
+    _check(lib().trit_quant_gemv_many(ctypes.cast(qlist.array, ctypes.c_void_p), qlist.count,
+                                      _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_quant_gemv_many")
 
 
 def trit_quant_act_many(alist: ActList, err_flag: torch.Tensor, stream=None):

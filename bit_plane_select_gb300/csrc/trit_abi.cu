@@ -63,6 +63,8 @@ ProjDev to_dev(const trit_proj &p) {
     ProjDev d;
     d.planes = reinterpret_cast<const uint4 *>(p.planes);
     d.x = p.x_i8;
+    d.xf = nullptr;
+    d.x_i8_out = nullptr;
     d.x_scale = p.x_scale;
     d.y_i32 = p.y_i32;
     d.y_f32 = p.y_f32;
@@ -110,6 +112,34 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
     cudaError_t e = flush1();
     if (e == cudaSuccess) e = flushm();
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+trit_status check_qproj(const trit_qproj &p) {
+    if (!p.planes || !p.x || (!p.y_i32 && !p.y_f32) || p.reserved != 0) return TRIT_E_ARG;
+    if (!aligned(p.planes, 16) || !aligned(p.x, 4) || !aligned(p.x_i8, 16) ||
+        !aligned(p.x_scale, 4) || !aligned(p.y_i32, 4) || !aligned(p.y_f32, 4))
+        return TRIT_E_ARG;
+    if (!rows_ok(p.N) || !cols_ok(p.K) || p.K > TRIT_MAX_FUSED_K) return TRIT_E_SHAPE;
+    if (!isfinite(p.w_scale) || !(p.w_scale > 0.0f)) return TRIT_E_SCALE;
+    return TRIT_OK;
+}
+
+ProjDev to_dev(const trit_qproj &p) {
+    ProjDev d;
+    d.planes = reinterpret_cast<const uint4 *>(p.planes);
+    d.x = nullptr;
+    d.xf = p.x;
+    d.x_i8_out = p.x_i8;
+    d.x_scale = p.x_scale;
+    d.y_i32 = p.y_i32;
+    d.y_f32 = p.y_f32;
+    d.M = 1;
+    d.N = p.N;
+    d.K = int32_t(p.K);
+    d.B = int32_t(beats_per_row(p.K));
+    d.w_scale = p.w_scale;
+    d.pad_ = 0;
+    return d;
 }
 
 }  // namespace
@@ -223,6 +253,26 @@ TRIT_API trit_status trit_quant_act(const float *x, int64_t M, int64_t K, int8_t
 TRIT_API trit_status trit_gemm_many(const trit_proj *list, int32_t count, uint32_t *err_flag,
                                     trit_stream_t stream) {
     return run_many(list, count, err_flag, reinterpret_cast<cudaStream_t>(stream));
+}
+
+TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count, uint32_t *err_flag,
+                                          trit_stream_t stream) {
+    if (!list || count <= 0 || !err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        trit_status st = check_qproj(list[i]);
+        if (st != TRIT_OK) return st;
+    }
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    static thread_local ProjDev buf[TRIT_MAX_LIST_PER_LAUNCH];
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t base = 0; base < count; base += TRIT_MAX_LIST_PER_LAUNCH) {
+        const int n = count - base < TRIT_MAX_LIST_PER_LAUNCH ? count - base : TRIT_MAX_LIST_PER_LAUNCH;
+        for (int i = 0; i < n; ++i) buf[i] = to_dev(list[base + i]);
+        cudaError_t e = launch_gemv_many(buf, n, err_flag, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TRIT_OK;
 }
 
 TRIT_API trit_status trit_gemm(const uint8_t *planes, float w_scale, const int8_t *x_i8,

@@ -33,6 +33,14 @@
 // int32, is zeroed first and a final pass applies the fp32 dequantisation.
 // No scratch memory is used.
 //
+// Fused quantisation (M = 1).  An entry may carry its fp32 activation row
+// instead of int8 codes: the CTA then quantises the row itself while staging
+// it (the same arithmetic as trit_quant_act), so a whole decode token is one
+// launch; the CTA that owns the entry's first group also writes the codes and
+// the scale to global memory when asked.  The first plane loads of each warp
+// are announced to L2 with a bulk prefetch before the staging barrier, so HBM
+// streaming starts at once.
+//
 // M > 1 (+-1 bytes).  Each beat is expanded once into sixteen words of bytes in
 // {+1, 0, -1} (shift + sign-replicating byte permute + one LOP3 per word) and
 // reused for every activation row held by the CTA: 16 dp4a per row.
@@ -57,7 +65,9 @@ __host__ __device__ constexpr int seg_beats(int mt) { return 1152 / mt; }
 struct Entry {
     const uint4 *planes;
     const int8_t *x;        // first activation row of this entry, stride xld
-    const float *x_scale;   // first scale of this entry
+    const float *xf;        // fused: the fp32 activation row (x is unused)
+    int8_t *x_i8_out;       // fused: codes out (natural layout, K_pad bytes), may be NULL
+    const float *x_scale;   // first scale of this entry (fused: scale out, may be NULL)
     int32_t *y_i32;         // first output row of this entry, stride N
     float *y_f32;
     int32_t *acc;           // non-NULL: atomically add the int32 partial here (stride N)
@@ -121,6 +131,83 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
     }
 }
 
+// Fused path: quantise the fp32 row of entry E (K <= seg_beats(1)*64 columns)
+// straight into the permuted shared-memory layout, with the arithmetic of
+// trit_quant_act.  Each thread owns 32-column half-blocks; the second pass
+// re-reads its half-blocks (from L1).  The owner CTA also writes the
+// natural-layout codes (zero tail to K_pad) and the scale.  Returns the scale.
+__device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool owner,
+                                              uint32_t *err) {
+    __shared__ uint32_t s_red[2][kWarps];
+    const int K = E.K;
+    const int nhb = (K + 31) / 32;                   // half-blocks that hold columns
+    const int halves = E.iters * kLanesPerRow * 2;   // half-blocks staged (>= nhb)
+    const float *x = E.xf;
+    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+    auto load4 = [&](int c) -> float4 {   // columns c..c+3, zero past K
+        if (vec && c + 4 <= K) return *reinterpret_cast<const float4 *>(x + c);
+        float4 f;
+        f.x = c + 0 < K ? x[c + 0] : 0.0f;
+        f.y = c + 1 < K ? x[c + 1] : 0.0f;
+        f.z = c + 2 < K ? x[c + 2] : 0.0f;
+        f.w = c + 3 < K ? x[c + 3] : 0.0f;
+        return f;
+    };
+    uint32_t amax = 0, bad = 0;
+    for (int hb = threadIdx.x; hb < nhb; hb += kThreads) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 f = load4(hb * 32 + 4 * q);
+            bad |= !isfinite(f.x) | !isfinite(f.y) | !isfinite(f.z) | !isfinite(f.w);
+            amax = max(amax, max(max(quant_abs_bits(f.x), quant_abs_bits(f.y)),
+                                 max(quant_abs_bits(f.z), quant_abs_bits(f.w))));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        amax = max(amax, __shfl_xor_sync(~0u, amax, o));
+        bad |= __shfl_xor_sync(~0u, bad, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_red[0][threadIdx.x >> 5] = amax;
+        s_red[1][threadIdx.x >> 5] = bad;
+    }
+    __syncthreads();
+    amax = 0;
+    bad = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+        amax = max(amax, s_red[0][i]);
+        bad |= s_red[1][i];
+    }
+    const QuantScale qs = quant_scale(amax, bad != 0);
+    const int64_t Kp = beats_per_row(K) * 64;
+    for (int hb = threadIdx.x; hb < halves; hb += kThreads) {
+        uint32_t in[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 f = hb < nhb ? load4(hb * 32 + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            in[q] = pack4(quant_code(f.x, qs), quant_code(f.y, qs), quant_code(f.z, qs),
+                          quant_code(f.w, qs));
+        }
+        if (owner && E.x_i8_out && int64_t(hb) * 32 < Kp) {
+            uint4 *o = reinterpret_cast<uint4 *>(E.x_i8_out + int64_t(hb) * 32);
+            o[0] = make_uint4(in[0], in[1], in[2], in[3]);
+            o[1] = make_uint4(in[4], in[5], in[6], in[7]);
+        }
+        uint32_t out[8];
+        permute_block(in, out);
+        uint32_t *dst = xs + (hb >> 1) * kXBeatWords + (hb & 1) * 8;
+        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+    if (owner && threadIdx.x == 0) {
+        if (E.x_scale) *const_cast<float *>(E.x_scale) = qs.a;
+        if (bad) atomicOr(err, TRIT_ERR_NONFINITE);
+    }
+    return qs.a;
+}
+
 __device__ __forceinline__ int32_t row_sum4(int32_t v) {
     v += __shfl_xor_sync(~0u, v, 1);
     v += __shfl_xor_sync(~0u, v, 2);
@@ -130,7 +217,7 @@ __device__ __forceinline__ int32_t row_sum4(int32_t v) {
 // Process groups [gb, ge) of entry E with one warp.  Returns the OR of pos & neg.
 template <int MT>
 __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *xs, int xs_words,
-                                               int64_t gb, int64_t ge, int rs, int bs) {
+                                               float xsc, int64_t gb, int64_t ge, int rs, int bs) {
     const int it = E.iters;
     const int steps = int(ge - gb) * it;
     const int64_t N = E.N;
@@ -225,7 +312,7 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
                         atomicAdd(E.acc + row, y);
                     } else {
                         if (E.y_i32) E.y_i32[row] = y;
-                        if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, E.x_scale[0]);
+                        if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, xsc);
                     }
                 }
 #pragma unroll
@@ -267,32 +354,36 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
 // step, so every load, shared-memory read and accumulator index is static.
 // The ring depth D divides IT, so step t of every group uses ring slot t % D;
 // the last D loads of a group already fetch the next group's first beats.
+
+template <int IT>
+__device__ __forceinline__ const uint4 *fixed_row_ptr(const Entry &E, int64_t g, int64_t last_row,
+                                                      int rs, int bs) {
+    const int64_t r = g * kRowsPerGroup + rs;
+    return E.planes + (r < last_row ? r : last_row) * int64_t(E.bstride) + bs;
+}
+
+__device__ __forceinline__ int64_t fixed_last_row(const Entry &E, int64_t ge) {
+    return (ge * kRowsPerGroup < E.N ? ge * kRowsPerGroup : E.N) - 1;
+}
+
 template <int IT, int D>
-__device__ __forceinline__ uint32_t run_fixed(const Entry &E, const uint32_t *xs, int64_t gb,
-                                              int64_t ge, int rs, int bs) {
+__device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs, float x_scale,
+                                              int64_t gb, int64_t ge, int rs, int bs) {
     static_assert(IT % D == 0, "ring depth must divide the steps of a row");
-    const uint4 *const planes = E.planes;
-    const int64_t bstride = E.bstride;
     const int64_t N = E.N;
     int32_t *const y_i32 = E.y_i32;
     float *const y_f32 = E.y_f32;
     int32_t *const acc_out = E.acc;
     const float w_scale = E.w_scale;
-    const float x_scale = E.x_scale[0];
-    const int64_t last_row = (ge * kRowsPerGroup < N ? ge * kRowsPerGroup : N) - 1;
-    auto row_ptr = [&](int64_t g) -> const uint4 * {
-        const int64_t r = g * kRowsPerGroup + rs;
-        return planes + (r < last_row ? r : last_row) * bstride + bs;
-    };
+    const int64_t last_row = fixed_last_row(E, ge);
     const uint4 *xb = reinterpret_cast<const uint4 *>(xs) + bs * kXBeatVec;
 
     uint32_t viol = 0;
-    const uint4 *rp = row_ptr(gb);
-    const uint4 *rpn = row_ptr(gb + 1);
+    const uint4 *rp = fixed_row_ptr<IT>(E, gb, last_row, rs, bs);
+    const uint4 *rpn = fixed_row_ptr<IT>(E, gb + 1, last_row, rs, bs);
     uint4 ring[D];
 #pragma unroll
     for (int d = 0; d < D; ++d) ring[d] = ldg_stream(rp + d * kLanesPerRow);
-
     int64_t row = gb * kRowsPerGroup + rs;
     for (int64_t g = gb; g < ge; ++g) {
         int acc[16];
@@ -331,7 +422,7 @@ __device__ __forceinline__ uint32_t run_fixed(const Entry &E, const uint32_t *xs
         }
         row += kRowsPerGroup;
         rp = rpn;
-        rpn = row_ptr(g + 2);
+        rpn = fixed_row_ptr<IT>(E, g + 2, last_row, rs, bs);
     }
     return viol;
 }
@@ -365,23 +456,39 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
         int64_t g1 = (dhi + it - 1) / it;
         if (g1 > E.groups) g1 = E.groups;
         if (g0 >= g1) continue;
-        __syncthreads();   // the previous entry's readers are done with xs
-        stage_x<MT>(E, xs, L.xs_words);
-        __syncthreads();
         const int64_t n = g1 - g0;
         const int64_t wb = g0 + n * warp / kWarps, we = g0 + n * (warp + 1) / kWarps;
+        // 1: rows of 40 beats, 2: rows of 108 beats (unrolled paths), 0: generic
+        const int path = (MT == 1 && E.B == 40 && E.iters == 10) ? 1
+                       : (MT == 1 && E.B == 108 && E.iters == 27) ? 2 : 0;
+        // start this warp's first two groups streaming into L2 before the barrier
+        if (lane == 0 && wb < we && E.B == E.bstride) {
+            const int64_t r0 = wb * kRowsPerGroup;
+            int64_t r1 = (wb + 2 < we ? wb + 2 : we) * kRowsPerGroup;
+            r1 = r1 < E.N ? r1 : E.N;
+            prefetch_l2_bulk(E.planes + r0 * E.bstride, uint32_t((r1 - r0) * E.bstride * 16));
+        }
+        __syncthreads();   // the previous entry's readers are done with xs
+        float xsc;
+        if (MT == 1 && E.xf) {
+            xsc = stage_x_fp32(E, xs, g0 == 0, L.err);
+        } else {
+            stage_x<MT>(E, xs, L.xs_words);
+            xsc = E.x_scale[0];
+        }
+        __syncthreads();
         if (wb < we) {
             if constexpr (MT == 1) {
-                if (E.B == 40 && E.iters == 10) {
-                    viol |= run_fixed<10, 5>(E, xs, wb, we, rs, bs);
+                if (path == 1) {
+                    viol |= fixed_run<10, 5>(E, xs, xsc, wb, we, rs, bs);
                     continue;
                 }
-                if (E.B == 108 && E.iters == 27) {
-                    viol |= run_fixed<27, 3>(E, xs, wb, we, rs, bs);
+                if (path == 2) {
+                    viol |= fixed_run<27, 3>(E, xs, xsc, wb, we, rs, bs);
                     continue;
                 }
             }
-            viol |= run_groups<MT>(E, xs, L.xs_words, wb, we, rs, bs);
+            viol |= run_groups<MT>(E, xs, L.xs_words, xsc, wb, we, rs, bs);
         }
     }
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
@@ -453,8 +560,10 @@ Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb
     Entry E;
     const int64_t Kp = int64_t(p.B) * 64;
     E.planes = p.planes + b0;
-    E.x = p.x + m0 * Kp + b0 * 64;
-    E.x_scale = p.x_scale + m0;
+    E.x = p.x ? p.x + m0 * Kp + b0 * 64 : nullptr;
+    E.xf = p.xf;                 // fused entries are single-segment, M = 1
+    E.x_i8_out = p.x_i8_out;
+    E.x_scale = p.x_scale ? p.x_scale + m0 : nullptr;
     E.y_i32 = p.y_i32 ? p.y_i32 + m0 * p.N : nullptr;
     E.y_f32 = p.y_f32 ? p.y_f32 + m0 * p.N : nullptr;
     E.acc = acc ? acc + m0 * p.N : nullptr;

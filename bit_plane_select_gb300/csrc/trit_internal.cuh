@@ -49,6 +49,12 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
     return v;
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned source) into L2;
+// no registers are held and nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // The fp32 dequantisation of one output, one rounding per step, never contracted.
 __device__ __forceinline__ float dequant(int32_t y, float w_scale, float x_scale) {
     float f = __int2float_rn(y);
@@ -79,12 +85,50 @@ __device__ __forceinline__ void permute_block(const uint32_t in[8], uint32_t out
     }
 }
 
+// ---- activation quantiser arithmetic ------------------------------------------
+// Shared by trit_quant_act and the fused quantise-and-multiply path so that both
+// produce identical codes ("Tritium ..." -- Numerics; reading: q = clamp(rint(x *
+// (127/a)), -127, 127) with a = max|x|, prescaled by 2^96 when a < 2^-96).
+
+// |x| as an integer: non-negative floats order like their bit patterns.
+__device__ __forceinline__ uint32_t quant_abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
+
+struct QuantScale {
+    float a;      // the row's absmax (the stored x_scale), 0 for a zero or rejected row
+    float pre;    // 2^96 when a < 2^-96, else 1
+    float inv;    // 127 / (a * pre)
+    bool zero;    // every code is 0
+};
+
+__device__ __forceinline__ QuantScale quant_scale(uint32_t amax_bits, bool bad) {
+    QuantScale q;
+    const float a = __uint_as_float(amax_bits);
+    q.zero = bad || amax_bits == 0;
+    q.a = q.zero ? 0.0f : a;
+    q.pre = a < 0x1p-96f ? 0x1p96f : 1.0f;
+    q.inv = q.zero ? 0.0f : __fdiv_rn(127.0f, __fmul_rn(a, q.pre));
+    return q;
+}
+
+__device__ __forceinline__ int quant_code(float v, const QuantScale &q) {
+    if (q.zero) return 0;
+    int c = __float2int_rn(__fmul_rn(__fmul_rn(v, q.pre), q.inv));
+    return c > 127 ? 127 : (c < -127 ? -127 : c);
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+    return (uint32_t(a) & 0xffu) | ((uint32_t(b) & 0xffu) << 8) | ((uint32_t(c) & 0xffu) << 16) |
+           (uint32_t(d) << 24);
+}
+
 // ---- launchers (host) ---------------------------------------------------------
 
 struct ProjDev {            // one product as a kernel sees it
     const uint4 *planes;
-    const int8_t *x;
-    const float *x_scale;
+    const int8_t *x;        // int8 activations (unfused)
+    const float *xf;        // fp32 activations (fused quantise-and-multiply), else NULL
+    const float *x_scale;   // input scales (unfused) / output scale, may be NULL (fused)
+    int8_t *x_i8_out;       // fused: output codes, may be NULL
     int32_t *y_i32;
     float *y_f32;
     int64_t M, N;
@@ -101,7 +145,7 @@ cudaError_t launch_verify(const uint8_t *planes, int64_t N, int64_t K, uint32_t 
                           unsigned long long *first_bad, cudaStream_t s);
 cudaError_t launch_quant_many(const trit_act *list, int count, uint32_t *err, cudaStream_t s);
 
-// M = 1 products.
+// M = 1 products (int8 activations, or fp32 activations quantised in the launch).
 cudaError_t launch_gemv_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
 // 2 <= M products, dp4a with beats reused across rows held in registers.
 cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);

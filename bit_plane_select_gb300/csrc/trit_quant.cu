@@ -39,8 +39,6 @@ __device__ __forceinline__ int find_entry(const QuantList &L, int64_t row) {
     return lo;
 }
 
-__device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
-
 // Block-wide max of the |x| bit patterns and OR of the non-finite flags.
 __device__ __forceinline__ void block_reduce(uint32_t &amax, uint32_t &bad) {
     __shared__ uint32_t s_max[kThreads / 32], s_bad[kThreads / 32];
@@ -61,16 +59,6 @@ __device__ __forceinline__ void block_reduce(uint32_t &amax, uint32_t &bad) {
         amax = max(amax, s_max[i]);
         bad |= s_bad[i];
     }
-}
-
-__device__ __forceinline__ int code(float v, float pre, float inv) {
-    int q = __float2int_rn(__fmul_rn(__fmul_rn(v, pre), inv));
-    return q > 127 ? 127 : (q < -127 ? -127 : q);
-}
-
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
-    return (uint32_t(a) & 0xffu) | ((uint32_t(b) & 0xffu) << 8) | ((uint32_t(c) & 0xffu) << 16) |
-           (uint32_t(d) << 24);
 }
 
 // V > 0: the row lives in registers (V float4 per thread); V == 0: two passes.
@@ -105,33 +93,27 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const __grid_constant__
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             bad |= !isfinite(r[i].x) | !isfinite(r[i].y) | !isfinite(r[i].z) | !isfinite(r[i].w);
-            amax = max(amax, max(max(abs_bits(r[i].x), abs_bits(r[i].y)),
-                                 max(abs_bits(r[i].z), abs_bits(r[i].w))));
+            amax = max(amax, max(max(quant_abs_bits(r[i].x), quant_abs_bits(r[i].y)),
+                                 max(quant_abs_bits(r[i].z), quant_abs_bits(r[i].w))));
         }
     } else {
         for (int64_t c = threadIdx.x; c < K; c += kThreads) {
             const float v = x[c];
             bad |= !isfinite(v);
-            amax = max(amax, abs_bits(v));
+            amax = max(amax, quant_abs_bits(v));
         }
     }
     block_reduce(amax, bad);
-    const float a = __uint_as_float(amax);
-    const bool zero = bad || amax == 0;
-    const float pre = a < 0x1p-96f ? 0x1p96f : 1.0f;
-    const float inv = zero ? 0.0f : __fdiv_rn(127.0f, __fmul_rn(a, pre));
+    const QuantScale qs = quant_scale(amax, bad != 0);
 
     if constexpr (V > 0) {
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int64_t c = (int64_t(threadIdx.x) + i * kThreads) * 4;
             if (c < Kp) {
-                uint32_t w = 0;
-                if (!zero) {   // columns >= K hold 0 and code to 0
-                    w = pack4(code(r[i].x, pre, inv), code(r[i].y, pre, inv),
-                              code(r[i].z, pre, inv), code(r[i].w, pre, inv));
-                }
-                q4[c / 4] = w;
+                // columns >= K hold 0 and code to 0
+                q4[c / 4] = pack4(quant_code(r[i].x, qs), quant_code(r[i].y, qs),
+                                  quant_code(r[i].z, qs), quant_code(r[i].w, qs));
             }
         }
     } else {
@@ -140,13 +122,13 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const __grid_constant__
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int64_t c = c4 * 4 + k;
-                v[k] = (!zero && c < K) ? code(x[c], pre, inv) : 0;
+                v[k] = c < K ? quant_code(x[c], qs) : 0;
             }
             q4[c4] = pack4(v[0], v[1], v[2], v[3]);
         }
     }
     if (threadIdx.x == 0) {
-        A.x_scale[m] = zero ? 0.0f : a;
+        A.x_scale[m] = qs.a;
         if (bad) atomicOr(L.err, TRIT_ERR_NONFINITE);
     }
 }

@@ -1,8 +1,9 @@
 """A resident stack of ternary projections: packed planes in HBM plus one
-contiguous arena for each of the step's inputs and outputs, so that a decode
-step is two launches (quantise every activation row, then every product) and
-an end-to-end step is one host-to-device and one device-to-host copy around
-them.
+contiguous arena for each of the step's inputs and outputs, so that a batch-1
+decode step is one launch (every activation row quantised and every product
+computed by the fused kernel; the two-launch path -- quantise, then multiply --
+stays available) and an end-to-end step is one host-to-device and one
+device-to-host copy around it.
 
 This is the runtime around the kernels for the layer-by-layer decode of
 "Tritium: One Weight Format for Ternary Inference ..." -- Why it does not
@@ -13,8 +14,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (ActList, ProjList, k_pad, payload_bytes, trit_gemm_many, trit_pack,
-               trit_quant_act_many)
+from . import (MAX_FUSED_K, ActList, ProjList, QProjList, k_pad, payload_bytes,
+               trit_gemm_many, trit_pack, trit_quant_act_many, trit_quant_gemv_many)
 
 
 class TernaryStack:
@@ -68,6 +69,12 @@ class TernaryStack:
         self.projs = ProjList([(self.planes[i], self.specs[i][4], self.q[i], self.s[i],
                                 self.specs[i][2], self.y[i], self.f[i])
                                for i in range(len(self.specs))])
+        self.fusable = all(M == 1 and K <= MAX_FUSED_K for _, N, K, M, _ in self.specs)
+        self.qprojs = None
+        if self.fusable:
+            self.qprojs = QProjList([(self.planes[i], self.specs[i][4], self.x[i], self.q[i],
+                                      self.s[i], self.y[i], self.f[i])
+                                     for i in range(len(self.specs))])
         self.finalized = True
 
     # -- one decode step ------------------------------------------------------
@@ -78,7 +85,18 @@ class TernaryStack:
     def products(self, stream=None):
         trit_gemm_many(self.projs, self.err, stream)
 
+    def fused(self, stream=None):
+        """Quantise and multiply every entry in one launch (M = 1 stacks)."""
+        trit_quant_gemv_many(self.qprojs, self.err, stream)
+
     def step(self, stream=None):
+        if self.fusable:
+            self.fused(stream)
+        else:
+            self.quantize(stream)
+            self.products(stream)
+
+    def step_two_launch(self, stream=None):
         self.quantize(stream)
         self.products(stream)
 
@@ -99,6 +117,15 @@ class TernaryStack:
         b = 0
         for _, N, K, M, _ in self.specs:
             b += payload_bytes(N, K) + M * k_pad(K) + 4 * M + 8 * M * N
+        return b
+
+    def fused_bytes(self) -> int:
+        """Algorithmic bytes of the fused launch: planes read once, the fp32
+        activations read, int8 codes (K_pad per row) and scales written, y_i32
+        and y_f32 written."""
+        b = 0
+        for _, N, K, M, _ in self.specs:
+            b += payload_bytes(N, K) + M * (4 * K + k_pad(K) + 4) + 8 * M * N
         return b
 
     def quant_bytes(self) -> int:

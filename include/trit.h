@@ -191,6 +191,33 @@ typedef struct trit_proj {
 TRIT_API trit_status trit_gemm_many(const trit_proj *list, int32_t count, uint32_t *err_flag,
                                     trit_stream_t stream);
 
+/* One fused decode product: an fp32 activation row quantised and multiplied in
+ * the same launch.  M = 1. */
+typedef struct trit_qproj {
+    const uint8_t *planes;
+    const float *x;      /* [K] fp32 activation row */
+    int8_t *x_i8;        /* out, may be NULL: the row's codes, K_pad bytes, zero tail */
+    float *x_scale;      /* out, may be NULL: the row's absmax */
+    int32_t *y_i32;      /* may be NULL */
+    float *y_f32;        /* may be NULL (not both) */
+    int64_t N, K;
+    float w_scale;
+    uint32_t reserved;   /* must be 0 */
+} trit_qproj;
+
+/*
+ * trit_quant_gemv_many -- for each entry, trit_quant_act of its fp32 row
+ * followed by trit_gemv, computed by one persistent launch for the whole list
+ * (the quantiser runs inside the product kernel while it stages the
+ * activations; no int8 round trip through memory).  Results -- y_i32, y_f32
+ * and, when asked for, x_i8 and x_scale -- are bit-identical to the two-call
+ * path.  K is limited to 73,728 (1,152 beats) per entry; longer rows return
+ * TRIT_E_SHAPE and take the two-call path.  `list` is a host array.
+ */
+#define TRIT_MAX_FUSED_K 73728
+TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count,
+                                          uint32_t *err_flag, trit_stream_t stream);
+
 /* One quantisation of a list: the arguments of trit_quant_act. */
 typedef struct trit_act {
     const float *x;

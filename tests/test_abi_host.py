@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act", "trit_gemv",
-                     "trit_gemm", "trit_gemm_many", "trit_quant_act_many"):
+                     "trit_gemm", "trit_gemm_many", "trit_quant_act_many",
+                     "trit_quant_gemv_many"):
         assert required in names
 
 
@@ -43,6 +44,7 @@ def test_struct_layouts(trit):
     assert ctypes.sizeof(trit.TritProj) == 72
     assert trit.TritProj.w_scale.offset == 64
     assert ctypes.sizeof(trit.TritAct) == 40
+    assert ctypes.sizeof(trit.TritQProj) == 72 and trit.TritQProj.w_scale.offset == 64
 
 
 def test_payload_bytes(trit):

@@ -111,10 +111,17 @@ def test_config1_one_layer(t, orc):
 
 def test_config2_stack_sampled(t, orc):
     st, items, wss = build_stack(t, synth.LAYERS, 2, 1)
-    for _ in range(2):     # the benchmark's warm-up and timed steps repeat the same calls
-        st.step()
+    assert st.fusable
+    st.step_two_launch()       # quantise, then multiply: two launches
+    y2, f2, q2 = st.y_arena.clone(), st.f_arena.clone(), st.q_arena.clone()
+    st.y_arena.zero_(), st.f_arena.zero_(), st.q_arena.zero_()
+    for _ in range(2):     # the benchmark's warm-up and timed steps repeat the same call
+        st.step()          # one fused launch
     assert int(host(st.err)[0]) == 0
     assert st.plane_bytes == 521011200
+    # the fused launch and the two-launch path agree bit for bit on every output
+    assert torch.equal(st.y_arena, y2) and torch.equal(st.q_arena, q2)
+    assert torch.equal(st.f_arena.view(torch.int32), f2.view(torch.int32))
     for i, (layer, idx, name, N, K) in enumerate(items):
         w = synth.stack_weights(2, layer, idx)
         x = synth.projection_acts(2, layer, idx, 1)

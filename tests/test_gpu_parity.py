@@ -353,3 +353,66 @@ def test_error_status_raises(t):
     with pytest.raises(t.TritError) as e:
         t.trit_gemm(planes, 1.0, x, xs, 1 << 24)
     assert e.value.status == 2
+
+
+# ---- fused quantise-and-multiply --------------------------------------------
+
+FUSED_K = [1, 65, 200, 2560, 6912, 6913, 40000, 73728]
+
+
+@pytest.mark.parametrize("K", FUSED_K)
+def test_quant_gemv_many_matches_oracle(t, orc, K):
+    """One launch quantises each fp32 row and multiplies it: codes, scale and
+    products equal the oracle's quantiser followed by its product."""
+    rng = synth.rng_for(120, K)
+    rows = quant_cases(rng, K)          # normal, zero, denormal, ties, huge, NaN, Inf rows
+    Ns = [37, 8, 5, 64, 129, 3, 250, 17]
+    entries, refs = [], []
+    for i, N in enumerate(Ns):
+        w = synth.ternary(rng, N, K, synth.P_ZERO)
+        ws = float(synth.w_scale(w))
+        planes, _ = t.trit_pack(dev(w), ws)
+        x = rows[i % rows.shape[0]]
+        q = torch.full((((K + 63) // 64) * 64,), 55, dtype=torch.int8, device="cuda")
+        s = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+        y = torch.empty(N, dtype=torch.int32, device="cuda")
+        f = torch.empty(N, dtype=torch.float32, device="cuda")
+        entries.append((planes, ws, dev(x), q, s, y, f))
+        q_ref, s_ref, e_ref = orc.quant(x[None, :])
+        ry, rf, _ = orc.gemm(orc.pack(w), ws, q_ref, s_ref, K)
+        refs.append((q_ref[0], s_ref, ry[0], rf[0], e_ref[0]))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t.trit_quant_gemv_many(t.QProjList(entries), err)
+    any_bad = any(r[4] for r in refs)
+    assert int(host(err)[0]) == (t.ERR_NONFINITE if any_bad else 0)
+    for (_, _, _, q, s, y, f), (q_ref, s_ref, ry, rf, _) in zip(entries, refs):
+        np.testing.assert_array_equal(host(q), q_ref)
+        np.testing.assert_array_equal(host(s), s_ref)
+        np.testing.assert_array_equal(host(y), ry)
+        assert_f32_close(host(f), rf)
+        np.testing.assert_array_equal(host(f).view(np.uint32), rf.view(np.uint32))
+
+
+def test_quant_gemv_many_without_code_outputs(t, orc):
+    rng = synth.rng_for(121)
+    K, N = 2560, 1000
+    w = synth.ternary(rng, N, K, 0.45)
+    x = rng.standard_normal(K).astype(np.float32)
+    planes, _ = t.trit_pack(dev(w), 1.25)
+    y = torch.empty(N, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t.trit_quant_gemv_many(t.QProjList([(planes, 1.25, dev(x), None, None, y, None)]), err)
+    q_ref, s_ref, _ = orc.quant(x[None, :])
+    ry, _, _ = orc.gemm(orc.pack(w), 1.25, q_ref, s_ref, K)
+    np.testing.assert_array_equal(host(y), ry[0])
+
+
+def test_quant_gemv_many_rejects_long_rows(t):
+    K = t.MAX_FUSED_K + 1
+    planes = torch.zeros((1, (K + 63) // 64, 16), dtype=torch.uint8, device="cuda")
+    x = torch.zeros(K, dtype=torch.float32, device="cuda")
+    y = torch.empty(1, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(t.TritError) as e:
+        t.trit_quant_gemv_many(t.QProjList([(planes, 1.0, x, None, None, y, None)]), err)
+    assert e.value.status == 2
