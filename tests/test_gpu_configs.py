@@ -36,9 +36,12 @@ def host(x):
 
 
 def assert_f32_close(got, ref, tol=1e-6):
+    """Relative error <= tol; identical values (infinities included) match."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
-    rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30)
+    with np.errstate(invalid="ignore"):
+        rel = np.where(got == ref, 0.0, np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30))
+    assert not np.isnan(rel).any()
     assert float(rel.max(initial=0.0)) <= tol
 
 
