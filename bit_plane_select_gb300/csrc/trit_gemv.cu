@@ -57,6 +57,25 @@ constexpr int kDepth = 4;                   // 16-byte loads in flight per lane
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 
+// Groups ahead of the one being computed that each warp bulk-prefetches into
+// L2 (0 disables: measured slower at every distance on the 30-layer stack),
+// whether the first group of each warp is prefetched before the staging
+// barrier, and the register ring depths of the unrolled paths (measured: depth
+// matters little once 24 warps per SM are resident).
+#ifndef TRIT_L2_AHEAD
+#define TRIT_L2_AHEAD 0
+#endif
+#ifndef TRIT_RING_40
+#define TRIT_RING_40 5
+#endif
+#ifndef TRIT_RING_108
+#define TRIT_RING_108 3
+#endif
+#ifndef TRIT_PREFETCH_FIRST
+#define TRIT_PREFETCH_FIRST 1
+#endif
+constexpr int kL2Ahead = TRIT_L2_AHEAD;
+
 // Beats per column segment for MT staged rows: MT * seg_beats * 80 bytes of
 // shared memory stay at 90 KB.  A segment takes at most 288 steps per row, so
 // the 2^j-weighted accumulators (at most 2^17 per step) stay below 2^26.
@@ -354,6 +373,8 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
 // step, so every load, shared-memory read and accumulator index is static.
 // The ring depth D divides IT, so step t of every group uses ring slot t % D;
 // the last D loads of a group already fetch the next group's first beats.
+// Optionally (kL2Ahead > 0) the group kL2Ahead further on (8 contiguous rows)
+// is bulk-prefetched into L2 while a group is computed.
 
 template <int IT>
 __device__ __forceinline__ const uint4 *fixed_row_ptr(const Entry &E, int64_t g, int64_t last_row,
@@ -385,7 +406,14 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
 #pragma unroll
     for (int d = 0; d < D; ++d) ring[d] = ldg_stream(rp + d * kLanesPerRow);
     int64_t row = gb * kRowsPerGroup + rs;
+    const bool pf = kL2Ahead > 0 && rs == 0 && bs == 0 && E.B == E.bstride;
     for (int64_t g = gb; g < ge; ++g) {
+        if (pf && g + kL2Ahead < ge) {   // group g + kL2Ahead: 8 contiguous rows
+            const int64_t r0 = (g + kL2Ahead) * kRowsPerGroup;
+            const int64_t r1 = r0 + kRowsPerGroup < N ? r0 + kRowsPerGroup : N;
+            if (r0 < r1)
+                prefetch_l2_bulk(E.planes + r0 * E.bstride, uint32_t((r1 - r0) * E.bstride * 16));
+        }
         int acc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0;
@@ -427,8 +455,11 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
     return viol;
 }
 
+#ifndef TRIT_MIN_BLOCKS
+#define TRIT_MIN_BLOCKS 3
+#endif
 template <int MT>
-__global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
     select_accumulate_kernel(const __grid_constant__ List L) {
     extern __shared__ __align__(16) uint32_t xs[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -461,10 +492,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
         // 1: rows of 40 beats, 2: rows of 108 beats (unrolled paths), 0: generic
         const int path = (MT == 1 && E.B == 40 && E.iters == 10) ? 1
                        : (MT == 1 && E.B == 108 && E.iters == 27) ? 2 : 0;
-        // start this warp's first two groups streaming into L2 before the barrier
-        if (lane == 0 && wb < we && E.B == E.bstride) {
+        // start this warp's first groups streaming into L2 before the barrier
+        if (TRIT_PREFETCH_FIRST && lane == 0 && wb < we && E.B == E.bstride) {
             const int64_t r0 = wb * kRowsPerGroup;
-            int64_t r1 = (wb + 2 < we ? wb + 2 : we) * kRowsPerGroup;
+            const int64_t ahead = kL2Ahead > 0 ? kL2Ahead : 1;
+            int64_t r1 = (wb + ahead < we ? wb + ahead : we) * kRowsPerGroup;
             r1 = r1 < E.N ? r1 : E.N;
             prefetch_l2_bulk(E.planes + r0 * E.bstride, uint32_t((r1 - r0) * E.bstride * 16));
         }
@@ -480,11 +512,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 3 : 2)
         if (wb < we) {
             if constexpr (MT == 1) {
                 if (path == 1) {
-                    viol |= fixed_run<10, 5>(E, xs, xsc, wb, we, rs, bs);
+                    viol |= fixed_run<10, TRIT_RING_40>(E, xs, xsc, wb, we, rs, bs);
                     continue;
                 }
                 if (path == 2) {
-                    viol |= fixed_run<27, 3>(E, xs, xsc, wb, we, rs, bs);
+                    viol |= fixed_run<27, TRIT_RING_108>(E, xs, xsc, wb, we, rs, bs);
                     continue;
                 }
             }

@@ -40,12 +40,26 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// 16-byte streaming load of read-once data: not kept in L1.
+// 16-byte streaming load of read-once data: not kept in L1.  TRIT_LDG_L2_FETCH
+// selects the L2 fetch granularity hint on a miss (0: default, 128 or 256 bytes).
+#ifndef TRIT_LDG_L2_FETCH
+#define TRIT_LDG_L2_FETCH 0
+#endif
 __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
     uint4 v;
+#if TRIT_LDG_L2_FETCH == 256
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+#elif TRIT_LDG_L2_FETCH == 128
+    asm volatile("ld.global.nc.L1::no_allocate.L2::128B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+#else
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
+#endif
     return v;
 }
 
