@@ -74,6 +74,12 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 #ifndef TRIT_PREFETCH_FIRST
 #define TRIT_PREFETCH_FIRST 1
 #endif
+#ifndef TRIT_COST_108
+#define TRIT_COST_108 100
+#endif
+#ifndef TRIT_WAVES
+#define TRIT_WAVES 1
+#endif
 constexpr int kL2Ahead = TRIT_L2_AHEAD;
 
 // Beats per column segment for MT staged rows: MT * seg_beats * 80 bytes of
@@ -92,13 +98,15 @@ struct Entry {
     int32_t *acc;           // non-NULL: atomically add the int32 partial here (stride N)
     int64_t N;
     int64_t groups;         // ceil(N / 8)
-    int64_t cost_begin;     // prefix sum of groups * iters over the list
-    int64_t xld;            // activation row stride (K_pad)
+    int64_t cost_begin;     // prefix sum of groups * gcost over the list
+    int32_t xld;            // activation row stride (K_pad)
     int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / 4)
     int32_t bstride;        // beats per full row of the planes
     int32_t mrows;          // activation rows of this entry (<= MT)
+    int32_t gcost;          // cost units of one group: iters x a per-step weight
     float w_scale;
 };
+static_assert(sizeof(Entry) == 120, "the list of 256 entries must fit the 32 KB parameter space");
 
 struct List {
     int32_t count;
@@ -480,11 +488,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
     }
     for (; e < L.count && L.e[e].cost_begin < hi; ++e) {
         const Entry &E = L.e[e];
-        const int64_t it = E.iters;
-        // groups whose first step lies in [lo, hi)
+        const int64_t gc = E.gcost;
+        // groups whose first cost unit lies in [lo, hi)
         const int64_t dlo = lo - E.cost_begin, dhi = hi - E.cost_begin;
-        const int64_t g0 = dlo <= 0 ? 0 : (dlo + it - 1) / it;
-        int64_t g1 = (dhi + it - 1) / it;
+        const int64_t g0 = dlo <= 0 ? 0 : (dlo + gc - 1) / gc;
+        int64_t g1 = (dhi + gc - 1) / gc;
         if (g1 > E.groups) g1 = E.groups;
         if (g0 >= g1) continue;
         const int64_t n = g1 - g0;
@@ -495,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
         // start this warp's first groups streaming into L2 before the barrier
         if (TRIT_PREFETCH_FIRST && lane == 0 && wb < we && E.B == E.bstride) {
             const int64_t r0 = wb * kRowsPerGroup;
-            const int64_t ahead = kL2Ahead > 0 ? kL2Ahead : 1;
+            const int64_t ahead = TRIT_PREFETCH_FIRST;
             int64_t r1 = (wb + ahead < we ? wb + ahead : we) * kRowsPerGroup;
             r1 = r1 < E.N ? r1 : E.N;
             prefetch_l2_bulk(E.planes + r0 * E.bstride, uint32_t((r1 - r0) * E.bstride * 16));
@@ -554,7 +562,7 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
     for (int i = 0; i < n; ++i) {
         L.e[i] = entries[i];
         L.e[i].cost_begin = cost;
-        cost += entries[i].groups * entries[i].iters;
+        cost += entries[i].groups * entries[i].gcost;
         groups += entries[i].groups;
         if (entries[i].iters > max_iters) max_iters = entries[i].iters;
     }
@@ -567,7 +575,7 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
                                              int(smem));
         if (e != cudaSuccess) return e;
     }
-    const int64_t cap = int64_t(occupancy<MT>(smem)) * device_sm_count();
+    const int64_t cap = int64_t(occupancy<MT>(smem)) * device_sm_count() * TRIT_WAVES;
     const int64_t want = (groups + kWarps - 1) / kWarps;
     const int grid = int(want < cap ? (want < 1 ? 1 : want) : cap);
     select_accumulate_kernel<MT><<<grid, kThreads, smem, s>>>(L);
@@ -602,13 +610,14 @@ Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb
     E.N = p.N;
     E.groups = (p.N + kRowsPerGroup - 1) / kRowsPerGroup;
     E.cost_begin = 0;
-    E.xld = Kp;
+    E.xld = int32_t(Kp);
     const int64_t kseg = int64_t(p.K) - b0 * 64;
     E.K = int32_t(kseg < nb * 64 ? kseg : nb * 64);
     E.B = int32_t(nb);
     E.iters = int32_t((nb + kLanesPerRow - 1) / kLanesPerRow);
     E.bstride = p.B;
     E.mrows = mrows;
+    E.gcost = E.iters * (nb == 108 ? TRIT_COST_108 : 100);
     E.w_scale = p.w_scale;
     return E;
 }
