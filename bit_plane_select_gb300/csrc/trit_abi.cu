@@ -87,7 +87,8 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
     if (st != TRIT_OK) return st;
     static thread_local ProjDev one[TRIT_MAX_LIST_PER_LAUNCH];
     static thread_local ProjDev many[TRIT_MAX_LIST_PER_LAUNCH];
-    int n1 = 0, nm = 0;
+    static thread_local ProjDev dense[TRIT_MAX_LIST_PER_LAUNCH];
+    int n1 = 0, nm = 0, nd = 0;
     auto flush1 = [&]() -> cudaError_t {
         cudaError_t e = n1 ? launch_gemv_many(one, n1, err_flag, s) : cudaSuccess;
         n1 = 0;
@@ -98,19 +99,29 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
         nm = 0;
         return e;
     };
+    auto flushd = [&]() -> cudaError_t {
+        cudaError_t e = nd ? launch_prefill_many(dense, nd, err_flag, s) : cudaSuccess;
+        nd = 0;
+        return e;
+    };
     for (int32_t i = 0; i < count; ++i) {
         cudaError_t e = cudaSuccess;
-        if (list[i].M == 1) {
-            one[n1++] = to_dev(list[i]);
+        const ProjDev d = to_dev(list[i]);
+        if (d.M == 1) {
+            one[n1++] = d;
             if (n1 == TRIT_MAX_LIST_PER_LAUNCH) e = flush1();
+        } else if (prefill_supported(d)) {
+            dense[nd++] = d;
+            if (nd == TRIT_MAX_LIST_PER_LAUNCH) e = flushd();
         } else {
-            many[nm++] = to_dev(list[i]);
+            many[nm++] = d;
             if (nm == TRIT_MAX_LIST_PER_LAUNCH) e = flushm();
         }
         if (e != cudaSuccess) return cuda_fail(e);
     }
     cudaError_t e = flush1();
     if (e == cudaSuccess) e = flushm();
+    if (e == cudaSuccess) e = flushd();
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
 

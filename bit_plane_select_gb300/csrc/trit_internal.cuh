@@ -164,6 +164,12 @@ cudaError_t launch_gemv_many(const ProjDev *list, int count, uint32_t *err, cuda
 // 2 <= M products, dp4a with beats reused across rows held in registers.
 cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
 
+// M >= kPrefillMinM (and K < 2^17, where fp32 accumulation of integer partial
+// sums stays exact) runs on the tensor cores.
+constexpr int64_t kPrefillMinM = 64;
+bool prefill_supported(const ProjDev &p);
+cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
+
 int device_sm_count();
 
 }  // namespace trit

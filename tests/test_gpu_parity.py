@@ -419,3 +419,87 @@ def test_quant_gemv_many_rejects_long_rows(t):
     with pytest.raises(t.TritError) as e:
         t.trit_quant_gemv_many(t.QProjList([(planes, 1.0, x, None, None, y, None)]), err)
     assert e.value.status == 2
+
+
+# ---- prefill: tensor-core path (M >= 64) -------------------------------------
+
+PREFILL_CASES = [(64, 33, 65), (128, 256, 64), (129, 257, 2560), (200, 300, 130), (64, 17, 6912),
+                 (255, 513, 1000), (512, 6912, 2560), (320, 2560, 6912)]
+
+
+@pytest.mark.parametrize("M,N,K", PREFILL_CASES)
+def test_prefill_matches_oracle(t, orc, M, N, K):
+    rng = synth.rng_for(130, M, N, K)
+    w = synth.ternary(rng, N, K, synth.P_ZERO)
+    x = padded_x(rng, M, K)
+    x[:, K:] = 9                       # bytes past K are not columns
+    x[0, :K] = -128
+    xs = (rng.random(M) + 0.25).astype(np.float32)
+    ws = float(synth.w_scale(w))
+    planes, _ = t.trit_pack(dev(w), ws)
+    y, f, err = t.trit_gemm(planes, ws, dev(x), dev(xs), K)
+    assert int(host(err)[0]) == 0
+    rows = np.arange(N) if N * M * K <= 2e8 else \
+        np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 62)]))
+    ry, rf, _ = orc.gemm(orc.pack(w[rows]), ws, x, xs, K)
+    np.testing.assert_array_equal(host(y)[:, rows], ry)
+    assert_f32_close(host(f)[:, rows], rf)
+    colsum = w.astype(np.int64).sum(axis=0)
+    np.testing.assert_array_equal(host(y).astype(np.int64).sum(axis=1),
+                                  x[:, :K].astype(np.int64) @ colsum)
+
+
+@pytest.mark.parametrize("K", [131071, 131072])
+def test_prefill_exactness_boundary(t, orc, K):
+    """|y| = 128*K: 16,777,088 at K = 131071 is still an exact fp32 integer on
+    the tensor-core path; K = 131072 is routed to the integer path."""
+    M = 64
+    w = np.stack([np.full(K, -1, np.int8), synth.ternary(synth.rng_for(131), 1, K, 0.4)[0]])
+    x = np.zeros((M, ((K + 63) // 64) * 64), np.int8)
+    x[:, :K] = -128
+    x[1::2, :K] = 127
+    xs = np.ones(M, np.float32)
+    planes, _ = t.trit_pack(dev(w), 1.0)
+    y, f, err = t.trit_gemm(planes, 1.0, dev(x), dev(xs), K)
+    ry, _, _ = orc.gemm(orc.pack(w), 1.0, x, xs, K)
+    assert int(ry[0, 0]) == 128 * K
+    np.testing.assert_array_equal(host(y), ry)
+
+
+def test_prefill_flags_both_set_other_rows_exact(t, orc):
+    rng = synth.rng_for(132)
+    M, N, K = 96, 300, 2560
+    w = synth.ternary(rng, N, K, synth.P_ZERO)
+    p = orc.pack(w)
+    for r in (3, 200, 299):
+        b, k = int(rng.integers(0, p.shape[1])), int(rng.integers(0, 64))
+        p[r, b, k // 8] |= 1 << (k % 8)
+        p[r, b, 8 + k // 8] |= 1 << (k % 8)
+    x = padded_x(rng, M, K)
+    xs = np.ones(M, np.float32)
+    y, f, err = t.trit_gemm(dev(p), 1.0, dev(x), dev(xs), K)
+    ry, _, rerr = orc.gemm(p, 1.0, x, xs, K)
+    assert int(host(err)[0]) == t.ERR_P1
+    keep = rerr == 0
+    assert keep.sum() == N - 3
+    np.testing.assert_array_equal(host(y)[:, keep], ry[:, keep])
+
+
+def test_prefill_outputs_optional_and_guarded(t, orc):
+    rng = synth.rng_for(133)
+    M, N, K = 130, 250, 640
+    w = synth.ternary(rng, N, K, 0.4)
+    x = padded_x(rng, M, K)
+    xs = (rng.random(M) + 0.5).astype(np.float32)
+    planes, _ = t.trit_pack(dev(w), 0.75)
+    ry, rf, _ = orc.gemm(orc.pack(w), 0.75, x, xs, K)
+    g = 4096
+    yb = torch.full((M * N + g,), -7, dtype=torch.int32, device="cuda")
+    fb = torch.full((M * N + g,), -7.0, dtype=torch.float32, device="cuda")
+    t.trit_gemm(planes, 0.75, dev(x), dev(xs), K, y_i32=yb[:M * N].view(M, N), want=())
+    t.trit_gemm(planes, 0.75, dev(x), dev(xs), K, y_f32=fb[:M * N].view(M, N), want=())
+    yh, fh = host(yb), host(fb)
+    np.testing.assert_array_equal(yh[:M * N].reshape(M, N), ry)
+    assert_f32_close(fh[:M * N].reshape(M, N), rf)
+    np.testing.assert_array_equal(fh[:M * N].reshape(M, N).view(np.uint32), rf.view(np.uint32))
+    assert (yh[M * N:] == -7).all() and (fh[M * N:] == -7.0).all()
