@@ -420,6 +420,128 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+# ---- other workloads (extra lines; the default run is the decode stack) --------
+
+def _timed(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_prefill(args):
+    """Prefill GEMMs: M tokens through gate/up/down of 30 layers (90 products,
+    distinct weights, P(0) = 0.4219): quantise the fp32 activations, then one
+    trit_gemm_many over the 90 products (tensor-core path)."""
+    import torch
+
+    import __graft_entry__
+    import synth
+    import bit_plane_select_gb300 as t
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    items = list(synth.prefill_items(args.layers))
+    planes, wss = [], []
+    for layer, idx, name, N, K in items:
+        w = synth.projection_weights(4, layer, idx)
+        ws = float(synth.w_scale(w))
+        pl, _ = t.trit_pack(torch.from_numpy(w).to(dev), ws)
+        planes.append(pl)
+        wss.append(ws)
+    Mmax = max(synth.PREFILL_M)
+    xs = [torch.from_numpy(synth.projection_acts(4, layer, idx, Mmax)).to(dev)
+          for layer, idx, name, N, K in items]
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+        peak_kind = "measured (bf16 burst; kind::f16 has the same nominal dense rate)"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+    results = {}
+    for M in synth.PREFILL_M:
+        acts, projs, keep = [], [], []
+        for i, (layer, idx, name, N, K) in enumerate(items):
+            x = xs[i][:M].contiguous()
+            q = torch.empty((M, t.k_pad(K)), dtype=torch.int8, device=dev)
+            sc = torch.empty(M, dtype=torch.float32, device=dev)
+            y = torch.empty((M, N), dtype=torch.int32, device=dev)
+            f = torch.empty((M, N), dtype=torch.float32, device=dev)
+            acts.append((x, q, sc))
+            projs.append((planes[i], wss[i], q, sc, K, y, f))
+            keep.append((x, q, sc, y, f))
+        alist, plist = t.ActList(acts), t.ProjList(projs)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        flops = sum(2 * M * N * K for _, _, _, N, K in items)
+        ms_q = _timed(lambda: t.trit_quant_act_many(alist, err), args.steps, args.warmup, stream)
+        ms_g = _timed(lambda: t.trit_gemm_many(plist, err), args.steps, args.warmup, stream)
+        results[M] = {"gemm_ms": round(ms_g, 4), "quant_ms": round(ms_q, 4),
+                      "tflops": round(flops / (ms_g * 1e-3) / 1e12, 1),
+                      "tok_per_s": round(M / ((ms_g + ms_q) * 1e-3), 1),
+                      "frac_of_peak": round(flops / (ms_g * 1e-3) / 1e12 / peak, 4),
+                      "err_flag": int(err.item())}
+        del alist, plist, keep, acts, projs
+        torch.cuda.empty_cache()
+    M = Mmax
+    out = {"metric": "prefill ternary GEMM TFLOP/s (30 layers x gate/up/down, tensor cores)",
+           "value": results[M]["tflops"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "higher_is_better": True, "dtype": "int8 (fp16 tensor operands, fp32 accumulation)",
+           "data": "synthetic", "config": {"workload": f"prefill-gate-up-down-30layers-M{M}",
+                                            "layers": args.layers, "gemms": len(items)},
+           "roofline": {"bound": "tensor", "achieved": results[M]["tflops"], "peak": peak,
+                        "peak_kind": peak_kind, "unit": "TFLOP/s",
+                        "frac": results[M]["frac_of_peak"]},
+           "by_M": results}
+    print(json.dumps(out), flush=True)
+
+
+def run_batch_sweep(args):
+    """Batched decode over the 30-layer stack: M activation rows per projection."""
+    import torch
+
+    import __graft_entry__
+    import synth
+    import bit_plane_select_gb300 as t
+    from bit_plane_select_gb300.stack import TernaryStack
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    Mmax = max(synth.BATCH_SWEEP)
+    st = TernaryStack(dev)
+    for layer, idx, name, N, K in synth.stack_items(args.layers):
+        w = synth.stack_weights(3, layer, idx)
+        st.add(torch.from_numpy(w), float(synth.w_scale(w)), M=Mmax)
+    st.finalize()
+    for i, (layer, idx, name, N, K) in enumerate(synth.stack_items(args.layers)):
+        st.x[i].copy_(torch.from_numpy(synth.projection_acts(3, layer, idx, Mmax)))
+    st.quantize()
+    out = {}
+    for M in synth.BATCH_SWEEP:
+        plist = t.ProjList([(st.planes[i], st.specs[i][4], st.q[i][:M], st.s[i][:M], st.specs[i][2],
+                             st.y[i][:M], st.f[i][:M]) for i in range(len(st.specs))])
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ms = _timed(lambda: t.trit_gemm_many(plist, err), max(3, args.steps // M), args.warmup, stream)
+        nbytes = sum(t.payload_bytes(N, K) + M * (t.k_pad(K) + 4 + 8 * N)
+                     for _, N, K, _, _ in st.specs)
+        out[M] = {"ms_per_step": round(ms, 4), "tok_per_s": round(M / (ms * 1e-3), 1),
+                  "GBs": round(nbytes / (ms * 1e-3) / 1e9, 1), "err_flag": int(err.item())}
+    print(json.dumps({"metric": "batched ternary decode over the 30-layer stack",
+                      "unit": "tok/s", "value": out[Mmax]["tok_per_s"],
+                      "config": {"workload": "bitnet-2b4t-30layer-batch-sweep"}, "by_M": out}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,11 +554,18 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=90.0)
+    ap.add_argument("--workload", choices=["decode", "prefill", "batch"], default="decode",
+                    help="decode (default): the 30-layer batch-1 stack; prefill and batch "
+                         "print extra lines for the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
+    elif args.workload == "batch":
+        run_batch_sweep(args)
     else:
         run_ours(args)
 

@@ -9,8 +9,12 @@
 // 2^24 (the host sends K < 131072 here), so no fp32 addition rounds.  (The
 // int8 tensor-core kind is not available on sm_103a.)
 //
-// Tile: 128 activation rows (TMEM lanes) x 256 weight rows (MMA N); one beat of
-// 64 columns per pipeline stage, four stages.  Warps 0-7 produce each stage:
+// Tile: 256 activation rows (two 128-row MMA sub-tiles, two TMEM accumulators
+// of 256 columns) x 256 weight rows (MMA N): every expanded weight stage feeds
+// both sub-tiles.  One beat of 64 columns per pipeline stage, two operand stages.  Raw inputs (the beat
+// of each weight row, the int8 activation halves) arrive kRaw stages ahead by
+// 16-byte cp.async copies, each thread copying only what it later converts.
+// Warps 0-15 produce each stage:
 //   - weights: the beat (pos, neg words) is expanded to 64 fp16 values, two per
 //     32-bit word -- (P & m_s) * (0x3C00 >> s) puts +1.0 (0x3C00) in each half
 //     whose bit is set (-1.0 = 0xBC00 likewise), m_s = 0x00010001 << s;
@@ -18,8 +22,8 @@
 //     minus 1152.
 // Both operands use the same column order inside a beat (word k of half h holds
 // columns 32h+k and 32h+k+16), so the contraction is unchanged.  Stores go to
-// the 128-byte-swizzled K-major layout the MMA descriptors describe.  Warp 8
-// issues the MMAs (one thread); the eight producer warps then read the
+// the 128-byte-swizzled K-major layout the MMA descriptors describe.  Warp 16
+// issues the MMAs (one thread); the sixteen producer warps then read the
 // accumulators (tcgen05.ld), convert to int32 (exact) and write y_i32 / y_f32.
 // Every mbarrier wait is bounded: after kWaitNs it sets TRIT_ERR_TIMEOUT and
 // the CTA unwinds (waiting, again bounded, for its MMAs before freeing TMEM).
@@ -28,19 +32,22 @@
 namespace trit {
 namespace {
 
-constexpr int kBM = 128;                  // activation rows per tile (TMEM lanes)
+constexpr int kBM = 256;                  // activation rows per tile: two 128-row MMA sub-tiles
+constexpr int kSubM = 128;                // rows per MMA (TMEM lanes)
 constexpr int kBN = 256;                  // weight rows per tile (MMA N)
 constexpr int kBK = 64;                   // columns per stage (one beat)
-constexpr int kStages = 4;
-constexpr int kProducerWarps = 8;
+constexpr int kStages = 2;               // MMA operand stages
+constexpr int kRaw = 4;                  // raw (plane + int8) copies in flight per producer thread
+constexpr int kProducerWarps = 16;
 constexpr int kThreads = (kProducerWarps + 1) * 32;
-constexpr int kAStage = kBM * kBK * 2;    // 16 KB of fp16
+constexpr int kAStage = kBM * kBK * 2;    // 32 KB of fp16 (two 16 KB sub-tiles)
 constexpr int kBStage = kBN * kBK * 2;    // 32 KB of fp16
 constexpr int kStage = kAStage + kBStage;
-constexpr int kTmemCols = 256;
+constexpr int kRawStage = kBN * 16 + 2 * (2 * kBM) * 16;   // 256 beats + 512 x-halves x 2 x 16 B
+constexpr int kTmemCols = 512;          // two 128 x 256 fp32 accumulators
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s
-constexpr size_t kSmemBytes = size_t(kStages) * kStage + 1024 + 256;
+constexpr size_t kSmemBytes = size_t(kStages) * kStage + size_t(kRaw) * kRawStage + 1024 + 256;
 
 struct PEntry {
     const uint4 *planes;
@@ -133,7 +140,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
 // K-major, N = 256, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(kBN >> 3) << 17) |
-                            (uint32_t(kBM >> 4) << 24);
+                            (uint32_t(kSubM >> 4) << 24);
 
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                         uint32_t accumulate) {
@@ -148,6 +155,20 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
         : "memory");
+}
+
+// 16-byte asynchronous global -> shared copy through L2; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
@@ -194,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStage);
+    uint8_t *raw = smem + kStages * kStage;   // kRaw slots of kRawStage bytes
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw + kRaw * kRawStage);
     uint64_t *empty = full + kStages;
     uint64_t *done = empty + kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
@@ -242,41 +264,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kProducerWarps) {
-        // thread p: weight row n0 + p (one beat per stage) and half (p & 1) of
-        // activation row m0 + (p >> 1)
+        // thread p: weight row n0 + p (p < 256; one beat per stage) and half
+        // (p & 1) of activation row m0 + (p >> 1) (sub-tile (p >> 1) / 128)
         const int p = threadIdx.x;
+        const bool has_w = p < kBN;
         const int64_t wn = n0 + p;
-        const bool w_ok = wn < E.N;
+        const bool w_ok = has_w && wn < E.N;
         const uint4 *wrow = E.planes + (w_ok ? wn : 0) * E.B;
         const int ar = p >> 1, ah = p & 1;
+        const int ast = ar / kSubM, arr = ar % kSubM;
         const int64_t xm = m0 + ar;
         const bool x_ok = xm < E.M;
         const int64_t kpad = int64_t(E.B) * 64;
         const uint4 *xrow = reinterpret_cast<const uint4 *>(E.x + (x_ok ? xm : 0) * kpad) + ah * 2;
         uint32_t viol = 0;
 
-        auto load = [&](int kb, uint4 &wv, uint4 &x0, uint4 &x1) {
-            wv = w_ok ? ldg_stream(wrow + kb) : make_uint4(0u, 0u, 0u, 0u);
-            if (x_ok) {
-                x0 = xrow[kb * 4];
-                x1 = xrow[kb * 4 + 1];
-            } else {
-                x0 = x1 = make_uint4(0u, 0u, 0u, 0u);
-            }
+        // raw slot layout: [256 beats][512 x-low halves][512 x-high halves], 16 B each;
+        // every thread copies and later reads only its own pieces
+        auto issue = [&](int kb) {
+            uint8_t *slot = raw + (kb % kRaw) * kRawStage;
+            if (has_w)
+                cp_async16(slot + p * 16, w_ok ? static_cast<const void *>(wrow + kb) : E.planes,
+                           w_ok ? 16u : 0u);
+            const uint4 *xs = x_ok ? xrow + kb * 4 : reinterpret_cast<const uint4 *>(E.x);
+            cp_async16(slot + kBN * 16 + p * 16, xs, x_ok ? 16u : 0u);
+            cp_async16(slot + kBN * 16 + 2 * kBM * 16 + p * 16, xs + 1, x_ok ? 16u : 0u);
         };
-        uint4 wv, x0, x1;
-        load(0, wv, x0, x1);
+#pragma unroll 1
+        for (int r = 0; r < kRaw; ++r) {
+            if (r < nk) issue(r);
+            cp_async_commit();
+        }
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % kStages;
             const uint32_t ph = uint32_t(kb / kStages) & 1u;
-            uint4 nwv, nx0, nx1;
-            if (kb + 1 < nk) load(kb + 1, nwv, nx0, nx1);
+            cp_async_wait<kRaw - 1>();
+            const uint8_t *slot = raw + (kb % kRaw) * kRawStage;
+            uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+            if (has_w) wv = *reinterpret_cast<const uint4 *>(slot + p * 16);
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(slot + kBN * 16 + p * 16);
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(slot + kBN * 16 + 2 * kBM * 16 + p * 16);
             if (!mbar_wait(&empty[s], ph ^ 1u, timed_out)) break;
             uint8_t *a_st = smem + s * kStage;
             uint8_t *b_st = a_st + kAStage;
-            viol |= (wv.x & wv.z) | (wv.y & wv.w);
-            // weights: 8 chunks of row p
-            {
+            if (has_w) {   // weights: 8 chunks of row p
+                viol |= (wv.x & wv.z) | (wv.y & wv.w);
                 uint32_t w[16];
                 expand_half(wv.x, wv.z, w);
 #pragma unroll
@@ -289,8 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     *reinterpret_cast<uint4 *>(b_st + sw128_off(p, 4 + c)) =
                         make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
             }
-            // activations: chunks 4*ah .. 4*ah + 3 of row ar, zero past column K
-            {
+            {   // activations: chunks 4*ah .. 4*ah + 3 of row arr of sub-tile ast
                 uint32_t in[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
                 const int c0 = kb * 64 + ah * 32;
                 if (c0 + 32 > E.K) {
@@ -304,21 +335,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 uint32_t w[16];
                 convert_half(in, w);
+                uint8_t *a_sub = a_st + ast * (kSubM * kBK * 2);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(a_st + sw128_off(ar, 4 * ah + c)) =
+                    *reinterpret_cast<uint4 *>(a_sub + sw128_off(arr, 4 * ah + c)) =
                         make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
             }
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[s]);
-            wv = nwv;
-            x0 = nx0;
-            x1 = nx1;
+            // the slot's data is consumed (stored above): refill it kRaw stages ahead
+            if (kb + kRaw < nk) issue(kb + kRaw);
+            cp_async_commit();
         }
+        cp_async_wait<0>();
         if (viol) atomicOr(viol_any, 1u);
     } else if (lane == 0) {
-        // MMA issue: four K-steps of 16 per stage
+        // MMA issue: two 128-row sub-tiles x four K-steps of 16 per stage
         const uint32_t base = smem_u32(smem);
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % kStages;
@@ -327,28 +360,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc_fence_after();
             const uint32_t a_addr = base + s * kStage, b_addr = a_addr + kAStage;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-                mma_f16(tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                        (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int st = 0; st < 2; ++st)
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_f16(tmem + uint32_t(st * kBN),
+                            sw128_desc(a_addr + st * (kSubM * kBK * 2) + kk * 32),
+                            sw128_desc(b_addr + kk * 32), (kb > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&empty[s]);
         }
         mma_commit(done);   // tracks every MMA issued above
     }
 
-    // epilogue: warp w reads TMEM lanes 32*(w%4).. and columns 128*(w/4)..
+    // epilogue: warp w reads sub-tile w/8, TMEM lanes 32*(w%4).. and columns
+    // 128*((w/4)%2)..; each lane owns one activation row
     if (warp < kProducerWarps) {
         const bool ok = __all_sync(~0u, mbar_wait(done, 0, timed_out));
         tc_fence_after();
-        const int q = warp & 3, ch = warp >> 2;
-        const int64_t m = m0 + 32 * q + lane;
+        const int q = warp & 3, ch = (warp >> 2) & 1, st = warp >> 3;
+        const int64_t m = m0 + st * kSubM + 32 * q + lane;
         const bool row_ok = ok && !*reinterpret_cast<volatile uint32_t *>(timed_out) && m < E.M;
         const float xs = row_ok ? E.x_scale[m] : 0.0f;
+        const bool vec = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
+                         ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
             const int col = ch * 128 + cc * 32;
             uint32_t r[32];
             if (ok) {
-                const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(col);
+                const uint32_t taddr =
+                    tmem + (uint32_t(32 * q) << 16) + uint32_t(st * kBN + col);
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
                     "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -362,13 +402,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             }
             if (row_ok) {
+                const int64_t nb = n0 + col;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int64_t n = n0 + col + i;
-                    if (n < E.N) {
-                        const int32_t y = __float2int_rn(__uint_as_float(r[i]));
-                        if (E.y_i32) E.y_i32[m * E.N + n] = y;
-                        if (E.y_f32) E.y_f32[m * E.N + n] = dequant(y, E.w_scale, xs);
+                for (int i = 0; i < 32; i += 4) {
+                    int32_t y[4];
+                    float f[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        y[k] = __float2int_rn(__uint_as_float(r[i + k]));
+                        f[k] = dequant(y[k], E.w_scale, xs);
+                    }
+                    const int64_t n = nb + i;
+                    if (vec && n + 3 < E.N) {
+                        if (E.y_i32)
+                            *reinterpret_cast<int4 *>(E.y_i32 + m * E.N + n) =
+                                make_int4(y[0], y[1], y[2], y[3]);
+                        if (E.y_f32)
+                            *reinterpret_cast<float4 *>(E.y_f32 + m * E.N + n) =
+                                make_float4(f[0], f[1], f[2], f[3]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (n + k < E.N) {
+                                if (E.y_i32) E.y_i32[m * E.N + n + k] = y[k];
+                                if (E.y_f32) E.y_f32[m * E.N + n + k] = f[k];
+                            }
+                        }
                     }
                 }
             }
