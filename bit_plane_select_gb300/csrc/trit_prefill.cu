@@ -37,13 +37,13 @@ constexpr int kSubM = 128;                // rows per MMA (TMEM lanes)
 constexpr int kBN = 256;                  // weight rows per tile (MMA N)
 constexpr int kBK = 64;                   // columns per stage (one beat)
 constexpr int kStages = 2;               // MMA operand stages
-constexpr int kRaw = 4;                  // raw (plane + int8) copies in flight per producer thread
+constexpr int kRaw = 3;                  // raw (plane + int8) copies in flight per producer thread
 constexpr int kProducerWarps = 16;
 constexpr int kThreads = (kProducerWarps + 1) * 32;
 constexpr int kAStage = kBM * kBK * 2;    // 32 KB of fp16 (two 16 KB sub-tiles)
 constexpr int kBStage = kBN * kBK * 2;    // 32 KB of fp16
 constexpr int kStage = kAStage + kBStage;
-constexpr int kRawStage = kBN * 16 + 2 * (2 * kBM) * 16;   // 256 beats + 512 x-halves x 2 x 16 B
+constexpr int kRawStage = 2 * kBN * 16 + 2 * (2 * kBM) * 16;   // 512 beats + 512 x-halves x 2 x 16 B
 constexpr int kTmemCols = 512;          // two 128 x 256 fp32 accumulators
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s
@@ -171,6 +171,23 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// 1-D bulk copy shared -> global (both 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Barrier among the producer warps only (the MMA warp does not take part).
+__device__ __forceinline__ void producers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kProducerWarps * 32) : "memory");
+}
+
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -264,14 +281,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kProducerWarps) {
-        // thread p: weight row n0 + p (p < 256; one beat per stage) and half
-        // (p & 1) of activation row m0 + (p >> 1) (sub-tile (p >> 1) / 128)
+        // thread p: half (p & 1) of weight row n0 + (p >> 1) and half (p & 1) of
+        // activation row m0 + (p >> 1) (sub-tile (p >> 1) / 128): equal work per thread
         const int p = threadIdx.x;
-        const bool has_w = p < kBN;
-        const int64_t wn = n0 + p;
-        const bool w_ok = has_w && wn < E.N;
+        const int hr = p >> 1, hh = p & 1;
+        const int64_t wn = n0 + hr;
+        const bool w_ok = wn < E.N;
         const uint4 *wrow = E.planes + (w_ok ? wn : 0) * E.B;
-        const int ar = p >> 1, ah = p & 1;
+        const int ar = hr, ah = hh;
         const int ast = ar / kSubM, arr = ar % kSubM;
         const int64_t xm = m0 + ar;
         const bool x_ok = xm < E.M;
@@ -279,16 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint4 *xrow = reinterpret_cast<const uint4 *>(E.x + (x_ok ? xm : 0) * kpad) + ah * 2;
         uint32_t viol = 0;
 
-        // raw slot layout: [256 beats][512 x-low halves][512 x-high halves], 16 B each;
-        // every thread copies and later reads only its own pieces
+        // raw slot layout: [512 beats][512 x-low halves][512 x-high halves], 16 B each
+        // (each weight row's beat is copied by both of its threads); every thread
+        // copies and later reads only its own pieces
         auto issue = [&](int kb) {
             uint8_t *slot = raw + (kb % kRaw) * kRawStage;
-            if (has_w)
-                cp_async16(slot + p * 16, w_ok ? static_cast<const void *>(wrow + kb) : E.planes,
-                           w_ok ? 16u : 0u);
+            cp_async16(slot + p * 16, w_ok ? static_cast<const void *>(wrow + kb) : E.planes,
+                       w_ok ? 16u : 0u);
             const uint4 *xs = x_ok ? xrow + kb * 4 : reinterpret_cast<const uint4 *>(E.x);
-            cp_async16(slot + kBN * 16 + p * 16, xs, x_ok ? 16u : 0u);
-            cp_async16(slot + kBN * 16 + 2 * kBM * 16 + p * 16, xs + 1, x_ok ? 16u : 0u);
+            cp_async16(slot + 2 * kBN * 16 + p * 16, xs, x_ok ? 16u : 0u);
+            cp_async16(slot + 2 * kBN * 16 + 2 * kBM * 16 + p * 16, xs + 1, x_ok ? 16u : 0u);
         };
 #pragma unroll 1
         for (int r = 0; r < kRaw; ++r) {
@@ -300,25 +317,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const uint32_t ph = uint32_t(kb / kStages) & 1u;
             cp_async_wait<kRaw - 1>();
             const uint8_t *slot = raw + (kb % kRaw) * kRawStage;
-            uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-            if (has_w) wv = *reinterpret_cast<const uint4 *>(slot + p * 16);
-            const uint4 x0 = *reinterpret_cast<const uint4 *>(slot + kBN * 16 + p * 16);
-            const uint4 x1 = *reinterpret_cast<const uint4 *>(slot + kBN * 16 + 2 * kBM * 16 + p * 16);
+            const uint4 wv = *reinterpret_cast<const uint4 *>(slot + p * 16);
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(slot + 2 * kBN * 16 + p * 16);
+            const uint4 x1 =
+                *reinterpret_cast<const uint4 *>(slot + 2 * kBN * 16 + 2 * kBM * 16 + p * 16);
             if (!mbar_wait(&empty[s], ph ^ 1u, timed_out)) break;
             uint8_t *a_st = smem + s * kStage;
             uint8_t *b_st = a_st + kAStage;
-            if (has_w) {   // weights: 8 chunks of row p
-                viol |= (wv.x & wv.z) | (wv.y & wv.w);
+            {   // weights: chunks 4*hh .. 4*hh + 3 of row hr
+                viol |= hh ? (wv.y & wv.w) : (wv.x & wv.z);
                 uint32_t w[16];
-                expand_half(wv.x, wv.z, w);
+                expand_half(hh ? wv.y : wv.x, hh ? wv.w : wv.z, w);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(b_st + sw128_off(p, c)) =
-                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                expand_half(wv.y, wv.w, w);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(b_st + sw128_off(p, 4 + c)) =
+                    *reinterpret_cast<uint4 *>(b_st + sw128_off(hr, 4 * hh + c)) =
                         make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
             }
             {   // activations: chunks 4*ah .. 4*ah + 3 of row arr of sub-tile ast
@@ -371,64 +383,85 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mma_commit(done);   // tracks every MMA issued above
     }
 
-    // epilogue: warp w reads sub-tile w/8, TMEM lanes 32*(w%4).. and columns
-    // 128*((w/4)%2)..; each lane owns one activation row
+    // epilogue.  For each sub-tile and each output (int32, then fp32): warp w
+    // loads TMEM lanes 32*(w%4).. (one activation row per lane) and columns
+    // 64*(w/4)..+63, converts, and writes them into a padded row-major staging
+    // copy in the freed shared memory; then one 16-byte-aligned bulk copy per
+    // row writes it out asynchronously.  Without 16-byte alignment (N % 4 != 0
+    // or unaligned outputs) each lane stores its row directly.
     if (warp < kProducerWarps) {
         const bool ok = __all_sync(~0u, mbar_wait(done, 0, timed_out));
         tc_fence_after();
-        const int q = warp & 3, ch = (warp >> 2) & 1, st = warp >> 3;
-        const int64_t m = m0 + st * kSubM + 32 * q + lane;
-        const bool row_ok = ok && !*reinterpret_cast<volatile uint32_t *>(timed_out) && m < E.M;
-        const float xs = row_ok ? E.x_scale[m] : 0.0f;
-        const bool vec = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
-                         ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
+        const bool good = ok && !*reinterpret_cast<volatile uint32_t *>(timed_out);
+        const int q = warp & 3, cg = warp >> 2;
+        const int p = threadIdx.x;
+        const bool bulk = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
+                          ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
+        constexpr int kRowBytes = kBN * 4 + 16;
+        const int64_t ncols = E.N - n0 < kBN ? E.N - n0 : kBN;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-            const int col = ch * 128 + cc * 32;
-            uint32_t r[32];
-            if (ok) {
-                const uint32_t taddr =
-                    tmem + (uint32_t(32 * q) << 16) + uint32_t(st * kBN + col);
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-                    "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                    : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                      "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-                      "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
-                      "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-                      "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-                      "=r"(r[30]), "=r"(r[31])
-                    : "r"(taddr));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            }
-            if (row_ok) {
-                const int64_t nb = n0 + col;
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    int32_t y[4];
-                    float f[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        y[k] = __float2int_rn(__uint_as_float(r[i + k]));
-                        f[k] = dequant(y[k], E.w_scale, xs);
+        for (int st = 0; st < 2; ++st) {
+            const int64_t mrow0 = m0 + st * kSubM;
+            if (mrow0 >= E.M) break;
+            const int64_t m = mrow0 + 32 * q + lane;
+            const bool row_ok = good && m < E.M;
+            const float xs = row_ok ? E.x_scale[m] : 0.0f;
+#pragma unroll 1
+            for (int typ = 0; typ < 2; ++typ) {
+                int32_t *yi = typ == 0 ? E.y_i32 : nullptr;
+                float *yf = typ == 1 ? E.y_f32 : nullptr;
+                if (!yi && !yf) continue;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const int col = cg * 64 + half * 32;
+                    uint32_t r[32];
+                    if (good) {
+                        const uint32_t taddr =
+                            tmem + (uint32_t(32 * q) << 16) + uint32_t(st * kBN + col);
+                        asm volatile(
+                            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                            "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
+                            "%30,%31}, [%32];"
+                            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                              "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                              "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+                              "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),
+                              "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                            : "r"(taddr));
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                     }
-                    const int64_t n = nb + i;
-                    if (vec && n + 3 < E.N) {
-                        if (E.y_i32)
-                            *reinterpret_cast<int4 *>(E.y_i32 + m * E.N + n) =
-                                make_int4(y[0], y[1], y[2], y[3]);
-                        if (E.y_f32)
-                            *reinterpret_cast<float4 *>(E.y_f32 + m * E.N + n) =
-                                make_float4(f[0], f[1], f[2], f[3]);
-                    } else {
+                    uint32_t v[32];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            if (n + k < E.N) {
-                                if (E.y_i32) E.y_i32[m * E.N + n + k] = y[k];
-                                if (E.y_f32) E.y_f32[m * E.N + n + k] = f[k];
-                            }
-                        }
+                    for (int i = 0; i < 32; ++i) {
+                        const int32_t y = __float2int_rn(__uint_as_float(r[i]));
+                        v[i] = yi ? uint32_t(y) : __float_as_uint(dequant(y, E.w_scale, xs));
                     }
+                    if (bulk) {
+                        uint8_t *dst = smem + (32 * q + lane) * kRowBytes + col * 4;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<uint4 *>(dst + i * 4) =
+                                make_uint4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    } else if (row_ok) {
+                        uint32_t *o = yi ? reinterpret_cast<uint32_t *>(yi)
+                                         : reinterpret_cast<uint32_t *>(yf);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (n0 + col + i < E.N) o[m * E.N + n0 + col + i] = v[i];
+                    }
+                }
+                if (bulk) {
+                    fence_proxy_async();
+                    producers_sync();
+                    if (good && p < kSubM && mrow0 + p < E.M) {
+                        uint8_t *g = yi ? reinterpret_cast<uint8_t *>(yi) : reinterpret_cast<uint8_t *>(yf);
+                        bulk_store(g + ((mrow0 + p) * E.N + n0) * 4, smem + p * kRowBytes,
+                                   uint32_t(ncols * 4));
+                        bulk_commit();
+                        bulk_wait_read();   // the staging rows may be rewritten after this
+                    }
+                    producers_sync();
                 }
             }
         }
