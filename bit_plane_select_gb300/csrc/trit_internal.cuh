@@ -166,7 +166,7 @@ cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err,
 
 // M >= kPrefillMinM (and K < 2^17, where fp32 accumulation of integer partial
 // sums stays exact) runs on the tensor cores.
-constexpr int64_t kPrefillMinM = 64;
+constexpr int64_t kPrefillMinM = 17;
 bool prefill_supported(const ProjDev &p);
 cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
 

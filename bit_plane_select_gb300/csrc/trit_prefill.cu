@@ -1,4 +1,4 @@
-// Prefill: y = W x for many activation rows (M >= 64) on the 5th-generation
+// Prefill: y = W x for many activation rows (M >= 17) on the 5th-generation
 // tensor cores -- the dense-contraction case of the ternary product.
 //
 // The product y[m][n] = sum_c x[m][c] * W[n][c] ("Tritium: One Weight Format
@@ -9,22 +9,25 @@
 // 2^24 (the host sends K < 131072 here), so no fp32 addition rounds.  (The
 // int8 tensor-core kind is not available on sm_103a.)
 //
-// Tile: 256 activation rows (two 128-row MMA sub-tiles, two TMEM accumulators
-// of 256 columns) x 256 weight rows (MMA N): every expanded weight stage feeds
-// both sub-tiles.  One beat of 64 columns per pipeline stage, two operand stages.  Raw inputs (the beat
-// of each weight row, the int8 activation halves) arrive kRaw stages ahead by
-// 16-byte cp.async copies, each thread copying only what it later converts.
-// Warps 0-15 produce each stage:
-//   - weights: the beat (pos, neg words) is expanded to 64 fp16 values, two per
-//     32-bit word -- (P & m_s) * (0x3C00 >> s) puts +1.0 (0x3C00) in each half
-//     whose bit is set (-1.0 = 0xBC00 likewise), m_s = 0x00010001 << s;
-//   - activations: int8 -> fp16 by the 1024-bias trick (0x6400 | (x ^ 0x80))
-//     minus 1152.
-// Both operands use the same column order inside a beat (word k of half h holds
-// columns 32h+k and 32h+k+16), so the contraction is unchanged.  Stores go to
-// the 128-byte-swizzled K-major layout the MMA descriptors describe.  Warp 16
-// issues the MMAs (one thread); the sixteen producer warps then read the
-// accumulators (tcgen05.ld), convert to int32 (exact) and write y_i32 / y_f32.
+// Two launches per list of products:
+//  1. act_f16_kernel converts each product's int8 activations once into a
+//     temporary fp16 copy laid out as 16 KB blocks of 128 rows x one beat (64
+//     columns), each block already in the MMA's 128-byte-swizzled K-major
+//     order, with columns permuted inside the beat (word k of half h holds
+//     columns 32h+k and 32h+k+16) and zeros past column K and past row M.
+//  2. prefill_kernel: tile = 512 activation rows (four 128-row MMA sub-tiles,
+//     four TMEM accumulators of 128 columns) x 128 weight rows (MMA N); one
+//     beat per pipeline stage, two stages.  Per stage one thread brings the
+//     four activation blocks with bulk copies that complete on the stage's
+//     mbarrier; the sixteen producer warps expand the 128 weight beats to fp16
+//     +-1 in the same column order ((P & m_s) * (0x3C00 >> s) sets +1.0 in each
+//     half whose bit is set, -1.0 = 0xBC00 likewise) -- so each expanded beat
+//     feeds four sub-tiles.  One thread of warp 16 issues the MMAs; the
+//     producer warps then read the fp32 accumulators (exact integers), convert,
+//     and write them through a per-warp transpose in the freed shared memory so
+//     that stores cover whole row segments.
+// The fp16 copy of the activations is scratch memory: the host allocates it
+// stream-ordered around the two launches.
 // Every mbarrier wait is bounded: after kWaitNs it sets TRIT_ERR_TIMEOUT and
 // the CTA unwinds (waiting, again bounded, for its MMAs before freeing TMEM).
 #include "trit_internal.cuh"
@@ -32,26 +35,29 @@
 namespace trit {
 namespace {
 
-constexpr int kBM = 256;                  // activation rows per tile: two 128-row MMA sub-tiles
 constexpr int kSubM = 128;                // rows per MMA (TMEM lanes)
-constexpr int kBN = 256;                  // weight rows per tile (MMA N)
+constexpr int kSubs = 4;                  // MMA sub-tiles per tile
+constexpr int kBM = kSubM * kSubs;        // activation rows per tile
+constexpr int kBN = 128;                  // weight rows per tile (MMA N)
 constexpr int kBK = 64;                   // columns per stage (one beat)
-constexpr int kStages = 2;               // MMA operand stages
-constexpr int kRaw = 3;                  // raw (plane + int8) copies in flight per producer thread
+constexpr int kStages = 2;                // MMA operand stages
+constexpr int kRaw = 4;                   // plane beats in flight per producer thread
 constexpr int kProducerWarps = 16;
 constexpr int kThreads = (kProducerWarps + 1) * 32;
-constexpr int kAStage = kBM * kBK * 2;    // 32 KB of fp16 (two 16 KB sub-tiles)
-constexpr int kBStage = kBN * kBK * 2;    // 32 KB of fp16
+constexpr int kBlock = kSubM * kBK * 2;   // one 16 KB activation block (fp16)
+constexpr int kAStage = kSubs * kBlock;   // 64 KB
+constexpr int kBStage = kBN * kBK * 2;    // 16 KB
 constexpr int kStage = kAStage + kBStage;
-constexpr int kRawStage = 2 * kBN * 16 + 2 * (2 * kBM) * 16;   // 512 beats + 512 x-halves x 2 x 16 B
-constexpr int kTmemCols = 512;          // two 128 x 256 fp32 accumulators
+constexpr int kRawStage = kProducerWarps * 32 * 16;   // one beat copy per producer thread
+constexpr int kTmemCols = kSubs * kBN;    // 512: four 128 x 128 fp32 accumulators
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s
 constexpr size_t kSmemBytes = size_t(kStages) * kStage + size_t(kRaw) * kRawStage + 1024 + 256;
+static_assert(kProducerWarps * 32 == 4 * kBN, "four producer threads per weight beat");
 
 struct PEntry {
     const uint4 *planes;
-    const int8_t *x;        // [M][K_pad]
+    const uint8_t *xh;      // blocked fp16 activations: [mblocks][B][kBlock bytes]
     const float *x_scale;
     int32_t *y_i32;
     float *y_f32;
@@ -59,8 +65,8 @@ struct PEntry {
     int64_t tile_begin;     // prefix sum of tiles over the list
     int32_t K, B;
     int32_t mtiles, ntiles;
+    int32_t mblocks;        // ceil(M / 128)
     float w_scale;
-    int32_t pad_;
 };
 
 struct PList {
@@ -138,7 +144,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N = 256, M = 128.
+// K-major, N = 128, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(kBN >> 3) << 17) |
                             (uint32_t(kSubM >> 4) << 24);
 
@@ -171,21 +177,20 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// 1-D bulk copy shared -> global (both 16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_u32(ssrc)), "r"(bytes)
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Barrier among the producer warps only (the MMA warp does not take part).
-__device__ __forceinline__ void producers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kProducerWarps * 32) : "memory");
+// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned,
+// size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
@@ -200,6 +205,16 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 }
 
 // ---- producers -------------------------------------------------------------------
+
+// 8 fp16x2 words (cols 32h + k and 32h + k + 16, k = k0..k0+7, k0 = 0 or 8) of one
+// plane half; for k0 = 8 the caller passes the words shifted right by 8.
+__device__ __forceinline__ void expand_quarter(uint32_t P, uint32_t N, uint32_t (&w)[8]) {
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const uint32_t m = 0x00010001u << s;
+        w[s] = (P & m) * (0x3C00u >> s) + (N & m) * (0xBC00u >> s);
+    }
+}
 
 // 16 fp16x2 words (cols 32h + k and 32h + k + 16, k = 0..15) of one plane half.
 __device__ __forceinline__ void expand_half(uint32_t P, uint32_t N, uint32_t (&w)[16]) {
@@ -227,6 +242,68 @@ __device__ __forceinline__ void convert_half(const uint32_t (&in)[8], uint32_t (
         }
     }
 }
+
+// ---- activation conversion: int8 [M][K_pad] -> blocked, swizzled fp16 -------------
+
+struct CEntry {
+    const int8_t *x;       // [M][K_pad]
+    uint8_t *xh;           // [mblocks][B][kBlock bytes]
+    int64_t M;
+    int64_t half_begin;    // prefix sum of mblocks*128*2*B (one thread per row half-beat)
+    int32_t K, B;
+};
+
+struct CList {
+    int32_t count;
+    int32_t pad_;
+    int64_t total;
+    CEntry e[kMaxList];
+};
+
+// One thread per (row, half-beat): 32 int8 in, 4 fp16 chunks of 16 bytes out.
+__global__ void __launch_bounds__(256) act_f16_kernel(const __grid_constant__ CList L) {
+    for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < L.total;
+         g += int64_t(gridDim.x) * blockDim.x) {
+        int a = 0, b = L.count - 1;
+        while (a < b) {
+            const int mid = (a + b + 1) >> 1;
+            if (L.e[mid].half_begin <= g) a = mid;
+            else b = mid - 1;
+        }
+        const CEntry &E = L.e[a];
+        const int64_t i = g - E.half_begin;
+        const int64_t halves_per_row = 2 * int64_t(E.B);
+        const int64_t m = i / halves_per_row;
+        const int hb = int(i - m * halves_per_row);     // half-beat index along the row
+        const int kb = hb >> 1, h = hb & 1;
+        uint32_t in[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        const int c0 = hb * 32;
+        if (m < E.M) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(E.x + m * (int64_t(E.B) * 64) + c0);
+            const uint4 u0 = src[0], u1 = src[1];
+            in[0] = u0.x; in[1] = u0.y; in[2] = u0.z; in[3] = u0.w;
+            in[4] = u1.x; in[5] = u1.y; in[6] = u1.z; in[7] = u1.w;
+            if (c0 + 32 > E.K) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int lim = E.K - (c0 + 4 * q);
+                    const uint32_t keep = lim >= 4 ? 0xFFFFFFFFu : (lim <= 0 ? 0u : ((1u << (8 * lim)) - 1u));
+                    in[q] &= keep;
+                }
+            }
+        }
+        uint32_t w[16];
+        convert_half(in, w);   // rows past M hold x = 0 and convert to +0.0
+        const int r = int(m % kSubM);
+        uint8_t *blk = E.xh + ((m / kSubM) * E.B + kb) * int64_t(kBlock);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4 *>(blk + sw128_off(r, 4 * h + c)) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+}
+
+// ---- the tensor-core product ---------------------------------------------------------
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PList L) {
     extern __shared__ uint8_t smem_raw[];
@@ -258,10 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int64_t mt = tl / E.ntiles, nt = tl - mt * E.ntiles;
     const int64_t m0 = mt * kBM, n0 = nt * kBN;
     const int nk = E.B;
+    const int nsub = int(E.mblocks - mt * kSubs < kSubs ? E.mblocks - mt * kSubs : kSubs);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], kProducerWarps);
+            mbar_init(&full[s], kProducerWarps + 1);   // 16 warps + the expect_tx arrival
             mbar_init(&empty[s], 1);
         }
         mbar_init(done, 1);
@@ -281,31 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kProducerWarps) {
-        // thread p: half (p & 1) of weight row n0 + (p >> 1) and half (p & 1) of
-        // activation row m0 + (p >> 1) (sub-tile (p >> 1) / 128): equal work per thread
+        // thread p: quarter (p & 3) of weight row n0 + (p >> 2)
         const int p = threadIdx.x;
-        const int hr = p >> 1, hh = p & 1;
-        const int64_t wn = n0 + hr;
+        const int br = p >> 2, bq = p & 3;
+        const int bh = bq >> 1, bk8 = bq & 1;   // plane half, and k range 8*bk8 .. 8*bk8+7
+        const int64_t wn = n0 + br;
         const bool w_ok = wn < E.N;
         const uint4 *wrow = E.planes + (w_ok ? wn : 0) * E.B;
-        const int ar = hr, ah = hh;
-        const int ast = ar / kSubM, arr = ar % kSubM;
-        const int64_t xm = m0 + ar;
-        const bool x_ok = xm < E.M;
-        const int64_t kpad = int64_t(E.B) * 64;
-        const uint4 *xrow = reinterpret_cast<const uint4 *>(E.x + (x_ok ? xm : 0) * kpad) + ah * 2;
+        const uint8_t *xblk = E.xh + (mt * kSubs) * int64_t(E.B) * kBlock;   // block (mt*4, 0)
         uint32_t viol = 0;
-
-        // raw slot layout: [512 beats][512 x-low halves][512 x-high halves], 16 B each
-        // (each weight row's beat is copied by both of its threads); every thread
-        // copies and later reads only its own pieces
         auto issue = [&](int kb) {
             uint8_t *slot = raw + (kb % kRaw) * kRawStage;
             cp_async16(slot + p * 16, w_ok ? static_cast<const void *>(wrow + kb) : E.planes,
                        w_ok ? 16u : 0u);
-            const uint4 *xs = x_ok ? xrow + kb * 4 : reinterpret_cast<const uint4 *>(E.x);
-            cp_async16(slot + 2 * kBN * 16 + p * 16, xs, x_ok ? 16u : 0u);
-            cp_async16(slot + 2 * kBN * 16 + 2 * kBM * 16 + p * 16, xs + 1, x_ok ? 16u : 0u);
         };
 #pragma unroll 1
         for (int r = 0; r < kRaw; ++r) {
@@ -315,55 +381,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % kStages;
             const uint32_t ph = uint32_t(kb / kStages) & 1u;
-            cp_async_wait<kRaw - 1>();
-            const uint8_t *slot = raw + (kb % kRaw) * kRawStage;
-            const uint4 wv = *reinterpret_cast<const uint4 *>(slot + p * 16);
-            const uint4 x0 = *reinterpret_cast<const uint4 *>(slot + 2 * kBN * 16 + p * 16);
-            const uint4 x1 =
-                *reinterpret_cast<const uint4 *>(slot + 2 * kBN * 16 + 2 * kBM * 16 + p * 16);
             if (!mbar_wait(&empty[s], ph ^ 1u, timed_out)) break;
             uint8_t *a_st = smem + s * kStage;
             uint8_t *b_st = a_st + kAStage;
-            {   // weights: chunks 4*hh .. 4*hh + 3 of row hr
-                viol |= hh ? (wv.y & wv.w) : (wv.x & wv.z);
-                uint32_t w[16];
-                expand_half(hh ? wv.y : wv.x, hh ? wv.w : wv.z, w);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(b_st + sw128_off(hr, 4 * hh + c)) =
-                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            if (p == 0) {   // the activation blocks of this stage
+                mbar_arrive_expect_tx(&full[s], uint32_t(nsub) * kBlock);
+                for (int st = 0; st < nsub; ++st)
+                    bulk_load(a_st + st * kBlock, xblk + (int64_t(st) * E.B + kb) * kBlock, kBlock,
+                              &full[s]);
             }
-            {   // activations: chunks 4*ah .. 4*ah + 3 of row arr of sub-tile ast
-                uint32_t in[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                const int c0 = kb * 64 + ah * 32;
-                if (c0 + 32 > E.K) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int lim = E.K - (c0 + 4 * q);   // valid bytes in this word
-                        const uint32_t keep = lim >= 4 ? 0xFFFFFFFFu
-                                            : (lim <= 0 ? 0u : ((1u << (8 * lim)) - 1u));
-                        in[q] &= keep;
-                    }
-                }
-                uint32_t w[16];
-                convert_half(in, w);
-                uint8_t *a_sub = a_st + ast * (kSubM * kBK * 2);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(a_sub + sw128_off(arr, 4 * ah + c)) =
-                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            cp_async_wait<kRaw - 1>();
+            const uint4 wv = *reinterpret_cast<const uint4 *>(raw + (kb % kRaw) * kRawStage + p * 16);
+            {   // weights: chunks 4*bh + 2*bk8 and +1 of row br
+                const uint32_t P = bh ? wv.y : wv.x, Nw = bh ? wv.w : wv.z;
+                viol |= P & Nw;
+                uint32_t w[8];
+                expand_quarter(bk8 ? P >> 8 : P, bk8 ? Nw >> 8 : Nw, w);
+                const int c = 4 * bh + 2 * bk8;
+                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, c + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[s]);
-            // the slot's data is consumed (stored above): refill it kRaw stages ahead
+            // the raw slot is consumed: refill it kRaw stages ahead
             if (kb + kRaw < nk) issue(kb + kRaw);
             cp_async_commit();
         }
         cp_async_wait<0>();
         if (viol) atomicOr(viol_any, 1u);
     } else if (lane == 0) {
-        // MMA issue: two 128-row sub-tiles x four K-steps of 16 per stage
+        // MMA issue: up to four 128-row sub-tiles x four K-steps of 16 per stage
         const uint32_t base = smem_u32(smem);
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % kStages;
@@ -371,98 +419,90 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (!mbar_wait(&full[s], ph, timed_out)) break;
             tc_fence_after();
             const uint32_t a_addr = base + s * kStage, b_addr = a_addr + kAStage;
-#pragma unroll
-            for (int st = 0; st < 2; ++st)
+            for (int st = 0; st < nsub; ++st)
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_f16(tmem + uint32_t(st * kBN),
-                            sw128_desc(a_addr + st * (kSubM * kBK * 2) + kk * 32),
+                    mma_f16(tmem + uint32_t(st * kBN), sw128_desc(a_addr + st * kBlock + kk * 32),
                             sw128_desc(b_addr + kk * 32), (kb > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&empty[s]);
         }
         mma_commit(done);   // tracks every MMA issued above
     }
 
-    // epilogue.  For each sub-tile and each output (int32, then fp32): warp w
-    // loads TMEM lanes 32*(w%4).. (one activation row per lane) and columns
-    // 64*(w/4)..+63, converts, and writes them into a padded row-major staging
-    // copy in the freed shared memory; then one 16-byte-aligned bulk copy per
-    // row writes it out asynchronously.  Without 16-byte alignment (N % 4 != 0
-    // or unaligned outputs) each lane stores its row directly.
+    // epilogue.  For each sub-tile: warp w loads TMEM lanes 32*(w%4).. (one
+    // activation row per lane) and columns 32*(w/4)..+31; for each output
+    // (int32, then fp32) the lanes write their rows into the warp's own padded
+    // 32 x 32 staging tile in the freed shared memory and read it back
+    // transposed, so every store instruction writes whole 128-byte row
+    // segments (16-byte vectors when the rows are 16-byte aligned).
     if (warp < kProducerWarps) {
         const bool ok = __all_sync(~0u, mbar_wait(done, 0, timed_out));
         tc_fence_after();
         const bool good = ok && !*reinterpret_cast<volatile uint32_t *>(timed_out);
         const int q = warp & 3, cg = warp >> 2;
-        const int p = threadIdx.x;
-        const bool bulk = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
-                          ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
-        constexpr int kRowBytes = kBN * 4 + 16;
-        const int64_t ncols = E.N - n0 < kBN ? E.N - n0 : kBN;
+        const bool vec = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
+                         ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
+        constexpr int kPitch = 36;   // words per staging row: 32 + 4 of padding
+        uint32_t *sw = reinterpret_cast<uint32_t *>(smem) + warp * (32 * kPitch);
+        const int col = cg * 32;
 #pragma unroll 1
-        for (int st = 0; st < 2; ++st) {
-            const int64_t mrow0 = m0 + st * kSubM;
-            if (mrow0 >= E.M) break;
-            const int64_t m = mrow0 + 32 * q + lane;
-            const bool row_ok = good && m < E.M;
-            const float xs = row_ok ? E.x_scale[m] : 0.0f;
+        for (int st = 0; st < nsub; ++st) {
+            const int64_t mbase = m0 + st * kSubM + 32 * q;   // rows of this warp
+            const int64_t m = mbase + lane;
+            const float xs = (good && m < E.M) ? E.x_scale[m] : 0.0f;
+            uint32_t r[32];
+            if (good) {
+                const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(st * kBN + col);
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                    "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
+                    "%30,%31}, [%32];"
+                    : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                      "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                      "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+                      "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                      "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),
+                      "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                    : "r"(taddr));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = 0;
+            }
+            if (!good) continue;
 #pragma unroll 1
             for (int typ = 0; typ < 2; ++typ) {
-                int32_t *yi = typ == 0 ? E.y_i32 : nullptr;
-                float *yf = typ == 1 ? E.y_f32 : nullptr;
-                if (!yi && !yf) continue;
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    const int col = cg * 64 + half * 32;
-                    uint32_t r[32];
-                    if (good) {
-                        const uint32_t taddr =
-                            tmem + (uint32_t(32 * q) << 16) + uint32_t(st * kBN + col);
-                        asm volatile(
-                            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
-                            "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
-                            "%30,%31}, [%32];"
-                            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                              "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-                              "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-                              "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-                              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),
-                              "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                            : "r"(taddr));
-                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                uint32_t *out = typ == 0 ? reinterpret_cast<uint32_t *>(E.y_i32)
+                                         : reinterpret_cast<uint32_t *>(E.y_f32);
+                if (!out) continue;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    uint32_t v[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int32_t y = __float2int_rn(__uint_as_float(r[i + k]));
+                        v[k] = typ == 0 ? uint32_t(y) : __float_as_uint(dequant(y, E.w_scale, xs));
                     }
-                    uint32_t v[32];
+                    *reinterpret_cast<uint4 *>(sw + lane * kPitch + i) = make_uint4(v[0], v[1], v[2], v[3]);
+                }
+                __syncwarp();
+                if (vec) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int32_t y = __float2int_rn(__uint_as_float(r[i]));
-                        v[i] = yi ? uint32_t(y) : __float_as_uint(dequant(y, E.w_scale, xs));
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = it * 4 + (lane >> 3), c4 = (lane & 7) * 4;
+                        const int64_t mm = mbase + rr, n = n0 + col + c4;
+                        const uint4 val = *reinterpret_cast<const uint4 *>(sw + rr * kPitch + c4);
+                        if (mm < E.M && n < E.N)
+                            *reinterpret_cast<uint4 *>(out + mm * E.N + n) = val;
                     }
-                    if (bulk) {
-                        uint8_t *dst = smem + (32 * q + lane) * kRowBytes + col * 4;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<uint4 *>(dst + i * 4) =
-                                make_uint4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                    } else if (row_ok) {
-                        uint32_t *o = yi ? reinterpret_cast<uint32_t *>(yi)
-                                         : reinterpret_cast<uint32_t *>(yf);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (n0 + col + i < E.N) o[m * E.N + n0 + col + i] = v[i];
+                } else {
+#pragma unroll 4
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int64_t mm = mbase + rr, n = n0 + col + lane;
+                        if (mm < E.M && n < E.N) out[mm * E.N + n] = sw[rr * kPitch + lane];
                     }
                 }
-                if (bulk) {
-                    fence_proxy_async();
-                    producers_sync();
-                    if (good && p < kSubM && mrow0 + p < E.M) {
-                        uint8_t *g = yi ? reinterpret_cast<uint8_t *>(yi) : reinterpret_cast<uint8_t *>(yf);
-                        bulk_store(g + ((mrow0 + p) * E.N + n0) * 4, smem + p * kRowBytes,
-                                   uint32_t(ncols * 4));
-                        bulk_commit();
-                        bulk_wait_read();   // the staging rows may be rewritten after this
-                    }
-                    producers_sync();
-                }
+                __syncwarp();
             }
         }
     }
@@ -480,46 +520,99 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                      "r"(kTmemCols));
 }
 
+// Bytes of the blocked fp16 activation copy of one product.
+int64_t act_f16_bytes(const ProjDev &p) {
+    return ((p.M + kSubM - 1) / kSubM) * int64_t(p.B) * kBlock;
+}
+
+// Convert and multiply the products list[0..n) with their fp16 activation
+// copies at xh[i] (each act_f16_bytes long, 16-byte aligned).
+cudaError_t launch_two(const ProjDev *list, int n, uint8_t *const *xh, uint32_t *err, cudaStream_t s) {
+    static thread_local CList C;
+    static thread_local PList L;
+    C.count = n;
+    C.pad_ = 0;
+    L.count = n;
+    L.pad_ = 0;
+    L.err = err;
+    int64_t halves = 0, tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const ProjDev &p = list[i];
+        const int64_t mblocks = (p.M + kSubM - 1) / kSubM;
+        CEntry &c = C.e[i];
+        c.x = p.x;
+        c.xh = xh[i];
+        c.M = p.M;
+        c.K = p.K;
+        c.B = p.B;
+        c.half_begin = halves;
+        halves += mblocks * kSubM * 2 * int64_t(p.B);
+        PEntry &E = L.e[i];
+        E.planes = p.planes;
+        E.xh = xh[i];
+        E.x_scale = p.x_scale;
+        E.y_i32 = p.y_i32;
+        E.y_f32 = p.y_f32;
+        E.M = p.M;
+        E.N = p.N;
+        E.K = p.K;
+        E.B = p.B;
+        E.mblocks = int32_t(mblocks);
+        E.mtiles = int32_t((p.M + kBM - 1) / kBM);
+        E.ntiles = int32_t((p.N + kBN - 1) / kBN);
+        E.w_scale = p.w_scale;
+        E.tile_begin = tiles;
+        tiles += int64_t(E.mtiles) * E.ntiles;
+    }
+    C.total = halves;
+    L.total_tiles = tiles;
+    int64_t cblocks = (halves + 255) / 256;
+    const int64_t cap = int64_t(device_sm_count()) * 16;
+    cblocks = cblocks < cap ? cblocks : cap;
+    act_f16_kernel<<<int(cblocks), 256, 0, s>>>(C);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prefill_kernel<<<dim3(unsigned(tiles)), kThreads, kSmemBytes, s>>>(L);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool prefill_supported(const ProjDev &p) {
     return p.M >= kPrefillMinM && p.K < 131072;
 }
 
+// The fp16 activation copies are allocated stream-ordered (cudaMallocAsync on
+// `s`) and freed after the launches, in groups of at most kScratchGroup bytes.
 cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {
-    static thread_local PList L;
+    constexpr int64_t kScratchGroup = int64_t(1) << 30;
     cudaError_t ae = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           int(kSmemBytes));
     if (ae != cudaSuccess) return ae;
-    for (int base = 0; base < count; base += kMaxList) {
-        const int n = count - base < kMaxList ? count - base : kMaxList;
-        L.count = n;
-        L.pad_ = 0;
-        L.err = err;
-        int64_t tiles = 0;
-        for (int i = 0; i < n; ++i) {
-            const ProjDev &p = list[base + i];
-            PEntry &E = L.e[i];
-            E.planes = p.planes;
-            E.x = p.x;
-            E.x_scale = p.x_scale;
-            E.y_i32 = p.y_i32;
-            E.y_f32 = p.y_f32;
-            E.M = p.M;
-            E.N = p.N;
-            E.K = p.K;
-            E.B = p.B;
-            E.mtiles = int32_t((p.M + kBM - 1) / kBM);
-            E.ntiles = int32_t((p.N + kBN - 1) / kBN);
-            E.w_scale = p.w_scale;
-            E.pad_ = 0;
-            E.tile_begin = tiles;
-            tiles += int64_t(E.mtiles) * E.ntiles;
+    static thread_local uint8_t *xh[kMaxList];
+    int base = 0;
+    while (base < count) {
+        int n = 0;
+        int64_t bytes = 0;
+        while (base + n < count && n < kMaxList) {
+            const int64_t b = (act_f16_bytes(list[base + n]) + 255) & ~int64_t(255);
+            if (n > 0 && bytes + b > kScratchGroup) break;
+            bytes += b;
+            ++n;
         }
-        L.total_tiles = tiles;
-        prefill_kernel<<<dim3(unsigned(tiles)), kThreads, kSmemBytes, s>>>(L);
-        cudaError_t e = cudaGetLastError();
+        uint8_t *buf = nullptr;
+        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&buf), size_t(bytes), s);
         if (e != cudaSuccess) return e;
+        int64_t off = 0;
+        for (int i = 0; i < n; ++i) {
+            xh[i] = buf + off;
+            off += (act_f16_bytes(list[base + i]) + 255) & ~int64_t(255);
+        }
+        e = launch_two(list + base, n, xh, err, s);
+        cudaError_t f = cudaFreeAsync(buf, s);
+        if (e != cudaSuccess) return e;
+        if (f != cudaSuccess) return f;
+        base += n;
     }
     return cudaSuccess;
 }

@@ -26,7 +26,11 @@
  *
  * Conventions for every entry point
  *   - Data pointers are DEVICE pointers to caller-owned memory.  The library
- *     keeps no pointer after the call returns and allocates no device memory.
+ *     keeps no pointer after the call returns.  The only device memory it
+ *     allocates is the temporary fp16 copy of the activations used by the
+ *     tensor-core path of trit_gemm / trit_gemm_many (M >= 17): allocated with
+ *     cudaMallocAsync on the call's stream and freed, stream-ordered, after the
+ *     launches (failure returns TRIT_E_CUDA).
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and the
  *     call returns without synchronising; results are valid once the stream
  *     has synchronised.
@@ -151,8 +155,9 @@ TRIT_API trit_status trit_quant_act(const float *x, int64_t M, int64_t K, int8_t
  * trit_gemm -- y = W x for M activation rows (layouts above).  Integer
  * accumulation is exact (int32; every kernel gives identical bits, "Tritium
  * ..." -- CPU kernels, Verification).  The kernel is chosen by M: one row per
- * pass for M = 1, beats reused across up to 8 rows held in registers for small
- * M, and tensor cores with planes expanded to +-1 in shared memory for large M.
+ * pass for M = 1, beats reused across up to 8 rows held in registers for
+ * 2 <= M <= 16, and tensor cores with planes expanded to +-1 in shared memory
+ * for M >= 17 (K < 131072; longer rows stay on the integer path).
  *   w_scale   finite, > 0
  *   y_i32, y_f32  outputs, either may be NULL (not both)
  *   err_flag  TRIT_ERR_P1 if any beat has both bits set; the outputs of a row
