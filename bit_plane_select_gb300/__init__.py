@@ -9,7 +9,7 @@ built, or the device is not an sm_103 GPU, the calls raise.
 
 Functions carry the C names:
   trit_pack, trit_unpack, trit_verify, trit_quant_act, trit_quant_act_many,
-  trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many
+  trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many, trit_gemm_noalloc
 """
 from __future__ import annotations
 
@@ -25,7 +25,7 @@ __all__ = [
     "library_path", "lib", "payload_bytes", "k_pad", "trit_pack", "trit_unpack", "trit_verify",
     "trit_quant_act", "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
     "trit_quant_gemv_many", "ProjList", "ActList", "QProjList", "TritProj", "TritAct",
-    "TritQProj", "MAX_FUSED_K",
+    "TritQProj", "MAX_FUSED_K", "trit_gemm_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 ERR_P1 = 1
@@ -34,9 +34,10 @@ ERR_NOT_TERNARY = 4
 ERR_NONFINITE = 8
 ERR_TIMEOUT = 16
 MAX_FUSED_K = 73728
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _STATUS = {0: "TRIT_OK", 1: "TRIT_E_ARG", 2: "TRIT_E_SHAPE", 4: "TRIT_E_SCALE",
-           6: "TRIT_E_CUDA", 7: "TRIT_E_DEVICE"}
+           6: "TRIT_E_CUDA", 7: "TRIT_E_DEVICE", 8: "TRIT_E_SCRATCH"}
 
 
 class TritError(RuntimeError):
@@ -98,9 +99,10 @@ def lib():
         L.trit_gemm.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         L.trit_gemm_many.argtypes = [p, i32, p, p]
         L.trit_quant_gemv_many.argtypes = [p, i32, p, p]
+        L.trit_gemm_noalloc.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
                      "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
-                     "trit_quant_gemv_many"):
+                     "trit_quant_gemv_many", "trit_gemm_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -217,6 +219,23 @@ def trit_gemm(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale:
                            M, N, K, _dev(y_i32, torch.int32, "y_i32", True),
                            _dev(y_f32, torch.float32, "y_f32", True),
                            _dev(err_flag, torch.int32, "err_flag"), _stream(stream)), "trit_gemm")
+    return y_i32, y_f32, err_flag
+
+
+def trit_gemm_noalloc(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor,
+                      x_scale: torch.Tensor, K: int, y_i32, y_f32, err_flag, stream=None):
+    """trit_gemm through the entry point that allocates nothing: every buffer,
+    outputs and err_flag included, is the caller's (pass None for one output to
+    skip it).  Returns (y_i32, y_f32, err_flag)."""
+    N = planes.shape[0]
+    M = x_i8.shape[0] if x_i8.dim() == 2 else 1
+    _check(lib().trit_gemm_noalloc(_dev(planes, torch.uint8, "planes"), float(w_scale),
+                                   _dev(x_i8, torch.int8, "x_i8"),
+                                   _dev(x_scale, torch.float32, "x_scale"), M, N, K,
+                                   _dev(y_i32, torch.int32, "y_i32", True),
+                                   _dev(y_f32, torch.float32, "y_f32", True),
+                                   _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_gemm_noalloc")
     return y_i32, y_f32, err_flag
 
 

@@ -178,6 +178,8 @@ TRIT_API const char *trit_status_string(trit_status s) {
         case TRIT_E_SCALE: return "TRIT_E_SCALE: w_scale must be finite and > 0";
         case TRIT_E_CUDA: return "TRIT_E_CUDA: a CUDA call failed";
         case TRIT_E_DEVICE: return "TRIT_E_DEVICE: the current device is not sm_103";
+        case TRIT_E_SCRATCH:
+            return "TRIT_E_SCRATCH: the product needs more than TRIT_NOALLOC_SCRATCH_BYTES of scratch";
     }
     return "unknown trit_status";
 }
@@ -308,6 +310,37 @@ TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_
                                const float *x_scale, int64_t N, int64_t K, int32_t *y_i32,
                                float *y_f32, uint32_t *err_flag, trit_stream_t stream) {
     return trit_gemm(planes, w_scale, x_i8, x_scale, 1, N, K, y_i32, y_f32, err_flag, stream);
+}
+
+TRIT_API trit_status trit_gemm_noalloc(const uint8_t *planes, float w_scale, const int8_t *x_i8,
+                                       const float *x_scale, int64_t M, int64_t N, int64_t K,
+                                       int32_t *y_i32, float *y_f32, uint32_t *err_flag,
+                                       trit_stream_t stream) {
+    trit_proj p;
+    p.planes = planes;
+    p.x_i8 = x_i8;
+    p.x_scale = x_scale;
+    p.y_i32 = y_i32;
+    p.y_f32 = y_f32;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.w_scale = w_scale;
+    p.reserved = 0;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
+    trit_status st = check_proj(p);
+    if (st != TRIT_OK) return st;
+    const ProjDev d = to_dev(p);
+    // Only the tensor-core path uses scratch; the others allocate nothing.
+    if (!prefill_supported(d)) return run_many(&p, 1, err_flag, s);
+    if (prefill_scratch_bytes(d) > TRIT_NOALLOC_SCRATCH_BYTES) return TRIT_E_SCRATCH;
+    st = check_device();
+    if (st != TRIT_OK) return st;
+    uint8_t *xh = nullptr;
+    cudaError_t e = fixed_scratch(&xh);
+    if (e == cudaSuccess) e = launch_prefill_into(d, xh, err_flag, s);
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
 
 }  // extern "C"

@@ -169,6 +169,13 @@ cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err,
 constexpr int64_t kPrefillMinM = 17;
 bool prefill_supported(const ProjDev &p);
 cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
+// Bytes of the fp16 activation copy the tensor-core path needs for p.
+int64_t prefill_scratch_bytes(const ProjDev &p);
+// The tensor-core path for one product with its activation copy at xh
+// (prefill_scratch_bytes(p) bytes, 16-byte aligned, caller-provided).
+cudaError_t launch_prefill_into(const ProjDev &p, uint8_t *xh, uint32_t *err, cudaStream_t s);
+// This device's fixed scratch buffer (TRIT_NOALLOC_SCRATCH_BYTES long).
+cudaError_t fixed_scratch(uint8_t **out);
 
 int device_sm_count();
 

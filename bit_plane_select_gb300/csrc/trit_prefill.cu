@@ -582,6 +582,16 @@ bool prefill_supported(const ProjDev &p) {
     return p.M >= kPrefillMinM && p.K < 131072;
 }
 
+int64_t prefill_scratch_bytes(const ProjDev &p) { return act_f16_bytes(p); }
+
+cudaError_t launch_prefill_into(const ProjDev &p, uint8_t *xh, uint32_t *err, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    uint8_t *const one[1] = {xh};
+    return launch_two(&p, 1, one, err, s);
+}
+
 // The fp16 activation copies are allocated stream-ordered (cudaMallocAsync on
 // `s`) and freed after the launches, in groups of at most kScratchGroup bytes.
 cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {

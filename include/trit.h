@@ -30,7 +30,8 @@
  *     allocates is the temporary fp16 copy of the activations used by the
  *     tensor-core path of trit_gemm / trit_gemm_many (M >= 17): allocated with
  *     cudaMallocAsync on the call's stream and freed, stream-ordered, after the
- *     launches (failure returns TRIT_E_CUDA).
+ *     launches (failure returns TRIT_E_CUDA).  trit_gemm_noalloc allocates
+ *     nothing (it uses a fixed buffer instead, see there).
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and the
  *     call returns without synchronising; results are valid once the stream
  *     has synchronised.
@@ -70,7 +71,9 @@ typedef enum trit_status {
     TRIT_E_SHAPE = 2,       /* a size outside the supported range */
     TRIT_E_SCALE = 4,       /* w_scale not finite or <= 0 ("The .trit format, version 1" -- 2.2) */
     TRIT_E_CUDA = 6,        /* a CUDA runtime call or launch failed */
-    TRIT_E_DEVICE = 7       /* the current device is not an sm_103 GPU */
+    TRIT_E_DEVICE = 7,      /* the current device is not an sm_103 GPU */
+    TRIT_E_SCRATCH = 8      /* trit_gemm_noalloc: the call needs more than
+                               TRIT_NOALLOC_SCRATCH_BYTES of scratch */
 } trit_status;
 
 /* Bits of *err_flag. */
@@ -222,6 +225,47 @@ typedef struct trit_qproj {
 #define TRIT_MAX_FUSED_K 73728
 TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count,
                                           uint32_t *err_flag, trit_stream_t stream);
+
+/*
+ * trit_gemm_noalloc -- trit_gemm with the same arguments, results and error
+ * behaviour, that allocates no device memory in any form.  The methods on
+ * ternary bit planes have nothing like it; it is a service for callers that
+ * cannot let a library allocate while they run: engines that hand all device
+ * memory to their own pools or caches up front and have no headroom left for
+ * a driver allocation, and loops that must not meet an out-of-memory failure
+ * or a memory-pool growth (which may wait on the device) in the middle of a
+ * step.  trit_gemm's tensor-core path (M >= 17, K < 131072) needs a temporary
+ * fp16 copy of the activations, which trit_gemm allocates on the stream; this
+ * entry point puts that copy in one buffer of TRIT_NOALLOC_SCRATCH_BYTES that
+ * is part of the library's device image instead.  The other paths use no
+ * scratch and are those of trit_gemm.
+ *
+ *   Limit     the copy takes 16384 * ceil(M/128) * ceil(K/64) bytes when
+ *             M >= 17 and K < 131072 (0 otherwise); the call returns
+ *             TRIT_E_SCRATCH, enqueuing nothing, when that exceeds
+ *             TRIT_NOALLOC_SCRATCH_BYTES (32 MiB: ceil(M/128) * ceil(K/64)
+ *             <= 2048, e.g. M = 2048 with K <= 8192).  Split M to stay inside.
+ *   Set-up    the first call on each device looks the buffer's address up with
+ *             that device current (cudaGetSymbolAddress, which may load the
+ *             library's device image and reserve the buffer) and keeps it for
+ *             later calls.  Make that first call before any stream capture
+ *             begins.  After cudaDeviceReset the kept address is stale: do not
+ *             call this entry point again in that process.
+ *   Zeroing   *err_flag must be zero before the call, as for trit_gemm.  The
+ *             outputs and the buffer need not be: every byte of the buffer a
+ *             call reads is written earlier in the same call.
+ *   Overlap   there is one buffer per device.  Two calls on the same device
+ *             whose work can run at the same time (different streams with no
+ *             ordering between them, or host threads issuing to different
+ *             streams) race on it and give wrong results.  Calls on one stream,
+ *             or ordered by events, are safe; calls on different devices use
+ *             different buffers.
+ */
+#define TRIT_NOALLOC_SCRATCH_BYTES (32ll * 1024 * 1024)
+TRIT_API trit_status trit_gemm_noalloc(const uint8_t *planes, float w_scale, const int8_t *x_i8,
+                                       const float *x_scale, int64_t M, int64_t N, int64_t K,
+                                       int32_t *y_i32, float *y_f32, uint32_t *err_flag,
+                                       trit_stream_t stream);
 
 /* One quantisation of a list: the arguments of trit_quant_act. */
 typedef struct trit_act {
