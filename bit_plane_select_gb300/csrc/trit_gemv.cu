@@ -41,6 +41,13 @@
 // are announced to L2 with a bulk prefetch before the staging barrier, so HBM
 // streaming starts at once.
 //
+// Back-to-back launches.  Launches go out with programmatic stream
+// serialisation: a launch that follows another one of these kernels may start
+// while the first still runs (its CTAs take the SMs the first one frees), do
+// its search and L2 prefetch, and wait for the first grid to finish before it
+// reads activations or writes outputs -- the prefetch of the next token's
+// planes overlaps the tail of the current one.
+//
 // M > 1 (+-1 bytes).  Each beat is expanded once into sixteen words of bytes in
 // {+1, 0, -1} (shift + sign-replicating byte permute + one LOP3 per word) and
 // reused for every activation row held by the CTA: 16 dp4a per row.
@@ -59,7 +66,7 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 
 // Groups ahead of the one being computed that each warp bulk-prefetches into
 // L2 (0 disables: measured slower at every distance on the 30-layer stack),
-// whether the first group of each warp is prefetched before the staging
+// how many of the first groups of each warp are prefetched before the staging
 // barrier, and the register ring depths of the unrolled paths (measured: depth
 // matters little once 24 warps per SM are resident).
 #ifndef TRIT_L2_AHEAD
@@ -72,7 +79,7 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 #define TRIT_RING_108 3
 #endif
 #ifndef TRIT_PREFETCH_FIRST
-#define TRIT_PREFETCH_FIRST 1
+#define TRIT_PREFETCH_FIRST 2
 #endif
 #ifndef TRIT_COST_108
 #define TRIT_COST_108 100
@@ -475,6 +482,12 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
     const int64_t lo = int64_t(blockIdx.x) * L.total_cost / gridDim.x;
     const int64_t hi = (int64_t(blockIdx.x) + 1) * L.total_cost / gridDim.x;
     uint32_t viol = 0;
+    // A launch that follows on the stream with programmatic serialisation may
+    // start its own set-up now (search, L2 prefetch of its first planes); every
+    // CTA waits for the preceding grid (griddepcontrol.wait) before it reads
+    // activations or writes anything.
+    asm volatile("griddepcontrol.launch_dependents;");
+    bool waited = false;
 
     int e = 0;   // last entry whose cost range starts at or before lo
     {
@@ -509,6 +522,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
             prefetch_l2_bulk(E.planes + r0 * E.bstride, uint32_t((r1 - r0) * E.bstride * 16));
         }
         __syncthreads();   // the previous entry's readers are done with xs
+        if (!waited) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            waited = true;
+        }
         float xsc;
         if (MT == 1 && E.xf) {
             xsc = stage_x_fp32(E, xs, g0 == 0, L.err);
@@ -578,8 +595,17 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
     const int64_t cap = int64_t(occupancy<MT>(smem)) * device_sm_count() * TRIT_WAVES;
     const int64_t want = (groups + kWarps - 1) / kWarps;
     const int grid = int(want < cap ? (want < 1 ? 1 : want) : cap);
-    select_accumulate_kernel<MT><<<grid, kThreads, smem, s>>>(L);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, select_accumulate_kernel<MT>, L);
 }
 
 // The fp32 pass of segmented products: y_f32 = dequant(acc) where acc is the
