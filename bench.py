@@ -50,6 +50,25 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over all ranks of the process group (x itself when there is
+    no group or one rank): every replica's time, the job's time is the slowest."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rates(step_bytes: int, steps: int, total_ms: float, world: int):
+    """Whole-job GB/s and tok/s of `world` replicas that each ran `steps` steps
+    of `step_bytes` in (at most) total_ms."""
+    secs = total_ms * 1e-3
+    return world * step_bytes * steps / secs / 1e9, world * steps / secs
+
+
 # ---- clocks -----------------------------------------------------------------
 
 class ClockSampler:
@@ -222,15 +241,11 @@ def run_ours(args):
     two_quant = sum(ev2[i][0].elapsed_time(ev2[i][1]) for i in range(T)) / T
     two_prod = sum(ev2[i][1].elapsed_time(ev2[i][2]) for i in range(T)) / T
 
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev)
 
     ms_per_step = total_ms / K
     step_bytes = st.fused_bytes()
-    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9        # GB/s, whole job
-    tok_s = world * K / (total_ms * 1e-3)
+    value, tok_s = replica_rates(step_bytes, K, total_ms, world)     # whole job
     peak, peak_kind = peaks()
 
     # dominant (only) kernel of the step: the fused quantise-and-multiply launch;
@@ -261,11 +276,7 @@ def run_ours(args):
         f_host.copy_(st.f_arena, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / E
-    if world > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dev)
     h2d = st.x_arena.numel() * 4
     d2h = st.y_arena.numel() * 4 + st.f_arena.numel() * 4
 

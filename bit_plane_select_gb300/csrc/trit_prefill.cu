@@ -216,19 +216,6 @@ __device__ __forceinline__ void expand_quarter(uint32_t P, uint32_t N, uint32_t 
     }
 }
 
-// 16 fp16x2 words (cols 32h + k and 32h + k + 16, k = 0..15) of one plane half.
-__device__ __forceinline__ void expand_half(uint32_t P, uint32_t N, uint32_t (&w)[16]) {
-    const uint32_t P8 = P >> 8, N8 = N >> 8;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const int s = k & 7;
-        const uint32_t m = 0x00010001u << s;
-        const uint32_t ps = (k < 8 ? P : P8) & m;
-        const uint32_t ns = (k < 8 ? N : N8) & m;
-        w[k] = ps * (0x3C00u >> s) + ns * (0xBC00u >> s);
-    }
-}
-
 // 16 fp16x2 words of activation columns 32h..32h+31 (natural int8 words in[0..7]).
 __device__ __forceinline__ void convert_half(const uint32_t (&in)[8], uint32_t (&w)[16]) {
 #pragma unroll
