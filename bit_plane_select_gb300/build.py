@@ -32,12 +32,13 @@ def nvcc() -> str:
 
 
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _deps():
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(INCLUDE, "trit.h"))
+    deps.append(os.path.join(INCLUDE, "trit_file.h"))
     deps.append(os.path.abspath(__file__))
     return deps
 
@@ -50,7 +51,7 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile every .cu under csrc/ and link libtrit.so; returns its path."""
+    """Compile every .cu and .cpp under csrc/ and link libtrit.so; returns its path."""
     os.makedirs(OUT_DIR, exist_ok=True)
     deps = _deps()
     if not force and not _stale(LIB, deps):
@@ -59,7 +60,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     extra = ["-Xptxas", "-v"] if verbose_ptxas or os.environ.get("TRIT_PTXAS_VERBOSE") else []
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [cc] + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -9,7 +9,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "trit.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +22,7 @@ def trit():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"TRIT_API\s+[\w\s\*]+?\b(trit_\w+)\s*\(", text)))
 
 
@@ -29,7 +30,9 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act", "trit_gemv",
                      "trit_gemm", "trit_gemm_many", "trit_quant_act_many",
-                     "trit_quant_gemv_many"):
+                     "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_file_open",
+                     "trit_file_open_memory", "trit_file_verify", "trit_file_upload",
+                     "trit_fnv1a64"):
         assert required in names
 
 
