@@ -62,6 +62,9 @@ def _load():
             lib.oracle_gemm.argtypes = [p, ctypes.c_float, p, i64, p, i64, i64, i64, p, i64,
                                         p, p, p, p]
             lib.oracle_gemm_popcount.argtypes = [p, p, i64, i64, i64, i64, p]
+            lib.oracle_quant_folded.argtypes = [p, p, i64, i64, ctypes.c_double, i64, p, p, p, p]
+            lib.oracle_intmlp_quant.argtypes = [p, p, i64, i64, i64, ctypes.c_float,
+                                                ctypes.c_float, p, i64, p, p]
             _lib = lib
     return _lib
 
@@ -180,3 +183,43 @@ def gemm_popcount(payload: np.ndarray, x_i8: np.ndarray, K: int) -> np.ndarray:
     if rc:
         raise OracleReject(rc)
     return y
+
+
+def quant_folded(x: np.ndarray, g: np.ndarray, eps: float, ldq: int | None = None):
+    """Folded normalisation + quantisation: codes of x (.) g, scale absmax/rms.
+    Returns (q int8 [M, ldq], scale fp32 [M], row_err uint8 [M])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    M, K = x.shape
+    assert g.shape == (K,)
+    if ldq is None:
+        ldq = beats_per_row(K) * 64
+    q = np.empty((M, ldq), dtype=np.int8)
+    s = np.empty(M, dtype=np.float32)
+    e = np.empty(M, dtype=np.uint8)
+    u = np.empty(K, dtype=np.float32)
+    _load().oracle_quant_folded(_ptr(x), _ptr(g), M, K, float(eps), ldq, _ptr(q), _ptr(s),
+                                _ptr(e), _ptr(u))
+    return q, s, e
+
+
+def intmlp_quant(a_g: np.ndarray, a_u: np.ndarray, w_g: float, w_u: float, x_scale,
+                 ldq: int | None = None):
+    """IntMlp + absmax quantisation of the next projection's input.
+    a_g, a_u int32 [M, N]; returns (q int8 [M, ldq], h_scale fp32 [M])."""
+    a_g = np.ascontiguousarray(a_g, dtype=np.int32)
+    a_u = np.ascontiguousarray(a_u, dtype=np.int32)
+    if a_g.ndim == 1:
+        a_g, a_u = a_g[None, :], a_u[None, :]
+    M, N = a_g.shape
+    assert a_u.shape == (M, N)
+    xs = np.ascontiguousarray(np.atleast_1d(x_scale), dtype=np.float32)
+    if ldq is None:
+        ldq = beats_per_row(N) * 64
+    q = np.empty((M, ldq), dtype=np.int8)
+    h = np.empty(M, dtype=np.float32)
+    _load().oracle_intmlp_quant(_ptr(a_g), _ptr(a_u), M, N, N, ctypes.c_float(w_g),
+                                ctypes.c_float(w_u), _ptr(xs), ldq, _ptr(q), _ptr(h))
+    return q, h

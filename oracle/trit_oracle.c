@@ -337,3 +337,95 @@ int oracle_gemm_popcount(const uint8_t *payload, const int8_t *x, int64_t ldx, i
     }
     return 0;
 }
+
+/*
+ * [TRI] Numerics -- Folded.  The 1/rms of the normalisation never touches the
+ * elements: absmax codes are unchanged by a uniform positive scale, so they are
+ * the codes of u = x (.) g (the elements times the norm gains, each product one
+ * fp32 rounding), computed exactly as oracle_quant computes them, and the rms
+ * appears only in the row's scale.  Readings (the pages give neither the rms
+ * formula nor its epsilon): rms = sqrt(sum over c of x_c^2 / K + eps) in
+ * double, summed in column order; the scale is (float)(a / rms) with a = max|u|,
+ * i.e. the absmax of the normalised row.  A row with a non-finite x, g or u is
+ * rejected as in oracle_quant (codes 0, scale 0, row error 8).
+ */
+int oracle_quant_folded(const float *x, const float *g, int64_t M, int64_t K, double eps,
+                        int64_t ldq, int8_t *q, float *scale, uint8_t *row_err, float *u)
+{
+    int any = 0;
+    for (int64_t m = 0; m < M; m++) {
+        const float *xr = x + m * K;
+        double s2 = 0.0;
+        for (int64_t c = 0; c < K; c++) {
+            u[c] = xr[c] * g[c];
+            s2 += (double)xr[c] * (double)xr[c];
+        }
+        any |= oracle_quant(u, 1, K, ldq, q + m * ldq, scale + m, row_err + m);
+        if (row_err[m] == 0 && scale[m] != 0.0f) {
+            const double rms = sqrt(s2 / (double)K + eps);
+            scale[m] = (float)((double)scale[m] / rms);
+        }
+    }
+    return any;
+}
+
+/*
+ * [TRI] Numerics -- IntMlp.  With the gate output g = a_g S_g and the up output
+ * u = a_u S_u (integer products times uniform positive scales), the squared-ReLU
+ * product relu(g)^2 u equals t K with the integer t = relu(a_g)^2 a_u and
+ * K = S_g^2 S_u; it never exists in floating point.  The next projection's
+ * activations h = t K are quantised per row by absmax, and since K > 0 is
+ * uniform the codes are those of t.  Readings:
+ *   - t is formed in 128-bit integers (exact for any int32 inputs; the page
+ *     bounds it below 2^55 for its model, where it equals the i64 value);
+ *   - codes q_c = round-half-even(127 t_c / A) with A = max_c |t_c|, an exact
+ *     rational rounding (|q_c| <= 127 without a clamp); all 0 when A = 0;
+ *   - the row's scale is the absmax of h, A K, in double:
+ *     S_g = w_g * s / 127, S_u = w_u * s / 127 (s the input row's x_scale),
+ *     K = (S_g * S_g) * S_u, A as a double = hi * 2^64 + lo (its two 64-bit
+ *     halves, each converted, then summed), scale = (float)(A * K).
+ * ag, au: M rows of N int32 with row stride ld; q: M rows of ldq >= N codes,
+ * zero past N.
+ */
+typedef __int128 i128;
+
+static i128 intmlp_t(int32_t g, int32_t u)
+{
+    if (g <= 0) return 0;
+    return (i128)g * (i128)g * (i128)u;
+}
+
+static int round_ratio_127(i128 t, i128 A)
+{
+    const int neg = t < 0;
+    const i128 n = 127 * (neg ? -t : t);
+    i128 q = n / A;
+    const i128 r = n - q * A;
+    if (2 * r > A || (2 * r == A && (q & 1))) q += 1;
+    return (int)(neg ? -q : q);
+}
+
+int oracle_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t N, int64_t ld,
+                        float w_g, float w_u, const float *x_scale, int64_t ldq, int8_t *q,
+                        float *h_scale)
+{
+    for (int64_t m = 0; m < M; m++) {
+        i128 A = 0;
+        for (int64_t c = 0; c < N; c++) {
+            i128 t = intmlp_t(ag[m * ld + c], au[m * ld + c]);
+            if (t < 0) t = -t;
+            if (t > A) A = t;
+        }
+        int8_t *qr = q + m * ldq;
+        memset(qr, 0, (size_t)ldq);
+        for (int64_t c = 0; c < N && A > 0; c++)
+            qr[c] = (int8_t)round_ratio_127(intmlp_t(ag[m * ld + c], au[m * ld + c]), A);
+        const double sg = (double)w_g * (double)x_scale[m] / 127.0;
+        const double su = (double)w_u * (double)x_scale[m] / 127.0;
+        const double k = (sg * sg) * su;
+        const uint64_t hi = (uint64_t)(A >> 64), lo = (uint64_t)A;
+        const double a = (double)hi * 18446744073709551616.0 + (double)lo;
+        h_scale[m] = (float)(a * k);
+    }
+    return 0;
+}
