@@ -9,7 +9,8 @@ built, or the device is not an sm_103 GPU, the calls raise.
 
 Functions carry the C names:
   trit_pack, trit_unpack, trit_verify, trit_quant_act, trit_quant_act_many,
-  trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many, trit_gemm_noalloc
+  trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many, trit_gemm_noalloc,
+  trit_quant_act_folded, trit_intmlp_quant
 """
 from __future__ import annotations
 
@@ -26,6 +27,7 @@ __all__ = [
     "trit_quant_act", "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
     "trit_quant_gemv_many", "ProjList", "ActList", "QProjList", "TritProj", "TritAct",
     "TritQProj", "MAX_FUSED_K", "trit_gemm_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "trit_quant_act_folded", "trit_intmlp_quant",
 ]
 
 ERR_P1 = 1
@@ -100,9 +102,12 @@ def lib():
         L.trit_gemm_many.argtypes = [p, i32, p, p]
         L.trit_quant_gemv_many.argtypes = [p, i32, p, p]
         L.trit_gemm_noalloc.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
+        L.trit_quant_act_folded.argtypes = [p, p, i64, i64, f32, p, p, p, p]
+        L.trit_intmlp_quant.argtypes = [p, p, i64, i64, f32, f32, p, p, p, p]
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
                      "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
-                     "trit_quant_gemv_many", "trit_gemm_noalloc"):
+                     "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_quant_act_folded",
+                     "trit_intmlp_quant"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -237,6 +242,47 @@ def trit_gemm_noalloc(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor,
                                    _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
            "trit_gemm_noalloc")
     return y_i32, y_f32, err_flag
+
+
+def trit_quant_act_folded(x: torch.Tensor, gain: torch.Tensor, eps: float, x_i8=None,
+                          x_scale=None, err_flag=None, stream=None):
+    """Folded normalisation + quantisation: codes of x * gain, scale absmax / rms.
+    fp32 [M, K] -> (x_i8 [M, K_pad], x_scale [M], err_flag)."""
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    M, K = x.shape
+    if x_i8 is None:
+        x_i8 = torch.empty((M, k_pad(K)), dtype=torch.int8, device=x.device)
+    if x_scale is None:
+        x_scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    err_flag = _err(err_flag, x.device)
+    _check(lib().trit_quant_act_folded(_dev(x, torch.float32, "x"), _dev(gain, torch.float32, "gain"),
+                                       M, K, float(eps), _dev(x_i8, torch.int8, "x_i8"),
+                                       _dev(x_scale, torch.float32, "x_scale"),
+                                       _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_quant_act_folded")
+    return x_i8, x_scale, err_flag
+
+
+def trit_intmlp_quant(a_gate: torch.Tensor, a_up: torch.Tensor, w_scale_gate: float,
+                      w_scale_up: float, x_scale: torch.Tensor, h_i8=None, h_scale=None,
+                      stream=None):
+    """relu(a_gate)^2 * a_up kept integer, quantised for the next projection.
+    int32 [M, N] x 2 -> (h_i8 [M, N_pad], h_scale [M])."""
+    if a_gate.dim() == 1:
+        a_gate, a_up = a_gate.unsqueeze(0), a_up.unsqueeze(0)
+    M, N = a_gate.shape
+    if h_i8 is None:
+        h_i8 = torch.empty((M, k_pad(N)), dtype=torch.int8, device=a_gate.device)
+    if h_scale is None:
+        h_scale = torch.empty(M, dtype=torch.float32, device=a_gate.device)
+    _check(lib().trit_intmlp_quant(_dev(a_gate, torch.int32, "a_gate"), _dev(a_up, torch.int32, "a_up"),
+                                   M, N, float(w_scale_gate), float(w_scale_up),
+                                   _dev(x_scale, torch.float32, "x_scale"),
+                                   _dev(h_i8, torch.int8, "h_i8"),
+                                   _dev(h_scale, torch.float32, "h_scale"), _stream(stream)),
+           "trit_intmlp_quant")
+    return h_i8, h_scale
 
 
 def trit_gemv(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale: torch.Tensor,

@@ -312,6 +312,39 @@ TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_
     return trit_gemm(planes, w_scale, x_i8, x_scale, 1, N, K, y_i32, y_f32, err_flag, stream);
 }
 
+TRIT_API trit_status trit_quant_act_folded(const float *x, const float *gain, int64_t M, int64_t K,
+                                           float eps, int8_t *x_i8, float *x_scale,
+                                           uint32_t *err_flag, trit_stream_t stream) {
+    if (!x || !gain || !x_i8 || !x_scale || !err_flag || !aligned(x, 4) || !aligned(gain, 4) ||
+        !aligned(x_i8, 16) || !aligned(x_scale, 4) || !aligned(err_flag, 4))
+        return TRIT_E_ARG;
+    if (!rows_ok(M) || !cols_ok(K)) return TRIT_E_SHAPE;
+    if (!isfinite(eps) || eps < 0.0f) return TRIT_E_SCALE;
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_quant_folded(x, gain, M, K, eps, x_i8, x_scale, err_flag,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+TRIT_API trit_status trit_intmlp_quant(const int32_t *a_gate, const int32_t *a_up, int64_t M,
+                                       int64_t N, float w_scale_gate, float w_scale_up,
+                                       const float *x_scale, int8_t *h_i8, float *h_scale,
+                                       trit_stream_t stream) {
+    if (!a_gate || !a_up || !x_scale || !h_i8 || !h_scale || !aligned(a_gate, 4) ||
+        !aligned(a_up, 4) || !aligned(x_scale, 4) || !aligned(h_i8, 16) || !aligned(h_scale, 4))
+        return TRIT_E_ARG;
+    if (!rows_ok(M) || !cols_ok(N)) return TRIT_E_SHAPE;
+    if (!isfinite(w_scale_gate) || !(w_scale_gate > 0.0f) || !isfinite(w_scale_up) ||
+        !(w_scale_up > 0.0f))
+        return TRIT_E_SCALE;
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_intmlp_quant(a_gate, a_up, M, N, w_scale_gate, w_scale_up, x_scale, h_i8,
+                                        h_scale, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
 TRIT_API trit_status trit_gemm_noalloc(const uint8_t *planes, float w_scale, const int8_t *x_i8,
                                        const float *x_scale, int64_t M, int64_t N, int64_t K,
                                        int32_t *y_i32, float *y_f32, uint32_t *err_flag,

@@ -176,6 +176,11 @@ int64_t prefill_scratch_bytes(const ProjDev &p);
 cudaError_t launch_prefill_into(const ProjDev &p, uint8_t *xh, uint32_t *err, cudaStream_t s);
 // This device's fixed scratch buffer (TRIT_NOALLOC_SCRATCH_BYTES long).
 cudaError_t fixed_scratch(uint8_t **out);
+cudaError_t launch_quant_folded(const float *x, const float *g, int64_t M, int64_t K, float eps,
+                                int8_t *q, float *x_scale, uint32_t *err, cudaStream_t s);
+cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t N,
+                                float w_g, float w_u, const float *x_scale, int8_t *q,
+                                float *h_scale, cudaStream_t s);
 
 int device_sm_count();
 

@@ -1,0 +1,195 @@
+// Numerics epilogues around the ternary products ("Tritium: One Weight Format
+// for Ternary Inference ..." -- Numerics):
+//
+//  - Folded: the normalisation's 1/rms never touches the elements.  Absmax
+//    codes are unchanged by a uniform positive scale, so the codes are those of
+//    u = x (.) g, computed with the quantiser's own arithmetic, and the rms
+//    (sqrt(mean(x^2) + eps), in double) only divides the row's scale.
+//  - IntMlp: relu(g)^2 u of the gate and up outputs equals t K with the integer
+//    t = relu(a_g)^2 a_u and the uniform K = S_g^2 S_u, so the squared-ReLU
+//    stage stays integer: t is formed exactly (128-bit), the next projection's
+//    codes are round-half-even(127 t / max|t|) as an exact rational, and the
+//    row's scale is max|t| K.
+//
+// One CTA per row, two passes over the row (the second re-reads from L1/L2).
+#include "trit_internal.cuh"
+
+namespace trit {
+namespace {
+
+constexpr int kNThreads = 256;
+constexpr int kNWarps = kNThreads / 32;
+
+__device__ __forceinline__ double block_sum_f64(double v, double *red) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(~0u, v, o);
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    double s = 0.0;
+    for (int i = 0; i < kNWarps; ++i) s += red[i];   // same order in every thread
+    return s;
+}
+
+// ---- Folded ----------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kNThreads) quant_folded_kernel(const float *x, const float *g,
+                                                                 int64_t M, int64_t K, float eps,
+                                                                 int64_t ldq, int8_t *q,
+                                                                 float *x_scale, uint32_t *err) {
+    __shared__ double red[kNWarps];
+    __shared__ uint32_t redu[2][kNWarps];
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        const float *xr = x + m * K;
+        uint32_t amax = 0, bad = 0;
+        double s2 = 0.0;
+        for (int64_t c = threadIdx.x; c < K; c += kNThreads) {
+            const float xv = xr[c];
+            const float u = __fmul_rn(xv, g[c]);
+            bad |= !isfinite(u);
+            amax = max(amax, quant_abs_bits(u));
+            s2 = __dadd_rn(s2, __dmul_rn(double(xv), double(xv)));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            amax = max(amax, __shfl_xor_sync(~0u, amax, o));
+            bad |= __shfl_xor_sync(~0u, bad, o);
+        }
+        if ((threadIdx.x & 31) == 0) {
+            redu[0][threadIdx.x >> 5] = amax;
+            redu[1][threadIdx.x >> 5] = bad;
+        }
+        const double sum2 = block_sum_f64(s2, red);   // includes a barrier
+        amax = 0;
+        bad = 0;
+        for (int i = 0; i < kNWarps; ++i) {
+            amax = max(amax, redu[0][i]);
+            bad |= redu[1][i];
+        }
+        const QuantScale qs = quant_scale(amax, bad != 0);
+        int8_t *qr = q + m * ldq;
+        for (int64_t c = threadIdx.x; c < ldq; c += kNThreads)
+            qr[c] = c < K ? int8_t(quant_code(__fmul_rn(xr[c], g[c]), qs)) : int8_t(0);
+        if (threadIdx.x == 0) {
+            float s = 0.0f;
+            if (!qs.zero) {
+                const double rms = __dsqrt_rn(__dadd_rn(__ddiv_rn(sum2, double(K)), double(eps)));
+                s = __double2float_rn(__ddiv_rn(double(qs.a), rms));
+            }
+            x_scale[m] = s;
+            if (bad) atomicOr(err, TRIT_ERR_NONFINITE);
+        }
+        __syncthreads();   // red / redu reused by the next row
+    }
+}
+
+// ---- IntMlp ----------------------------------------------------------------------
+
+typedef unsigned __int128 u128;
+
+__device__ __forceinline__ u128 intmlp_abs_t(int32_t ag, int32_t au, bool &neg) {
+    neg = false;
+    if (ag <= 0 || au == 0) return 0;
+    const uint64_t g2 = uint64_t(ag) * uint64_t(ag);            // < 2^62
+    neg = au < 0;
+    const uint64_t uu = neg ? uint64_t(-int64_t(au)) : uint64_t(au);   // <= 2^31
+    return u128(g2) * u128(uu);                                  // < 2^93
+}
+
+// round-half-even(127 a / A) for 0 <= a <= A, A > 0, without a 128-bit divide:
+// the quotient is at most 127, found by a 7-step binary search.
+__device__ __forceinline__ int round_127_ratio(u128 a, u128 A) {
+    const u128 n = a * 127u;
+    int q = 0;
+#pragma unroll
+    for (int b = 64; b; b >>= 1)
+        if (u128(q + b) * A <= n) q += b;
+    const u128 r = n - u128(q) * A;
+    if (2 * r > A || (2 * r == A && (q & 1))) ++q;
+    return q;
+}
+
+__global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *ag, const int32_t *au,
+                                                                 int64_t M, int64_t N, int64_t ldq,
+                                                                 float w_g, float w_u,
+                                                                 const float *x_scale, int8_t *q,
+                                                                 float *h_scale) {
+    __shared__ uint64_t red[2][kNWarps];
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        const int32_t *gr = ag + m * N, *ur = au + m * N;
+        u128 amax = 0;
+        for (int64_t c = threadIdx.x; c < N; c += kNThreads) {
+            bool neg;
+            const u128 t = intmlp_abs_t(gr[c], ur[c], neg);
+            amax = t > amax ? t : amax;
+        }
+        uint64_t hi = uint64_t(amax >> 64), lo = uint64_t(amax);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const uint64_t h2 = __shfl_xor_sync(~0u, hi, o), l2 = __shfl_xor_sync(~0u, lo, o);
+            if (h2 > hi || (h2 == hi && l2 > lo)) {
+                hi = h2;
+                lo = l2;
+            }
+        }
+        if ((threadIdx.x & 31) == 0) {
+            red[0][threadIdx.x >> 5] = hi;
+            red[1][threadIdx.x >> 5] = lo;
+        }
+        __syncthreads();
+        hi = red[0][0];
+        lo = red[1][0];
+        for (int i = 1; i < kNWarps; ++i)
+            if (red[0][i] > hi || (red[0][i] == hi && red[1][i] > lo)) {
+                hi = red[0][i];
+                lo = red[1][i];
+            }
+        const u128 A = (u128(hi) << 64) | u128(lo);
+        int8_t *qr = q + m * ldq;
+        for (int64_t c = threadIdx.x; c < ldq; c += kNThreads) {
+            int v = 0;
+            if (c < N && A != 0) {
+                bool neg;
+                const u128 t = intmlp_abs_t(gr[c], ur[c], neg);
+                v = round_127_ratio(t, A);
+                v = neg ? -v : v;
+            }
+            qr[c] = int8_t(v);
+        }
+        if (threadIdx.x == 0) {
+            const double s = double(x_scale[m]);
+            const double sg = __ddiv_rn(__dmul_rn(double(w_g), s), 127.0);
+            const double su = __ddiv_rn(__dmul_rn(double(w_u), s), 127.0);
+            const double k = __dmul_rn(__dmul_rn(sg, sg), su);
+            const double a = __dadd_rn(__dmul_rn(__ull2double_rn(hi), 18446744073709551616.0),
+                                       __ull2double_rn(lo));
+            h_scale[m] = __double2float_rn(__dmul_rn(a, k));
+        }
+        __syncthreads();   // red reused by the next row
+    }
+}
+
+int rows_grid(int64_t M) {
+    const int64_t cap = int64_t(device_sm_count()) * 8;
+    return int(M < cap ? M : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_folded(const float *x, const float *g, int64_t M, int64_t K, float eps,
+                                int8_t *q, float *x_scale, uint32_t *err, cudaStream_t s) {
+    const int64_t ldq = beats_per_row(K) * 64;
+    quant_folded_kernel<<<rows_grid(M), kNThreads, 0, s>>>(x, g, M, K, eps, ldq, q, x_scale, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t N,
+                                float w_g, float w_u, const float *x_scale, int8_t *q,
+                                float *h_scale, cudaStream_t s) {
+    const int64_t ldq = beats_per_row(N) * 64;
+    intmlp_quant_kernel<<<rows_grid(M), kNThreads, 0, s>>>(ag, au, M, N, ldq, w_g, w_u, x_scale, q,
+                                                            h_scale);
+    return cudaGetLastError();
+}
+
+}  // namespace trit

@@ -227,6 +227,45 @@ TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count,
                                           uint32_t *err_flag, trit_stream_t stream);
 
 /*
+ * trit_quant_act_folded -- quantise the normalised activations of a layer
+ * without dividing by the rms ("Tritium ..." -- Numerics, Folded).  For each
+ * row m of x (M x K fp32, row-major) and the norm gains g (K fp32):
+ *   u = x (.) g (one fp32 rounding per element); x_i8 row m = the codes of u,
+ *   exactly as trit_quant_act computes them (absmax codes are unchanged by the
+ *   uniform factor 1/rms); x_scale[m] = max|u| / rms with
+ *   rms = sqrt(sum(x^2) / K + eps) in double, rounded once to fp32 -- the
+ *   absmax of the normalised row, so the products' dequantisation is that of
+ *   the normalised activations.
+ * eps >= 0 and finite (the pages give no value: it is the caller's).  A row
+ * whose u holds a NaN or infinity gets codes 0, scale 0 and TRIT_ERR_NONFINITE.
+ * x_i8 is M x K_pad with a zero tail, as trit_quant_act writes it.
+ */
+TRIT_API trit_status trit_quant_act_folded(const float *x, const float *gain, int64_t M, int64_t K,
+                                           float eps, int8_t *x_i8, float *x_scale,
+                                           uint32_t *err_flag, trit_stream_t stream);
+
+/*
+ * trit_intmlp_quant -- the squared-ReLU stage of the MLP, kept integer, fused
+ * with the absmax quantisation of the next projection's input ("Tritium ..."
+ * -- Numerics, IntMlp).  a_gate and a_up are the exact int32 outputs (M x N,
+ * row-major, as trit_gemm writes y_i32) of the gate and up projections of the
+ * same M input rows, whose scales are S_g = w_scale_gate * x_scale[m] / 127 and
+ * S_u = w_scale_up * x_scale[m] / 127.  For each row:
+ *   t_c = relu(a_gate_c)^2 * a_up_c, formed exactly (128-bit integers);
+ *   h_i8 row m = round-half-even(127 * t_c / max|t|), an exact rational
+ *   rounding (all 0 when max|t| = 0), zero tail to N_pad = 64 * ceil(N / 64);
+ *   h_scale[m] = max|t| * (S_g^2 * S_u) in double, rounded once to fp32 (the
+ *   absmax of relu(g)^2 u; max|t| enters as the double sum of its two 64-bit
+ *   halves).
+ * (h_i8, h_scale) are then the x_i8 / x_scale of the next projection (K' = N).
+ * w_scale_* finite and > 0.  No data errors exist here.
+ */
+TRIT_API trit_status trit_intmlp_quant(const int32_t *a_gate, const int32_t *a_up, int64_t M,
+                                       int64_t N, float w_scale_gate, float w_scale_up,
+                                       const float *x_scale, int8_t *h_i8, float *h_scale,
+                                       trit_stream_t stream);
+
+/*
  * trit_gemm_noalloc -- trit_gemm with the same arguments, results and error
  * behaviour, that allocates no device memory in any form.  The methods on
  * ternary bit planes have nothing like it; it is a service for callers that
