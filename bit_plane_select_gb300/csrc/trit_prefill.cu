@@ -15,17 +15,19 @@
 //     columns), each block already in the MMA's 128-byte-swizzled K-major
 //     order, with columns permuted inside the beat (word k of half h holds
 //     columns 32h+k and 32h+k+16) and zeros past column K and past row M.
-//  2. prefill_kernel: tile = 512 activation rows (four 128-row MMA sub-tiles,
-//     four TMEM accumulators of 128 columns) x 128 weight rows (MMA N); one
+//  2. prefill_kernel: tile = 256 activation rows (two 128-row MMA sub-tiles,
+//     two TMEM accumulators of 128 columns) x 128 weight rows (MMA N); one
 //     beat per pipeline stage, two stages.  Per stage one thread brings the
-//     four activation blocks with bulk copies that complete on the stage's
-//     mbarrier; the sixteen producer warps expand the 128 weight beats to fp16
-//     +-1 in the same column order ((P & m_s) * (0x3C00 >> s) sets +1.0 in each
-//     half whose bit is set, -1.0 = 0xBC00 likewise) -- so each expanded beat
-//     feeds four sub-tiles.  One thread of warp 16 issues the MMAs; the
-//     producer warps then read the fp32 accumulators (exact integers), convert,
-//     and write them through a per-warp transpose in the freed shared memory so
-//     that stores cover whole row segments.
+//     two activation blocks with bulk copies that complete on the stage's
+//     mbarrier; eight producer warps (two threads per weight row, half a beat
+//     each) expand the 128 weight beats to fp16 +-1 in the same column order
+//     ((P & m_s) * (0x3C00 >> s) sets +1.0 in each half whose bit is set, -1.0 =
+//     0xBC00 likewise), so each expanded beat feeds both sub-tiles.  One thread
+//     of warp 8 issues the MMAs; the producer warps then read the fp32
+//     accumulators (exact integers), convert, and write them through a per-warp
+//     transpose in the freed shared memory so that stores cover whole row
+//     segments.  Two CTAs share an SM (256 tensor-memory columns and ~106 KB of
+//     shared memory each), so one CTA's epilogue runs while the other's MMAs do.
 // The fp16 copy of the activations is scratch memory: the host allocates it
 // stream-ordered around the two launches.
 // Every mbarrier wait is bounded: after kWaitNs it sets TRIT_ERR_TIMEOUT and
@@ -36,24 +38,28 @@ namespace trit {
 namespace {
 
 constexpr int kSubM = 128;                // rows per MMA (TMEM lanes)
-constexpr int kSubs = 4;                  // MMA sub-tiles per tile
+constexpr int kSubs = 2;                  // MMA sub-tiles per tile
 constexpr int kBM = kSubM * kSubs;        // activation rows per tile
 constexpr int kBN = 128;                  // weight rows per tile (MMA N)
 constexpr int kBK = 64;                   // columns per stage (one beat)
 constexpr int kStages = 2;                // MMA operand stages
-constexpr int kRaw = 4;                   // plane beats in flight per producer thread
-constexpr int kProducerWarps = 16;
+constexpr int kRaw = 4;                   // plane half-beats in flight per producer thread
+constexpr int kProducerWarps = 8;
 constexpr int kThreads = (kProducerWarps + 1) * 32;
 constexpr int kBlock = kSubM * kBK * 2;   // one 16 KB activation block (fp16)
-constexpr int kAStage = kSubs * kBlock;   // 64 KB
+constexpr int kAStage = kSubs * kBlock;   // 32 KB
 constexpr int kBStage = kBN * kBK * 2;    // 16 KB
 constexpr int kStage = kAStage + kBStage;
-constexpr int kRawStage = kProducerWarps * 32 * 16;   // one beat copy per producer thread
-constexpr int kTmemCols = kSubs * kBN;    // 512: four 128 x 128 fp32 accumulators
+constexpr int kRawStage = kProducerWarps * 32 * 8;    // per thread: its half of pos and neg
+constexpr int kTmemCols = kSubs * kBN;    // 256: two 128 x 128 fp32 accumulators
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s
 constexpr size_t kSmemBytes = size_t(kStages) * kStage + size_t(kRaw) * kRawStage + 1024 + 256;
-static_assert(kProducerWarps * 32 == 4 * kBN, "four producer threads per weight beat");
+static_assert(kProducerWarps * 32 == 2 * kBN, "two producer threads per weight beat");
+// two CTAs share an SM (tensor memory 2 x 256 columns, shared memory 2 x ~106 KB),
+// so one CTA's epilogue overlaps the other's MMAs
+constexpr int kCtasPerSm = 2;
+static_assert(kCtasPerSm * kTmemCols <= 512, "tensor memory of the resident CTAs");
 
 struct PEntry {
     const uint4 *planes;
@@ -166,6 +172,12 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // 16-byte asynchronous global -> shared copy through L2; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// 4-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
                  "r"(src_bytes)
                  : "memory");
 }
@@ -292,7 +304,7 @@ __global__ void __launch_bounds__(256) act_f16_kernel(const __grid_constant__ CL
 
 // ---- the tensor-core product ---------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PList L) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_kernel(const __grid_constant__ PList L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -346,19 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kProducerWarps) {
-        // thread p: quarter (p & 3) of weight row n0 + (p >> 2)
+        // thread p: half (p & 1) of weight row n0 + (p >> 1)
         const int p = threadIdx.x;
-        const int br = p >> 2, bq = p & 3;
-        const int bh = bq >> 1, bk8 = bq & 1;   // plane half, and k range 8*bk8 .. 8*bk8+7
+        const int br = p >> 1, bh = p & 1;
         const int64_t wn = n0 + br;
         const bool w_ok = wn < E.N;
-        const uint4 *wrow = E.planes + (w_ok ? wn : 0) * E.B;
-        const uint8_t *xblk = E.xh + (mt * kSubs) * int64_t(E.B) * kBlock;   // block (mt*4, 0)
+        const uint8_t *wrow = reinterpret_cast<const uint8_t *>(E.planes + (w_ok ? wn : 0) * E.B);
+        const uint8_t *xblk = E.xh + (mt * kSubs) * int64_t(E.B) * kBlock;   // block (mt*kSubs, 0)
         uint32_t viol = 0;
-        auto issue = [&](int kb) {
-            uint8_t *slot = raw + (kb % kRaw) * kRawStage;
-            cp_async16(slot + p * 16, w_ok ? static_cast<const void *>(wrow + kb) : E.planes,
-                       w_ok ? 16u : 0u);
+        auto issue = [&](int kb) {   // this half's pos word and neg word of beat kb
+            uint8_t *slot = raw + (kb % kRaw) * kRawStage + p * 8;
+            const uint8_t *beat = wrow + int64_t(kb) * 16;
+            cp_async4(slot, beat + 4 * bh, w_ok ? 4u : 0u);
+            cp_async4(slot + 4, beat + 8 + 4 * bh, w_ok ? 4u : 0u);
         };
 #pragma unroll 1
         for (int r = 0; r < kRaw; ++r) {
@@ -378,15 +390,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                               &full[s]);
             }
             cp_async_wait<kRaw - 1>();
-            const uint4 wv = *reinterpret_cast<const uint4 *>(raw + (kb % kRaw) * kRawStage + p * 16);
-            {   // weights: chunks 4*bh + 2*bk8 and +1 of row br
-                const uint32_t P = bh ? wv.y : wv.x, Nw = bh ? wv.w : wv.z;
-                viol |= P & Nw;
+            const uint2 pn = *reinterpret_cast<const uint2 *>(raw + (kb % kRaw) * kRawStage + p * 8);
+            viol |= pn.x & pn.y;
+            {   // weights: chunks 4*bh .. 4*bh+3 of row br
                 uint32_t w[8];
-                expand_quarter(bk8 ? P >> 8 : P, bk8 ? Nw >> 8 : Nw, w);
-                const int c = 4 * bh + 2 * bk8;
-                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, c)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, c + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+                expand_quarter(pn.x, pn.y, w);
+                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+                expand_quarter(pn.x >> 8, pn.y >> 8, w);
+                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 2)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 3)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
             fence_proxy_async();
             __syncwarp();
@@ -426,14 +439,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const bool ok = __all_sync(~0u, mbar_wait(done, 0, timed_out));
         tc_fence_after();
         const bool good = ok && !*reinterpret_cast<volatile uint32_t *>(timed_out);
-        const int q = warp & 3, cg = warp >> 2;
+        const int q = warp & 3;
         const bool vec = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
                          ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
         constexpr int kPitch = 36;   // words per staging row: 32 + 4 of padding
         uint32_t *sw = reinterpret_cast<uint32_t *>(smem) + warp * (32 * kPitch);
-        const int col = cg * 32;
 #pragma unroll 1
-        for (int st = 0; st < nsub; ++st) {
+        for (int sc = 0; sc < nsub * 2; ++sc) {   // (sub-tile, column group) pairs of this warp
+            const int st = sc >> 1;
+            const int cg = (warp >> 2) + 2 * (sc & 1);
+            const int col = cg * 32;
             const int64_t mbase = m0 + st * kSubM + 32 * q;   // rows of this warp
             const int64_t m = mbase + lane;
             const float xs = (good && m < E.M) ? E.x_scale[m] : 0.0f;
@@ -575,6 +590,8 @@ cudaError_t launch_prefill_into(const ProjDev &p, uint8_t *xh, uint32_t *err, cu
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     uint8_t *const one[1] = {xh};
     return launch_two(&p, 1, one, err, s);
 }
@@ -585,6 +602,8 @@ cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, c
     constexpr int64_t kScratchGroup = int64_t(1) << 30;
     cudaError_t ae = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           int(kSmemBytes));
+    if (ae != cudaSuccess) return ae;
+    ae = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (ae != cudaSuccess) return ae;
     static thread_local uint8_t *xh[kMaxList];
     int base = 0;
