@@ -255,28 +255,68 @@ def run_ours(args):
     achieved = step_bytes / (kern_avg_ms * 1e-3) / 1e9
     traffic = committed_traffic(step_bytes)
 
-    # e2e: host fp32 activations in, host y_i32 + y_f32 out, every step
+    # e2e: host fp32 activations in, host y_i32 + y_f32 out, every step.  Two
+    # buffer sets (twin stacks over the same planes) and three streams: the
+    # copy in of step i+1 and the copy out of step i-1 run while step i
+    # computes; every step still moves its own inputs and outputs.
+    sts = [st, st.twin()]
     x_host = st.x_arena.cpu().pin_memory()
-    y_host = torch.empty_like(st.y_arena, device="cpu").pin_memory()
-    f_host = torch.empty_like(st.f_arena, device="cpu").pin_memory()
+    y_host = [torch.empty_like(st.y_arena, device="cpu").pin_memory() for _ in range(2)]
+    f_host = [torch.empty_like(st.f_arena, device="cpu").pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for k in range(2):
+        ev_out[k].record(s_out)
+
+    def e2e_step(i):
+        k = i & 1
+        b = sts[k]
+        s_in.wait_event(ev_out[k])                # this slot's previous outputs are home
+        with torch.cuda.stream(s_in):
+            b.x_arena.copy_(x_host, non_blocking=True)
+        ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        b.step(stream)
+        ev_comp[k].record(stream)
+        s_out.wait_event(ev_comp[k])
+        with torch.cuda.stream(s_out):
+            y_host[k].copy_(b.y_arena, non_blocking=True)
+            f_host[k].copy_(b.f_arena, non_blocking=True)
+        ev_out[k].record(s_out)
+
     E = max(1, min(K, args.e2e_steps))
-    for _ in range(3):
-        st.x_arena.copy_(x_host, non_blocking=True)
-        st.step()
-        y_host.copy_(st.y_arena, non_blocking=True)
-        f_host.copy_(st.f_arena, non_blocking=True)
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(E):
-        st.x_arena.copy_(x_host, non_blocking=True)
-        st.step()
-        y_host.copy_(st.y_arena, non_blocking=True)
-        f_host.copy_(st.f_arena, non_blocking=True)
+    e0.record(s_in)
+    for i in range(E):
+        e2e_step(i)
+    stream.wait_stream(s_out)
+    stream.wait_stream(s_in)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dev)
+    # the serial form for context: copy in, step, copy out on one stream
+    for _ in range(3):
+        st.x_arena.copy_(x_host, non_blocking=True)
+        st.step()
+        y_host[0].copy_(st.y_arena, non_blocking=True)
+        f_host[0].copy_(st.f_arena, non_blocking=True)
+    torch.cuda.synchronize()
+    S = max(1, min(E, 500))
+    e0.record(stream)
+    for _ in range(S):
+        st.x_arena.copy_(x_host, non_blocking=True)
+        st.step()
+        y_host[0].copy_(st.y_arena, non_blocking=True)
+        f_host[0].copy_(st.f_arena, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = e0.elapsed_time(e1) / S
     h2d = st.x_arena.numel() * 4
     d2h = st.y_arena.numel() * 4 + st.f_arena.numel() * 4
 
@@ -336,6 +376,9 @@ def run_ours(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "steps": E,
+            "pipelining": "two buffer sets; copy in of step i+1 and copy out of step i-1 "
+                          "overlap step i",
+            "serial_ms_per_step": round(serial_ms, 5),
         },
         "gpu_launches": K,
         "err_flag": err,
@@ -515,12 +558,14 @@ def run_prefill(args):
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         flops = sum(2 * M * N * K for _, _, _, N, K in items)
         ms_q = _timed(lambda: t.trit_quant_act_many(alist, err), args.steps, args.warmup, stream)
-        ms_g = _timed(lambda: t.trit_gemm_many(plist, err), args.steps, args.warmup, stream)
+        with ClockSampler(0) as clk:
+            ms_g = _timed(lambda: t.trit_gemm_many(plist, err), args.steps, args.warmup, stream)
+        clocks = clk.summary()
         results[M] = {"gemm_ms": round(ms_g, 4), "quant_ms": round(ms_q, 4),
                       "tflops": round(flops / (ms_g * 1e-3) / 1e12, 1),
                       "tok_per_s": round(M / ((ms_g + ms_q) * 1e-3), 1),
                       "frac_of_peak": round(flops / (ms_g * 1e-3) / 1e12 / peak, 4),
-                      "err_flag": int(err.item())}
+                      "err_flag": int(err.item()), "clocks": clocks}
         del alist, plist, keep, acts, projs
         torch.cuda.empty_cache()
     M = Mmax
@@ -532,7 +577,7 @@ def run_prefill(args):
            "roofline": {"bound": "tensor", "achieved": results[M]["tflops"], "peak": peak,
                         "peak_kind": peak_kind, "unit": "TFLOP/s",
                         "frac": results[M]["frac_of_peak"]},
-           "by_M": results}
+           "clocks": results[M]["clocks"], "by_M": results}
     print(json.dumps(out), flush=True)
 
 

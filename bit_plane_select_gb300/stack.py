@@ -40,6 +40,19 @@ class TernaryStack:
         self.specs.append((name, N, K, M, float(w_scale)))
         return len(self.specs) - 1
 
+    def twin(self) -> "TernaryStack":
+        """A finalized stack over the same planes with arenas of its own: two
+        twins let consecutive steps use different activation and output
+        buffers, so a step's copies can overlap the next step's products."""
+        assert self.finalized
+        t = TernaryStack.__new__(TernaryStack)
+        t.device = self.device
+        t.specs = list(self.specs)
+        t.planes = self.planes
+        t.finalized = False
+        t.finalize()
+        return t
+
     def finalize(self):
         """Allocate the arenas and build the launch lists."""
         dev = self.device
