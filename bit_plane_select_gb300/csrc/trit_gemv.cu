@@ -384,6 +384,133 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
     return viol;
 }
 
+// M > 1: groups of 16 rows.  Lane (rs, bs) takes rows 16g + rs and 16g + 8 + rs
+// at beats bs, bs + 4, ...: each beat is expanded once into +-1 bytes for both
+// rows, and every activation word read from shared memory (the dominant
+// shared-memory traffic at M > 1) serves both rows.
+constexpr int kRowsPerGroupM = 16;
+
+template <int MT>
+__device__ __forceinline__ uint32_t run_groups2(const Entry &E, const uint32_t *xs, int xs_words,
+                                                int64_t gb, int64_t ge, int rs, int bs) {
+    constexpr int D = 2;   // loads in flight per row and lane
+    const int it = E.iters;
+    const int steps = int(ge - gb) * it;
+    const int64_t N = E.N;
+    uint32_t viol = 0;
+
+    // ---- load cursor (rows past the warp's last valid row and beats past the
+    // row's last beat are clamped to valid addresses)
+    const int last_beat = E.B - 1;
+    const int64_t last_row = (ge * kRowsPerGroupM < N ? ge * kRowsPerGroupM : N) - 1;
+    int64_t lrow = gb * kRowsPerGroupM + rs;
+    auto row_at = [&](int64_t r) { return E.planes + (r < last_row ? r : last_row) * E.bstride; };
+    const uint4 *la = row_at(lrow), *lb = row_at(lrow + 8);
+    int lt = 0, loff = bs;
+    auto next_load = [&](uint4 &va, uint4 &vb) {
+        const int o = loff < last_beat ? loff : last_beat;
+        va = ldg_stream(la + o);
+        vb = ldg_stream(lb + o);
+        loff += kLanesPerRow;
+        if (++lt == it) {
+            lt = 0;
+            loff = bs;
+            lrow += kRowsPerGroupM;
+            la = row_at(lrow);
+            lb = row_at(lrow + 8);
+        }
+    };
+    uint4 ra[D], rb[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) next_load(ra[d], rb[d]);
+
+    int accA[MT], accB[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) accA[m] = accB[m] = 0;
+    int64_t row = gb * kRowsPerGroupM + rs;
+    int ct = 0;
+    const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
+    const int xbase = bs * kXBeatVec;
+    int xoff = xbase;
+
+    // bytes of w: +1 where pos, -1 (0xFF) where neg, 0 elsewhere
+    auto expand = [](const uint4 &v, uint32_t (&wl)[8], uint32_t (&wh)[8]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t nl = prmt(v.z << (7 - j), 0u, 0xBA98u);
+            const uint32_t nh = prmt(v.w << (7 - j), 0u, 0xBA98u);
+            wl[j] = ((v.x >> j) & 0x01010101u) | nl;
+            wh[j] = ((v.y >> j) & 0x01010101u) | nh;
+        }
+    };
+    auto dot16 = [](const uint4 &a0, const uint4 &a1, const uint4 &a2, const uint4 &a3,
+                    const uint32_t (&wl)[8], const uint32_t (&wh)[8], int a) {
+        a = dp4a_ss(a0.x, wl[0], a); a = dp4a_ss(a0.y, wl[1], a);
+        a = dp4a_ss(a0.z, wl[2], a); a = dp4a_ss(a0.w, wl[3], a);
+        a = dp4a_ss(a1.x, wl[4], a); a = dp4a_ss(a1.y, wl[5], a);
+        a = dp4a_ss(a1.z, wl[6], a); a = dp4a_ss(a1.w, wl[7], a);
+        a = dp4a_ss(a2.x, wh[0], a); a = dp4a_ss(a2.y, wh[1], a);
+        a = dp4a_ss(a2.z, wh[2], a); a = dp4a_ss(a2.w, wh[3], a);
+        a = dp4a_ss(a3.x, wh[4], a); a = dp4a_ss(a3.y, wh[5], a);
+        a = dp4a_ss(a3.z, wh[6], a); a = dp4a_ss(a3.w, wh[7], a);
+        return a;
+    };
+
+    auto body = [&](int slot) {
+        const uint4 va = ra[slot], vb = rb[slot];
+        next_load(ra[slot], rb[slot]);
+        viol |= (va.x & va.z) | (va.y & va.w) | (vb.x & vb.z) | (vb.y & vb.w);
+        uint32_t wlA[8], whA[8], wlB[8], whB[8];
+        expand(va, wlA, whA);
+        expand(vb, wlB, whB);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const uint4 *X = xs4 + m * (xs_words / 4) + xoff;
+            const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
+            accA[m] = dot16(a0, a1, a2, a3, wlA, whA, accA[m]);
+            accB[m] = dot16(a0, a1, a2, a3, wlB, whB, accB[m]);
+        }
+        xoff += kLanesPerRow * kXBeatVec;
+        if (++ct == it) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const int32_t ya = row_sum4(accA[m]);
+                const int32_t yb = row_sum4(accB[m]);
+                accA[m] = accB[m] = 0;
+                if (bs == 0 && m < E.mrows) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t r = row + 8 * h;
+                        const int32_t y = h ? yb : ya;
+                        if (r < N) {
+                            const int64_t o = int64_t(m) * N + r;
+                            if (E.acc) {
+                                atomicAdd(E.acc + o, y);
+                            } else {
+                                if (E.y_i32) E.y_i32[o] = y;
+                                if (E.y_f32) E.y_f32[o] = dequant(y, E.w_scale, E.x_scale[m]);
+                            }
+                        }
+                    }
+                }
+            }
+            ct = 0;
+            xoff = xbase;
+            row += kRowsPerGroupM;
+        }
+    };
+
+    int s = 0;
+    for (; s + D <= steps; s += D) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) body(d);
+    }
+#pragma unroll
+    for (int d = 0; d < D - 1; ++d)
+        if (s + d < steps) body(d);
+    return viol;
+}
+
 // M = 1 with rows of exactly 4*IT beats: the group loop is unrolled step by
 // step, so every load, shared-memory read and accumulator index is static.
 // The ring depth D divides IT, so step t of every group uses ring slot t % D;
@@ -514,10 +641,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
         const int path = (MT == 1 && E.B == 40 && E.iters == 10) ? 1
                        : (MT == 1 && E.B == 108 && E.iters == 27) ? 2 : 0;
         // start this warp's first groups streaming into L2 before the barrier
+        constexpr int kRows = MT == 1 ? kRowsPerGroup : kRowsPerGroupM;
         if (TRIT_PREFETCH_FIRST && lane == 0 && wb < we && E.B == E.bstride) {
-            const int64_t r0 = wb * kRowsPerGroup;
+            const int64_t r0 = wb * kRows;
             const int64_t ahead = TRIT_PREFETCH_FIRST;
-            int64_t r1 = (wb + ahead < we ? wb + ahead : we) * kRowsPerGroup;
+            int64_t r1 = (wb + ahead < we ? wb + ahead : we) * kRows;
             r1 = r1 < E.N ? r1 : E.N;
             prefetch_l2_bulk(E.planes + r0 * E.bstride, uint32_t((r1 - r0) * E.bstride * 16));
         }
@@ -545,7 +673,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
                     continue;
                 }
             }
-            viol |= run_groups<MT>(E, xs, L.xs_words, xsc, wb, we, rs, bs);
+            if constexpr (MT == 1)
+                viol |= run_groups<MT>(E, xs, L.xs_words, xsc, wb, we, rs, bs);
+            else
+                viol |= run_groups2<MT>(E, xs, L.xs_words, wb, we, rs, bs);
         }
     }
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
@@ -681,7 +812,9 @@ cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaS
             const int rows = int(p.M - m0 < MT ? p.M - m0 : MT);
             for (int64_t b0 = 0; b0 < p.B && e == cudaSuccess; b0 += seg_beats(MT)) {
                 const int64_t nb = p.B - b0 < seg_beats(MT) ? p.B - b0 : seg_beats(MT);
-                buf[n++] = make_entry(p, m0, rows, b0, nb, acc);
+                buf[n] = make_entry(p, m0, rows, b0, nb, acc);
+                if (MT > 1) buf[n].groups = (p.N + kRowsPerGroupM - 1) / kRowsPerGroupM;
+                ++n;
                 if (n == kMaxList) {
                     e = launch_entries<MT>(buf, n, err, s);
                     n = 0;
