@@ -18,12 +18,18 @@
 // are clamped to the last valid address (their data meets zero activations or
 // an unwritten row), so the hot loop carries no predicates.
 //
-// M = 1 (2^j-weighted masks).  For plane word P (32 columns) and j = 0..7,
-// P & (0x01010101 << j) has byte i equal to 2^j exactly when column 8i+j is
-// selected, so dp4a(X_j, P & mask_j) adds 2^j * (sum of the selected x in
-// {j, 8+j, 16+j, 24+j}).  Eight accumulators per plane, one per j, are
-// divided by 2^j (exact: each is a multiple of 2^j) only when a row ends.
-// Cost per beat: 32 AND + 32 dp4a -- no shifts, no byte-mask expansion.
+// M = 1 (two-bit codes, 4^j-weighted masks).  Column k of a beat gets the code
+// c_k = 1 + pos_k - neg_k in {0, 1, 2}, so y = sum_k c_k x_k - sum_k x_k: the
+// second sum is the activation row's own column sum, formed once while the
+// row is staged.  Bit 1 of c_k is pos_k and bit 0 is NOR(pos_k, neg_k).  From
+// the plane words P, N (32 columns) two words are built: ze holds the pairs
+// (NOR_k, pos_k) of the even columns k at bits (k, k+1), zo those of the odd
+// columns at bits (k-1, k) -- five logic instructions.  ze & (0x03030303 << 2j)
+// then has byte i equal to 4^j c_k for column k = 8i + 2j (zo: 8i + 2j + 1),
+// so one dp4a against the staged activation word of those columns covers both
+// planes.  Eight accumulators, one per (j, parity), are divided by 4^j (exact:
+// each is a multiple of 4^j) only when a row ends.  Cost per beat: 10 logic
+// instructions to build the code words, then 16 AND + 16 dp4a.
 //
 // Long rows.  The staged activations must fit in shared memory, so a product
 // whose rows exceed seg_beats(MT) beats is split into column segments.  Each
@@ -91,7 +97,7 @@ constexpr int kL2Ahead = TRIT_L2_AHEAD;
 
 // Beats per column segment for MT staged rows: MT * seg_beats * 80 bytes of
 // shared memory stay at 90 KB.  A segment takes at most 288 steps per row, so
-// the 2^j-weighted accumulators (at most 2^17 per step) stay below 2^26.
+// the 4^j-weighted accumulators (at most 2^17 per step) stay below 2^26.
 __host__ __device__ constexpr int seg_beats(int mt) { return 1152 / mt; }
 
 struct Entry {
@@ -123,11 +129,47 @@ struct List {
     Entry e[kMaxList];
 };
 
+// Code-word multiply-accumulate of one 32-column plane word pair (M = 1).
+__device__ __forceinline__ void mac_codes(uint32_t P, uint32_t N, const uint32_t (&x)[8],
+                                          int (&acc)[8]) {
+    const uint32_t nor = ~(P | N);
+    const uint32_t ze = (nor & 0x55555555u) | ((P << 1) & 0xAAAAAAAAu);
+    const uint32_t zo = ((nor >> 1) & 0x55555555u) | (P & 0xAAAAAAAAu);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t m = 0x03030303u << (2 * j);
+        acc[j] = dp4a_su(x[2 * j], ze & m, acc[j]);
+        acc[4 + j] = dp4a_su(x[2 * j + 1], zo & m, acc[4 + j]);
+    }
+}
+
+// sum_k c_k x_k of a lane from its eight 4^j-weighted accumulators.
+__device__ __forceinline__ int32_t codes_total(const int (&acc)[8]) {
+    return (acc[0] + acc[4]) + ((acc[1] + acc[5]) >> 2) + ((acc[2] + acc[6]) >> 4) +
+           ((acc[3] + acc[7]) >> 6);
+}
+
+// Column sum of the staged activation row (M = 1): each warp publishes its
+// part; every thread adds the parts after the staging barrier.
+__device__ __forceinline__ void publish_xsum(int32_t v, int32_t *s_xsum) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(~0u, v, o);
+    if ((threadIdx.x & 31) == 0) s_xsum[threadIdx.x >> 5] = v;
+}
+__device__ __forceinline__ int32_t read_xsum(const int32_t *s_xsum) {
+    int32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) s += s_xsum[i];
+    return s;
+}
+
 // Stage activation rows 0..MT-1 of entry E into shared memory, permuted, zero
 // past column K and for rows >= mrows, covering iters*4 beats.
 template <int MT>
-__device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_words) {
+__device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_words,
+                                        int32_t *s_xsum) {
     const int halves = E.iters * kLanesPerRow * 2;
+    int32_t xsum = 0;
     for (int idx = threadIdx.x; idx < halves * MT; idx += kThreads) {
         const int m = idx / halves;
         const int hb = idx - m * halves;
@@ -155,6 +197,10 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
                 }
             }
             permute_block(in, out);
+            if (MT == 1) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) xsum = dp4a_ss(in[k], 0x01010101u, xsum);
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) out[j] = 0;
@@ -163,6 +209,7 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
         reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
         reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
     }
+    if (MT == 1) publish_xsum(xsum, s_xsum);
 }
 
 // Fused path: quantise the fp32 row of entry E (K <= seg_beats(1)*64 columns)
@@ -171,7 +218,7 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
 // re-reads its half-blocks (from L1).  The owner CTA also writes the
 // natural-layout codes (zero tail to K_pad) and the scale.  Returns the scale.
 __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool owner,
-                                              uint32_t *err) {
+                                              uint32_t *err, int32_t *s_xsum) {
     __shared__ uint32_t s_red[2][kWarps];
     const int K = E.K;
     const int nhb = (K + 31) / 32;                   // half-blocks that hold columns
@@ -216,6 +263,7 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
     }
     const QuantScale qs = quant_scale(amax, bad != 0);
     const int64_t Kp = beats_per_row(K) * 64;
+    int32_t xsum = 0;
     for (int hb = threadIdx.x; hb < halves; hb += kThreads) {
         uint32_t in[8];
 #pragma unroll
@@ -223,6 +271,7 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
             const float4 f = hb < nhb ? load4(hb * 32 + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
             in[q] = pack4(quant_code(f.x, qs), quant_code(f.y, qs), quant_code(f.z, qs),
                           quant_code(f.w, qs));
+            xsum = dp4a_ss(in[q], 0x01010101u, xsum);
         }
         if (owner && E.x_i8_out && int64_t(hb) * 32 < Kp) {
             uint4 *o = reinterpret_cast<uint4 *>(E.x_i8_out + int64_t(hb) * 32);
@@ -235,6 +284,7 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
         reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
         reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
     }
+    publish_xsum(xsum, s_xsum);
     if (owner && threadIdx.x == 0) {
         if (E.x_scale) *const_cast<float *>(E.x_scale) = qs.a;
         if (bad) atomicOr(err, TRIT_ERR_NONFINITE);
@@ -251,7 +301,8 @@ __device__ __forceinline__ int32_t row_sum4(int32_t v) {
 // Process groups [gb, ge) of entry E with one warp.  Returns the OR of pos & neg.
 template <int MT>
 __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *xs, int xs_words,
-                                               float xsc, int64_t gb, int64_t ge, int rs, int bs) {
+                                               float xsc, int32_t xsum, int64_t gb, int64_t ge,
+                                               int rs, int bs) {
     const int it = E.iters;
     const int steps = int(ge - gb) * it;
     const int64_t N = E.N;
@@ -282,9 +333,9 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
     for (int d = 0; d < kDepth; ++d) ring[d] = next_load();
 
     // ---- compute cursor
-    int acc[MT == 1 ? 16 : MT];
+    int acc[MT == 1 ? 8 : MT];
 #pragma unroll
-    for (int i = 0; i < (MT == 1 ? 16 : MT); ++i) acc[i] = 0;
+    for (int i = 0; i < (MT == 1 ? 8 : MT); ++i) acc[i] = 0;
     int64_t row = gb * kRowsPerGroup + rs;
     int ct = 0;
     const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
@@ -299,14 +350,8 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
             const uint4 a0 = xs4[xoff], a1 = xs4[xoff + 1], a2 = xs4[xoff + 2], a3 = xs4[xoff + 3];
             const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t msk = 0x01010101u << j;
-                acc[j] = dp4a_su(xl[j], v.x & msk, acc[j]);
-                acc[j] = dp4a_su(xh[j], v.y & msk, acc[j]);
-                acc[8 + j] = dp4a_su(xl[j], v.z & msk, acc[8 + j]);
-                acc[8 + j] = dp4a_su(xh[j], v.w & msk, acc[8 + j]);
-            }
+            mac_codes(v.x, v.z, xl, acc);
+            mac_codes(v.y, v.w, xh, acc);
         } else {
             // bytes of w: +1 where pos, -1 (0xFF) where neg, 0 elsewhere
             uint32_t wl[8], wh[8];
@@ -336,11 +381,7 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
         xoff += kLanesPerRow * kXBeatVec;
         if (++ct == it) {
             if constexpr (MT == 1) {
-                const int32_t y = row_sum4(
-                    (acc[0] - acc[8]) + ((acc[1] - acc[9]) >> 1) + ((acc[2] - acc[10]) >> 2) +
-                    ((acc[3] - acc[11]) >> 3) + ((acc[4] - acc[12]) >> 4) +
-                    ((acc[5] - acc[13]) >> 5) + ((acc[6] - acc[14]) >> 6) +
-                    ((acc[7] - acc[15]) >> 7));
+                const int32_t y = row_sum4(codes_total(acc)) - xsum;
                 if (bs == 0 && row < N) {
                     if (E.acc) {
                         atomicAdd(E.acc + row, y);
@@ -350,7 +391,7 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = 0;
+                for (int i = 0; i < 8; ++i) acc[i] = 0;
             } else {
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
@@ -531,7 +572,7 @@ __device__ __forceinline__ int64_t fixed_last_row(const Entry &E, int64_t ge) {
 
 template <int IT, int D>
 __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs, float x_scale,
-                                              int64_t gb, int64_t ge, int rs, int bs) {
+                                              int32_t xsum, int64_t gb, int64_t ge, int rs, int bs) {
     static_assert(IT % D == 0, "ring depth must divide the steps of a row");
     const int64_t N = E.N;
     int32_t *const y_i32 = E.y_i32;
@@ -556,9 +597,9 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
             if (r0 < r1)
                 prefetch_l2_bulk(E.planes + r0 * E.bstride, uint32_t((r1 - r0) * E.bstride * 16));
         }
-        int acc[16];
+        int acc[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0;
+        for (int i = 0; i < 8; ++i) acc[i] = 0;
 #pragma unroll
         for (int t = 0; t < IT; ++t) {
             const uint4 v = ring[t % D];
@@ -569,19 +610,10 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
             const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
             const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t msk = 0x01010101u << j;
-                acc[j] = dp4a_su(xl[j], v.x & msk, acc[j]);
-                acc[j] = dp4a_su(xh[j], v.y & msk, acc[j]);
-                acc[8 + j] = dp4a_su(xl[j], v.z & msk, acc[8 + j]);
-                acc[8 + j] = dp4a_su(xh[j], v.w & msk, acc[8 + j]);
-            }
+            mac_codes(v.x, v.z, xl, acc);
+            mac_codes(v.y, v.w, xh, acc);
         }
-        const int32_t y = row_sum4(
-            (acc[0] - acc[8]) + ((acc[1] - acc[9]) >> 1) + ((acc[2] - acc[10]) >> 2) +
-            ((acc[3] - acc[11]) >> 3) + ((acc[4] - acc[12]) >> 4) + ((acc[5] - acc[13]) >> 5) +
-            ((acc[6] - acc[14]) >> 6) + ((acc[7] - acc[15]) >> 7));
+        const int32_t y = row_sum4(codes_total(acc)) - xsum;
         if (bs == 0 && row < N) {
             if (acc_out) {
                 atomicAdd(acc_out + row, y);
@@ -604,6 +636,7 @@ template <int MT>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
     select_accumulate_kernel(const __grid_constant__ List L) {
     extern __shared__ __align__(16) uint32_t xs[];
+    __shared__ int32_t s_xsum[kWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rs = lane / kLanesPerRow, bs = lane % kLanesPerRow;
     const int64_t lo = int64_t(blockIdx.x) * L.total_cost / gridDim.x;
@@ -656,25 +689,26 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
         }
         float xsc;
         if (MT == 1 && E.xf) {
-            xsc = stage_x_fp32(E, xs, g0 == 0, L.err);
+            xsc = stage_x_fp32(E, xs, g0 == 0, L.err, s_xsum);
         } else {
-            stage_x<MT>(E, xs, L.xs_words);
+            stage_x<MT>(E, xs, L.xs_words, s_xsum);
             xsc = E.x_scale[0];
         }
         __syncthreads();
+        const int32_t xsum = MT == 1 ? read_xsum(s_xsum) : 0;
         if (wb < we) {
             if constexpr (MT == 1) {
                 if (path == 1) {
-                    viol |= fixed_run<10, TRIT_RING_40>(E, xs, xsc, wb, we, rs, bs);
+                    viol |= fixed_run<10, TRIT_RING_40>(E, xs, xsc, xsum, wb, we, rs, bs);
                     continue;
                 }
                 if (path == 2) {
-                    viol |= fixed_run<27, TRIT_RING_108>(E, xs, xsc, wb, we, rs, bs);
+                    viol |= fixed_run<27, TRIT_RING_108>(E, xs, xsc, xsum, wb, we, rs, bs);
                     continue;
                 }
             }
             if constexpr (MT == 1)
-                viol |= run_groups<MT>(E, xs, L.xs_words, xsc, wb, we, rs, bs);
+                viol |= run_groups<MT>(E, xs, L.xs_words, xsc, xsum, wb, we, rs, bs);
             else
                 viol |= run_groups2<MT>(E, xs, L.xs_words, wb, we, rs, bs);
         }
