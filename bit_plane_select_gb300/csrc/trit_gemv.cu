@@ -54,9 +54,10 @@
 // reads activations or writes outputs -- the prefetch of the next token's
 // planes overlaps the tail of the current one.
 //
-// M > 1 (+-1 bytes).  Each beat is expanded once into sixteen words of bytes in
-// {+1, 0, -1} (shift + sign-replicating byte permute + one LOP3 per word) and
-// reused for every activation row held by the CTA: 16 dp4a per row.
+// M > 1 (code bytes).  Each beat is expanded once into sixteen words of code
+// bytes c in {0, 1, 2} (the M = 1 code words, then a shift and a mask per word:
+// 38 logic instructions per beat) and reused for every activation row held by
+// the CTA: 16 dp4a per row, then the row's column sum is subtracted.
 #include "trit_internal.cuh"
 
 namespace trit {
@@ -162,17 +163,43 @@ __device__ __forceinline__ int32_t read_xsum(const int32_t *s_xsum) {
     for (int i = 0; i < kWarps; ++i) s += s_xsum[i];
     return s;
 }
+// Column sum of staged row m of MT (the parts of the warps that staged it).
+template <int MT>
+__device__ __forceinline__ int32_t read_xsum_row(const int32_t *s_xsum, int m) {
+    constexpr int kWpr = kWarps / MT;
+    int32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < kWpr; ++i) s += s_xsum[m * kWpr + i];
+    return s;
+}
+
+// Code bytes of one 32-column plane word pair: c[j] has byte i = c of column
+// 8i + j (c = 1 + pos - neg in {0, 1, 2}), matching staged activation word j.
+__device__ __forceinline__ void code_bytes(uint32_t P, uint32_t N, uint32_t (&c)[8]) {
+    const uint32_t nor = ~(P | N);
+    const uint32_t ze = (nor & 0x55555555u) | ((P << 1) & 0xAAAAAAAAu);
+    const uint32_t zo = ((nor >> 1) & 0x55555555u) | (P & 0xAAAAAAAAu);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        c[2 * j] = (ze >> (2 * j)) & 0x03030303u;
+        c[2 * j + 1] = (zo >> (2 * j)) & 0x03030303u;
+    }
+}
 
 // Stage activation rows 0..MT-1 of entry E into shared memory, permuted, zero
-// past column K and for rows >= mrows, covering iters*4 beats.
+// past column K and for rows >= mrows, covering iters*4 beats.  Row m is
+// staged by warps m*kWarps/MT .. (m+1)*kWarps/MT - 1, each of which publishes
+// its part of the row's column sum in s_xsum[warp].
 template <int MT>
 __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_words,
                                         int32_t *s_xsum) {
+    static_assert(kWarps % MT == 0, "whole warps per staged row");
+    constexpr int kWpr = kWarps / MT;
     const int halves = E.iters * kLanesPerRow * 2;
+    const int m = (threadIdx.x >> 5) / kWpr;
     int32_t xsum = 0;
-    for (int idx = threadIdx.x; idx < halves * MT; idx += kThreads) {
-        const int m = idx / halves;
-        const int hb = idx - m * halves;
+    for (int hb = ((threadIdx.x >> 5) % kWpr) * 32 + (threadIdx.x & 31); hb < halves;
+         hb += kWpr * 32) {
         uint32_t out[8];
         if (m < E.mrows) {
             const int c0 = hb * 32;
@@ -197,10 +224,8 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
                 }
             }
             permute_block(in, out);
-            if (MT == 1) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) xsum = dp4a_ss(in[k], 0x01010101u, xsum);
-            }
+            for (int k = 0; k < 8; ++k) xsum = dp4a_ss(in[k], 0x01010101u, xsum);
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) out[j] = 0;
@@ -209,7 +234,7 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
         reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
         reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
     }
-    if (MT == 1) publish_xsum(xsum, s_xsum);
+    publish_xsum(xsum, s_xsum);
 }
 
 // Fused path: quantise the fp32 row of entry E (K <= seg_beats(1)*64 columns)
@@ -426,14 +451,15 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
 }
 
 // M > 1: groups of 16 rows.  Lane (rs, bs) takes rows 16g + rs and 16g + 8 + rs
-// at beats bs, bs + 4, ...: each beat is expanded once into +-1 bytes for both
-// rows, and every activation word read from shared memory (the dominant
+// at beats bs, bs + 4, ...: each beat is expanded once into code bytes, and
+// every activation word read from shared memory (the dominant
 // shared-memory traffic at M > 1) serves both rows.
 constexpr int kRowsPerGroupM = 16;
 
 template <int MT>
 __device__ __forceinline__ uint32_t run_groups2(const Entry &E, const uint32_t *xs, int xs_words,
-                                                int64_t gb, int64_t ge, int rs, int bs) {
+                                                const int32_t *s_xsum, int64_t gb, int64_t ge,
+                                                int rs, int bs) {
     constexpr int D = 2;   // loads in flight per row and lane
     const int it = E.iters;
     const int steps = int(ge - gb) * it;
@@ -474,26 +500,21 @@ __device__ __forceinline__ uint32_t run_groups2(const Entry &E, const uint32_t *
     const int xbase = bs * kXBeatVec;
     int xoff = xbase;
 
-    // bytes of w: +1 where pos, -1 (0xFF) where neg, 0 elsewhere
+    // code bytes c = 1 + pos - neg of the beat's columns
     auto expand = [](const uint4 &v, uint32_t (&wl)[8], uint32_t (&wh)[8]) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t nl = prmt(v.z << (7 - j), 0u, 0xBA98u);
-            const uint32_t nh = prmt(v.w << (7 - j), 0u, 0xBA98u);
-            wl[j] = ((v.x >> j) & 0x01010101u) | nl;
-            wh[j] = ((v.y >> j) & 0x01010101u) | nh;
-        }
+        code_bytes(v.x, v.z, wl);
+        code_bytes(v.y, v.w, wh);
     };
     auto dot16 = [](const uint4 &a0, const uint4 &a1, const uint4 &a2, const uint4 &a3,
                     const uint32_t (&wl)[8], const uint32_t (&wh)[8], int a) {
-        a = dp4a_ss(a0.x, wl[0], a); a = dp4a_ss(a0.y, wl[1], a);
-        a = dp4a_ss(a0.z, wl[2], a); a = dp4a_ss(a0.w, wl[3], a);
-        a = dp4a_ss(a1.x, wl[4], a); a = dp4a_ss(a1.y, wl[5], a);
-        a = dp4a_ss(a1.z, wl[6], a); a = dp4a_ss(a1.w, wl[7], a);
-        a = dp4a_ss(a2.x, wh[0], a); a = dp4a_ss(a2.y, wh[1], a);
-        a = dp4a_ss(a2.z, wh[2], a); a = dp4a_ss(a2.w, wh[3], a);
-        a = dp4a_ss(a3.x, wh[4], a); a = dp4a_ss(a3.y, wh[5], a);
-        a = dp4a_ss(a3.z, wh[6], a); a = dp4a_ss(a3.w, wh[7], a);
+        a = dp4a_su(a0.x, wl[0], a); a = dp4a_su(a0.y, wl[1], a);
+        a = dp4a_su(a0.z, wl[2], a); a = dp4a_su(a0.w, wl[3], a);
+        a = dp4a_su(a1.x, wl[4], a); a = dp4a_su(a1.y, wl[5], a);
+        a = dp4a_su(a1.z, wl[6], a); a = dp4a_su(a1.w, wl[7], a);
+        a = dp4a_su(a2.x, wh[0], a); a = dp4a_su(a2.y, wh[1], a);
+        a = dp4a_su(a2.z, wh[2], a); a = dp4a_su(a2.w, wh[3], a);
+        a = dp4a_su(a3.x, wh[4], a); a = dp4a_su(a3.y, wh[5], a);
+        a = dp4a_su(a3.z, wh[6], a); a = dp4a_su(a3.w, wh[7], a);
         return a;
     };
 
@@ -515,8 +536,9 @@ __device__ __forceinline__ uint32_t run_groups2(const Entry &E, const uint32_t *
         if (++ct == it) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                const int32_t ya = row_sum4(accA[m]);
-                const int32_t yb = row_sum4(accB[m]);
+                const int32_t xsum = read_xsum_row<MT>(s_xsum, m);
+                const int32_t ya = row_sum4(accA[m]) - xsum;
+                const int32_t yb = row_sum4(accB[m]) - xsum;
                 accA[m] = accB[m] = 0;
                 if (bs == 0 && m < E.mrows) {
 #pragma unroll
@@ -710,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
             if constexpr (MT == 1)
                 viol |= run_groups<MT>(E, xs, L.xs_words, xsc, xsum, wb, we, rs, bs);
             else
-                viol |= run_groups2<MT>(E, xs, L.xs_words, wb, we, rs, bs);
+                viol |= run_groups2<MT>(E, xs, L.xs_words, s_xsum, wb, we, rs, bs);
         }
     }
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
