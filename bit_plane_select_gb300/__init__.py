@@ -10,7 +10,7 @@ built, or the device is not an sm_103 GPU, the calls raise.
 Functions carry the C names:
   trit_pack, trit_unpack, trit_verify, trit_quant_act, trit_quant_act_many,
   trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many, trit_gemm_noalloc,
-  trit_quant_act_folded, trit_intmlp_quant
+  trit_quant_act_folded, trit_intmlp_quant, trit_check_div127
 """
 from __future__ import annotations
 
@@ -27,7 +27,7 @@ __all__ = [
     "trit_quant_act", "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
     "trit_quant_gemv_many", "ProjList", "ActList", "QProjList", "TritProj", "TritAct",
     "TritQProj", "MAX_FUSED_K", "trit_gemm_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "trit_quant_act_folded", "trit_intmlp_quant",
+    "trit_quant_act_folded", "trit_intmlp_quant", "trit_check_div127",
 ]
 
 ERR_P1 = 1
@@ -104,10 +104,11 @@ def lib():
         L.trit_gemm_noalloc.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         L.trit_quant_act_folded.argtypes = [p, p, i64, i64, f32, p, p, p, p]
         L.trit_intmlp_quant.argtypes = [p, p, i64, i64, f32, f32, p, p, p, p]
+        L.trit_check_div127.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
                      "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
                      "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_quant_act_folded",
-                     "trit_intmlp_quant"):
+                     "trit_intmlp_quant", "trit_check_div127"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -283,6 +284,14 @@ def trit_intmlp_quant(a_gate: torch.Tensor, a_up: torch.Tensor, w_scale_gate: fl
                                    _dev(h_scale, torch.float32, "h_scale"), _stream(stream)),
            "trit_intmlp_quant")
     return h_i8, h_scale
+
+
+def trit_check_div127() -> int:
+    """Number of float32 bit patterns where the library's division by 127 (used
+    by every fp32 dequantisation) differs from the IEEE divide; 0 = identical."""
+    n = ctypes.c_uint64(0)
+    _check(lib().trit_check_div127(ctypes.byref(n)), "trit_check_div127")
+    return int(n.value)
 
 
 def trit_gemv(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale: torch.Tensor,

@@ -327,6 +327,24 @@ TRIT_API trit_status trit_quant_act_folded(const float *x, const float *gain, in
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
 
+TRIT_API trit_status trit_check_div127(uint64_t *mismatches) {
+    if (!mismatches) return TRIT_E_ARG;
+    *mismatches = ~uint64_t(0);
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    unsigned long long *d = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&d), sizeof(unsigned long long));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemset(d, 0, sizeof(unsigned long long));
+    if (e == cudaSuccess) e = launch_check_div127(0, uint64_t(1) << 32, d, 0);
+    unsigned long long h = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&h, d, sizeof(h), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *mismatches = h;
+    return TRIT_OK;
+}
+
 TRIT_API trit_status trit_intmlp_quant(const int32_t *a_gate, const int32_t *a_up, int64_t M,
                                        int64_t N, float w_scale_gate, float w_scale_up,
                                        const float *x_scale, int8_t *h_i8, float *h_scale,

@@ -69,12 +69,30 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// f / 127 rounded to nearest even -- the result of one IEEE division -- at the
+// cost of a multiply and two FMAs: q = RN(f * c) with c = RN(1/127), then one
+// correction step in the manner of Markstein (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): the residual r = f - 127 q is exact under an FMA, and
+// q + r c is rounded once.  Zeros, non-finite values and magnitudes outside
+// [2^-100, 2^120] take the IEEE divide.  Over the fast range the result equals
+// __fdiv_rn(f, 127.0f) for every float: trit_check_div127 compares all 2^32
+// bit patterns on the device.
+__device__ __forceinline__ float div127_rn(float f) {
+    const float a = fabsf(f);
+    if (!(a >= 0x1p-100f && a <= 0x1p120f)) return __fdiv_rn(f, 127.0f);
+    const float c = 0x1.020408p-7f;   // RN(1/127)
+    const float q = __fmul_rn(f, c);
+    const float r = __fmaf_rn(-q, 127.0f, f);
+    return __fmaf_rn(r, c, q);
+}
+
 // The fp32 dequantisation of one output, one rounding per step, never contracted.
 __device__ __forceinline__ float dequant(int32_t y, float w_scale, float x_scale) {
     float f = __int2float_rn(y);
     f = __fmul_rn(f, w_scale);
     f = __fmul_rn(f, x_scale);
-    return __fdiv_rn(f, 127.0f);
+    return div127_rn(f);
 }
 
 // Permuted activation layout used by the select-accumulate kernels.  For each
@@ -178,6 +196,8 @@ cudaError_t launch_prefill_into(const ProjDev &p, uint8_t *xh, uint32_t *err, cu
 cudaError_t fixed_scratch(uint8_t **out);
 cudaError_t launch_quant_folded(const float *x, const float *g, int64_t M, int64_t K, float eps,
                                 int8_t *q, float *x_scale, uint32_t *err, cudaStream_t s);
+cudaError_t launch_check_div127(uint64_t lo, uint64_t hi, unsigned long long *mismatches,
+                                cudaStream_t s);
 cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t N,
                                 float w_g, float w_u, const float *x_scale, int8_t *q,
                                 float *h_scale, cudaStream_t s);

@@ -12,6 +12,9 @@
 //    row's scale is max|t| K.
 //
 // One CTA per row, two passes over the row (the second re-reads from L1/L2).
+//
+// Also: the exhaustive device check of div127_rn, the division used by every
+// fp32 dequantisation.
 #include "trit_internal.cuh"
 
 namespace trit {
@@ -169,6 +172,24 @@ __global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *
     }
 }
 
+// ---- division by 127 --------------------------------------------------------------
+
+// Every float32 bit pattern i in [lo, hi): count those where div127_rn(f) and
+// the IEEE divide disagree (NaN results agree with any NaN).
+__global__ void __launch_bounds__(256) check_div127_kernel(uint64_t lo, uint64_t hi,
+                                                           unsigned long long *mismatches) {
+    unsigned long long bad = 0;
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t i = lo + uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < hi; i += stride) {
+        const float f = __uint_as_float(uint32_t(i));
+        const float a = div127_rn(f), b = __fdiv_rn(f, 127.0f);
+        bad += (__float_as_uint(a) != __float_as_uint(b)) && !(isnan(a) && isnan(b));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) bad += __shfl_xor_sync(~0u, bad, o);
+    if ((threadIdx.x & 31) == 0 && bad) atomicAdd(mismatches, bad);
+}
+
 int rows_grid(int64_t M) {
     const int64_t cap = int64_t(device_sm_count()) * 8;
     return int(M < cap ? M : cap);
@@ -180,6 +201,12 @@ cudaError_t launch_quant_folded(const float *x, const float *g, int64_t M, int64
                                 int8_t *q, float *x_scale, uint32_t *err, cudaStream_t s) {
     const int64_t ldq = beats_per_row(K) * 64;
     quant_folded_kernel<<<rows_grid(M), kNThreads, 0, s>>>(x, g, M, K, eps, ldq, q, x_scale, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_check_div127(uint64_t lo, uint64_t hi, unsigned long long *mismatches,
+                                cudaStream_t s) {
+    check_div127_kernel<<<device_sm_count() * 8, 256, 0, s>>>(lo, hi, mismatches);
     return cudaGetLastError();
 }
 

@@ -14,52 +14,65 @@
 //     temporary fp16 copy laid out as 16 KB blocks of 128 rows x one beat (64
 //     columns), each block already in the MMA's 128-byte-swizzled K-major
 //     order, with columns permuted inside the beat (word k of half h holds
-//     columns 32h+k and 32h+k+16) and zeros past column K and past row M.
-//  2. prefill_kernel: tile = 256 activation rows (two 128-row MMA sub-tiles,
-//     two TMEM accumulators of 128 columns) x 128 weight rows (MMA N); one
-//     beat per pipeline stage, two stages.  Per stage one thread brings the
-//     two activation blocks with bulk copies that complete on the stage's
-//     mbarrier; eight producer warps (two threads per weight row, half a beat
-//     each) expand the 128 weight beats to fp16 +-1 in the same column order
-//     ((P & m_s) * (0x3C00 >> s) sets +1.0 in each half whose bit is set, -1.0 =
-//     0xBC00 likewise), so each expanded beat feeds both sub-tiles.  One thread
-//     of warp 8 issues the MMAs; the producer warps then read the fp32
-//     accumulators (exact integers), convert, and write them through a per-warp
-//     transpose in the freed shared memory so that stores cover whole row
-//     segments.  Two CTAs share an SM (256 tensor-memory columns and ~106 KB of
-//     shared memory each), so one CTA's epilogue runs while the other's MMAs do.
+//     columns 32h+k and 32h+k+16) and zeros past column K and past row M (the
+//     row blocks are padded to an even count).
+//  2. prefill_kernel: persistent, one CTA pair (a cluster of two CTAs on two
+//     SMs) per pair tile of 256 activation rows x 256 weight rows.  The pair
+//     issues tcgen05.mma.cta_group::2 with M = 256, N = 256: CTA r holds
+//     activation rows 128r.. of the tile (operand A) and expands weight rows
+//     128r.. of the tile (its half of operand B); its tensor memory receives
+//     its 128 rows x all 256 columns.  One beat per pipeline stage, five stages
+//     of 32 KB per CTA.  Per stage one thread brings the CTA's activation block
+//     with a bulk copy; eight producer warps (two threads per weight row, half
+//     a beat each) expand the 128 weight beats to fp16 +-1 in the same column
+//     order ((P & m_s) * (0x3C00 >> s) sets +1.0 in each half whose bit is
+//     set, -1.0 = 0xBC00 likewise).  In the leader CTA (rank 0) one thread
+//     issues the MMAs once both CTAs' stages are full (the peer's MMA warp
+//     relays its CTA's stage completion to the leader's barrier) and commits
+//     to barriers in both CTAs.  Two 256-column accumulators alternate between
+//     tiles, so eight epilogue warps per CTA read one tile's accumulator
+//     (exact integers), convert, and write it through a per-warp transpose in
+//     shared memory (whole 128-byte row segments per store) while the MMAs of
+//     the next tile run.
+// Per SM this takes N = 256 MMAs (each SM computes 128 x 256 per instruction)
+// with 128 expanded weight rows per 256 activation rows of the pair, and reads
+// each activation block once per 256 weight rows.
 // The fp16 copy of the activations is scratch memory: the host allocates it
 // stream-ordered around the two launches.
 // Every mbarrier wait is bounded: after kWaitNs it sets TRIT_ERR_TIMEOUT and
-// the CTA unwinds (waiting, again bounded, for its MMAs before freeing TMEM).
+// the roles unwind; before tensor memory is freed each CTA waits, again
+// bounded, for the last MMA commit.
 #include "trit_internal.cuh"
 
 namespace trit {
 namespace {
 
-constexpr int kSubM = 128;                // rows per MMA (TMEM lanes)
-constexpr int kSubs = 2;                  // MMA sub-tiles per tile
-constexpr int kBM = kSubM * kSubs;        // activation rows per tile
-constexpr int kBN = 128;                  // weight rows per tile (MMA N)
+constexpr int kSubM = 128;                // activation rows per CTA (TMEM lanes)
+constexpr int kPairM = 2 * kSubM;         // activation rows per pair tile (MMA M)
+constexpr int kHalfN = 128;               // weight rows expanded per CTA
+constexpr int kPairN = 2 * kHalfN;        // weight rows per pair tile (MMA N)
 constexpr int kBK = 64;                   // columns per stage (one beat)
-constexpr int kStages = 2;                // MMA operand stages
+constexpr int kStages = 5;                // MMA operand stages
 constexpr int kRaw = 4;                   // plane half-beats in flight per producer thread
 constexpr int kProducerWarps = 8;
-constexpr int kThreads = (kProducerWarps + 1) * 32;
+constexpr int kMmaWarp = kProducerWarps;  // MMA issue (leader) or relay (peer)
+constexpr int kEpiWarp0 = kMmaWarp + 1;
+constexpr int kEpiWarps = 8;              // two per TMEM lane quarter, 128 columns each
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr int kBlock = kSubM * kBK * 2;   // one 16 KB activation block (fp16)
-constexpr int kAStage = kSubs * kBlock;   // 32 KB
-constexpr int kBStage = kBN * kBK * 2;    // 16 KB
-constexpr int kStage = kAStage + kBStage;
+constexpr int kBStage = kHalfN * kBK * 2; // 16 KB of expanded weights
+constexpr int kStage = kBlock + kBStage;
 constexpr int kRawStage = kProducerWarps * 32 * 8;    // per thread: its half of pos and neg
-constexpr int kTmemCols = kSubs * kBN;    // 256: two 128 x 128 fp32 accumulators
+constexpr int kAccCols = kPairN;          // fp32 columns of one accumulator
+constexpr int kTmemCols = 2 * kAccCols;   // two accumulators: all 512 columns
+constexpr int kPitch = 36;                // words per epilogue staging row: 32 + 4 of padding
+constexpr int kEpiBytes = kEpiWarps * 32 * kPitch * 4;
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s
-constexpr size_t kSmemBytes = size_t(kStages) * kStage + size_t(kRaw) * kRawStage + 1024 + 256;
-static_assert(kProducerWarps * 32 == 2 * kBN, "two producer threads per weight beat");
-// two CTAs share an SM (tensor memory 2 x 256 columns, shared memory 2 x ~106 KB),
-// so one CTA's epilogue overlaps the other's MMAs
-constexpr int kCtasPerSm = 2;
-static_assert(kCtasPerSm * kTmemCols <= 512, "tensor memory of the resident CTAs");
+constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStage + size_t(kRaw) * kRawStage +
+                              kEpiBytes + 256;
+static_assert(kProducerWarps * 32 == 2 * kHalfN, "two producer threads per weight beat");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 struct PEntry {
     const uint4 *planes;
@@ -68,11 +81,11 @@ struct PEntry {
     int32_t *y_i32;
     float *y_f32;
     int64_t M, N;
-    int64_t tile_begin;     // prefix sum of tiles over the list
+    int64_t tile_begin;     // prefix sum of pair tiles over the list
     int32_t K, B;
-    int32_t mtiles, ntiles;
-    int32_t mblocks;        // ceil(M / 128)
+    int32_t mtiles, ntiles; // pair tiles along M (256 rows) and N (256 rows)
     float w_scale;
+    int32_t pad_;
 };
 
 struct PList {
@@ -82,6 +95,8 @@ struct PList {
     int64_t total_tiles;
     PEntry e[kMaxList];
 };
+static_assert(sizeof(PList) <= 32764, "kernel parameter space");
+
 
 // ---- PTX wrappers -------------------------------------------------------------
 
@@ -107,14 +122,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
 
-// Wait for the phase of the given parity; false after kWaitNs (then *timed_out is set).
+// Wait for the phase of the given parity (acquire at cluster scope: some arrivals
+// come from the peer CTA); false after kWaitNs (then *timed_out is set).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *timed_out) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
@@ -141,6 +157,7 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+
 // 128-byte-swizzled K-major shared-memory matrix descriptor (version 1): start
 // address, leading offset 16 B (unused for this layout), stride 1024 B between
 // groups of eight 128-byte rows.
@@ -150,24 +167,59 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N = 128, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(kBN >> 3) << 17) |
-                            (uint32_t(kSubM >> 4) << 24);
+// K-major, N = 256, M = 256 (the pair).
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (uint32_t(kPairN >> 3) << 17) |
+                            (uint32_t(kPairM >> 4) << 24);
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t accumulate) {
+__device__ __forceinline__ void mma_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
         "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+// Arrive on the barrier at the same offset in both CTAs of the pair once every
+// MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(uint16_t(3))
         : "memory");
 }
+
+// Arrive (release, cluster scope) on the barrier at the same offset in CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_at(uint64_t *bar, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+
+// The same arrive without release semantics.  Measured: a cluster-scope release
+// costs the issuing SM about 0.7 us and does not overlap with others, so the
+// per-stage relay uses this form.  It is issued only after the relaying thread
+// has observed (acquire) the completion of its own CTA's stage barrier -- the
+// bulk copy's bytes and the producer warps' stores (each fenced to the async
+// proxy and released at CTA scope) are then in that CTA's shared memory, which
+// the leader's MMA reads directly.
+__device__ __forceinline__ void mbar_arrive_at_relaxed(uint64_t *bar, uint32_t rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
 
 // 16-byte asynchronous global -> shared copy through L2; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
@@ -216,7 +268,6 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
     return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// ---- producers -------------------------------------------------------------------
 
 // 8 fp16x2 words (cols 32h + k and 32h + k + 16, k = k0..k0+7, k0 = 0 or 8) of one
 // plane half; for k0 = 8 the caller passes the words shifted right by 8.
@@ -302,230 +353,328 @@ __global__ void __launch_bounds__(256) act_f16_kernel(const __grid_constant__ CL
     }
 }
 
+
 // ---- the tensor-core product ---------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_kernel(const __grid_constant__ PList L) {
+// Pair tile t -> entry, m tile, n tile.
+struct TileRef {
+    int e;
+    int64_t mt, nt;
+};
+__device__ __forceinline__ TileRef tile_ref(const PList &L, int64_t t) {
+    int a = 0, b = L.count - 1;
+    while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (L.e[mid].tile_begin <= t) a = mid;
+        else b = mid - 1;
+    }
+    TileRef r;
+    r.e = a;
+    const int64_t tl = t - L.e[a].tile_begin;
+    r.mt = tl / L.e[a].ntiles;
+    r.nt = tl - r.mt * L.e[a].ntiles;
+    return r;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ PList L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *raw = smem + kStages * kStage;   // kRaw slots of kRawStage bytes
-    uint64_t *full = reinterpret_cast<uint64_t *>(raw + kRaw * kRawStage);
+    uint8_t *raw = smem + kStages * kStage;            // kRaw slots of kRawStage bytes
+    uint32_t *epi = reinterpret_cast<uint32_t *>(raw + kRaw * kRawStage);
+    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(epi) + kEpiBytes);
     uint64_t *empty = full + kStages;
-    uint64_t *done = empty + kStages;
+    uint64_t *tfull = empty + kStages;      // accumulator a holds a finished tile
+    uint64_t *tempty = tfull + 2;           // accumulator a has been read (leader's counts)
+    uint64_t *done = tempty + 2;            // every MMA has completed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     uint32_t *timed_out = tmem_slot + 1;
     uint32_t *viol_any = timed_out + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // tile -> (entry, m tile, n tile)
-    int e = 0;
-    {
-        int a = 0, b = L.count - 1;
-        while (a < b) {
-            const int mid = (a + b + 1) >> 1;
-            if (L.e[mid].tile_begin <= int64_t(blockIdx.x)) a = mid;
-            else b = mid - 1;
-        }
-        e = a;
-    }
-    const PEntry &E = L.e[e];
-    const int64_t tl = int64_t(blockIdx.x) - E.tile_begin;
-    const int64_t mt = tl / E.ntiles, nt = tl - mt * E.ntiles;
-    const int64_t m0 = mt * kBM, n0 = nt * kBN;
-    const int nk = E.B;
-    const int nsub = int(E.mblocks - mt * kSubs < kSubs ? E.mblocks - mt * kSubs : kSubs);
+    const uint32_t rank = cluster_rank();
+    const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], kProducerWarps + 1);   // 16 warps + the expect_tx arrival
+            // producer warps + the expect_tx arrival (+ the peer's relay in the leader)
+            mbar_init(&full[s], kProducerWarps + 1 + (rank == 0 ? 1 : 0));
             mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 2 * kEpiWarps);
         }
         mbar_init(done, 1);
         *timed_out = 0;
         *viol_any = 0;
         fence_barrier_init();
     }
-    if (warp == kProducerWarps) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kProducerWarps) {
-        // thread p: half (p & 1) of weight row n0 + (p >> 1)
+        // thread p: half (p & 1) of weight row 128*rank + (p >> 1) of each tile
         const int p = threadIdx.x;
         const int br = p >> 1, bh = p & 1;
-        const int64_t wn = n0 + br;
-        const bool w_ok = wn < E.N;
-        const uint8_t *wrow = reinterpret_cast<const uint8_t *>(E.planes + (w_ok ? wn : 0) * E.B);
-        const uint8_t *xblk = E.xh + (mt * kSubs) * int64_t(E.B) * kBlock;   // block (mt*kSubs, 0)
-        uint32_t viol = 0;
-        auto issue = [&](int kb) {   // this half's pos word and neg word of beat kb
-            uint8_t *slot = raw + (kb % kRaw) * kRawStage + p * 8;
-            const uint8_t *beat = wrow + int64_t(kb) * 16;
-            cp_async4(slot, beat + 4 * bh, w_ok ? 4u : 0u);
-            cp_async4(slot + 4, beat + 8 + 4 * bh, w_ok ? 4u : 0u);
+        // load cursor (kRaw stages ahead of the consume cursor, across tiles)
+        int64_t lt = pair;
+        int lkb = 0, lnk = 0;
+        const uint8_t *lrow = nullptr;
+        uint32_t lbytes = 0;
+        auto load_tile = [&](int64_t t) {
+            const TileRef r = tile_ref(L, t);
+            const PEntry &E = L.e[r.e];
+            const int64_t wn = r.nt * kPairN + int64_t(rank) * kHalfN + br;
+            const bool ok = wn < E.N;
+            lrow = reinterpret_cast<const uint8_t *>(E.planes + (ok ? wn : 0) * E.B);
+            lbytes = ok ? 4u : 0u;
+            lnk = E.B;
+            lkb = 0;
+        };
+        if (lt < L.total_tiles) load_tile(lt);
+        int64_t li = 0;   // loads issued
+        auto issue_next = [&]() {   // this half's pos word and neg word of the next beat
+            if (lt < L.total_tiles) {
+                uint8_t *slot = raw + int(li % kRaw) * kRawStage + p * 8;
+                const uint8_t *beat = lrow + int64_t(lkb) * 16;
+                cp_async4(slot, beat + 4 * bh, lbytes);
+                cp_async4(slot + 4, beat + 8 + 4 * bh, lbytes);
+                ++li;
+                if (++lkb == lnk) {
+                    lt += npairs;
+                    if (lt < L.total_tiles) load_tile(lt);
+                }
+            }
+            cp_async_commit();
         };
 #pragma unroll 1
-        for (int r = 0; r < kRaw; ++r) {
-            if (r < nk) issue(r);
-            cp_async_commit();
-        }
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = uint32_t(kb / kStages) & 1u;
-            if (!mbar_wait(&empty[s], ph ^ 1u, timed_out)) break;
-            uint8_t *a_st = smem + s * kStage;
-            uint8_t *b_st = a_st + kAStage;
-            if (p == 0) {   // the activation blocks of this stage
-                mbar_arrive_expect_tx(&full[s], uint32_t(nsub) * kBlock);
-                for (int st = 0; st < nsub; ++st)
-                    bulk_load(a_st + st * kBlock, xblk + (int64_t(st) * E.B + kb) * kBlock, kBlock,
-                              &full[s]);
+        for (int r = 0; r < kRaw; ++r) issue_next();
+        uint32_t viol = 0;
+        int64_t it = 0;   // stages consumed
+        bool stop = false;
+        for (int64_t t = pair; t < L.total_tiles && !stop; t += npairs) {
+            const TileRef r = tile_ref(L, t);
+            const PEntry &E = L.e[r.e];
+            const int nk = E.B;
+            const uint8_t *xblk = E.xh + (2 * r.mt + rank) * int64_t(E.B) * kBlock;
+            for (int kb = 0; kb < nk; ++kb, ++it) {
+                const int s = int(it % kStages);
+                const uint32_t ph = uint32_t(it / kStages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u, timed_out)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t *a_st = smem + s * kStage;
+                uint8_t *b_st = a_st + kBlock;
+                if (p == 0) {   // the activation block of this stage
+                    mbar_arrive_expect_tx(&full[s], kBlock);
+                    bulk_load(a_st, xblk + int64_t(kb) * kBlock, kBlock, &full[s]);
+                }
+                cp_async_wait<kRaw - 1>();
+                const uint2 pn = *reinterpret_cast<const uint2 *>(raw + int(it % kRaw) * kRawStage + p * 8);
+                viol |= pn.x & pn.y;
+                {   // weights: chunks 4*bh .. 4*bh+3 of row br
+                    uint32_t w[8];
+                    expand_quarter(pn.x, pn.y, w);
+                    *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+                    expand_quarter(pn.x >> 8, pn.y >> 8, w);
+                    *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 2)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 3)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+                issue_next();   // the raw slot is consumed: refill it kRaw stages ahead
             }
-            cp_async_wait<kRaw - 1>();
-            const uint2 pn = *reinterpret_cast<const uint2 *>(raw + (kb % kRaw) * kRawStage + p * 8);
-            viol |= pn.x & pn.y;
-            {   // weights: chunks 4*bh .. 4*bh+3 of row br
-                uint32_t w[8];
-                expand_quarter(pn.x, pn.y, w);
-                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-                expand_quarter(pn.x >> 8, pn.y >> 8, w);
-                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 2)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 3)) = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[s]);
-            // the raw slot is consumed: refill it kRaw stages ahead
-            if (kb + kRaw < nk) issue(kb + kRaw);
-            cp_async_commit();
         }
         cp_async_wait<0>();
         if (viol) atomicOr(viol_any, 1u);
-    } else if (lane == 0) {
-        // MMA issue: up to four 128-row sub-tiles x four K-steps of 16 per stage
-        const uint32_t base = smem_u32(smem);
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = uint32_t(kb / kStages) & 1u;
-            if (!mbar_wait(&full[s], ph, timed_out)) break;
-            tc_fence_after();
-            const uint32_t a_addr = base + s * kStage, b_addr = a_addr + kAStage;
-            for (int st = 0; st < nsub; ++st)
+    } else if (warp == kMmaWarp) {
+        if (lane == 0 && rank == 0) {
+            // MMA issue: per stage four K-steps of 16 into the tile's accumulator
+            const uint32_t base = smem_u32(smem);
+            int64_t it = 0, i = 0;
+            bool stop = false;
+            for (int64_t t = pair; t < L.total_tiles && !stop; t += npairs, ++i) {
+                const int a = int(i & 1);
+                const uint32_t use = uint32_t(i >> 1);
+                if (!mbar_wait(&tempty[a], (use & 1u) ^ 1u, timed_out)) break;
+                tc_fence_after();
+                const int nk = L.e[tile_ref(L, t).e].B;
+                const uint32_t d = tmem + uint32_t(a * kAccCols);
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = int(it % kStages);
+                    const uint32_t ph = uint32_t(it / kStages) & 1u;
+                    if (!mbar_wait(&full[s], ph, timed_out)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = base + s * kStage, b_addr = a_addr + kBlock;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_f16(tmem + uint32_t(st * kBN), sw128_desc(a_addr + st * kBlock + kk * 32),
-                            sw128_desc(b_addr + kk * 32), (kb > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&empty[s]);
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_pair(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_pair(&empty[s]);
+                }
+                if (!stop) mma_commit_pair(&tfull[a]);
+            }
+            mma_commit_pair(done);   // tracks every MMA issued above
+        } else if (lane == 0) {
+            // peer: relay each full stage of this CTA to the leader's barrier
+            int64_t it = 0;
+            bool stop = false;
+            for (int64_t t = pair; t < L.total_tiles && !stop; t += npairs) {
+                const int nk = L.e[tile_ref(L, t).e].B;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = int(it % kStages);
+                    const uint32_t ph = uint32_t(it / kStages) & 1u;
+                    if (!mbar_wait(&full[s], ph, timed_out)) {
+                        stop = true;
+                        break;
+                    }
+                    mbar_arrive_at_relaxed(&full[s], 0);
+                }
+            }
         }
-        mma_commit(done);   // tracks every MMA issued above
-    }
-
-    // epilogue.  For each sub-tile: warp w loads TMEM lanes 32*(w%4).. (one
-    // activation row per lane) and columns 32*(w/4)..+31; for each output
-    // (int32, then fp32) the lanes write their rows into the warp's own padded
-    // 32 x 32 staging tile in the freed shared memory and read it back
-    // transposed, so every store instruction writes whole 128-byte row
-    // segments (16-byte vectors when the rows are 16-byte aligned).
-    if (warp < kProducerWarps) {
-        const bool ok = __all_sync(~0u, mbar_wait(done, 0, timed_out));
-        tc_fence_after();
-        const bool good = ok && !*reinterpret_cast<volatile uint32_t *>(timed_out);
+        __syncwarp();
+    } else {
+        // epilogue: warp w reads TMEM lanes 32*(w%4).. (one activation row per
+        // lane) and columns 128*h .. 128*h+127 (h = which of the two warps of
+        // that lane quarter) and, 32 columns at a time, writes the int32 and
+        // the fp32 outputs through its padded 32 x 32 staging tile, read back
+        // transposed so every store writes whole 128-byte row segments.
         const int q = warp & 3;
-        const bool vec = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
-                         ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
-        constexpr int kPitch = 36;   // words per staging row: 32 + 4 of padding
-        uint32_t *sw = reinterpret_cast<uint32_t *>(smem) + warp * (32 * kPitch);
-#pragma unroll 1
-        for (int sc = 0; sc < nsub * 2; ++sc) {   // (sub-tile, column group) pairs of this warp
-            const int st = sc >> 1;
-            const int cg = (warp >> 2) + 2 * (sc & 1);
-            const int col = cg * 32;
-            const int64_t mbase = m0 + st * kSubM + 32 * q;   // rows of this warp
+        const int h = (warp - kEpiWarp0) >> 2;
+        uint32_t *sw = epi + (warp - kEpiWarp0) * (32 * kPitch);
+        int64_t i = 0;
+        for (int64_t t = pair; t < L.total_tiles; t += npairs, ++i) {
+            const int a = int(i & 1);
+            const uint32_t use = uint32_t(i >> 1);
+            const bool ok = __all_sync(~0u, mbar_wait(&tfull[a], use & 1u, timed_out));
+            if (!ok) break;
+            tc_fence_after();
+            const TileRef r = tile_ref(L, t);
+            const PEntry &E = L.e[r.e];
+            const bool vec = (E.N % 4 == 0) && ((reinterpret_cast<uintptr_t>(E.y_i32) & 15) == 0) &&
+                             ((reinterpret_cast<uintptr_t>(E.y_f32) & 15) == 0);
+            const int64_t mbase = r.mt * kPairM + int64_t(rank) * kSubM + 32 * q;   // rows of this warp
             const int64_t m = mbase + lane;
-            const float xs = (good && m < E.M) ? E.x_scale[m] : 0.0f;
-            uint32_t r[32];
-            if (good) {
-                const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(st * kBN + col);
+            const float xs = m < E.M ? E.x_scale[m] : 0.0f;
+            const int64_t n0 = r.nt * kPairN;
+#pragma unroll 1
+            for (int cg = 0; cg < kAccCols / 64; ++cg) {
+                const int col = h * (kAccCols / 2) + cg * 32;
+                uint32_t v32[32];
+                const uint32_t taddr = tmem + (uint32_t(32 * q) << 16) + uint32_t(a * kAccCols + col);
                 asm volatile(
                     "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
                     "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,"
                     "%30,%31}, [%32];"
-                    : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                      "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-                      "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-                      "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-                      "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),
-                      "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                    : "=r"(v32[0]), "=r"(v32[1]), "=r"(v32[2]), "=r"(v32[3]), "=r"(v32[4]),
+                      "=r"(v32[5]), "=r"(v32[6]), "=r"(v32[7]), "=r"(v32[8]), "=r"(v32[9]),
+                      "=r"(v32[10]), "=r"(v32[11]), "=r"(v32[12]), "=r"(v32[13]), "=r"(v32[14]),
+                      "=r"(v32[15]), "=r"(v32[16]), "=r"(v32[17]), "=r"(v32[18]), "=r"(v32[19]),
+                      "=r"(v32[20]), "=r"(v32[21]), "=r"(v32[22]), "=r"(v32[23]), "=r"(v32[24]),
+                      "=r"(v32[25]), "=r"(v32[26]), "=r"(v32[27]), "=r"(v32[28]), "=r"(v32[29]),
+                      "=r"(v32[30]), "=r"(v32[31])
                     : "r"(taddr));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            } else {
+                if (n0 + col >= E.N) continue;   // past the last weight row
+                // the int32 values into this lane's staging row
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = 0;
-            }
-            if (!good) continue;
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<uint4 *>(sw + lane * kPitch + c) = make_uint4(
+                        uint32_t(__float2int_rn(__uint_as_float(v32[c]))),
+                        uint32_t(__float2int_rn(__uint_as_float(v32[c + 1]))),
+                        uint32_t(__float2int_rn(__uint_as_float(v32[c + 2]))),
+                        uint32_t(__float2int_rn(__uint_as_float(v32[c + 3]))));
 #pragma unroll 1
-            for (int typ = 0; typ < 2; ++typ) {
-                uint32_t *out = typ == 0 ? reinterpret_cast<uint32_t *>(E.y_i32)
-                                         : reinterpret_cast<uint32_t *>(E.y_f32);
-                if (!out) continue;
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    uint32_t v[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int32_t y = __float2int_rn(__uint_as_float(r[i + k]));
-                        v[k] = typ == 0 ? uint32_t(y) : __float_as_uint(dequant(y, E.w_scale, xs));
+                for (int typ = 0; typ < 2; ++typ) {
+                    uint32_t *out = typ == 0 ? reinterpret_cast<uint32_t *>(E.y_i32)
+                                             : reinterpret_cast<uint32_t *>(E.y_f32);
+                    if (typ == 1) {
+                        if (!out) break;
+                        // dequantise the staged row in place (after the int32 pass read it)
+#pragma unroll 2
+                        for (int c = 0; c < 32; c += 4) {
+                            uint4 u = *reinterpret_cast<const uint4 *>(sw + lane * kPitch + c);
+                            u.x = __float_as_uint(dequant(int32_t(u.x), E.w_scale, xs));
+                            u.y = __float_as_uint(dequant(int32_t(u.y), E.w_scale, xs));
+                            u.z = __float_as_uint(dequant(int32_t(u.z), E.w_scale, xs));
+                            u.w = __float_as_uint(dequant(int32_t(u.w), E.w_scale, xs));
+                            *reinterpret_cast<uint4 *>(sw + lane * kPitch + c) = u;
+                        }
                     }
-                    *reinterpret_cast<uint4 *>(sw + lane * kPitch + i) = make_uint4(v[0], v[1], v[2], v[3]);
-                }
-                __syncwarp();
-                if (vec) {
+                    __syncwarp();
+                    if (out) {
+                        if (vec) {
 #pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = it * 4 + (lane >> 3), c4 = (lane & 7) * 4;
-                        const int64_t mm = mbase + rr, n = n0 + col + c4;
-                        const uint4 val = *reinterpret_cast<const uint4 *>(sw + rr * kPitch + c4);
-                        if (mm < E.M && n < E.N)
-                            *reinterpret_cast<uint4 *>(out + mm * E.N + n) = val;
-                    }
-                } else {
+                            for (int k8 = 0; k8 < 8; ++k8) {
+                                const int rr = k8 * 4 + (lane >> 3), c4 = (lane & 7) * 4;
+                                const int64_t mm = mbase + rr, n = n0 + col + c4;
+                                const uint4 val = *reinterpret_cast<const uint4 *>(sw + rr * kPitch + c4);
+                                if (mm < E.M && n < E.N)
+                                    *reinterpret_cast<uint4 *>(out + mm * E.N + n) = val;
+                            }
+                        } else {
 #pragma unroll 4
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int64_t mm = mbase + rr, n = n0 + col + lane;
-                        if (mm < E.M && n < E.N) out[mm * E.N + n] = sw[rr * kPitch + lane];
+                            for (int rr = 0; rr < 32; ++rr) {
+                                const int64_t mm = mbase + rr, n = n0 + col + lane;
+                                if (mm < E.M && n < E.N) out[mm * E.N + n] = sw[rr * kPitch + lane];
+                            }
+                        }
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_at(&tempty[a], 0);   // the leader's count
         }
     }
+
+    // teardown: every MMA of the pair has completed before tensor memory is freed
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
+    if (warp == kMmaWarp) {
+        bool fin = true;
+        if (lane == 0) fin = mbar_wait(done, 0, timed_out);
+        fin = __shfl_sync(~0u, fin, 0);
+        (void)fin;
+    }
     if (threadIdx.x == 0) {
         uint32_t f = 0;
         if (*timed_out) f |= TRIT_ERR_TIMEOUT;
         if (*viol_any) f |= TRIT_ERR_P1;
         if (f) atomicOr(L.err, f);
     }
-    if (warp == kProducerWarps)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+    tc_fence_before();
+    cluster_sync_all();   // neither CTA frees tensor memory while the pair's MMAs may run
+    tc_fence_after();
+    if (warp == kMmaWarp)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
 }
 
+// Row blocks of 128 of the fp16 activation copy: an even count (pair tiles).
+int64_t act_blocks(const ProjDev &p) { return 2 * ((p.M + kPairM - 1) / kPairM); }
+
 // Bytes of the blocked fp16 activation copy of one product.
-int64_t act_f16_bytes(const ProjDev &p) {
-    return ((p.M + kSubM - 1) / kSubM) * int64_t(p.B) * kBlock;
-}
+int64_t act_f16_bytes(const ProjDev &p) { return act_blocks(p) * int64_t(p.B) * kBlock; }
 
 // Convert and multiply the products list[0..n) with their fp16 activation
 // copies at xh[i] (each act_f16_bytes long, 16-byte aligned).
@@ -540,7 +689,7 @@ cudaError_t launch_two(const ProjDev *list, int n, uint8_t *const *xh, uint32_t 
     int64_t halves = 0, tiles = 0;
     for (int i = 0; i < n; ++i) {
         const ProjDev &p = list[i];
-        const int64_t mblocks = (p.M + kSubM - 1) / kSubM;
+        const int64_t mblocks = act_blocks(p);
         CEntry &c = C.e[i];
         c.x = p.x;
         c.xh = xh[i];
@@ -559,10 +708,10 @@ cudaError_t launch_two(const ProjDev *list, int n, uint8_t *const *xh, uint32_t 
         E.N = p.N;
         E.K = p.K;
         E.B = p.B;
-        E.mblocks = int32_t(mblocks);
-        E.mtiles = int32_t((p.M + kBM - 1) / kBM);
-        E.ntiles = int32_t((p.N + kBN - 1) / kBN);
+        E.mtiles = int32_t(mblocks / 2);
+        E.ntiles = int32_t((p.N + kPairN - 1) / kPairN);
         E.w_scale = p.w_scale;
+        E.pad_ = 0;
         E.tile_begin = tiles;
         tiles += int64_t(E.mtiles) * E.ntiles;
     }
@@ -574,7 +723,12 @@ cudaError_t launch_two(const ProjDev *list, int n, uint8_t *const *xh, uint32_t 
     act_f16_kernel<<<int(cblocks), 256, 0, s>>>(C);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    prefill_kernel<<<dim3(unsigned(tiles)), kThreads, kSmemBytes, s>>>(L);
+    if (tiles == 0) return cudaSuccess;
+    // persistent: one pair per two SMs (at most one pair per tile)
+    int64_t pairs = device_sm_count() / 2;
+    pairs = pairs < tiles ? pairs : tiles;
+    pairs = pairs < 1 ? 1 : pairs;
+    prefill_kernel<<<dim3(unsigned(2 * pairs)), kThreads, kSmemBytes, s>>>(L);
     return cudaGetLastError();
 }
 

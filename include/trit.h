@@ -318,6 +318,18 @@ typedef struct trit_act {
 TRIT_API trit_status trit_quant_act_many(const trit_act *list, int32_t count,
                                          uint32_t *err_flag, trit_stream_t stream);
 
+/* trit_check_div127 -- diagnostic: every fp32 dequantisation divides by 127
+ * ("Tritium: One Weight Format for Ternary Inference ..." -- Numerics: y_f32 =
+ * ((y * w_scale) * x_scale) / 127, each step rounded once) with a multiply and
+ * two FMAs (a reciprocal product and one Markstein residual correction) in place
+ * of the IEEE divide.  This call evaluates both forms for all 2^32 float bit
+ * patterns on the current device and stores the number of disagreements (NaN
+ * against NaN counts as agreement) in *mismatches (host pointer; 0 means the two
+ * are bit-identical).  Synchronous on the default stream; allocates 8 bytes of
+ * device memory for the count.  TRIT_E_ARG for a null pointer; CUDA failures as
+ * for the other calls (then *mismatches = UINT64_MAX). */
+TRIT_API trit_status trit_check_div127(uint64_t *mismatches);
+
 #ifdef __cplusplus
 }
 #endif

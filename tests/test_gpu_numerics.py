@@ -120,3 +120,10 @@ def test_mlp_chain_through_the_abi(t, orc):
     np.testing.assert_array_equal(host(d_i32), yd)
     np.testing.assert_array_equal(host(d_f32).view(np.int32), yfd.view(np.int32))
     assert int(host(derr)[0]) == 0 and int(host(gerr)[0]) == 0
+
+
+def test_div127_matches_ieee_division_on_every_float(t):
+    """The dequantisation divides by 127 with a reciprocal product and one
+    residual correction; over all 2^32 float bit patterns it equals the IEEE
+    divide (the fp32 outputs the oracle's y_f32 formula rounds once per step)."""
+    assert t.trit_check_div127() == 0
