@@ -552,9 +552,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // epilogue: warp w reads TMEM lanes 32*(w%4).. (one activation row per
         // lane) and columns 128*h .. 128*h+127 (h = which of the two warps of
-        // that lane quarter) and, 32 columns at a time, writes the int32 and
-        // the fp32 outputs through its padded 32 x 32 staging tile, read back
-        // transposed so every store writes whole 128-byte row segments.
+        // that lane quarter) and, 32 columns at a time, passes the int32 sums
+        // through its padded 32 x 32 staging tile, read back transposed so every
+        // store (int32, and the fp32 dequantisation computed from the same
+        // read) writes whole 128-byte row segments.
         const int q = warp & 3;
         const int h = (warp - kEpiWarp0) >> 2;
         uint32_t *sw = epi + (warp - kEpiWarp0) * (32 * kPitch);
@@ -592,7 +593,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     : "r"(taddr));
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 if (n0 + col >= E.N) continue;   // past the last weight row
-                // the int32 values into this lane's staging row
+                // the int32 values into this lane's staging row, read back transposed;
+                // each value read back is stored as int32 and, dequantised with its
+                // row's scale (from the lane that holds that row), as fp32
 #pragma unroll
                 for (int c = 0; c < 32; c += 4)
                     *reinterpret_cast<uint4 *>(sw + lane * kPitch + c) = make_uint4(
@@ -600,44 +603,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         uint32_t(__float2int_rn(__uint_as_float(v32[c + 1]))),
                         uint32_t(__float2int_rn(__uint_as_float(v32[c + 2]))),
                         uint32_t(__float2int_rn(__uint_as_float(v32[c + 3]))));
-#pragma unroll 1
-                for (int typ = 0; typ < 2; ++typ) {
-                    uint32_t *out = typ == 0 ? reinterpret_cast<uint32_t *>(E.y_i32)
-                                             : reinterpret_cast<uint32_t *>(E.y_f32);
-                    if (typ == 1) {
-                        if (!out) break;
-                        // dequantise the staged row in place (after the int32 pass read it)
+                __syncwarp();
+                int32_t *const yi = E.y_i32;
+                float *const yf = E.y_f32;
+                if (vec) {
 #pragma unroll 2
-                        for (int c = 0; c < 32; c += 4) {
-                            uint4 u = *reinterpret_cast<const uint4 *>(sw + lane * kPitch + c);
-                            u.x = __float_as_uint(dequant(int32_t(u.x), E.w_scale, xs));
-                            u.y = __float_as_uint(dequant(int32_t(u.y), E.w_scale, xs));
-                            u.z = __float_as_uint(dequant(int32_t(u.z), E.w_scale, xs));
-                            u.w = __float_as_uint(dequant(int32_t(u.w), E.w_scale, xs));
-                            *reinterpret_cast<uint4 *>(sw + lane * kPitch + c) = u;
+                    for (int k8 = 0; k8 < 8; ++k8) {
+                        const int rr = k8 * 4 + (lane >> 3), c4 = (lane & 7) * 4;
+                        const float xr = __shfl_sync(~0u, xs, rr);
+                        const int64_t mm = mbase + rr, n = n0 + col + c4;
+                        const uint4 u = *reinterpret_cast<const uint4 *>(sw + rr * kPitch + c4);
+                        if (mm < E.M && n < E.N) {
+                            if (yi) *reinterpret_cast<uint4 *>(yi + mm * E.N + n) = u;
+                            if (yf)
+                                *reinterpret_cast<float4 *>(yf + mm * E.N + n) = make_float4(
+                                    dequant(int32_t(u.x), E.w_scale, xr), dequant(int32_t(u.y), E.w_scale, xr),
+                                    dequant(int32_t(u.z), E.w_scale, xr), dequant(int32_t(u.w), E.w_scale, xr));
                         }
                     }
-                    __syncwarp();
-                    if (out) {
-                        if (vec) {
-#pragma unroll
-                            for (int k8 = 0; k8 < 8; ++k8) {
-                                const int rr = k8 * 4 + (lane >> 3), c4 = (lane & 7) * 4;
-                                const int64_t mm = mbase + rr, n = n0 + col + c4;
-                                const uint4 val = *reinterpret_cast<const uint4 *>(sw + rr * kPitch + c4);
-                                if (mm < E.M && n < E.N)
-                                    *reinterpret_cast<uint4 *>(out + mm * E.N + n) = val;
-                            }
-                        } else {
+                } else {
 #pragma unroll 4
-                            for (int rr = 0; rr < 32; ++rr) {
-                                const int64_t mm = mbase + rr, n = n0 + col + lane;
-                                if (mm < E.M && n < E.N) out[mm * E.N + n] = sw[rr * kPitch + lane];
-                            }
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const float xr = __shfl_sync(~0u, xs, rr);
+                        const int64_t mm = mbase + rr, n = n0 + col + lane;
+                        const int32_t y = int32_t(sw[rr * kPitch + lane]);
+                        if (mm < E.M && n < E.N) {
+                            if (yi) yi[mm * E.N + n] = y;
+                            if (yf) yf[mm * E.N + n] = dequant(y, E.w_scale, xr);
                         }
                     }
-                    __syncwarp();
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
