@@ -147,6 +147,32 @@ def build_stack(device, layers: int):
     return st
 
 
+def read_probe_gbs(dev, gib: int = 2, reps: int = 5):
+    """Same-run read rate of the device memory: trit_read_probe over a buffer far
+    larger than L2, best of `reps` launches timed with CUDA events."""
+    import torch
+
+    import bit_plane_select_gb300 as t
+    nbytes = gib << 30
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    t.trit_read_probe(buf, sink)
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        t.trit_read_probe(buf, sink)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None or ms < best else best
+    del buf
+    torch.cuda.empty_cache()
+    return round(nbytes / (best * 1e-3) / 1e9, 1)
+
+
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -254,6 +280,7 @@ def run_ours(args):
     kern_avg_ms = total_ms / K
     achieved = step_bytes / (kern_avg_ms * 1e-3) / 1e9
     traffic = committed_traffic(step_bytes)
+    probe_gbs = read_probe_gbs(dev)
 
     # e2e: host fp32 activations in, host y_i32 + y_f32 out, every step.  Two
     # buffer sets (twin stacks over the same planes) and three streams: the
@@ -361,6 +388,10 @@ def run_ours(args):
             "avg_launch_from": "CUDA events around the K back-to-back launches of the timed "
                                "region, divided by K",
             "isolated_launch_us": round(isolated_ms * 1e3, 3),
+            "probe_read_gbs": probe_gbs,
+            "frac_of_probe": round(achieved / probe_gbs, 4) if probe_gbs else None,
+            "probe": "trit_read_probe over a 2 GiB buffer in the same run, best of 5 "
+                     "(plain coalesced 16-byte reads)",
         },
         "two_launch_path": {
             "quant_us": round(two_quant * 1e3, 3),
@@ -386,6 +417,7 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_layers)
+        out["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores(args.cpu_layers)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -394,16 +426,19 @@ def run_ours(args):
 
 # ---- the CPU oracle ---------------------------------------------------------
 
-def oracle_sample(layers, rows_frac=1.0):
+def oracle_sample(layers, rows_frac=1.0, shard=0, nshards=1):
     """Pack (untimed) the sampled projections with the oracle; returns a list of
-    (payload, w_scale, x fp32, K, rows) items."""
+    (payload, w_scale, x fp32, K, rows) items (every nshards-th projection from
+    `shard` on)."""
     import numpy as np
 
     import oracle
     import synth
 
     items = []
-    for layer, idx, name, N, K in synth.stack_items(layers):
+    for i, (layer, idx, name, N, K) in enumerate(synth.stack_items(layers)):
+        if i % nshards != shard:
+            continue
         w = synth.stack_weights(SEED, layer, idx)
         n = max(1, int(round(N * rows_frac)))
         items.append((oracle.pack(w[:n]), float(synth.w_scale(w)),
@@ -440,6 +475,47 @@ def cpu_baseline(layers):
             "sample": f"layers 0..{layers - 1} of the 30-layer stack ({len(items)} projections, "
                       f"{weights} weights), quantise + product, {passes} passes of "
                       f"{dt:.2f} s each"}
+
+
+def _oracle_shard(layers, shard, nshards, seconds, barrier, q):
+    items = oracle_sample(layers, shard=shard, nshards=nshards)
+    import synth
+    weights = sum(N * K for i, (_, _, _, N, K) in enumerate(synth.stack_items(layers))
+                  if i % nshards == shard)
+    barrier.wait()
+    passes, t = 0, time.perf_counter()
+    while True:
+        oracle_step(items)
+        passes += 1
+        if time.perf_counter() - t >= seconds:
+            break
+    q.put((passes * weights, time.perf_counter() - t))
+
+
+def cpu_baseline_all_cores(layers, seconds: float = 8.0):
+    """The same oracle on every host core: the stack's projections dealt round
+    robin to one spawned process per core, each running whole passes over its
+    share for about `seconds`; throughput = weights processed / slowest time."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    ctx = mp.get_context("spawn")
+    barrier, q = ctx.Barrier(cores + 1), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_shard, args=(layers, i, cores, seconds, barrier, q))
+             for i in range(cores)]
+    for pr in procs:
+        pr.start()
+    barrier.wait()
+    res = [q.get() for _ in procs]
+    for pr in procs:
+        pr.join()
+    done = sum(w for w, _ in res)
+    wall = max(dt for _, dt in res)
+    import synth
+    full = sum(N * K for _, _, _, N, K in synth.stack_items(synth.LAYERS))
+    return {"value": round(done / 4 / wall / 1e9, 3), "unit": "GB/s",
+            "tok_per_s": round(done / full / wall, 4), "cores": cores, "kind": "oracle",
+            "sample": f"layers 0..{layers - 1}, projections dealt round robin to {cores} "
+                      f"processes, about {seconds:.0f} s of whole passes each"}
 
 
 def run_reference(args):

@@ -10,7 +10,7 @@ built, or the device is not an sm_103 GPU, the calls raise.
 Functions carry the C names:
   trit_pack, trit_unpack, trit_verify, trit_quant_act, trit_quant_act_many,
   trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many, trit_gemm_noalloc,
-  trit_quant_act_folded, trit_intmlp_quant, trit_check_div127
+  trit_quant_act_folded, trit_intmlp_quant, trit_check_div127, trit_read_probe
 """
 from __future__ import annotations
 
@@ -27,7 +27,7 @@ __all__ = [
     "trit_quant_act", "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
     "trit_quant_gemv_many", "ProjList", "ActList", "QProjList", "TritProj", "TritAct",
     "TritQProj", "MAX_FUSED_K", "trit_gemm_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "trit_quant_act_folded", "trit_intmlp_quant", "trit_check_div127",
+    "trit_quant_act_folded", "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
 ]
 
 ERR_P1 = 1
@@ -105,10 +105,11 @@ def lib():
         L.trit_quant_act_folded.argtypes = [p, p, i64, i64, f32, p, p, p, p]
         L.trit_intmlp_quant.argtypes = [p, p, i64, i64, f32, f32, p, p, p, p]
         L.trit_check_div127.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+        L.trit_read_probe.argtypes = [p, i64, p, p]
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
                      "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
                      "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_quant_act_folded",
-                     "trit_intmlp_quant", "trit_check_div127"):
+                     "trit_intmlp_quant", "trit_check_div127", "trit_read_probe"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -284,6 +285,20 @@ def trit_intmlp_quant(a_gate: torch.Tensor, a_up: torch.Tensor, w_scale_gate: fl
                                    _dev(h_scale, torch.float32, "h_scale"), _stream(stream)),
            "trit_intmlp_quant")
     return h_i8, h_scale
+
+
+def trit_read_probe(buf: torch.Tensor, sink: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Read every byte of the CUDA tensor `buf` once (a plain coalesced stream);
+    the launch's duration measures the device's memory read rate."""
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    nbytes = buf.numel() * buf.element_size()
+    if sink is None:
+        sink = torch.zeros(1, dtype=torch.int32, device=buf.device)
+    _check(lib().trit_read_probe(ctypes.c_void_p(buf.data_ptr()), nbytes - nbytes % 16,
+                                 ctypes.c_void_p(sink.data_ptr()), _stream(stream)),
+           "trit_read_probe")
+    return sink
 
 
 def trit_check_div127() -> int:

@@ -327,6 +327,16 @@ TRIT_API trit_status trit_quant_act_folded(const float *x, const float *gain, in
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
 
+TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *sink,
+                                     trit_stream_t stream) {
+    if (!buf || !sink || !aligned(buf, 16) || !aligned(sink, 4) || bytes < 16 || bytes % 16)
+        return TRIT_E_ARG;
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_read_probe(buf, bytes, sink, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
 TRIT_API trit_status trit_check_div127(uint64_t *mismatches) {
     if (!mismatches) return TRIT_E_ARG;
     *mismatches = ~uint64_t(0);

@@ -196,6 +196,7 @@ cudaError_t launch_prefill_into(const ProjDev &p, uint8_t *xh, uint32_t *err, cu
 cudaError_t fixed_scratch(uint8_t **out);
 cudaError_t launch_quant_folded(const float *x, const float *g, int64_t M, int64_t K, float eps,
                                 int8_t *q, float *x_scale, uint32_t *err, cudaStream_t s);
+cudaError_t launch_read_probe(const void *p, int64_t bytes, uint32_t *sink, cudaStream_t s);
 cudaError_t launch_check_div127(uint64_t lo, uint64_t hi, unsigned long long *mismatches,
                                 cudaStream_t s);
 cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t N,

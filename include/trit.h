@@ -318,6 +318,17 @@ typedef struct trit_act {
 TRIT_API trit_status trit_quant_act_many(const trit_act *list, int32_t count,
                                          uint32_t *err_flag, trit_stream_t stream);
 
+/* trit_read_probe -- measurement aid: read `bytes` (a multiple of 16, >= 16) of
+ * the device buffer `buf` (16-byte aligned) once, with the 16-byte L1-bypassing
+ * loads the products use for the planes, fully coalesced, and reduce them into
+ * *sink (device u32, 4-byte aligned; its value is meaningless).  Timing this
+ * launch gives the plain read rate of the device's memory, the reference the
+ * products' HBM rate is compared with ("Tritium ..." -- Results: the weight
+ * stream is the cost of a decode step).  Asynchronous on `stream`; TRIT_E_ARG
+ * for null or misaligned pointers or a bad size. */
+TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *sink,
+                                     trit_stream_t stream);
+
 /* trit_check_div127 -- diagnostic: every fp32 dequantisation divides by 127
  * ("Tritium: One Weight Format for Ternary Inference ..." -- Numerics: y_f32 =
  * ((y * w_scale) * x_scale) / 127, each step rounded once) with a multiply and
