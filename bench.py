@@ -694,6 +694,92 @@ def run_batch_sweep(args):
           flush=True)
 
 
+def run_mlp(args):
+    """The MLP blocks of the 30-layer stack at batch 1 (row f1): per layer, gate
+    and up from one fp32 activation row with the quantiser fused (one launch),
+    then the IntMlp codes of relu(a_gate)^2 a_up and the down product (one
+    launch) -- against the same chain with the standalone IntMlp quantiser
+    between (three launches).  Each step is one token through every layer."""
+    import torch
+
+    import __graft_entry__
+    import synth
+    import bit_plane_select_gb300 as t
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    names = [p[0] for p in synth.PROJECTIONS]
+    ig, iu, idn = names.index("gate"), names.index("up"), names.index("down")
+    K, N = synth.PROJECTIONS[ig][2], synth.PROJECTIONS[ig][1]      # 2560, 6912
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    fused, three, keep = [], [], []
+    plane_bytes = 0
+    for layer in range(args.layers):
+        pl, ws = [], []
+        for idx in (ig, iu, idn):
+            w = synth.stack_weights(SEED, layer, idx)
+            ws.append(float(synth.w_scale(w)))
+            pl.append(t.trit_pack(torch.from_numpy(w).to(dev), ws[-1])[0])
+            plane_bytes += pl[-1].numel()
+        x = torch.from_numpy(synth.projection_acts(SEED, layer, ig, 1)).to(dev).reshape(-1)
+        a_g = torch.empty(N, dtype=torch.int32, device=dev)
+        a_u = torch.empty(N, dtype=torch.int32, device=dev)
+        xs = torch.empty(1, dtype=torch.float32, device=dev)
+        h = torch.empty(t.k_pad(N), dtype=torch.int8, device=dev)
+        hs = torch.empty(1, dtype=torch.float32, device=dev)
+        y = torch.empty(K, dtype=torch.int32, device=dev)
+        yf = torch.empty(K, dtype=torch.float32, device=dev)
+        gu = t.QProjList([(pl[0], ws[0], x, None, xs, a_g, None), (pl[1], ws[1], x, None, None, a_u, None)])
+        dn = t.MlpProjList([(pl[2], ws[2], a_g, a_u, xs, ws[0], ws[1], None, None, y, yf)])
+        dn3 = t.ProjList([(pl[2], ws[2], h, hs, N, y, yf)])
+        fused.append((gu, dn))
+        three.append((gu, a_g, a_u, ws[0], ws[1], xs, h, hs, dn3))
+        keep.append((pl, x, a_g, a_u, xs, h, hs, y, yf))
+
+    def step_fused():
+        for gu, dn in fused:
+            t.trit_quant_gemv_many(gu, err)
+            t.trit_intmlp_gemv_many(dn, err)
+
+    def step_three():
+        for gu, a_g, a_u, wg, wu, xs, h, hs, dn3 in three:
+            t.trit_quant_gemv_many(gu, err)
+            t.trit_intmlp_quant(a_g, a_u, wg, wu, xs, h, hs)
+            t.trit_gemm_many(dn3, err)
+
+    steps = max(20, args.steps // 100)
+    eager_f = _timed(step_fused, steps, args.warmup, stream)
+    eager_3 = _timed(step_three, steps, args.warmup, stream)
+
+    # the launches of one step captured in a CUDA graph: replay time is device
+    # time, free of the per-call host work of the eager loop above
+    def graph_ms(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return _timed(g.replay, steps, args.warmup, stream)
+
+    ms_f = graph_ms(step_fused)
+    ms_3 = graph_ms(step_three)
+    act_bytes = args.layers * (K * 4 + 4 + 2 * N * 4 * 2 + K * 8)
+    nbytes = plane_bytes + act_bytes
+    out = {"metric": "MLP blocks of the 30-layer stack, batch 1 (gate+up fused quantise; IntMlp + down)",
+           "unit": "tok/s", "value": round(1e3 / ms_f, 1),
+           "ms_per_step": round(ms_f, 4), "GBs": round(nbytes / (ms_f * 1e-3) / 1e9, 1),
+           "launches_per_step": 2 * args.layers, "timing": "CUDA graph of one step, replayed",
+           "three_launch_path": {"ms_per_step": round(ms_3, 4), "tok_per_s": round(1e3 / ms_3, 1),
+                                 "launches_per_step": 3 * args.layers},
+           "eager_ms_per_step": {"fused": round(eager_f, 4), "three_launch": round(eager_3, 4)},
+           "algorithmic_bytes_per_step": nbytes, "err_flag": int(err.item()),
+           "config": {"workload": "bitnet-2b4t-30layer-mlp-batch1", "layers": args.layers,
+                      "gate_up": [N, K], "down": [K, N]}}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -706,8 +792,8 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=90.0)
-    ap.add_argument("--workload", choices=["decode", "prefill", "batch"], default="decode",
-                    help="decode (default): the 30-layer batch-1 stack; prefill and batch "
+    ap.add_argument("--workload", choices=["decode", "prefill", "batch", "mlp"], default="decode",
+                    help="decode (default): the 30-layer batch-1 stack; prefill, batch and mlp "
                          "print extra lines for the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -718,6 +804,8 @@ def main():
         run_prefill(args)
     elif args.workload == "batch":
         run_batch_sweep(args)
+    elif args.workload == "mlp":
+        run_mlp(args)
     else:
         run_ours(args)
 

@@ -10,7 +10,8 @@ built, or the device is not an sm_103 GPU, the calls raise.
 Functions carry the C names:
   trit_pack, trit_unpack, trit_verify, trit_quant_act, trit_quant_act_many,
   trit_gemv, trit_gemm, trit_gemm_many, trit_quant_gemv_many, trit_gemm_noalloc,
-  trit_quant_act_folded, trit_intmlp_quant, trit_check_div127, trit_read_probe
+  trit_quant_act_folded, trit_intmlp_quant, trit_intmlp_gemv_many, trit_check_div127,
+  trit_read_probe
 """
 from __future__ import annotations
 
@@ -28,6 +29,7 @@ __all__ = [
     "trit_quant_gemv_many", "ProjList", "ActList", "QProjList", "TritProj", "TritAct",
     "TritQProj", "MAX_FUSED_K", "trit_gemm_noalloc", "NOALLOC_SCRATCH_BYTES",
     "trit_quant_act_folded", "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
+    "trit_intmlp_gemv_many", "MlpProjList", "TritMlpProj",
 ]
 
 ERR_P1 = 1
@@ -60,6 +62,14 @@ class TritQProj(ctypes.Structure):
                 ("x_scale", ctypes.c_void_p), ("y_i32", ctypes.c_void_p),
                 ("y_f32", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+
+
+class TritMlpProj(ctypes.Structure):
+    _fields_ = [("planes", ctypes.c_void_p), ("a_gate", ctypes.c_void_p), ("a_up", ctypes.c_void_p),
+                ("x_scale", ctypes.c_void_p), ("w_gate", ctypes.c_float), ("w_up", ctypes.c_float),
+                ("h_i8", ctypes.c_void_p), ("h_scale", ctypes.c_void_p),
+                ("y_i32", ctypes.c_void_p), ("y_f32", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
 
 
 class TritAct(ctypes.Structure):
@@ -101,6 +111,7 @@ def lib():
         L.trit_gemm.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         L.trit_gemm_many.argtypes = [p, i32, p, p]
         L.trit_quant_gemv_many.argtypes = [p, i32, p, p]
+        L.trit_intmlp_gemv_many.argtypes = [p, i32, p, p]
         L.trit_gemm_noalloc.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         L.trit_quant_act_folded.argtypes = [p, p, i64, i64, f32, p, p, p, p]
         L.trit_intmlp_quant.argtypes = [p, p, i64, i64, f32, f32, p, p, p, p]
@@ -109,7 +120,8 @@ def lib():
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
                      "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
                      "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_quant_act_folded",
-                     "trit_intmlp_quant", "trit_check_div127", "trit_read_probe"):
+                     "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
+                     "trit_intmlp_gemv_many"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -367,6 +379,28 @@ class QProjList:
         self.array = (TritQProj * self.count)(*items)
 
 
+class MlpProjList:
+    """A prepared host array of trit_mlpproj entries (IntMlp down projections,
+    M = 1): (planes, w_scale, a_gate int32 [K], a_up int32 [K], x_scale [1],
+    w_gate, w_up, h_i8 out or None, h_scale out or None, y_i32, y_f32)."""
+
+    def __init__(self, entries):
+        self._keep = []
+        items = []
+        for planes, w_scale, a_gate, a_up, x_scale, w_gate, w_up, h_i8, h_scale, y_i32, y_f32 in entries:
+            K = a_gate.shape[-1]
+            items.append(TritMlpProj(
+                _dev(planes, torch.uint8, "planes"), _dev(a_gate, torch.int32, "a_gate"),
+                _dev(a_up, torch.int32, "a_up"), _dev(x_scale, torch.float32, "x_scale"),
+                float(w_gate), float(w_up), _dev(h_i8, torch.int8, "h_i8", True),
+                _dev(h_scale, torch.float32, "h_scale", True),
+                _dev(y_i32, torch.int32, "y_i32", True), _dev(y_f32, torch.float32, "y_f32", True),
+                planes.shape[0], K, float(w_scale), 0))
+            self._keep.append((planes, a_gate, a_up, x_scale, h_i8, h_scale, y_i32, y_f32))
+        self.count = len(items)
+        self.array = (TritMlpProj * self.count)(*items)
+
+
 class ActList:
     """A prepared host array of trit_act entries: (x fp32 [M, K], x_i8, x_scale)."""
 
@@ -392,6 +426,12 @@ def trit_quant_gemv_many(qlist: QProjList, err_flag: torch.Tensor, stream=None):
     _check(lib().trit_quant_gemv_many(ctypes.cast(qlist.array, ctypes.c_void_p), qlist.count,
                                       _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
            "trit_quant_gemv_many")
+
+
+def trit_intmlp_gemv_many(mlist: MlpProjList, err_flag: torch.Tensor, stream=None):
+    _check(lib().trit_intmlp_gemv_many(ctypes.cast(mlist.array, ctypes.c_void_p), mlist.count,
+                                       _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_intmlp_gemv_many")
 
 
 def trit_quant_act_many(alist: ActList, err_flag: torch.Tensor, stream=None):

@@ -288,6 +288,56 @@ TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count,
     return TRIT_OK;
 }
 
+TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t count,
+                                           uint32_t *err_flag, trit_stream_t stream) {
+    if (!list || count <= 0 || !err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        const trit_mlpproj &p = list[i];
+        if (!p.planes || !p.a_gate || !p.a_up || !p.x_scale || (!p.y_i32 && !p.y_f32) ||
+            p.reserved != 0)
+            return TRIT_E_ARG;
+        if (!aligned(p.planes, 16) || !aligned(p.a_gate, 4) || !aligned(p.a_up, 4) ||
+            !aligned(p.x_scale, 4) || !aligned(p.h_i8, 16) || !aligned(p.h_scale, 4) ||
+            !aligned(p.y_i32, 4) || !aligned(p.y_f32, 4))
+            return TRIT_E_ARG;
+        if (!rows_ok(p.N) || !cols_ok(p.K) || p.K > TRIT_MAX_FUSED_K) return TRIT_E_SHAPE;
+        for (float w : {p.w_scale, p.w_gate, p.w_up})
+            if (!isfinite(w) || !(w > 0.0f)) return TRIT_E_SCALE;
+    }
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    static thread_local MlpProjDev buf[TRIT_MAX_LIST_PER_LAUNCH];
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t base = 0; base < count; base += TRIT_MAX_LIST_PER_LAUNCH) {
+        const int n = count - base < TRIT_MAX_LIST_PER_LAUNCH ? count - base : TRIT_MAX_LIST_PER_LAUNCH;
+        for (int i = 0; i < n; ++i) {
+            const trit_mlpproj &p = list[base + i];
+            MlpProjDev &m = buf[i];
+            m.down.planes = reinterpret_cast<const uint4 *>(p.planes);
+            m.down.x = nullptr;
+            m.down.xf = nullptr;
+            m.down.x_i8_out = p.h_i8;
+            m.down.x_scale = p.h_scale;
+            m.down.y_i32 = p.y_i32;
+            m.down.y_f32 = p.y_f32;
+            m.down.M = 1;
+            m.down.N = p.N;
+            m.down.K = int32_t(p.K);
+            m.down.B = int32_t(beats_per_row(p.K));
+            m.down.w_scale = p.w_scale;
+            m.down.pad_ = 0;
+            m.a_gate = p.a_gate;
+            m.a_up = p.a_up;
+            m.x_scale_in = p.x_scale;
+            m.w_gate = p.w_gate;
+            m.w_up = p.w_up;
+        }
+        cudaError_t e = launch_intmlp_gemv_many(buf, n, err_flag, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TRIT_OK;
+}
+
 TRIT_API trit_status trit_gemm(const uint8_t *planes, float w_scale, const int8_t *x_i8,
                                const float *x_scale, int64_t M, int64_t N, int64_t K,
                                int32_t *y_i32, float *y_f32, uint32_t *err_flag,

@@ -116,19 +116,34 @@ struct Entry {
     int32_t xld;            // activation row stride (K_pad)
     int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / 4)
     int32_t bstride;        // beats per full row of the planes
-    int32_t mrows;          // activation rows of this entry (<= MT)
+    int32_t mrows;          // bits 0-7: activation rows of this entry (<= MT); bits 8-15:
+                            // 1 + index of its IntMlp descriptor (0: none)
     int32_t gcost;          // cost units of one group: iters x a per-step weight
     float w_scale;
 };
 static_assert(sizeof(Entry) == 120, "the list of 256 entries must fit the 32 KB parameter space");
+
+// An IntMlp input (M = 1): the entry's activation row is formed from the int32
+// outputs of the gate and up projections of the same token.
+struct MlpDesc {
+    const int32_t *a_gate, *a_up;   // [K] each
+    const float *x_scale;           // the gate/up input's activation scale
+    float w_gate, w_up;
+};
+constexpr int kMaxMlp = 8;
 
 struct List {
     int32_t count;
     int32_t xs_words;       // shared words per staged activation row
     int64_t total_cost;
     uint32_t *err;
+    MlpDesc mlp[kMaxMlp];
     Entry e[kMaxList];
 };
+static_assert(sizeof(List) <= 32764, "kernel parameter space");
+
+__host__ __device__ __forceinline__ int rows_of(const Entry &E) { return E.mrows & 0xff; }
+__host__ __device__ __forceinline__ int mlp_of(const Entry &E) { return (E.mrows >> 8) & 0xff; }
 
 // Code-word multiply-accumulate of one 32-column plane word pair (M = 1).
 __device__ __forceinline__ void mac_codes(uint32_t P, uint32_t N, const uint32_t (&x)[8],
@@ -201,7 +216,7 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
     for (int hb = ((threadIdx.x >> 5) % kWpr) * 32 + (threadIdx.x & 31); hb < halves;
          hb += kWpr * 32) {
         uint32_t out[8];
-        if (m < E.mrows) {
+        if (m < rows_of(E)) {
             const int c0 = hb * 32;
             const int8_t *xr = E.x + int64_t(m) * E.xld;
             uint32_t in[8];
@@ -317,6 +332,145 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
     return qs.a;
 }
 
+// IntMlp input (M = 1): the codes of t = relu(a_gate)^2 a_up for the row of
+// entry E, round-half-even(127 t / max|t|), straight into the permuted
+// shared-memory layout, with the arithmetic of trit_intmlp_quant.  Pass 1 finds
+// max|t| (one block reduction), pass 2 forms the codes (the second read of a_gate
+// and a_up hits L1).  The owner CTA also writes the natural-layout codes (zero
+// tail to K_pad) and the scale.  The scale goes to *s_scale (shared), readable
+// after the staging barrier.
+__device__ __forceinline__ void stage_x_intmlp(const Entry &E, const MlpDesc &D, uint32_t *xs,
+                                               bool owner, int32_t *s_xsum, float *s_scale) {
+    __shared__ uint64_t s_max[2][kWarps];
+    const int K = E.K;
+    const int halves = E.iters * kLanesPerRow * 2;
+    // 16-byte loads when the rows allow them (K % 4 == 0, 16-byte aligned)
+    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(D.a_gate) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(D.a_up) & 15) == 0);
+    trit_u128 amax = 0;
+    auto take = [&](int32_t g, int32_t u) {
+        bool neg;
+        const trit_u128 t = intmlp_abs_t(g, u, neg);
+        amax = t > amax ? t : amax;
+    };
+    // rounds of four loads per thread and array, issued together (the loads are
+    // predicated, not behind loop exits)
+    if (vec) {
+        const int4 *G = reinterpret_cast<const int4 *>(D.a_gate);
+        const int4 *U = reinterpret_cast<const int4 *>(D.a_up);
+        const int K4 = K / 4;
+        for (int base = 0; base < K4; base += 4 * kThreads) {
+            int4 g[4], u[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = base + r * kThreads + threadIdx.x;
+                g[r] = i < K4 ? G[i] : make_int4(0, 0, 0, 0);
+                u[r] = i < K4 ? U[i] : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                take(g[r].x, u[r].x);
+                take(g[r].y, u[r].y);
+                take(g[r].z, u[r].z);
+                take(g[r].w, u[r].w);
+            }
+        }
+    } else {
+        for (int base = 0; base < K; base += 4 * kThreads) {
+            int32_t g[4], u[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int c = base + r * kThreads + threadIdx.x;
+                g[r] = c < K ? D.a_gate[c] : 0;
+                u[r] = c < K ? D.a_up[c] : 0;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) take(g[r], u[r]);
+        }
+    }
+    uint64_t hi = uint64_t(amax >> 64), lo = uint64_t(amax);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const uint64_t h2 = __shfl_xor_sync(~0u, hi, o), l2 = __shfl_xor_sync(~0u, lo, o);
+        if (h2 > hi || (h2 == hi && l2 > lo)) {
+            hi = h2;
+            lo = l2;
+        }
+    }
+    if ((threadIdx.x & 31) == 0) {
+        s_max[0][threadIdx.x >> 5] = hi;
+        s_max[1][threadIdx.x >> 5] = lo;
+    }
+    __syncthreads();
+    hi = s_max[0][0];
+    lo = s_max[1][0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i)
+        if (s_max[0][i] > hi || (s_max[0][i] == hi && s_max[1][i] > lo)) {
+            hi = s_max[0][i];
+            lo = s_max[1][i];
+        }
+    const IntMlpRow R = intmlp_row(hi, lo);
+    const bool fast = R.small && !R.zero;
+    const int64_t Kp = beats_per_row(K) * 64;
+    int32_t xsum = 0;
+    for (int hb = threadIdx.x; hb < halves; hb += kThreads) {
+        const int c0 = hb * 32;
+        const bool full = vec && c0 + 32 <= K;
+        uint32_t in[8];
+#pragma unroll
+        for (int h8 = 0; h8 < 4; ++h8) {   // eight columns at a time
+            int32_t g[8], u[8];
+            const int cb = c0 + 8 * h8;
+            if (full) {
+                const int4 *G = reinterpret_cast<const int4 *>(D.a_gate + cb);
+                const int4 *U = reinterpret_cast<const int4 *>(D.a_up + cb);
+                const int4 a0 = G[0], a1 = G[1], b0 = U[0], b1 = U[1];
+                g[0] = a0.x; g[1] = a0.y; g[2] = a0.z; g[3] = a0.w;
+                g[4] = a1.x; g[5] = a1.y; g[6] = a1.z; g[7] = a1.w;
+                u[0] = b0.x; u[1] = b0.y; u[2] = b0.z; u[3] = b0.w;
+                u[4] = b1.x; u[5] = b1.y; u[6] = b1.z; u[7] = b1.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const bool ok = cb + j < K;
+                    g[j] = ok ? D.a_gate[cb + j] : 0;   // a zero gate output gives code 0
+                    u[j] = ok ? D.a_up[cb + j] : 0;
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                int v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = 4 * w + j;
+                    v[j] = fast ? intmlp_code_small(g[c], u[c], R) : intmlp_code(g[c], u[c], R);
+                }
+                in[2 * h8 + w] = pack4(v[0], v[1], v[2], v[3]);
+                xsum = dp4a_ss(in[2 * h8 + w], 0x01010101u, xsum);
+            }
+        }
+        if (owner && E.x_i8_out && int64_t(hb) * 32 < Kp) {
+            uint4 *o = reinterpret_cast<uint4 *>(E.x_i8_out + int64_t(hb) * 32);
+            o[0] = make_uint4(in[0], in[1], in[2], in[3]);
+            o[1] = make_uint4(in[4], in[5], in[6], in[7]);
+        }
+        uint32_t out[8];
+        permute_block(in, out);
+        uint32_t *dst = xs + (hb >> 1) * kXBeatWords + (hb & 1) * 8;
+        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+    publish_xsum(xsum, s_xsum);
+    // the scale (double arithmetic, slow on this device) by one thread; the
+    // others read it after the staging barrier
+    if (threadIdx.x == 0) {
+        const float scale = intmlp_scale(hi, lo, D.w_gate, D.w_up, *D.x_scale);
+        *s_scale = scale;
+        if (owner && E.x_scale) *const_cast<float *>(E.x_scale) = scale;
+    }
+}
+
 __device__ __forceinline__ int32_t row_sum4(int32_t v) {
     v += __shfl_xor_sync(~0u, v, 1);
     v += __shfl_xor_sync(~0u, v, 2);
@@ -422,7 +576,7 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
                 for (int m = 0; m < MT; ++m) {
                     const int32_t y = row_sum4(acc[m]);
                     acc[m] = 0;
-                    if (bs == 0 && row < N && m < E.mrows) {
+                    if (bs == 0 && row < N && m < rows_of(E)) {
                         const int64_t o = int64_t(m) * N + row;
                         if (E.acc) {
                             atomicAdd(E.acc + o, y);
@@ -540,7 +694,7 @@ __device__ __forceinline__ uint32_t run_groups2(const Entry &E, const uint32_t *
                 const int32_t ya = row_sum4(accA[m]) - xsum;
                 const int32_t yb = row_sum4(accB[m]) - xsum;
                 accA[m] = accB[m] = 0;
-                if (bs == 0 && m < E.mrows) {
+                if (bs == 0 && m < rows_of(E)) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int64_t r = row + 8 * h;
@@ -659,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
     select_accumulate_kernel(const __grid_constant__ List L) {
     extern __shared__ __align__(16) uint32_t xs[];
     __shared__ int32_t s_xsum[kWarps];
+    __shared__ float s_mlp_scale;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rs = lane / kLanesPerRow, bs = lane % kLanesPerRow;
     const int64_t lo = int64_t(blockIdx.x) * L.total_cost / gridDim.x;
@@ -710,7 +865,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
             waited = true;
         }
         float xsc;
-        if (MT == 1 && E.xf) {
+        if (MT == 1 && mlp_of(E)) {
+            stage_x_intmlp(E, L.mlp[mlp_of(E) - 1], xs, g0 == 0, s_xsum, &s_mlp_scale);
+            xsc = 0.0f;   // read from s_mlp_scale after the barrier
+        } else if (MT == 1 && E.xf) {
             xsc = stage_x_fp32(E, xs, g0 == 0, L.err, s_xsum);
         } else {
             stage_x<MT>(E, xs, L.xs_words, s_xsum);
@@ -718,6 +876,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
         }
         __syncthreads();
         const int32_t xsum = MT == 1 ? read_xsum(s_xsum) : 0;
+        if (MT == 1 && mlp_of(E)) xsc = s_mlp_scale;
         if (wb < we) {
             if constexpr (MT == 1) {
                 if (path == 1) {
@@ -757,10 +916,12 @@ int occupancy(size_t smem) {
 }
 
 template <int MT>
-cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t s) {
+cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
+                        const MlpDesc *mlp = nullptr, int nmlp = 0) {
     static thread_local List L;   // host staging for the by-value parameter block
     L.count = n;
     L.err = err;
+    for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = i < nmlp ? mlp[i] : MlpDesc{};
     int64_t cost = 0, groups = 0;
     int max_iters = 1;
     for (int i = 0; i < n; ++i) {
@@ -899,6 +1060,30 @@ cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaS
 
 cudaError_t launch_gemv_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {
     return launch_products<1>(list, count, err, s);
+}
+
+// IntMlp down projections: up to kMaxMlp per launch (each entry single-segment,
+// its row staged from the gate and up outputs).
+cudaError_t launch_intmlp_gemv_many(const MlpProjDev *list, int count, uint32_t *err,
+                                    cudaStream_t s) {
+    static thread_local Entry buf[kMaxMlp];
+    static thread_local MlpDesc desc[kMaxMlp];
+    for (int base = 0; base < count; base += kMaxMlp) {
+        const int n = count - base < kMaxMlp ? count - base : kMaxMlp;
+        for (int i = 0; i < n; ++i) {
+            const MlpProjDev &m = list[base + i];
+            buf[i] = make_entry(m.down, 0, 1, 0, m.down.B, nullptr);
+            buf[i].mrows |= (i + 1) << 8;
+            desc[i].a_gate = m.a_gate;
+            desc[i].a_up = m.a_up;
+            desc[i].x_scale = m.x_scale_in;
+            desc[i].w_gate = m.w_gate;
+            desc[i].w_up = m.w_up;
+        }
+        cudaError_t e = launch_list<1>(buf, n, err, s, desc, n);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Activation rows are taken 8 at a time (4 or 2 when every product of the list

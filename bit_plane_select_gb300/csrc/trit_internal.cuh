@@ -87,6 +87,104 @@ __device__ __forceinline__ float div127_rn(float f) {
     return __fmaf_rn(r, c, q);
 }
 
+// ---- IntMlp arithmetic ("Tritium: One Weight Format for Ternary Inference ..." --
+// Numerics, IntMlp): t = relu(a_g)^2 * a_u kept integer; the next projection's
+// codes are round-half-even(127 t / max|t|) and its scale is max|t| * S_g^2 S_u
+// with S = w_scale * x_scale / 127.  Shared by the standalone quantiser and the
+// down-projection staging so both give the same codes and scale.
+
+typedef unsigned __int128 trit_u128;
+
+// |t| (exact, < 2^93) and the sign of t.
+__device__ __forceinline__ trit_u128 intmlp_abs_t(int32_t ag, int32_t au, bool &neg) {
+    neg = false;
+    if (ag <= 0 || au == 0) return 0;
+    const uint64_t g2 = uint64_t(ag) * uint64_t(ag);                  // < 2^62
+    neg = au < 0;
+    const uint64_t uu = neg ? uint64_t(-int64_t(au)) : uint64_t(au);   // <= 2^31
+    return trit_u128(g2) * trit_u128(uu);
+}
+
+// Per-row constants of the code computation: A = max|t| (hi:lo), whether the
+// 64-bit path applies (A < 2^56, so 127 A < 2^63) and k = 127 / A in fp32.
+struct IntMlpRow {
+    trit_u128 A;
+    bool small, zero;
+    float k;
+};
+__device__ __forceinline__ IntMlpRow intmlp_row(uint64_t hi, uint64_t lo) {
+    IntMlpRow R;
+    R.A = (trit_u128(hi) << 64) | trit_u128(lo);
+    R.zero = hi == 0 && lo == 0;
+    R.small = hi == 0 && lo < (uint64_t(1) << 56);
+    R.k = R.small && !R.zero ? __fdiv_rn(127.0f, __ull2float_rn(lo)) : 0.0f;
+    return R;
+}
+
+// round-half-even(127 a / A) for 0 <= a <= A, A > 0 (the quotient is <= 127).
+// A < 2^56: q0 = trunc(fl(a) * k) is within one of floor(127 a / A) (fp32
+// relative error below 2^-21, times at most 127), then the exact remainder
+// r = 127 a - q A in 64-bit integers fixes q to the floor and decides the
+// rounding.  Otherwise: a 7-step binary search in 128-bit integers.
+__device__ __forceinline__ int round_127_ratio_small(uint64_t a64, uint64_t A, float k) {
+    int q = __float2int_rz(__fmul_rn(__ull2float_rn(a64), k));
+    q = q > 127 ? 127 : q;
+    int64_t r = int64_t(a64 * 127u) - int64_t(q) * int64_t(A);
+    if (r < 0) {
+        --q;
+        r += int64_t(A);
+    } else if (r >= int64_t(A)) {
+        ++q;
+        r -= int64_t(A);
+    }
+    const uint64_t r2 = uint64_t(r) * 2u;
+    if (r2 > A || (r2 == A && (q & 1))) ++q;
+    return q;
+}
+
+__device__ __forceinline__ int round_127_ratio(trit_u128 a, const IntMlpRow &R) {
+    if (R.small) return round_127_ratio_small(uint64_t(a), uint64_t(R.A), R.k);
+    const trit_u128 n = a * 127u;
+    int q = 0;
+#pragma unroll
+    for (int b = 64; b; b >>= 1)
+        if (trit_u128(q + b) * R.A <= n) q += b;
+    const trit_u128 r = n - trit_u128(q) * R.A;
+    if (2 * r > R.A || (2 * r == R.A && (q & 1))) ++q;
+    return q;
+}
+
+// The signed code of one column.
+__device__ __forceinline__ int intmlp_code(int32_t ag, int32_t au, const IntMlpRow &R) {
+    if (R.zero) return 0;
+    bool neg;
+    const trit_u128 t = intmlp_abs_t(ag, au, neg);
+    const int v = round_127_ratio(t, R);
+    return neg ? -v : v;
+}
+
+// The same for a row with A < 2^56 (R.small, not R.zero): every |t| <= A fits
+// 64 bits, so |t| is formed in 64-bit arithmetic.
+__device__ __forceinline__ int intmlp_code_small(int32_t ag, int32_t au, const IntMlpRow &R) {
+    if (ag <= 0 || au == 0) return 0;
+    const uint64_t uu = au < 0 ? uint64_t(-int64_t(au)) : uint64_t(au);
+    const uint64_t t = uint64_t(ag) * uint64_t(ag) * uu;
+    const int v = round_127_ratio_small(t, uint64_t(R.A), R.k);
+    return au < 0 ? -v : v;
+}
+
+// max|t| (hi:lo) * ((S_g * S_g) * S_u), S = w * x_scale / 127, in double, rounded once.
+__device__ __forceinline__ float intmlp_scale(uint64_t hi, uint64_t lo, float w_g, float w_u,
+                                              float x_scale) {
+    const double s = double(x_scale);
+    const double sg = __ddiv_rn(__dmul_rn(double(w_g), s), 127.0);
+    const double su = __ddiv_rn(__dmul_rn(double(w_u), s), 127.0);
+    const double k = __dmul_rn(__dmul_rn(sg, sg), su);
+    const double a = __dadd_rn(__dmul_rn(__ull2double_rn(hi), 18446744073709551616.0),
+                               __ull2double_rn(lo));
+    return __double2float_rn(__dmul_rn(a, k));
+}
+
 // The fp32 dequantisation of one output, one rounding per step, never contracted.
 __device__ __forceinline__ float dequant(int32_t y, float w_scale, float x_scale) {
     float f = __int2float_rn(y);
@@ -168,6 +266,19 @@ struct ProjDev {            // one product as a kernel sees it
     float w_scale;
     int32_t pad_;
 };
+
+// One IntMlp down projection (M = 1): its activation row is formed in the
+// launch from the gate and up projections' int32 outputs.  `down` carries the
+// planes, the outputs (x_i8_out = the codes, x_scale = their scale, both
+// optional), N, K, B and w_scale; its x and xf are NULL.
+struct MlpProjDev {
+    ProjDev down;
+    const int32_t *a_gate, *a_up;
+    const float *x_scale_in;
+    float w_gate, w_up;
+};
+cudaError_t launch_intmlp_gemv_many(const MlpProjDev *list, int count, uint32_t *err,
+                                    cudaStream_t s);
 
 cudaError_t launch_pack(const int8_t *w, int64_t N, int64_t K, float w_scale, uint8_t *planes,
                         float *scale_out, uint32_t *err, cudaStream_t s);

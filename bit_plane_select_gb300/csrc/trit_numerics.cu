@@ -88,30 +88,6 @@ __global__ void __launch_bounds__(kNThreads) quant_folded_kernel(const float *x,
 
 // ---- IntMlp ----------------------------------------------------------------------
 
-typedef unsigned __int128 u128;
-
-__device__ __forceinline__ u128 intmlp_abs_t(int32_t ag, int32_t au, bool &neg) {
-    neg = false;
-    if (ag <= 0 || au == 0) return 0;
-    const uint64_t g2 = uint64_t(ag) * uint64_t(ag);            // < 2^62
-    neg = au < 0;
-    const uint64_t uu = neg ? uint64_t(-int64_t(au)) : uint64_t(au);   // <= 2^31
-    return u128(g2) * u128(uu);                                  // < 2^93
-}
-
-// round-half-even(127 a / A) for 0 <= a <= A, A > 0, without a 128-bit divide:
-// the quotient is at most 127, found by a 7-step binary search.
-__device__ __forceinline__ int round_127_ratio(u128 a, u128 A) {
-    const u128 n = a * 127u;
-    int q = 0;
-#pragma unroll
-    for (int b = 64; b; b >>= 1)
-        if (u128(q + b) * A <= n) q += b;
-    const u128 r = n - u128(q) * A;
-    if (2 * r > A || (2 * r == A && (q & 1))) ++q;
-    return q;
-}
-
 __global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *ag, const int32_t *au,
                                                                  int64_t M, int64_t N, int64_t ldq,
                                                                  float w_g, float w_u,
@@ -120,11 +96,21 @@ __global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *
     __shared__ uint64_t red[2][kNWarps];
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const int32_t *gr = ag + m * N, *ur = au + m * N;
-        u128 amax = 0;
-        for (int64_t c = threadIdx.x; c < N; c += kNThreads) {
-            bool neg;
-            const u128 t = intmlp_abs_t(gr[c], ur[c], neg);
-            amax = t > amax ? t : amax;
+        trit_u128 amax = 0;
+        for (int64_t base = 0; base < N; base += 8 * kNThreads) {   // 8 predicated loads per array
+            int32_t g[8], u[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int64_t c = base + r * kNThreads + threadIdx.x;
+                g[r] = c < N ? gr[c] : 0;
+                u[r] = c < N ? ur[c] : 0;
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                bool neg;
+                const trit_u128 t = intmlp_abs_t(g[r], u[r], neg);
+                amax = t > amax ? t : amax;
+            }
         }
         uint64_t hi = uint64_t(amax >> 64), lo = uint64_t(amax);
 #pragma unroll
@@ -147,27 +133,25 @@ __global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *
                 hi = red[0][i];
                 lo = red[1][i];
             }
-        const u128 A = (u128(hi) << 64) | u128(lo);
+        const IntMlpRow R = intmlp_row(hi, lo);
         int8_t *qr = q + m * ldq;
-        for (int64_t c = threadIdx.x; c < ldq; c += kNThreads) {
-            int v = 0;
-            if (c < N && A != 0) {
-                bool neg;
-                const u128 t = intmlp_abs_t(gr[c], ur[c], neg);
-                v = round_127_ratio(t, A);
-                v = neg ? -v : v;
+        const bool fast = R.small && !R.zero;
+        for (int64_t base = 0; base < ldq; base += 8 * kNThreads) {
+            int32_t g[8], u[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int64_t c = base + r * kNThreads + threadIdx.x;
+                g[r] = c < N ? gr[c] : 0;   // past N: code 0
+                u[r] = c < N ? ur[c] : 0;
             }
-            qr[c] = int8_t(v);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int64_t c = base + r * kNThreads + threadIdx.x;
+                if (c < ldq)
+                    qr[c] = int8_t(fast ? intmlp_code_small(g[r], u[r], R) : intmlp_code(g[r], u[r], R));
+            }
         }
-        if (threadIdx.x == 0) {
-            const double s = double(x_scale[m]);
-            const double sg = __ddiv_rn(__dmul_rn(double(w_g), s), 127.0);
-            const double su = __ddiv_rn(__dmul_rn(double(w_u), s), 127.0);
-            const double k = __dmul_rn(__dmul_rn(sg, sg), su);
-            const double a = __dadd_rn(__dmul_rn(__ull2double_rn(hi), 18446744073709551616.0),
-                                       __ull2double_rn(lo));
-            h_scale[m] = __double2float_rn(__dmul_rn(a, k));
-        }
+        if (threadIdx.x == 0) h_scale[m] = intmlp_scale(hi, lo, w_g, w_u, x_scale[m]);
         __syncthreads();   // red reused by the next row
     }
 }

@@ -226,6 +226,40 @@ typedef struct trit_qproj {
 TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count,
                                           uint32_t *err_flag, trit_stream_t stream);
 
+/* One fused down projection of an IntMlp block ("Tritium: One Weight Format for
+ * Ternary Inference ..." -- Numerics, IntMlp): the int32 gate and up outputs of
+ * one token (a_gate, a_up, K values each, K = this projection's K) become this
+ * projection's codes -- round-half-even(127 t / max|t|) of t = relu(a_gate)^2 *
+ * a_up, exact -- and scale max|t| * S_g^2 * S_u (S = w * x_scale / 127), and
+ * are multiplied, in the same launch.  M = 1. */
+typedef struct trit_mlpproj {
+    const uint8_t *planes;    /* the down projection, N x K */
+    const int32_t *a_gate;    /* [K] gate output, device, 4-byte aligned */
+    const int32_t *a_up;      /* [K] up output */
+    const float *x_scale;     /* [1] the gate/up input's activation scale (device) */
+    float w_gate, w_up;       /* the gate and up projections' weight scales */
+    int8_t *h_i8;             /* out, may be NULL: the codes, K_pad bytes, zero tail */
+    float *h_scale;           /* out, may be NULL: their scale */
+    int32_t *y_i32;           /* may be NULL */
+    float *y_f32;             /* may be NULL (not both) */
+    int64_t N, K;
+    float w_scale;            /* the down projection's */
+    uint32_t reserved;        /* must be 0 */
+} trit_mlpproj;
+
+/*
+ * trit_intmlp_gemv_many -- for each entry, trit_intmlp_quant of its gate and up
+ * outputs followed by trit_gemv of the codes: y_i32, y_f32 and, when asked for,
+ * h_i8 and h_scale are bit-identical to that two-call path.  Every CTA of the
+ * launch forms the codes it needs while staging the row, so the int8 codes
+ * make no round trip through memory; up to 8 entries share one launch (longer
+ * lists take several).  K is limited to TRIT_MAX_FUSED_K (TRIT_E_SHAPE beyond);
+ * w_gate, w_up and w_scale must be finite and > 0 (TRIT_E_SCALE).  `list` is a
+ * host array; asynchronous on `stream`.
+ */
+TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t count,
+                                           uint32_t *err_flag, trit_stream_t stream);
+
 /*
  * trit_quant_act_folded -- quantise the normalised activations of a layer
  * without dividing by the rms ("Tritium ..." -- Numerics, Folded).  For each

@@ -48,6 +48,40 @@ def test_struct_layouts(trit):
     assert trit.TritProj.w_scale.offset == 64
     assert ctypes.sizeof(trit.TritAct) == 40
     assert ctypes.sizeof(trit.TritQProj) == 72 and trit.TritQProj.w_scale.offset == 64
+    assert ctypes.sizeof(trit.TritMlpProj) == 96
+
+
+def test_struct_layouts_match_the_c_compiler(trit, tmp_path):
+    """Every field offset of the ctypes mirrors equals what the C compiler lays
+    out from include/trit.h."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"trit_proj": trit.TritProj, "trit_qproj": trit.TritQProj,
+               "trit_act": trit.TritAct, "trit_mlpproj": trit.TritMlpProj}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "trit.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {}
+    for line in out:
+        if line:
+            c, f, v = line.split()
+            got[(c, f)] = int(v)
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
 
 
 def test_payload_bytes(trit):
