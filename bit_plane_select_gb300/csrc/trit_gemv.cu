@@ -12,7 +12,9 @@
 // 8 x 64 contiguous bytes (whole 32-byte sectors).  A "group" is 8 rows; it
 // takes ceil(B/4) steps.  The launch is persistent: every CTA gets an equal
 // share of the total steps of the list (groups never split) and each warp a
-// contiguous run of the CTA's groups.  The CTA keeps the activation row(s) of
+// contiguous run of the CTA's groups; every entry's cost is preceded by a fixed
+// staging charge, so CTAs that stage more entries get fewer groups.  The CTA
+// keeps the activation row(s) of
 // the current product in shared memory in the permuted layout of
 // trit_internal.cuh.  Loads past the end of a warp's rows or of a row's beats
 // are clamped to the last valid address (their data meets zero activations or
@@ -94,6 +96,14 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 #ifndef TRIT_WAVES
 #define TRIT_WAVES 1
 #endif
+// Cost units charged ahead of each entry's groups for staging its activations
+// (M = 1 launches; a group step costs 100; 0 disables): a CTA whose share starts
+// an entry gets that much less group work.  Measured on the 30-layer stack (3,000 ... 70,000
+// swept): 30,000 (the time of ~11 average CTA group-steps per warp) is best.
+#ifndef TRIT_STAGE_COST
+#define TRIT_STAGE_COST 30000
+#endif
+constexpr int64_t kStageCost = TRIT_STAGE_COST;
 constexpr int kL2Ahead = TRIT_L2_AHEAD;
 
 // Beats per column segment for MT staged rows: MT * seg_beats * 80 bytes of
@@ -926,6 +936,7 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
     int max_iters = 1;
     for (int i = 0; i < n; ++i) {
         L.e[i] = entries[i];
+        if (MT == 1) cost += kStageCost;   // staging the entry's row, charged to whoever starts it
         L.e[i].cost_begin = cost;
         cost += entries[i].groups * entries[i].gcost;
         groups += entries[i].groups;
