@@ -221,12 +221,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 
 
-// 16-byte asynchronous global -> shared copy through L2; src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
 // 4-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),

@@ -313,11 +313,11 @@ TRIT_API trit_status trit_intmlp_quant(const int32_t *a_gate, const int32_t *a_u
  * is part of the library's device image instead.  The other paths use no
  * scratch and are those of trit_gemm.
  *
- *   Limit     the copy takes 16384 * ceil(M/128) * ceil(K/64) bytes when
+ *   Limit     the copy takes 32768 * ceil(M/256) * ceil(K/64) bytes when
  *             M >= 17 and K < 131072 (0 otherwise); the call returns
  *             TRIT_E_SCRATCH, enqueuing nothing, when that exceeds
- *             TRIT_NOALLOC_SCRATCH_BYTES (32 MiB: ceil(M/128) * ceil(K/64)
- *             <= 2048, e.g. M = 2048 with K <= 8192).  Split M to stay inside.
+ *             TRIT_NOALLOC_SCRATCH_BYTES (32 MiB: ceil(M/256) * ceil(K/64)
+ *             <= 1024, e.g. M = 2048 with K <= 8192).  Split M to stay inside.
  *   Set-up    the first call on each device looks the buffer's address up with
  *             that device current (cudaGetSymbolAddress, which may load the
  *             library's device image and reserve the buffer) and keeps it for

@@ -26,10 +26,11 @@ def t():
 
 
 def scratch_bytes(M, K):
-    """Bytes of the fp16 activation copy the tensor-core path needs."""
+    """Bytes of the fp16 activation copy the tensor-core path needs: 16 KB
+    blocks of 128 rows x 64 columns, row blocks in pairs (256-row pair tiles)."""
     if M < 17 or K >= 131072:
         return 0
-    return 16384 * ((M + 127) // 128) * ((K + 63) // 64)
+    return 32768 * ((M + 255) // 256) * ((K + 63) // 64)
 
 
 def make_product(t, M, N, K, seed):
@@ -94,6 +95,21 @@ def test_two_calls_in_a_row_match_trit_gemm(t, first, second):
     same(ra, ea)
     same(rb, eb)
     assert int(ra[2].item()) == 0 and int(rb[2].item()) == 0
+
+
+def test_limit_counts_row_blocks_in_pairs(t):
+    """M = 1920 (15 blocks of 128 rows, padded to 16) with K = 8192 (128 beats)
+    needs exactly 32 MiB and runs; K = 8193 (129 beats) does not."""
+    M, N = 1920, 8
+    assert scratch_bytes(M, 8192) == t.NOALLOC_SCRATCH_BYTES
+    assert scratch_bytes(M, 8193) > t.NOALLOC_SCRATCH_BYTES
+    P = make_product(t, M, N, 8192, seed=5)
+    same(via_noalloc(t, P), via_gemm(t, P))
+    Q = make_product(t, M, N, 8193, seed=6)
+    y32, yf, err = outputs(Q)
+    with pytest.raises(t.TritError) as info:
+        t.trit_gemm_noalloc(Q["planes"], Q["ws"], Q["x"], Q["xs"], Q["K"], y32, yf, err)
+    assert info.value.status == 8
 
 
 def test_one_output_only(t):
