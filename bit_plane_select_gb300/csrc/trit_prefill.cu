@@ -23,8 +23,9 @@
 //     128r.. of the tile (its half of operand B); its tensor memory receives
 //     its 128 rows x all 256 columns.  One beat per pipeline stage, five stages
 //     of 32 KB per CTA.  Per stage one thread brings the CTA's activation block
-//     with a bulk copy; eight producer warps (two threads per weight row, half
-//     a beat each) expand the 128 weight beats to fp16 +-1 in the same column
+//     with a bulk copy; four producer warps (one thread per weight row: its
+//     beat arrives by a 16-byte cp.async) expand the 128 weight beats to fp16
+//     +-1 in the same column
 //     order ((P & m_s) * (0x3C00 >> s) sets +1.0 in each half whose bit is
 //     set, -1.0 = 0xBC00 likewise).  In the leader CTA (rank 0) one thread
 //     issues the MMAs once both CTAs' stages are full (the peer's MMA warp
@@ -54,7 +55,8 @@ constexpr int kPairN = 2 * kHalfN;        // weight rows per pair tile (MMA N)
 constexpr int kBK = 64;                   // columns per stage (one beat)
 constexpr int kStages = 5;                // MMA operand stages
 constexpr int kRaw = 4;                   // plane half-beats in flight per producer thread
-constexpr int kProducerWarps = 8;
+constexpr int kProducerWarps = 4;   // measured: 2 / 8 / 16 warps are slower (the
+                                    // per-thread proxy fence of each stage is the cost)
 constexpr int kMmaWarp = kProducerWarps;  // MMA issue (leader) or relay (peer)
 constexpr int kEpiWarp0 = kMmaWarp + 1;
 constexpr int kEpiWarps = 8;              // two per TMEM lane quarter, 128 columns each
@@ -62,7 +64,7 @@ constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr int kBlock = kSubM * kBK * 2;   // one 16 KB activation block (fp16)
 constexpr int kBStage = kHalfN * kBK * 2; // 16 KB of expanded weights
 constexpr int kStage = kBlock + kBStage;
-constexpr int kRawStage = kProducerWarps * 32 * 8;    // per thread: its half of pos and neg
+constexpr int kRawStage = kProducerWarps * 32 * 16;   // per thread: its row's beat
 constexpr int kAccCols = kPairN;          // fp32 columns of one accumulator
 constexpr int kTmemCols = 2 * kAccCols;   // two accumulators: all 512 columns
 constexpr int kPitch = 36;                // words per epilogue staging row: 32 + 4 of padding
@@ -71,7 +73,7 @@ constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s
 constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStage + size_t(kRaw) * kRawStage +
                               kEpiBytes + 256;
-static_assert(kProducerWarps * 32 == 2 * kHalfN, "two producer threads per weight beat");
+static_assert(kProducerWarps * 32 == kHalfN, "one producer thread per weight beat");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 struct PEntry {
@@ -221,9 +223,9 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 
 
-// 4-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+// 16-byte asynchronous global -> shared copy through L2; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
                  "r"(src_bytes)
                  : "memory");
 }
@@ -417,9 +419,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kProducerWarps) {
-        // thread p: half (p & 1) of weight row 128*rank + (p >> 1) of each tile
+        // thread p: weight row 128*rank + p of each tile, the whole beat
         const int p = threadIdx.x;
-        const int br = p >> 1, bh = p & 1;
+        const int br = p;
         // load cursor (kRaw stages ahead of the consume cursor, across tiles)
         int64_t lt = pair;
         int lkb = 0, lnk = 0;
@@ -431,18 +433,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int64_t wn = r.nt * kPairN + int64_t(rank) * kHalfN + br;
             const bool ok = wn < E.N;
             lrow = reinterpret_cast<const uint8_t *>(E.planes + (ok ? wn : 0) * E.B);
-            lbytes = ok ? 4u : 0u;
+            lbytes = ok ? 16u : 0u;
             lnk = E.B;
             lkb = 0;
         };
         if (lt < L.total_tiles) load_tile(lt);
         int64_t li = 0;   // loads issued
-        auto issue_next = [&]() {   // this half's pos word and neg word of the next beat
+        auto issue_next = [&]() {   // the row's next beat (pos and neg words)
             if (lt < L.total_tiles) {
-                uint8_t *slot = raw + int(li % kRaw) * kRawStage + p * 8;
+                uint8_t *slot = raw + int(li % kRaw) * kRawStage + p * 16;
                 const uint8_t *beat = lrow + int64_t(lkb) * 16;
-                cp_async4(slot, beat + 4 * bh, lbytes);
-                cp_async4(slot + 4, beat + 8 + 4 * bh, lbytes);
+                cp_async16(slot, beat, lbytes);
                 ++li;
                 if (++lkb == lnk) {
                     lt += npairs;
@@ -475,14 +476,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     bulk_load(a_st, xblk + int64_t(kb) * kBlock, kBlock, &full[s]);
                 }
                 cp_async_wait<kRaw - 1>();
-                const uint2 pn = *reinterpret_cast<const uint2 *>(raw + int(it % kRaw) * kRawStage + p * 8);
-                viol |= pn.x & pn.y;
-                {   // weights: chunks 4*bh .. 4*bh+3 of row br
+                const uint4 pn = *reinterpret_cast<const uint4 *>(raw + int(it % kRaw) * kRawStage + p * 16);
+                viol |= (pn.x & pn.z) | (pn.y & pn.w);
+#pragma unroll
+                for (int bh = 0; bh < 2; ++bh) {   // weights: chunks 4*bh .. 4*bh+3 of row br
+                    const uint32_t P = bh ? pn.y : pn.x, Q = bh ? pn.w : pn.z;
                     uint32_t w[8];
-                    expand_quarter(pn.x, pn.y, w);
+                    expand_quarter(P, Q, w);
                     *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh)) = make_uint4(w[0], w[1], w[2], w[3]);
                     *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-                    expand_quarter(pn.x >> 8, pn.y >> 8, w);
+                    expand_quarter(P >> 8, Q >> 8, w);
                     *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 2)) = make_uint4(w[0], w[1], w[2], w[3]);
                     *reinterpret_cast<uint4 *>(b_st + sw128_off(br, 4 * bh + 3)) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
