@@ -87,8 +87,9 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
     if (st != TRIT_OK) return st;
     static thread_local ProjDev one[TRIT_MAX_LIST_PER_LAUNCH];
     static thread_local ProjDev many[TRIT_MAX_LIST_PER_LAUNCH];
+    static thread_local ProjDev skinny[TRIT_MAX_LIST_PER_LAUNCH];
     static thread_local ProjDev dense[TRIT_MAX_LIST_PER_LAUNCH];
-    int n1 = 0, nm = 0, nd = 0;
+    int n1 = 0, nm = 0, ns = 0, nd = 0;
     auto flush1 = [&]() -> cudaError_t {
         cudaError_t e = n1 ? launch_gemv_many(one, n1, err_flag, s) : cudaSuccess;
         n1 = 0;
@@ -97,6 +98,11 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
     auto flushm = [&]() -> cudaError_t {
         cudaError_t e = nm ? launch_gemm_dp4a_many(many, nm, err_flag, s) : cudaSuccess;
         nm = 0;
+        return e;
+    };
+    auto flushs = [&]() -> cudaError_t {
+        cudaError_t e = ns ? launch_skinny_many(skinny, ns, err_flag, s) : cudaSuccess;
+        ns = 0;
         return e;
     };
     auto flushd = [&]() -> cudaError_t {
@@ -110,6 +116,9 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
         if (d.M == 1) {
             one[n1++] = d;
             if (n1 == TRIT_MAX_LIST_PER_LAUNCH) e = flush1();
+        } else if (skinny_supported(d)) {
+            skinny[ns++] = d;
+            if (ns == TRIT_MAX_LIST_PER_LAUNCH) e = flushs();
         } else if (prefill_supported(d)) {
             dense[nd++] = d;
             if (nd == TRIT_MAX_LIST_PER_LAUNCH) e = flushd();
@@ -121,6 +130,7 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
     }
     cudaError_t e = flush1();
     if (e == cudaSuccess) e = flushm();
+    if (e == cudaSuccess) e = flushs();
     if (e == cudaSuccess) e = flushd();
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
@@ -443,14 +453,17 @@ TRIT_API trit_status trit_gemm_noalloc(const uint8_t *planes, float w_scale, con
     trit_status st = check_proj(p);
     if (st != TRIT_OK) return st;
     const ProjDev d = to_dev(p);
-    // Only the tensor-core path uses scratch; the others allocate nothing.
-    if (!prefill_supported(d)) return run_many(&p, 1, err_flag, s);
-    if (prefill_scratch_bytes(d) > TRIT_NOALLOC_SCRATCH_BYTES) return TRIT_E_SCRATCH;
+    // Only the tensor-core paths use scratch; the others allocate nothing.
+    const bool small = skinny_supported(d);
+    if (!small && !prefill_supported(d)) return run_many(&p, 1, err_flag, s);
+    const int64_t need = small ? skinny_scratch_bytes(d) : prefill_scratch_bytes(d);
+    if (need > TRIT_NOALLOC_SCRATCH_BYTES) return TRIT_E_SCRATCH;
     st = check_device();
     if (st != TRIT_OK) return st;
     uint8_t *xh = nullptr;
     cudaError_t e = fixed_scratch(&xh);
-    if (e == cudaSuccess) e = launch_prefill_into(d, xh, err_flag, s);
+    if (e == cudaSuccess)
+        e = small ? launch_skinny_into(d, xh, err_flag, s) : launch_prefill_into(d, xh, err_flag, s);
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
 

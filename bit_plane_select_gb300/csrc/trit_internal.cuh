@@ -293,9 +293,18 @@ cudaError_t launch_gemv_many(const ProjDev *list, int count, uint32_t *err, cuda
 // 2 <= M products, dp4a with beats reused across rows held in registers.
 cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
 
-// M >= kPrefillMinM (and K < 2^17, where fp32 accumulation of integer partial
-// sums stays exact) runs on the tensor cores.
-constexpr int64_t kPrefillMinM = 17;
+// kSkinnyMinM <= M <= kSkinnyMaxM (and K < 2^17, where fp32 accumulation of
+// integer partial sums stays exact) runs on the tensor cores with the weights
+// as the 128-row operand; larger M on CTA pairs with 256 x 256 tiles.
+constexpr int64_t kSkinnyMinM = 17;
+constexpr int64_t kSkinnyMaxM = 128;
+bool skinny_supported(const ProjDev &p);
+cudaError_t launch_skinny_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
+// Bytes of the fp16 activation copy the small-M tensor-core path needs for p
+// (128 * ceil(M/16)*16 * ceil(K/64): at most 32 MiB).
+int64_t skinny_scratch_bytes(const ProjDev &p);
+cudaError_t launch_skinny_into(const ProjDev &p, uint8_t *xh, uint32_t *err, cudaStream_t s);
+constexpr int64_t kPrefillMinM = kSkinnyMaxM + 1;
 bool prefill_supported(const ProjDev &p);
 cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s);
 // Bytes of the fp16 activation copy the tensor-core path needs for p.

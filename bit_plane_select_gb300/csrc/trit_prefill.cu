@@ -43,16 +43,17 @@
 // Every mbarrier wait is bounded: after kWaitNs it sets TRIT_ERR_TIMEOUT and
 // the roles unwind; before tensor memory is freed each CTA waits, again
 // bounded, for the last MMA commit.
-#include "trit_internal.cuh"
+#include "trit_tc.cuh"
 
 namespace trit {
 namespace {
+
+using namespace tc;
 
 constexpr int kSubM = 128;                // activation rows per CTA (TMEM lanes)
 constexpr int kPairM = 2 * kSubM;         // activation rows per pair tile (MMA M)
 constexpr int kHalfN = 128;               // weight rows expanded per CTA
 constexpr int kPairN = 2 * kHalfN;        // weight rows per pair tile (MMA N)
-constexpr int kBK = 64;                   // columns per stage (one beat)
 constexpr int kStages = 5;                // MMA operand stages
 constexpr int kRaw = 4;                   // plane half-beats in flight per producer thread
 constexpr int kProducerWarps = 4;   // measured: 2 / 8 / 16 warps are slower (the
@@ -70,7 +71,6 @@ constexpr int kTmemCols = 2 * kAccCols;   // two accumulators: all 512 columns
 constexpr int kPitch = 36;                // words per epilogue staging row: 32 + 4 of padding
 constexpr int kEpiBytes = kEpiWarps * 32 * kPitch * 4;
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
-constexpr unsigned long long kWaitNs = 4000000000ull;   // 4 s
 constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStage + size_t(kRaw) * kRawStage +
                               kEpiBytes + 256;
 static_assert(kProducerWarps * 32 == kHalfN, "one producer thread per weight beat");
@@ -100,73 +100,7 @@ struct PList {
 static_assert(sizeof(PList) <= 32764, "kernel parameter space");
 
 
-// ---- PTX wrappers -------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase of the given parity (acquire at cluster scope: some arrivals
-// come from the peer CTA); false after kWaitNs (then *timed_out is set).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *timed_out) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*reinterpret_cast<volatile uint32_t *>(timed_out)) return false;
-        if (global_ns() - t0 > kWaitNs) {
-            atomicExch(timed_out, 1u);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-
-// 128-byte-swizzled K-major shared-memory matrix descriptor (version 1): start
-// address, leading offset 16 B (unused for this layout), stride 1024 B between
-// groups of eight 128-byte rows.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
-           (uint64_t(1) << 46) | (uint64_t(2) << 61);
-}
+// ---- pair-specific PTX wrappers (the shared ones are in trit_tc.cuh) ---------
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
 // K-major, N = 256, M = 256 (the pair).
@@ -223,88 +157,7 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 
 
-// 16-byte asynchronous global -> shared copy through L2; src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
-                     smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned,
-// size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(sdst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-    return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
-
-// 8 fp16x2 words (cols 32h + k and 32h + k + 16, k = k0..k0+7, k0 = 0 or 8) of one
-// plane half; for k0 = 8 the caller passes the words shifted right by 8.
-__device__ __forceinline__ void expand_quarter(uint32_t P, uint32_t N, uint32_t (&w)[8]) {
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-        const uint32_t m = 0x00010001u << s;
-        w[s] = (P & m) * (0x3C00u >> s) + (N & m) * (0xBC00u >> s);
-    }
-}
-
-// 16 fp16x2 words of activation columns 32h..32h+31 (natural int8 words in[0..7]).
-__device__ __forceinline__ void convert_half(const uint32_t (&in)[8], uint32_t (&w)[16]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t u = in[q] ^ 0x80808080u, v = in[q + 4] ^ 0x80808080u;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t t = prmt(u, v, uint32_t(i) | (uint32_t(4 + i) << 8));
-            const uint32_t h = (t & 0x00FF00FFu) | 0x64006400u;   // 1024 + (x + 128)
-            w[4 * q + i] = hsub2(h, 0x64806480u);                // minus 1152
-        }
-    }
-}
-
 // ---- activation conversion: int8 [M][K_pad] -> blocked, swizzled fp16 -------------
-
-struct CEntry {
-    const int8_t *x;       // [M][K_pad]
-    uint8_t *xh;           // [mblocks][B][kBlock bytes]
-    int64_t M;
-    int64_t half_begin;    // prefix sum of mblocks*128*2*B (one thread per row half-beat)
-    int32_t K, B;
-};
-
-struct CList {
-    int32_t count;
-    int32_t pad_;
-    int64_t total;
-    CEntry e[kMaxList];
-};
 
 // One thread per (row, half-beat): 32 int8 in, 4 fp16 chunks of 16 bytes out.
 __global__ void __launch_bounds__(256) act_f16_kernel(const __grid_constant__ CList L) {
@@ -340,8 +193,9 @@ __global__ void __launch_bounds__(256) act_f16_kernel(const __grid_constant__ CL
         }
         uint32_t w[16];
         convert_half(in, w);   // rows past M hold x = 0 and convert to +0.0
-        const int r = int(m % kSubM);
-        uint8_t *blk = E.xh + ((m / kSubM) * E.B + kb) * int64_t(kBlock);
+        const int64_t br = E.brows;
+        const int r = int(m % br);
+        uint8_t *blk = E.xh + ((m / br) * E.B + kb) * (br * 128);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4 *>(blk + sw128_off(r, 4 * h + c)) =
@@ -649,15 +503,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fin = __shfl_sync(~0u, fin, 0);
         (void)fin;
     }
-    if (threadIdx.x == 0) {
+    tc_fence_before();
+    cluster_sync_all();   // neither CTA frees tensor memory while the pair's MMAs may run
+    tc_fence_after();
+    if (threadIdx.x == 0) {   // after the last wait: every flag is set by now
         uint32_t f = 0;
         if (*timed_out) f |= TRIT_ERR_TIMEOUT;
         if (*viol_any) f |= TRIT_ERR_P1;
         if (f) atomicOr(L.err, f);
     }
-    tc_fence_before();
-    cluster_sync_all();   // neither CTA frees tensor memory while the pair's MMAs may run
-    tc_fence_after();
     if (warp == kMmaWarp)
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
@@ -679,7 +533,7 @@ cudaError_t launch_two(const ProjDev *list, int n, uint8_t *const *xh, uint32_t 
     L.count = n;
     L.pad_ = 0;
     L.err = err;
-    int64_t halves = 0, tiles = 0;
+    int64_t tiles = 0;
     for (int i = 0; i < n; ++i) {
         const ProjDev &p = list[i];
         const int64_t mblocks = act_blocks(p);
@@ -689,8 +543,8 @@ cudaError_t launch_two(const ProjDev *list, int n, uint8_t *const *xh, uint32_t 
         c.M = p.M;
         c.K = p.K;
         c.B = p.B;
-        c.half_begin = halves;
-        halves += mblocks * kSubM * 2 * int64_t(p.B);
+        c.brows = kSubM;
+        c.mblocks = int32_t(mblocks);
         PEntry &E = L.e[i];
         E.planes = p.planes;
         E.xh = xh[i];
@@ -708,13 +562,8 @@ cudaError_t launch_two(const ProjDev *list, int n, uint8_t *const *xh, uint32_t 
         E.tile_begin = tiles;
         tiles += int64_t(E.mtiles) * E.ntiles;
     }
-    C.total = halves;
     L.total_tiles = tiles;
-    int64_t cblocks = (halves + 255) / 256;
-    const int64_t cap = int64_t(device_sm_count()) * 16;
-    cblocks = cblocks < cap ? cblocks : cap;
-    act_f16_kernel<<<int(cblocks), 256, 0, s>>>(C);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_act_f16(C, s);
     if (e != cudaSuccess) return e;
     if (tiles == 0) return cudaSuccess;
     // persistent: one pair per two SMs (at most one pair per tile)
@@ -780,4 +629,22 @@ cudaError_t launch_prefill_many(const ProjDev *list, int count, uint32_t *err, c
     return cudaSuccess;
 }
 
+namespace tc {
+
+cudaError_t launch_act_f16(CList &C, cudaStream_t s) {
+    int64_t halves = 0;
+    for (int i = 0; i < C.count; ++i) {
+        C.e[i].half_begin = halves;
+        halves += int64_t(C.e[i].mblocks) * C.e[i].brows * 2 * C.e[i].B;
+    }
+    C.total = halves;
+    if (halves == 0) return cudaSuccess;
+    int64_t blocks = (halves + 255) / 256;
+    const int64_t cap = int64_t(device_sm_count()) * 16;
+    blocks = blocks < cap ? blocks : cap;
+    act_f16_kernel<<<int(blocks), 256, 0, s>>>(C);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
 }  // namespace trit

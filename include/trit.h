@@ -160,7 +160,9 @@ TRIT_API trit_status trit_quant_act(const float *x, int64_t M, int64_t K, int8_t
  * ..." -- CPU kernels, Verification).  The kernel is chosen by M: one row per
  * pass for M = 1, beats reused across up to 8 rows held in registers for
  * 2 <= M <= 16, and tensor cores with planes expanded to +-1 in shared memory
- * for M >= 17 (K < 131072; longer rows stay on the integer path).
+ * for M >= 17 (K < 131072; longer rows stay on the integer path): 128-row
+ * weight tiles against all M rows (rounded up to 16) for M <= 128, 256 x 256
+ * tiles on pairs of SMs above.
  *   w_scale   finite, > 0
  *   y_i32, y_f32  outputs, either may be NULL (not both)
  *   err_flag  TRIT_ERR_P1 if any beat has both bits set; the outputs of a row
@@ -313,11 +315,13 @@ TRIT_API trit_status trit_intmlp_quant(const int32_t *a_gate, const int32_t *a_u
  * is part of the library's device image instead.  The other paths use no
  * scratch and are those of trit_gemm.
  *
- *   Limit     the copy takes 32768 * ceil(M/256) * ceil(K/64) bytes when
- *             M >= 17 and K < 131072 (0 otherwise); the call returns
- *             TRIT_E_SCRATCH, enqueuing nothing, when that exceeds
- *             TRIT_NOALLOC_SCRATCH_BYTES (32 MiB: ceil(M/256) * ceil(K/64)
- *             <= 1024, e.g. M = 2048 with K <= 8192).  Split M to stay inside.
+ *   Limit     the copy takes 2048 * ceil(M/16) * ceil(K/64) bytes when
+ *             17 <= M <= 128 and K < 131072 (at most 32 MiB: always fits),
+ *             32768 * ceil(M/256) * ceil(K/64) bytes when M > 128 and
+ *             K < 131072, and 0 otherwise; the call returns TRIT_E_SCRATCH,
+ *             enqueuing nothing, when that exceeds TRIT_NOALLOC_SCRATCH_BYTES
+ *             (32 MiB: for M > 128, ceil(M/256) * ceil(K/64) <= 1024, e.g.
+ *             M = 2048 with K <= 8192).  Split M to stay inside.
  *   Set-up    the first call on each device looks the buffer's address up with
  *             that device current (cudaGetSymbolAddress, which may load the
  *             library's device image and reserve the buffer) and keeps it for

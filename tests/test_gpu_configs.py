@@ -162,7 +162,7 @@ def test_config3_batch_sweep_and_corruption(t, orc):
         flat[bi, byte] |= val
         flat[bi, byte + 8] |= val
         corrupted_rows[i] = (beats // B, beats, bits)
-    for M in (1, 4):
+    for M in (1, 4, 32):
         plist = t.ProjList([(st.planes[i], wss[i], st.q[i][:M], st.s[i][:M], items[i][4],
                              st.y[i][:M], st.f[i][:M]) for i in range(len(items))])
         err = torch.zeros(1, dtype=torch.int32, device="cuda")

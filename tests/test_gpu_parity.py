@@ -421,7 +421,8 @@ def test_quant_gemv_many_rejects_long_rows(t):
     assert e.value.status == 2
 
 
-# ---- prefill: tensor-core path (M >= 64) -------------------------------------
+# ---- tensor-core paths: weights as the 128-row operand for 17 <= M <= 128,
+# ---- CTA pairs with 256 x 256 tiles above --------------------------------------
 
 PREFILL_CASES = [(64, 33, 65), (128, 256, 64), (129, 257, 2560), (200, 300, 130), (64, 17, 6912),
                  (255, 513, 1000), (512, 6912, 2560), (320, 2560, 6912)]
@@ -449,11 +450,11 @@ def test_prefill_matches_oracle(t, orc, M, N, K):
                                   x[:, :K].astype(np.int64) @ colsum)
 
 
+@pytest.mark.parametrize("M", [17, 200])
 @pytest.mark.parametrize("K", [131071, 131072])
-def test_prefill_exactness_boundary(t, orc, K):
+def test_prefill_exactness_boundary(t, orc, M, K):
     """|y| = 128*K: 16,777,088 at K = 131071 is still an exact fp32 integer on
-    the tensor-core path; K = 131072 is routed to the integer path."""
-    M = 64
+    both tensor-core paths; K = 131072 is routed to the integer path."""
     w = np.stack([np.full(K, -1, np.int8), synth.ternary(synth.rng_for(131), 1, K, 0.4)[0]])
     x = np.zeros((M, ((K + 63) // 64) * 64), np.int8)
     x[:, :K] = -128
@@ -466,9 +467,10 @@ def test_prefill_exactness_boundary(t, orc, K):
     np.testing.assert_array_equal(host(y), ry)
 
 
-def test_prefill_flags_both_set_other_rows_exact(t, orc):
-    rng = synth.rng_for(132)
-    M, N, K = 96, 300, 2560
+@pytest.mark.parametrize("M", [96, 300])
+def test_prefill_flags_both_set_other_rows_exact(t, orc, M):
+    rng = synth.rng_for(132, M)
+    N, K = 300, 2560
     w = synth.ternary(rng, N, K, synth.P_ZERO)
     p = orc.pack(w)
     for r in (3, 200, 299):
@@ -485,9 +487,10 @@ def test_prefill_flags_both_set_other_rows_exact(t, orc):
     np.testing.assert_array_equal(host(y)[:, keep], ry[:, keep])
 
 
-def test_prefill_outputs_optional_and_guarded(t, orc):
-    rng = synth.rng_for(133)
-    M, N, K = 130, 250, 640
+@pytest.mark.parametrize("M", [40, 130])
+def test_prefill_outputs_optional_and_guarded(t, orc, M):
+    rng = synth.rng_for(133, M)
+    N, K = 250, 640
     w = synth.ternary(rng, N, K, 0.4)
     x = padded_x(rng, M, K)
     xs = (rng.random(M) + 0.5).astype(np.float32)
@@ -503,3 +506,61 @@ def test_prefill_outputs_optional_and_guarded(t, orc):
     assert_f32_close(fh[:M * N].reshape(M, N), rf)
     np.testing.assert_array_equal(fh[:M * N].reshape(M, N).view(np.uint32), rf.view(np.uint32))
     assert (yh[M * N:] == -7).all() and (fh[M * N:] == -7.0).all()
+
+
+# Small M on the tensor cores: every M from 17 to 128 rounds up to a multiple
+# of 16 (MMA N); N ragged against the 128-row weight tiles, K against the beat.
+SKINNY_CASES = [(17, 31, 191), (17, 129, 65), (24, 255, 2560), (32, 128, 64), (33, 9, 6912),
+                (48, 1000, 640), (63, 385, 1000), (64, 6912, 2560), (100, 130, 130),
+                (112, 257, 127), (127, 2560, 6912), (128, 300, 2560)]
+
+
+@pytest.mark.parametrize("M,N,K", SKINNY_CASES)
+def test_skinny_matches_oracle(t, orc, M, N, K):
+    rng = synth.rng_for(134, M, N, K)
+    w = synth.ternary(rng, N, K, synth.P_ZERO)
+    x = padded_x(rng, M, K)
+    x[:, K:] = -3                      # bytes past K are not columns
+    x[M // 2, :K] = -128
+    xs = (rng.random(M) + 0.25).astype(np.float32)
+    ws = float(synth.w_scale(w))
+    planes, _ = t.trit_pack(dev(w), ws)
+    y, f, err = t.trit_gemm(planes, ws, dev(x), dev(xs), K)
+    assert int(host(err)[0]) == 0
+    rows = np.arange(N) if N * M * K <= 2e8 else \
+        np.unique(np.concatenate([[0, 127, 128, N - 1], rng.integers(0, N, 60)]))
+    ry, rf, _ = orc.gemm(orc.pack(w[rows]), ws, x, xs, K)
+    np.testing.assert_array_equal(host(y)[:, rows], ry)
+    assert_f32_close(host(f)[:, rows], rf)
+    np.testing.assert_array_equal(host(f)[:, rows].view(np.uint32), rf.view(np.uint32))
+    colsum = w.astype(np.int64).sum(axis=0)
+    np.testing.assert_array_equal(host(y).astype(np.int64).sum(axis=1),
+                                  x[:, :K].astype(np.int64) @ colsum)
+
+
+def test_skinny_list_of_mixed_m(t, orc):
+    """One launch over products with different M (so different MMA N and
+    activation block sizes sharing one stage layout), different K and N, and
+    more tiles than CTAs, mixed with products for the other paths."""
+    rng = synth.rng_for(135)
+    shapes = [(17, 640, 2560), (128, 300, 65), (40, 2560, 6912), (64, 1, 64), (1, 200, 640),
+              (96, 6912, 2560), (8, 100, 300), (33, 129, 1000), (300, 260, 640), (20, 4000, 2560)]
+    entries, refs, ws_all = [], [], []
+    for M, N, K in shapes:
+        w = synth.ternary(rng, N, K, float(rng.uniform(0.385, 0.508)))
+        x = padded_x(rng, M, K)
+        xs = (rng.random(M) + 0.5).astype(np.float32)
+        ws = float(synth.w_scale(w))
+        planes, _ = t.trit_pack(dev(w), ws)
+        y = torch.empty((M, N), dtype=torch.int32, device="cuda")
+        f = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        entries.append((planes, ws, dev(x), dev(xs), K, y, f))
+        rows = np.arange(N) if N <= 1000 else np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 126)]))
+        refs.append((rows, orc.gemm(orc.pack(w[rows]), ws, x, xs, K)))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t.trit_gemm_many(t.ProjList(entries), err)
+    assert int(host(err)[0]) == 0
+    for (_, _, _, _, _, y, f), (rows, (ry, rf, _)) in zip(entries, refs):
+        np.testing.assert_array_equal(host(y)[:, rows], ry)
+        assert_f32_close(host(f)[:, rows], rf)
+
