@@ -20,10 +20,12 @@
 //  2. skinny_kernel: persistent, two CTAs per SM, tcgen05.mma.cta_group::1
 //     kind::f16, M = 128, N = nt, K = 16.  Each CTA takes a contiguous range of
 //     the list's tiles (128 weight rows x all K of one product), split by cost
-//     (beats).  Per stage (one beat) one thread brings the activation block
-//     with a bulk copy and four producer warps (one thread per weight row; its
-//     beat arrives by a 16-byte cp.async, four beats in flight) expand the
-//     planes to fp16 +-1 in shared memory; one thread issues four MMAs per stage
+//     (beats).  A loader warp streams the tiles' plane beats into eight raw
+//     slots (16-byte cp.async, completion tracked on each slot's barrier), so
+//     the producer warps' proxy fences have no loads of theirs to wait for.
+//     Per stage (one beat) one thread brings the activation block with a bulk
+//     copy and four producer warps (one thread per weight row) expand the
+//     row's beat to fp16 +-1 in shared memory; one thread issues four MMAs per stage
 //     and commits to the stage's `empty` barrier; two accumulators alternate
 //     between tiles so four epilogue warps (one per TMEM lane quarter) store
 //     one tile while the next is multiplied.
@@ -39,9 +41,10 @@ using namespace tc;
 
 constexpr int kTileN = 128;                       // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kMaxNt = int(kSkinnyMaxM + 15) / 16 * 16;   // activation rows per MMA, at most
-constexpr int kRaw = 4;                           // beats in flight per producer thread
+constexpr int kRaw = 8;                           // plane beats in flight (raw slots)
 constexpr int kProducerWarps = 4;
-constexpr int kMmaWarp = kProducerWarps;
+constexpr int kLoaderWarp = kProducerWarps;
+constexpr int kMmaWarp = kLoaderWarp + 1;
 constexpr int kEpiWarp0 = kMmaWarp + 1;
 constexpr int kEpiWarps = 4;                      // one per TMEM lane quarter
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
@@ -49,7 +52,7 @@ constexpr int kAStage = kTileN * kBK * 2;         // 16 KB of expanded weights
 constexpr int kRawStage = kProducerWarps * 32 * 16;
 constexpr int kTmemCols = 2 * kMaxNt;             // two accumulators
 constexpr int kMaxStages = 8;
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
 // dynamic shared memory of one CTA: two CTAs per SM
 constexpr int kSmemBytes = 110 * 1024;
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
@@ -57,7 +60,7 @@ static_assert(kProducerWarps * 32 == kTileN, "one producer thread per weight row
 static_assert(kTmemCols == 32 || kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256,
               "tensor memory is allocated in powers of two");
 static_assert(kMaxNt <= 256 && kMaxNt % 16 == 0, "MMA N for M = 128");
-static_assert((2 * kMaxStages + 5) * 8 + 16 <= kBarBytes, "barrier area");
+static_assert((2 * kMaxStages + 2 * kRaw + 5) * 8 + 16 <= kBarBytes, "barrier area");
 
 struct SEntry {
     const uint4 *planes;
@@ -142,6 +145,13 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
+// Arrive on the barrier once every cp.async this thread has issued has landed
+// (one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -161,7 +171,9 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
     uint8_t *raw = smem + nst * stage_bytes;           // kRaw slots of kRawStage bytes
     uint64_t *full = reinterpret_cast<uint64_t *>(raw + kRaw * kRawStage);
     uint64_t *empty = full + kMaxStages;
-    uint64_t *tfull = empty + kMaxStages;   // accumulator a holds a finished tile
+    uint64_t *rfull = empty + kMaxStages;   // raw slot r holds its beat
+    uint64_t *rempty = rfull + kRaw;        // raw slot r has been read
+    uint64_t *tfull = rempty + kRaw;        // accumulator a holds a finished tile
     uint64_t *tempty = tfull + 2;           // accumulator a has been read
     uint64_t *done = tempty + 2;            // every MMA has completed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
@@ -178,6 +190,10 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], kProducerWarps + 1);   // producer warps + the expect_tx arrival
             mbar_init(&empty[s], 1);
+        }
+        for (int r = 0; r < kRaw; ++r) {
+            mbar_init(&rfull[r], 32);              // the loader lanes' copy completions
+            mbar_init(&rempty[r], kProducerWarps);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -200,41 +216,10 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kProducerWarps) {
-        // thread p: weight row p of each tile, the whole beat
+        // thread p: weight row p of each tile; its beat comes from the raw slot
         const int p = threadIdx.x;
-        // load cursor, kRaw beats ahead of the consume cursor (across tiles)
-        Cursor lc = first;
-        bool lvalid = in_range(L, lc, end);
-        int lkb = 0, lnk = 0;
-        const uint8_t *lrow = nullptr;
-        uint32_t lbytes = 0;
-        auto load_tile = [&]() {
-            const SEntry &E = L.e[lc.e];
-            const int64_t n = lc.j * kTileN + p;
-            const bool ok = n < E.N;
-            lrow = reinterpret_cast<const uint8_t *>(E.planes + (ok ? n : 0) * E.B);
-            lbytes = ok ? 16u : 0u;
-            lnk = E.B;
-            lkb = 0;
-        };
-        if (lvalid) load_tile();
-        int64_t li = 0;   // loads issued
-        auto issue_next = [&]() {
-            if (lvalid) {
-                cp_async16(raw + int(li % kRaw) * kRawStage + p * 16, lrow + int64_t(lkb) * 16, lbytes);
-                ++li;
-                if (++lkb == lnk) {
-                    advance(L, lc);
-                    lvalid = in_range(L, lc, end);
-                    if (lvalid) load_tile();
-                }
-            }
-            cp_async_commit();
-        };
-#pragma unroll 1
-        for (int r = 0; r < kRaw; ++r) issue_next();
         uint32_t viol = 0;
-        int64_t it = 0;   // stages consumed
+        int64_t it = 0;   // stages filled
         bool stop = false;
         for (Cursor c = first; in_range(L, c, end) && !stop; advance(L, c)) {
             const SEntry &E = L.e[c.e];
@@ -242,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
             for (int kb = 0; kb < E.B; ++kb, ++it) {
                 const int s = int(it % nst);
                 const uint32_t ph = uint32_t(it / nst) & 1u;
+                const int r = int(it % kRaw);
+                const uint32_t rph = uint32_t(it / kRaw) & 1u;
                 if (!mbar_wait(&empty[s], ph ^ 1u, timed_out)) {
                     stop = true;
                     break;
@@ -251,8 +238,11 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
                     mbar_arrive_expect_tx(&full[s], bbytes);
                     bulk_load(a_st + kAStage, E.xh + int64_t(kb) * bbytes, bbytes, &full[s]);
                 }
-                cp_async_wait<kRaw - 1>();
-                const uint4 pn = *reinterpret_cast<const uint4 *>(raw + int(it % kRaw) * kRawStage + p * 16);
+                if (!mbar_wait(&rfull[r], rph, timed_out)) {
+                    stop = true;
+                    break;
+                }
+                const uint4 pn = *reinterpret_cast<const uint4 *>(raw + r * kRawStage + p * 16);
                 viol |= (pn.x & pn.z) | (pn.y & pn.w);
 #pragma unroll
                 for (int bh = 0; bh < 2; ++bh) {   // chunks 4*bh .. 4*bh+3 of row p
@@ -267,12 +257,45 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full[s]);
-                issue_next();   // the raw slot is consumed: refill it kRaw beats ahead
+                if (lane == 0) {
+                    mbar_arrive(&full[s]);
+                    mbar_arrive(&rempty[r]);
+                }
             }
         }
-        cp_async_wait<0>();
         if (viol) atomicOr(viol_any, 1u);
+    } else if (warp == kLoaderWarp) {
+        // lane l: weight rows l, l+32, l+64, l+96 of each tile, one beat per raw
+        // slot by 16-byte cp.async (zeros past the last row); the slot's barrier
+        // completes when every lane's copies have landed
+        int64_t li = 0;
+        bool stop = false;
+        for (Cursor c = first; in_range(L, c, end) && !stop; advance(L, c)) {
+            const SEntry &E = L.e[c.e];
+            const uint8_t *rowp[4];
+            uint32_t rbytes[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t n = c.j * kTileN + lane + 32 * q;
+                const bool ok = n < E.N;
+                rowp[q] = reinterpret_cast<const uint8_t *>(E.planes + (ok ? n : 0) * E.B);
+                rbytes[q] = ok ? 16u : 0u;
+            }
+            for (int kb = 0; kb < E.B; ++kb, ++li) {
+                const int r = int(li % kRaw);
+                const uint32_t ph = uint32_t(li / kRaw) & 1u;
+                if (!mbar_wait(&rempty[r], ph ^ 1u, timed_out)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t *slot = raw + r * kRawStage;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    cp_async16(slot + (lane + 32 * q) * 16, rowp[q] + int64_t(kb) * 16, rbytes[q]);
+                cp_async_arrive_noinc(&rfull[r]);
+            }
+        }
+        cp_async_wait_all();
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             const uint32_t base = smem_u32(smem);
