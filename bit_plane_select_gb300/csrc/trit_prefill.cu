@@ -1,4 +1,4 @@
-// Prefill: y = W x for many activation rows (M >= 17) on the 5th-generation
+// Prefill: y = W x for many activation rows (M > 128) on the 5th-generation
 // tensor cores -- the dense-contraction case of the ternary product.
 //
 // The product y[m][n] = sum_c x[m][c] * W[n][c] ("Tritium: One Weight Format

@@ -28,7 +28,7 @@
  *   - Data pointers are DEVICE pointers to caller-owned memory.  The library
  *     keeps no pointer after the call returns.  The only device memory it
  *     allocates is the temporary fp16 copy of the activations used by the
- *     tensor-core path of trit_gemm / trit_gemm_many (M >= 17): allocated with
+ *     tensor-core path of trit_gemm / trit_gemm_many (M >= 13): allocated with
  *     cudaMallocAsync on the call's stream and freed, stream-ordered, after the
  *     launches (failure returns TRIT_E_CUDA).  trit_gemm_noalloc allocates
  *     nothing (it uses a fixed buffer instead, see there).
@@ -159,8 +159,8 @@ TRIT_API trit_status trit_quant_act(const float *x, int64_t M, int64_t K, int8_t
  * accumulation is exact (int32; every kernel gives identical bits, "Tritium
  * ..." -- CPU kernels, Verification).  The kernel is chosen by M: one row per
  * pass for M = 1, beats reused across up to 8 rows held in registers for
- * 2 <= M <= 16, and tensor cores with planes expanded to +-1 in shared memory
- * for M >= 17 (K < 131072; longer rows stay on the integer path): 128-row
+ * 2 <= M <= 12, and tensor cores with planes expanded to +-1 in shared memory
+ * for M >= 13 (K < 131072; longer rows stay on the integer path): 128-row
  * weight tiles against all M rows (rounded up to 16) for M <= 128, 256 x 256
  * tiles on pairs of SMs above.
  *   w_scale   finite, > 0
@@ -309,14 +309,14 @@ TRIT_API trit_status trit_intmlp_quant(const int32_t *a_gate, const int32_t *a_u
  * memory to their own pools or caches up front and have no headroom left for
  * a driver allocation, and loops that must not meet an out-of-memory failure
  * or a memory-pool growth (which may wait on the device) in the middle of a
- * step.  trit_gemm's tensor-core path (M >= 17, K < 131072) needs a temporary
+ * step.  trit_gemm's tensor-core path (M >= 13, K < 131072) needs a temporary
  * fp16 copy of the activations, which trit_gemm allocates on the stream; this
  * entry point puts that copy in one buffer of TRIT_NOALLOC_SCRATCH_BYTES that
  * is part of the library's device image instead.  The other paths use no
  * scratch and are those of trit_gemm.
  *
  *   Limit     the copy takes 2048 * ceil(M/16) * ceil(K/64) bytes when
- *             17 <= M <= 128 and K < 131072 (at most 32 MiB: always fits),
+ *             13 <= M <= 128 and K < 131072 (at most 32 MiB: always fits),
  *             32768 * ceil(M/256) * ceil(K/64) bytes when M > 128 and
  *             K < 131072, and 0 otherwise; the call returns TRIT_E_SCRATCH,
  *             enqueuing nothing, when that exceeds TRIT_NOALLOC_SCRATCH_BYTES

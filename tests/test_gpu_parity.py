@@ -172,7 +172,7 @@ def test_quant_many_matches_single(t, orc):
 GEMM_CASES = [
     (1, 1, 1), (1, 3, 63), (1, 4, 64), (1, 5, 65), (1, 33, 200), (1, 257, 2560), (1, 1000, 6912),
     (1, 127, 1000), (2, 37, 130), (3, 64, 2560), (4, 33, 6912), (5, 100, 65), (7, 17, 640),
-    (8, 260, 2560), (9, 45, 300), (16, 70, 2560), (17, 31, 191), (33, 9, 6912),
+    (8, 260, 2560), (9, 45, 300), (12, 77, 1000), (13, 70, 2560), (16, 70, 2560), (17, 31, 191), (33, 9, 6912),
 ]
 
 
@@ -508,9 +508,9 @@ def test_prefill_outputs_optional_and_guarded(t, orc, M):
     assert (yh[M * N:] == -7).all() and (fh[M * N:] == -7.0).all()
 
 
-# Small M on the tensor cores: every M from 17 to 128 rounds up to a multiple
+# Small M on the tensor cores: every M from 13 to 128 rounds up to a multiple
 # of 16 (MMA N); N ragged against the 128-row weight tiles, K against the beat.
-SKINNY_CASES = [(17, 31, 191), (17, 129, 65), (24, 255, 2560), (32, 128, 64), (33, 9, 6912),
+SKINNY_CASES = [(13, 31, 191), (16, 129, 65), (17, 31, 191), (17, 129, 65), (24, 255, 2560), (32, 128, 64), (33, 9, 6912),
                 (48, 1000, 640), (63, 385, 1000), (64, 6912, 2560), (100, 130, 130),
                 (112, 257, 127), (127, 2560, 6912), (128, 300, 2560)]
 

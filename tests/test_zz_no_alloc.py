@@ -30,7 +30,7 @@ def scratch_bytes(M, K):
     M <= 128 one block of M rows (rounded up to 16) x 64 columns per beat; above,
     16 KB blocks of 128 rows x 64 columns, row blocks in pairs (256-row pair
     tiles)."""
-    if M < 17 or K >= 131072:
+    if M < 13 or K >= 131072:
         return 0
     if M <= 128:
         return 128 * ((M + 15) // 16 * 16) * ((K + 63) // 64)
@@ -83,7 +83,7 @@ PAIRS = [
     ((2048, 256, 6912), (517, 300, 2560)),      # a prefill-sized product, 27 MiB of scratch
     ((2048, 136, 8192), (2048, 136, 8192)),     # exactly the whole 32 MiB buffer, twice
     ((5, 300, 2560), (1, 700, 6913)),           # integer paths (no scratch)
-    ((40, 64, 140000), (17, 33, 64)),           # K past the tensor path, then the smallest M on it
+    ((40, 64, 140000), (13, 33, 64)),           # K past the tensor path, then the smallest M on it
     ((128, 300, 131071), (129, 300, 2560)),     # largest small-M copy (32 MiB), then a pair-tile one
 ]
 
