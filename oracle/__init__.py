@@ -65,6 +65,13 @@ def _load():
             lib.oracle_quant_folded.argtypes = [p, p, i64, i64, ctypes.c_double, i64, p, p, p, p]
             lib.oracle_intmlp_quant.argtypes = [p, p, i64, i64, i64, ctypes.c_float,
                                                 ctypes.c_float, p, i64, p, p]
+            lib.oracle_bitcos_pack_flat.argtypes = [p, i64, p, p, p]
+            lib.oracle_bitcos_unpack_flat.argtypes = [p, p, i64, p]
+            lib.oracle_bitcos_blocked_words.restype = i64
+            lib.oracle_bitcos_blocked_words.argtypes = [p, i64, i64]
+            lib.oracle_bitcos_pack_blocked.argtypes = [p, i64, i64, p, p, p]
+            lib.oracle_bitcos_gemv.argtypes = [p, p, p, i64, i64, ctypes.c_float, p,
+                                               ctypes.c_float, p, i64, p, p]
             _lib = lib
     return _lib
 
@@ -223,3 +230,75 @@ def intmlp_quant(a_g: np.ndarray, a_u: np.ndarray, w_g: float, w_u: float, x_sca
     _load().oracle_intmlp_quant(_ptr(a_g), _ptr(a_u), M, N, N, ctypes.c_float(w_g),
                                 ctypes.c_float(w_u), _ptr(xs), ldq, _ptr(q), _ptr(h))
     return q, h
+
+
+# ---- BITCOS ("BITCOS: Intel's Ternary LLM Weight Format Goes Below 1.58 Bits"
+# ---- -- A bitmap and a sign) ------------------------------------------------
+
+def bitcos_pack_flat(q: np.ndarray):
+    """Flat presence bitmap and sign vector of the ternary codes q (any shape,
+    taken in C order).  Returns (bitmap uint8 [ceil(n/8)], signs uint8
+    [ceil(nnz/8)])."""
+    q = np.ascontiguousarray(q, dtype=np.int8).reshape(-1)
+    n = q.shape[0]
+    bitmap = np.empty((n + 7) // 8, dtype=np.uint8)
+    signs = np.empty(max((n + 7) // 8, 1), dtype=np.uint8)
+    nnz = np.zeros(1, dtype=np.int64)
+    rc = _load().oracle_bitcos_pack_flat(_ptr(q), n, _ptr(bitmap), _ptr(signs), _ptr(nnz))
+    if rc:
+        raise OracleReject(rc)
+    return bitmap, signs[:(int(nnz[0]) + 7) // 8].copy()
+
+
+def bitcos_unpack_flat(bitmap: np.ndarray, signs: np.ndarray, n: int) -> np.ndarray:
+    bitmap = np.ascontiguousarray(bitmap, dtype=np.uint8)
+    signs = np.ascontiguousarray(signs, dtype=np.uint8)
+    if signs.size == 0:
+        signs = np.zeros(1, dtype=np.uint8)
+    q = np.empty(n, dtype=np.int8)
+    _load().oracle_bitcos_unpack_flat(_ptr(bitmap), _ptr(signs), n, _ptr(q))
+    return q
+
+
+def bitcos_pack_blocked(w: np.ndarray):
+    """Blocked BITCOS form of a [rows, cols] ternary matrix: (bitmap uint64
+    [rows, ceil(cols/64)], sign_off uint32 [rows+1], signs uint32
+    [sign_off[-1] + 2])."""
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    rows, cols = w.shape
+    lib = _load()
+    words = int(lib.oracle_bitcos_blocked_words(_ptr(w), rows, cols))
+    bitmap = np.empty((rows, (cols + 63) // 64), dtype=np.uint64)
+    sign_off = np.empty(rows + 1, dtype=np.uint32)
+    signs = np.empty(words + 2, dtype=np.uint32)
+    rc = lib.oracle_bitcos_pack_blocked(_ptr(w), rows, cols, _ptr(bitmap), _ptr(sign_off),
+                                        _ptr(signs))
+    if rc:
+        raise OracleReject(rc)
+    return bitmap, sign_off, signs
+
+
+def bitcos_gemv(bitmap: np.ndarray, sign_off: np.ndarray, signs: np.ndarray, cols: int,
+                w_scale: float, x_i8: np.ndarray, x_scale: float, rows=None):
+    """y = W x (one activation row) from the blocked form; returns (y_i32, y_f32)
+    for the selected rows (all when rows is None)."""
+    bitmap = np.ascontiguousarray(bitmap, dtype=np.uint64)
+    sign_off = np.ascontiguousarray(sign_off, dtype=np.uint32)
+    signs = np.ascontiguousarray(signs, dtype=np.uint32)
+    x_i8 = np.ascontiguousarray(x_i8, dtype=np.int8).reshape(-1)
+    assert x_i8.shape[0] >= cols
+    nrows = bitmap.shape[0]
+    if rows is None:
+        sel, nsel, psel = None, nrows, None
+    else:
+        sel = np.ascontiguousarray(rows, dtype=np.int64)
+        nsel, psel = sel.shape[0], _ptr(sel)
+    y = np.empty(nsel, dtype=np.int32)
+    yf = np.empty(nsel, dtype=np.float32)
+    rc = _load().oracle_bitcos_gemv(_ptr(bitmap), _ptr(sign_off), _ptr(signs), nrows, cols,
+                                    ctypes.c_float(w_scale), _ptr(x_i8), ctypes.c_float(x_scale),
+                                    psel, nsel, _ptr(y), _ptr(yf))
+    if rc & 64:
+        raise ValueError("oracle_bitcos_gemv: bad argument")
+    return y, yf
+

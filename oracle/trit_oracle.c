@@ -15,6 +15,8 @@
  *   [TRI] "Tritium: One Weight Format for Ternary Inference on Commodity CPUs
  *          and Multiplier-Free Hardware" -- The .trit v1 layout; Invariants;
  *          On popcount; The hardware core; Numerics; Why exactness, concretely
+ *   [BITCOS] "BITCOS: Intel's Ternary LLM Weight Format Goes Below 1.58 Bits"
+ *          -- A bitmap and a sign
  *
  * Readings where the pages are silent (the activation quantiser formula, the
  * zero row, the dequantisation order) are stated at each function.
@@ -428,4 +430,148 @@ int oracle_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t
         h_scale[m] = (float)(a * k);
     }
     return 0;
+}
+
+/*
+ * BITCOS ([BITCOS] "BITCOS: Intel's Ternary LLM Weight Format Goes Below 1.58
+ * Bits" -- A bitmap and a sign).  Two arrays: a presence bitmap with one bit
+ * per weight (set when the weight is non-zero) and a sign vector with one bit
+ * per non-zero weight, in the same order (set when the weight is -1).  Bits
+ * are filled from the least significant bit of each byte upward, as the
+ * page's packer does.  Rate: n + nnz bits, i.e. 2 - z bits per weight at zero
+ * density z.
+ *
+ * oracle_bitcos_pack_flat: q[0..n) in {-1, 0, +1} -> bitmap[ceil(n/8)],
+ * signs[ceil(nnz/8)] (the caller sizes signs for n weights), *nnz.  Returns
+ * OR_NOT_TERNARY (nothing defined) for a value outside {-1, 0, +1}.
+ */
+int oracle_bitcos_pack_flat(const int8_t *q, int64_t n, uint8_t *bitmap, uint8_t *signs,
+                            int64_t *nnz)
+{
+    if (n < 0) return OR_ARG;
+    for (int64_t i = 0; i < n; i++)
+        if (q[i] < -1 || q[i] > 1) return OR_NOT_TERNARY;
+    memset(bitmap, 0, (size_t)((n + 7) / 8));
+    memset(signs, 0, (size_t)((n + 7) / 8));
+    int64_t k = 0;
+    for (int64_t i = 0; i < n; i++) {
+        if (q[i] == 0) continue;
+        bitmap[i / 8] |= (uint8_t)(1u << (i % 8));
+        if (q[i] < 0) signs[k / 8] |= (uint8_t)(1u << (k % 8));
+        k++;
+    }
+    *nnz = k;
+    return 0;
+}
+
+/* The inverse: walk the bitmap; each set bit takes the next sign bit. */
+int oracle_bitcos_unpack_flat(const uint8_t *bitmap, const uint8_t *signs, int64_t n, int8_t *q)
+{
+    int64_t k = 0;
+    for (int64_t i = 0; i < n; i++) {
+        if ((bitmap[i / 8] >> (i % 8)) & 1) {
+            q[i] = ((signs[k / 8] >> (k % 8)) & 1) ? (int8_t)-1 : (int8_t)1;
+            k++;
+        } else {
+            q[i] = 0;
+        }
+    }
+    return 0;
+}
+
+/*
+ * The blocked form of the same two arrays for a matrix of `rows` x `cols`
+ * weights, so that a kernel can start any row (the page: a production kernel
+ * aligns both arrays to its block size).  Reading: the block is one row --
+ *   bitmap  uint64 [rows][B], B = ceil(cols/64): bit c%64 of word [r][c/64] is
+ *           row r's presence bit of column c; bits past cols are 0;
+ *   sign_off uint32 [rows+1]: sign_off[0] = 0, sign_off[r+1] = sign_off[r] +
+ *           ceil(nnz_r / 32);
+ *   signs   uint32 [sign_off[rows] + 2]: the k-th non-zero of row r (column
+ *           order) has its sign at bit k%32 of word sign_off[r] + k/32; every
+ *           other bit is 0, and so are the last two words.
+ * Row r's sign bits, taken in order and cut to nnz_r, are row r's part of the
+ * flat sign vector.  oracle_bitcos_blocked_words gives sign_off[rows] (call it
+ * first to size signs); oracle_bitcos_pack_blocked fills the three arrays.
+ */
+int64_t oracle_bitcos_blocked_words(const int8_t *w, int64_t rows, int64_t cols)
+{
+    int64_t words = 0;
+    for (int64_t r = 0; r < rows; r++) {
+        int64_t nnz = 0;
+        for (int64_t c = 0; c < cols; c++) nnz += w[r * cols + c] != 0;
+        words += (nnz + 31) / 32;
+    }
+    return words;
+}
+
+int oracle_bitcos_pack_blocked(const int8_t *w, int64_t rows, int64_t cols, uint64_t *bitmap,
+                               uint32_t *sign_off, uint32_t *signs)
+{
+    const int64_t B = (cols + 63) / 64;
+    if (rows < 0 || cols < 0) return OR_ARG;
+    for (int64_t i = 0; i < rows * cols; i++)
+        if (w[i] < -1 || w[i] > 1) return OR_NOT_TERNARY;
+    memset(bitmap, 0, (size_t)(rows * B) * sizeof(uint64_t));
+    int64_t off = 0;
+    sign_off[0] = 0;
+    for (int64_t r = 0; r < rows; r++) {
+        int64_t k = 0;
+        for (int64_t c = 0; c < cols; c++) {
+            const int8_t v = w[r * cols + c];
+            if (v == 0) continue;
+            bitmap[r * B + c / 64] |= (uint64_t)1 << (c % 64);
+            if (k % 32 == 0) signs[off + k / 32] = 0;
+            if (v < 0) signs[off + k / 32] |= (uint32_t)1 << (k % 32);
+            k++;
+        }
+        off += (k + 31) / 32;
+        sign_off[r + 1] = (uint32_t)off;
+    }
+    signs[off] = 0;
+    signs[off + 1] = 0;
+    return 0;
+}
+
+/*
+ * y = W x for one activation row with W given in the blocked BITCOS form:
+ * each row is decoded by walking its bitmap and taking the next sign bit at
+ * every set bit, then accumulated in int64 against x (int8, columns < cols),
+ * and dequantised exactly as oracle_gemm does:
+ *   y_f32 = (((float)acc * w_scale) * x_scale) / 127.0f
+ * `sel` selects rows (NULL: all).  Returns OR_OVERFLOW if an accumulator
+ * leaves the int32 range (that row's outputs are 0).
+ */
+int oracle_bitcos_gemv(const uint64_t *bitmap, const uint32_t *sign_off, const uint32_t *signs,
+                       int64_t rows, int64_t cols, float w_scale, const int8_t *x, float x_scale,
+                       const int64_t *sel, int64_t nsel, int32_t *y_i32, float *y_f32)
+{
+    const int64_t B = (cols + 63) / 64;
+    int any = 0;
+    if (sel == NULL) nsel = rows;
+    for (int64_t i = 0; i < nsel; i++) {
+        const int64_t r = sel ? sel[i] : i;
+        if (r < 0 || r >= rows) return OR_ARG;
+        int64_t acc = 0, k = 0;
+        for (int64_t c = 0; c < cols; c++) {
+            if (!((bitmap[r * B + c / 64] >> (c % 64)) & 1)) continue;
+            const int64_t word = (int64_t)sign_off[r] + k / 32;
+            const int neg = (signs[word] >> (k % 32)) & 1;
+            acc += neg ? -(int64_t)x[c] : (int64_t)x[c];
+            k++;
+        }
+        y_i32[i] = 0;
+        y_f32[i] = 0.0f;
+        if (acc > INT32_MAX || acc < INT32_MIN) {
+            any |= OR_OVERFLOW;
+            continue;
+        }
+        float f = (float)(int32_t)acc;
+        f = f * w_scale;
+        f = f * x_scale;
+        f = f / 127.0f;
+        y_i32[i] = (int32_t)acc;
+        y_f32[i] = f;
+    }
+    return any;
 }
