@@ -694,6 +694,72 @@ def run_batch_sweep(args):
           flush=True)
 
 
+def run_bitcos(args):
+    """Row f4: the 30-layer stack at batch 1 with the weights in the BITCOS
+    form (presence bitmap + compacted signs, 2 - z bits per weight) against the
+    same weights as 2-bit planes, both from int8 activation codes, in one run.
+    A step is one token through the 210 products."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import synth
+    import bit_plane_select_gb300 as t
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    items = list(synth.stack_items(args.layers))
+    bents, pents, keep = [], [], []
+    bytes_bitcos = bytes_planes = nnz = weights = 0
+    for layer, idx, name, N, K in items:
+        w = synth.stack_weights(SEED, layer, idx)
+        ws = float(synth.w_scale(w))
+        W = t.BitcosWeights(*t.trit_bitcos_pack(w), K, dev)
+        planes, _ = t.trit_pack(torch.from_numpy(w).to(dev), ws)
+        x = torch.from_numpy(synth.projection_acts(SEED, layer, idx, 1)).to(dev)
+        q, sc, _ = t.trit_quant_act(x)
+        y = torch.empty(N, dtype=torch.int32, device=dev)
+        f = torch.empty(N, dtype=torch.float32, device=dev)
+        y2 = torch.empty((1, N), dtype=torch.int32, device=dev)
+        f2 = torch.empty((1, N), dtype=torch.float32, device=dev)
+        bents.append((W, ws, q[0], sc, y, f))
+        pents.append((planes, ws, q, sc, K, y2, f2))
+        keep.append((W, planes, q, sc, y, f, y2, f2))
+        kp = t.k_pad(K)
+        bytes_bitcos += W.nbytes + kp + 4 + 8 * N
+        bytes_planes += planes.numel() + kp + 4 + 8 * N
+        nnz += int(np.count_nonzero(w))
+        weights += N * K
+    blist, plist = t.BitcosList(bents), t.ProjList(pents)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    steps = max(3, args.steps // 10)
+    with ClockSampler(0) as clk:
+        ms_b = _timed(lambda: t.trit_bitcos_gemv_many(blist), steps, args.warmup, stream)
+    clocks = clk.summary()
+    ms_p = _timed(lambda: t.trit_gemm_many(plist, err), steps, args.warmup, stream)
+    same = all(torch.equal(k[4], k[6][0]) and torch.equal(k[5].view(torch.int32), k[7][0].view(torch.int32))
+               for k in keep)
+    peak, peak_kind = peaks()
+    gbs = bytes_bitcos / (ms_b * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "BITCOS batch-1 ternary decode over the 30-layer stack",
+        "unit": "tok/s", "value": round(1e3 / ms_b, 1), "ms_per_step": round(ms_b, 4),
+        "higher_is_better": True, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": "bitnet-2b4t-30layer-bitcos-batch1", "layers": args.layers,
+                   "zero_density": round(1 - nnz / weights, 4),
+                   "bits_per_weight": round(8 * bytes_bitcos / weights, 4),
+                   "l2": "inputs larger than L2"},
+        "planes_same_run": {"ms_per_step": round(ms_p, 4), "tok_per_s": round(1e3 / ms_p, 1),
+                            "bytes_per_step": bytes_planes},
+        "speedup_vs_planes": round(ms_p / ms_b, 3),
+        "identical_to_planes": bool(same),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                     "bytes_per_step": bytes_bitcos},
+        "clocks": clocks, "err_flag": int(err.item())}), flush=True)
+
+
 def run_mlp(args):
     """The MLP blocks of the 30-layer stack at batch 1 (row f1): per layer, gate
     and up from one fp32 activation row with the quantiser fused (one launch),
@@ -792,9 +858,10 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=90.0)
-    ap.add_argument("--workload", choices=["decode", "prefill", "batch", "mlp"], default="decode",
-                    help="decode (default): the 30-layer batch-1 stack; prefill, batch and mlp "
-                         "print extra lines for the other configurations")
+    ap.add_argument("--workload", choices=["decode", "prefill", "batch", "mlp", "bitcos"],
+                    default="decode",
+                    help="decode (default): the 30-layer batch-1 stack; prefill, batch, mlp and "
+                         "bitcos print extra lines for the other configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -806,6 +873,8 @@ def main():
         run_batch_sweep(args)
     elif args.workload == "mlp":
         run_mlp(args)
+    elif args.workload == "bitcos":
+        run_bitcos(args)
     else:
         run_ours(args)
 

@@ -41,7 +41,8 @@ MAX_FUSED_K = 73728
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _STATUS = {0: "TRIT_OK", 1: "TRIT_E_ARG", 2: "TRIT_E_SHAPE", 4: "TRIT_E_SCALE",
-           6: "TRIT_E_CUDA", 7: "TRIT_E_DEVICE", 8: "TRIT_E_SCRATCH"}
+           6: "TRIT_E_CUDA", 7: "TRIT_E_DEVICE", 8: "TRIT_E_SCRATCH", 9: "TRIT_E_VALUE"}
+BITCOS_MAX_K = 16384
 
 
 class TritError(RuntimeError):
@@ -70,6 +71,14 @@ class TritMlpProj(ctypes.Structure):
                 ("h_i8", ctypes.c_void_p), ("h_scale", ctypes.c_void_p),
                 ("y_i32", ctypes.c_void_p), ("y_f32", ctypes.c_void_p), ("N", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+
+
+class TritBitcosProj(ctypes.Structure):
+    _fields_ = [("bitmap", ctypes.c_void_p), ("sign_off", ctypes.c_void_p), ("signs", ctypes.c_void_p),
+                ("x_i8", ctypes.c_void_p), ("x_scale", ctypes.c_void_p), ("y_i32", ctypes.c_void_p),
+                ("y_f32", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("sign_words", ctypes.c_int64), ("w_scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32)]
 
 
 class TritAct(ctypes.Structure):
@@ -117,11 +126,13 @@ def lib():
         L.trit_intmlp_quant.argtypes = [p, p, i64, i64, f32, f32, p, p, p, p]
         L.trit_check_div127.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
         L.trit_read_probe.argtypes = [p, i64, p, p]
+        L.trit_bitcos_pack.argtypes = [p, i64, i64, p, p, p, p]
+        L.trit_bitcos_gemv_many.argtypes = [p, i32, p]
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
                      "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
                      "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_quant_act_folded",
                      "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
-                     "trit_intmlp_gemv_many"):
+                     "trit_intmlp_gemv_many", "trit_bitcos_pack", "trit_bitcos_gemv_many"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -438,3 +449,66 @@ def trit_quant_act_many(alist: ActList, err_flag: torch.Tensor, stream=None):
     _check(lib().trit_quant_act_many(ctypes.cast(alist.array, ctypes.c_void_p), alist.count,
                                      _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
            "trit_quant_act_many")
+
+
+# ---- BITCOS weights (presence bitmap + compacted signs) ---------------------
+
+def trit_bitcos_pack(w):
+    """HOST packer: ternary int8 W [N, K] (numpy array or CPU tensor) -> host
+    numpy arrays (bitmap uint64 [N, ceil(K/64)], sign_off uint32 [N+1], signs
+    uint32 [sign_off[N] + 2])."""
+    import numpy as np
+    w = np.ascontiguousarray(w.numpy() if isinstance(w, torch.Tensor) else w, dtype=np.int8)
+    N, K = w.shape
+    wp = ctypes.c_void_p(w.ctypes.data)
+    words = ctypes.c_int64(0)
+    _check(lib().trit_bitcos_pack(wp, N, K, None, None, None, ctypes.byref(words)), "trit_bitcos_pack")
+    bitmap = np.empty((N, (K + 63) // 64), dtype=np.uint64)
+    sign_off = np.empty(N + 1, dtype=np.uint32)
+    signs = np.empty(words.value, dtype=np.uint32)
+    _check(lib().trit_bitcos_pack(wp, N, K, ctypes.c_void_p(bitmap.ctypes.data),
+                                  ctypes.c_void_p(sign_off.ctypes.data),
+                                  ctypes.c_void_p(signs.ctypes.data), ctypes.byref(words)),
+           "trit_bitcos_pack")
+    return bitmap, sign_off, signs
+
+
+class BitcosWeights:
+    """A BITCOS matrix uploaded to the device (the three arrays of trit_bitcos_pack)."""
+
+    def __init__(self, bitmap, sign_off, signs, K: int, device=None):
+        dev = torch.device("cuda") if device is None else device
+        self.bitmap = torch.from_numpy(bitmap.view("int64")).to(dev)
+        self.sign_off = torch.from_numpy(sign_off.view("int32")).to(dev)
+        self.signs = torch.from_numpy(signs.view("int32")).to(dev)
+        self.N = bitmap.shape[0]
+        self.K = int(K)
+
+    @property
+    def nbytes(self) -> int:
+        return (self.bitmap.numel() * 8 + self.sign_off.numel() * 4 + self.signs.numel() * 4)
+
+
+class BitcosList:
+    """Host array of trit_bitcos_proj entries: (weights, w_scale, x_i8 [K_pad],
+    x_scale [1], y_i32 [N] or None, y_f32 [N] or None)."""
+
+    def __init__(self, entries):
+        self._keep = []
+        items = []
+        for W, w_scale, x_i8, x_scale, y_i32, y_f32 in entries:
+            items.append(TritBitcosProj(
+                _dev(W.bitmap, torch.int64, "bitmap"), _dev(W.sign_off, torch.int32, "sign_off"),
+                _dev(W.signs, torch.int32, "signs"), _dev(x_i8, torch.int8, "x_i8"),
+                _dev(x_scale, torch.float32, "x_scale"),
+                _dev(y_i32, torch.int32, "y_i32", True), _dev(y_f32, torch.float32, "y_f32", True),
+                W.N, W.K, W.signs.numel(), float(w_scale), 0))
+            self._keep.append((W, x_i8, x_scale, y_i32, y_f32))
+        self.count = len(items)
+        self.array = (TritBitcosProj * self.count)(*items)
+
+
+def trit_bitcos_gemv_many(blist: BitcosList, stream=None):
+    _check(lib().trit_bitcos_gemv_many(ctypes.cast(blist.array, ctypes.c_void_p), blist.count,
+                                       _stream(stream)), "trit_bitcos_gemv_many")
+

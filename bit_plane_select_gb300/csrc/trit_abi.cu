@@ -190,13 +190,14 @@ TRIT_API const char *trit_status_string(trit_status s) {
         case TRIT_E_DEVICE: return "TRIT_E_DEVICE: the current device is not sm_103";
         case TRIT_E_SCRATCH:
             return "TRIT_E_SCRATCH: the product needs more than TRIT_NOALLOC_SCRATCH_BYTES of scratch";
+        case TRIT_E_VALUE: return "TRIT_E_VALUE: a weight outside {-1, 0, +1}";
     }
     return "unknown trit_status";
 }
 
 TRIT_API const char *trit_last_cuda_error(void) { return g_last_cuda_error; }
 
-TRIT_API int32_t trit_abi_version(void) { return 1; }
+TRIT_API int32_t trit_abi_version(void) { return 2; }
 
 TRIT_API int64_t trit_payload_bytes(int64_t N, int64_t K) {
     if (!rows_ok(N) || !cols_ok(K)) return -1;
@@ -465,6 +466,56 @@ TRIT_API trit_status trit_gemm_noalloc(const uint8_t *planes, float w_scale, con
     if (e == cudaSuccess)
         e = small ? launch_skinny_into(d, xh, err_flag, s) : launch_prefill_into(d, xh, err_flag, s);
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+TRIT_API trit_status trit_bitcos_pack(const int8_t *w, int64_t N, int64_t K, uint64_t *bitmap,
+                                      uint32_t *sign_off, uint32_t *signs, int64_t *sign_words) {
+    if (!w || !sign_words) return TRIT_E_ARG;
+    if (signs && (!bitmap || !sign_off)) return TRIT_E_ARG;
+    if (!rows_ok(N) || K < 1 || K > kBitcosMaxK) return TRIT_E_SHAPE;
+    return static_cast<trit_status>(bitcos_pack_host(w, N, K, bitmap, sign_off, signs, sign_words));
+}
+
+TRIT_API trit_status trit_bitcos_gemv_many(const trit_bitcos_proj *list, int32_t count,
+                                           trit_stream_t stream) {
+    if (!list || count <= 0) return TRIT_E_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        const trit_bitcos_proj &p = list[i];
+        if (!p.bitmap || !p.sign_off || !p.signs || !p.x_i8 || !p.x_scale || (!p.y_i32 && !p.y_f32) ||
+            p.reserved != 0)
+            return TRIT_E_ARG;
+        if (!aligned(p.bitmap, 16) || !aligned(p.sign_off, 4) || !aligned(p.signs, 4) ||
+            !aligned(p.x_i8, 16) || !aligned(p.x_scale, 4) || !aligned(p.y_i32, 4) ||
+            !aligned(p.y_f32, 4))
+            return TRIT_E_ARG;
+        if (!rows_ok(p.N) || p.K < 1 || p.K > kBitcosMaxK || p.sign_words < 2) return TRIT_E_SHAPE;
+        if (!isfinite(p.w_scale) || !(p.w_scale > 0.0f)) return TRIT_E_SCALE;
+    }
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    static thread_local BitcosDev devs[TRIT_MAX_LIST_PER_LAUNCH];
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t base = 0; base < count; base += TRIT_MAX_LIST_PER_LAUNCH) {
+        const int n = count - base < TRIT_MAX_LIST_PER_LAUNCH ? count - base : TRIT_MAX_LIST_PER_LAUNCH;
+        for (int i = 0; i < n; ++i) {
+            const trit_bitcos_proj &p = list[base + i];
+            BitcosDev &d = devs[i];
+            d.bitmap = p.bitmap;
+            d.sign_off = p.sign_off;
+            d.signs = p.signs;
+            d.x = p.x_i8;
+            d.x_scale = p.x_scale;
+            d.y_i32 = p.y_i32;
+            d.y_f32 = p.y_f32;
+            d.N = p.N;
+            d.K = p.K;
+            d.sign_words = p.sign_words;
+            d.w_scale = p.w_scale;
+        }
+        const cudaError_t e = launch_bitcos_many(devs, n, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TRIT_OK;
 }
 
 }  // extern "C"

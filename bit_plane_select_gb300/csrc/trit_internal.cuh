@@ -325,6 +325,24 @@ cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M,
                                 float w_g, float w_u, const float *x_scale, int8_t *q,
                                 float *h_scale, cudaStream_t s);
 
+// BITCOS weights (presence bitmap + compacted signs), one activation row.
+constexpr int64_t kBitcosMaxK = TRIT_BITCOS_MAX_K;
+struct BitcosDev {
+    const uint64_t *bitmap;
+    const uint32_t *sign_off;
+    const uint32_t *signs;
+    const int8_t *x;
+    const float *x_scale;
+    int32_t *y_i32;
+    float *y_f32;
+    int64_t N, K, sign_words;
+    float w_scale;
+};
+cudaError_t launch_bitcos_many(const BitcosDev *list, int count, cudaStream_t s);
+// Host packer (trit_bitcos_pack): returns a trit_status.
+int bitcos_pack_host(const int8_t *w, int64_t N, int64_t K, uint64_t *bitmap, uint32_t *sign_off,
+                     uint32_t *signs, int64_t *sign_words);
+
 int device_sm_count();
 
 }  // namespace trit

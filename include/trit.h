@@ -72,8 +72,9 @@ typedef enum trit_status {
     TRIT_E_SCALE = 4,       /* w_scale not finite or <= 0 ("The .trit format, version 1" -- 2.2) */
     TRIT_E_CUDA = 6,        /* a CUDA runtime call or launch failed */
     TRIT_E_DEVICE = 7,      /* the current device is not an sm_103 GPU */
-    TRIT_E_SCRATCH = 8      /* trit_gemm_noalloc: the call needs more than
+    TRIT_E_SCRATCH = 8,     /* trit_gemm_noalloc: the call needs more than
                                TRIT_NOALLOC_SCRATCH_BYTES of scratch */
+    TRIT_E_VALUE = 9        /* trit_bitcos_pack: a weight outside {-1, 0, +1} */
 } trit_status;
 
 /* Bits of *err_flag. */
@@ -378,6 +379,67 @@ TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *s
  * device memory for the count.  TRIT_E_ARG for a null pointer; CUDA failures as
  * for the other calls (then *mismatches = UINT64_MAX). */
 TRIT_API trit_status trit_check_div127(uint64_t *mismatches);
+
+/*
+ * ---- BITCOS weights -----------------------------------------------------------
+ * "BITCOS: Intel's Ternary LLM Weight Format Goes Below 1.58 Bits" -- A bitmap
+ * and a sign; Decoding is the other half of the bill.  A ternary matrix as a
+ * presence bitmap (one bit per weight, set for a non-zero weight) and a sign
+ * vector (one bit per non-zero weight in the same order, set for -1): 2 - z
+ * bits per weight at zero density z, against 2 for the planes.  Here in a
+ * blocked form so that every row can be started on its own:
+ *   bitmap   uint64 [N][ceil(K/64)]: bit c%64 of word [r][c/64] = (W[r][c] != 0);
+ *            bits past K are 0;
+ *   sign_off uint32 [N+1]: sign_off[0] = 0, sign_off[r+1] = sign_off[r] +
+ *            ceil(nnz_r / 32) (nnz_r: row r's non-zeros);
+ *   signs    uint32 [sign_off[N] + 2]: the k-th non-zero of row r (column order)
+ *            is -1 when bit k%32 of word sign_off[r] + k/32 is set; all other
+ *            bits, and the last two words, are 0.
+ * Row r's sign bits, in order and cut to nnz_r, are row r's part of the page's
+ * flat sign vector; its bitmap bits are row r's part of the flat bitmap.
+ */
+#define TRIT_BITCOS_MAX_K 16384
+
+/* trit_bitcos_pack -- HOST code, no CUDA call: W [N][K] int8 in {-1, 0, +1}
+ * (host memory, row-major, K columns, no padding) -> the three arrays above, in
+ * host memory.  Call with signs == NULL first: *sign_words receives the length of
+ * `signs` (sign_off[N] + 2) and bitmap / sign_off may be NULL.  Then call with
+ * bitmap [N * ceil(K/64)], sign_off [N+1] and signs [*sign_words].
+ *   TRIT_E_ARG    w or sign_words NULL; signs given without bitmap or sign_off
+ *   TRIT_E_SHAPE  N or K outside [1, 2^31) x [1, TRIT_BITCOS_MAX_K], or more
+ *                 than 2^32 - 3 sign words
+ *   TRIT_E_VALUE  a weight outside {-1, 0, +1} (the outputs are then undefined)
+ */
+TRIT_API trit_status trit_bitcos_pack(const int8_t *w, int64_t N, int64_t K, uint64_t *bitmap,
+                                      uint32_t *sign_off, uint32_t *signs, int64_t *sign_words);
+
+/* One product of trit_bitcos_gemv_many: y = W x for ONE activation row.
+ * All pointers are device pointers. */
+typedef struct trit_bitcos_proj {
+    const uint64_t *bitmap;     /* [N][ceil(K/64)], 16-byte aligned */
+    const uint32_t *sign_off;   /* [N+1], 4-byte aligned */
+    const uint32_t *signs;      /* [sign_words], 4-byte aligned */
+    const int8_t *x_i8;         /* [K_pad] activation codes, 16-byte aligned (columns >= K ignored) */
+    const float *x_scale;       /* [1] */
+    int32_t *y_i32;             /* [N], or NULL */
+    float *y_f32;               /* [N], or NULL (not both) */
+    int64_t N, K;
+    int64_t sign_words;         /* length of `signs`; reads are clamped to it */
+    float w_scale;              /* finite, > 0 */
+    int32_t reserved;           /* must be 0 */
+} trit_bitcos_proj;
+
+/* trit_bitcos_gemv_many -- y = W x for every product of the host list, W in the
+ * BITCOS form above: exact int32 sums, y_f32 = (((float)y * w_scale) *
+ * x_scale) / 127 as for trit_gemm, identical bits to trit_gemm on the planes of
+ * the same W.  A list longer than TRIT_MAX_LIST_PER_LAUNCH is split.  The first
+ * call on each device uploads a 64 KB table (cudaMemcpyToSymbol, synchronous):
+ * make it before any stream capture.  The arrays must be those trit_bitcos_pack
+ * produced (inconsistent ones give wrong results; every read stays inside the
+ * arrays' stated lengths).  TRIT_E_ARG / TRIT_E_SHAPE / TRIT_E_SCALE as for
+ * trit_gemm_many (K <= TRIT_BITCOS_MAX_K). */
+TRIT_API trit_status trit_bitcos_gemv_many(const trit_bitcos_proj *list, int32_t count,
+                                           trit_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
                      "trit_gemm", "trit_gemm_many", "trit_quant_act_many",
                      "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_file_open",
                      "trit_file_open_memory", "trit_file_verify", "trit_file_upload",
-                     "trit_fnv1a64"):
+                     "trit_fnv1a64", "trit_bitcos_pack", "trit_bitcos_gemv_many"):
         assert required in names
 
 
@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(trit):
     lib = ctypes.CDLL(trit.library_path())
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert trit.lib().trit_abi_version() == 1
+    assert trit.lib().trit_abi_version() == 2
 
 
 def test_struct_layouts(trit):
@@ -49,6 +49,7 @@ def test_struct_layouts(trit):
     assert ctypes.sizeof(trit.TritAct) == 40
     assert ctypes.sizeof(trit.TritQProj) == 72 and trit.TritQProj.w_scale.offset == 64
     assert ctypes.sizeof(trit.TritMlpProj) == 96
+    assert ctypes.sizeof(trit.TritBitcosProj) == 88
 
 
 def test_struct_layouts_match_the_c_compiler(trit, tmp_path):
@@ -60,7 +61,8 @@ def test_struct_layouts_match_the_c_compiler(trit, tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     structs = {"trit_proj": trit.TritProj, "trit_qproj": trit.TritQProj,
-               "trit_act": trit.TritAct, "trit_mlpproj": trit.TritMlpProj}
+               "trit_act": trit.TritAct, "trit_mlpproj": trit.TritMlpProj,
+               "trit_bitcos_proj": trit.TritBitcosProj}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "trit.h"', "int main(void) {"]
     for cname, cls in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -95,6 +97,7 @@ def test_status_strings(trit):
     L = trit.lib()
     assert L.trit_status_string(0) == b"TRIT_OK"
     assert L.trit_status_string(2).startswith(b"TRIT_E_SHAPE")
+    assert L.trit_status_string(9).startswith(b"TRIT_E_VALUE")
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(),
@@ -133,3 +136,19 @@ def test_argument_errors_are_rejected_on_the_host(trit):
     # trit_verify(planes, N, K, err, first_bad, stream)
     assert L.trit_verify(p, 2, 10, null, null, s) == 1
     assert L.trit_verify(p, 2, 10, p, ctypes.c_void_p(0x10004), s) == 1
+    # trit_bitcos_gemv_many(list, count, stream)
+    B = trit.TritBitcosProj
+    assert L.trit_bitcos_gemv_many(null, 1, s) == 1
+    ok = B(p, p, p, p, p, p, p, 8, 64, 10, 1.0, 0)
+    cases = [(B(p, p, p, p, p, p, p, 8, 64, 10, 1.0, 3), 1),              # reserved
+             (B(ctypes.c_void_p(0x10008), p, p, p, p, p, p, 8, 64, 10, 1.0, 0), 1),   # bitmap align
+             (B(p, p, p, p, p, null, null, 8, 64, 10, 1.0, 0), 1),        # no output
+             (B(p, p, p, p, p, p, p, 8, trit.BITCOS_MAX_K + 1, 10, 1.0, 0), 2),
+             (B(p, p, p, p, p, p, p, 0, 64, 10, 1.0, 0), 2),
+             (B(p, p, p, p, p, p, p, 8, 64, 1, 1.0, 0), 2),                # sign_words < 2
+             (B(p, p, p, p, p, p, p, 8, 64, 10, float("nan"), 0), 4)]
+    for bad, code in cases:
+        lst = (B * 2)(ok, bad)
+        assert L.trit_bitcos_gemv_many(ctypes.cast(lst, ctypes.c_void_p), 2, s) == code
+    lst = (B * 1)(ok)
+    assert L.trit_bitcos_gemv_many(ctypes.cast(lst, ctypes.c_void_p), 0, s) == 1
