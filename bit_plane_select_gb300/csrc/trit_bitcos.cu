@@ -19,12 +19,13 @@
 // code-word multiply-accumulate as the bit-plane kernel: y = sum c x - sum x
 // with c = 1 + pos - neg.
 //
-// One warp per row, lane l on 64-column words l, l+32, ...: each word's first
-// sign bit is the row's bit offset plus the popcounts of the earlier words (a
-// warp scan).  Each warp double-buffers its rows in shared memory: the next
-// row's bitmap and sign words are copied in (cp.async) while the current one
-// is decoded.  Persistent CTAs take contiguous ranges of the list's rows split
-// by cost (bitmap words) and stage each product's activation row once.
+// One thread per row: it walks the row's bitmap words in order and reads its
+// sign bits through a 64-bit cursor refilled 32 bits at a time, 32 columns per
+// step so that one refill always suffices; both streams are loaded four words
+// ahead, so no load waits on the decoding; the 32 rows of a warp move through the same columns
+// together, so the staged activation words are read as broadcasts.  Persistent
+// CTAs take contiguous ranges of the list's rows split by cost (bitmap words)
+// and stage each product's activation row once.
 #include <mutex>
 
 #include "trit_internal.cuh"
@@ -55,8 +56,6 @@ struct BEntry {
 
 struct BList {
     int32_t count;
-    int32_t rowbuf;       // bytes of one row buffer: bitmap part + sign part
-    int32_t bm_bytes;     // bytes of the bitmap part (16-byte multiple)
     int32_t max_beats;    // staged activation beats
     int64_t total_cost;
     BEntry e[kMaxListB];
@@ -66,24 +65,6 @@ static_assert(sizeof(BList) <= 32764, "kernel parameter space");
 // Deposit table: entry (m << 8) | s holds the low bits of s placed, in order,
 // at the set bits of the byte m (the rest 0).  Uploaded once per device.
 __device__ __align__(16) uint8_t g_deposit[kLutBytes];
-
-__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // Code-word multiply-accumulate of one 32-column word pair against the
 // permuted activation words (byte i of x[j] = column 8i + j): acc[j] gathers
@@ -105,13 +86,13 @@ __device__ __forceinline__ int32_t codes_sum(const int (&acc)[8]) {
            ((acc[3] + acc[7]) >> 6);
 }
 
-// Deposit the low bits of s into the set bits of b, a byte at a time.
-__device__ __forceinline__ uint64_t deposit64(uint64_t s, uint64_t b, const uint8_t *lut) {
-    uint64_t n = 0;
+// Deposit the low bits of s into the set bits of the 32-bit word b, a byte at a time.
+__device__ __forceinline__ uint32_t deposit32(uint32_t s, uint32_t b, const uint8_t *lut) {
+    uint32_t n = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t mb = uint32_t(b >> (8 * j)) & 0xFFu;
-        n |= uint64_t(lut[(mb << 8) | (uint32_t(s) & 0xFFu)]) << (8 * j);
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t mb = (b >> (8 * j)) & 0xFFu;
+        n |= uint32_t(lut[(mb << 8) | (s & 0xFFu)]) << (8 * j);
         s >>= __popc(mb);
     }
     return n;
@@ -164,9 +145,6 @@ __global__ void __launch_bounds__(kThreadsB) bitcos_gemv_kernel(const __grid_con
     uint8_t *lut = smem;
     uint32_t *xs = reinterpret_cast<uint32_t *>(smem + kLutBytes);
     int32_t *s_part = reinterpret_cast<int32_t *>(xs + L.max_beats * kXBeatWords);
-    uint8_t *bufs = reinterpret_cast<uint8_t *>(s_part + kWarpsB);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *mybuf = bufs + warp * 2 * L.rowbuf;
 
     for (int i = threadIdx.x; i < kLutBytes / 16; i += kThreadsB)
         reinterpret_cast<uint4 *>(lut)[i] = reinterpret_cast<const uint4 *>(g_deposit)[i];
@@ -181,89 +159,55 @@ __global__ void __launch_bounds__(kThreadsB) bitcos_gemv_kernel(const __grid_con
         const int32_t xsum = stage_row(E, xs, s_part);
         __syncthreads();
         const float xsc = *E.x_scale;
-
-        // this warp's rows: rb + warp, rb + warp + kWarpsB, ...
-        int64_t r = rb + warp;
-        auto offs = [&](int64_t row, uint32_t &a, uint32_t &b) {
-            if (row < re) {   // clamped to the array: nothing outside it is ever read
-                const int64_t sw = E.sign_words;
-                const int64_t o1 = E.sign_off[row + 1] < sw ? E.sign_off[row + 1] : sw;
-                const int64_t o0 = E.sign_off[row] < o1 ? E.sign_off[row] : o1;
-                const int64_t cap = 2 * int64_t(E.B);   // a row's sign words, at most
-                a = uint32_t(o0);
-                b = uint32_t(o1 - o0 < cap ? o1 : o0 + cap);
-            }
-        };
-        auto issue = [&](int64_t row, int slot, uint32_t so0, uint32_t so1) {
-            if (row < re) {
-                uint8_t *buf = mybuf + slot * L.rowbuf;
-                const uint64_t *bm = E.bitmap + row * E.B;
-                for (int i = lane; i < E.B; i += 32) cp_async8(buf + 8 * i, bm + i);
-                const int nw = int(so1 - so0);
-                uint8_t *sb = buf + L.bm_bytes;
-                for (int i = lane; i < nw; i += 32) cp_async4(sb + 4 * i, E.signs + so0 + i);
-            }
-            cp_commit();
-        };
-        uint32_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
-        offs(r, a0, a1);
-        offs(r + kWarpsB, b0, b1);
-        issue(r, 0, a0, a1);
-        int slot = 0;
-        for (; r < re; r += kWarpsB, slot ^= 1) {
-            // the next row's copies, and the offsets of the one after it
-            issue(r + kWarpsB, slot ^ 1, b0, b1);
-            uint32_t c0 = 0, c1 = 0;
-            offs(r + 2 * kWarpsB, c0, c1);
-            cp_wait<1>();
-            __syncwarp();
-            const uint64_t *bmb = reinterpret_cast<const uint64_t *>(mybuf + slot * L.rowbuf);
-            const uint32_t *sgb = reinterpret_cast<const uint32_t *>(mybuf + slot * L.rowbuf + L.bm_bytes);
+        const int B = E.B;
+        for (int64_t row = rb + threadIdx.x; row < re; row += kThreadsB) {
+            // the row's sign words, clamped to the array: nothing outside it is read
+            const int64_t sw = E.sign_words;
+            const int64_t o1 = E.sign_off[row + 1] < sw ? int64_t(E.sign_off[row + 1]) : sw;
+            const int64_t o0 = E.sign_off[row] < o1 ? int64_t(E.sign_off[row]) : o1;
+            const int64_t nw = o1 - o0;
+            const uint32_t *sp = E.signs + o0;
+            const uint64_t *bm = E.bitmap + row * B;
+            uint64_t cur = 0;    // sign bits not yet used, lowest first
+            int avail = 0;       // how many
             int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            uint32_t run = 0;
-            for (int i0 = 0; i0 < E.B; i0 += 32) {
-                const int i = i0 + lane;
-                const uint64_t b = i < E.B ? bmb[i] : 0ull;
-                const uint32_t k = uint32_t(__popcll(b));
-                uint32_t incl = k;
+            // both streams are read in order, so their next words are loaded four
+            // ahead: bitmap words i..i+3 in b0..b3, the next sign words in q0..q3
+            uint64_t b0 = __ldg(bm), b1 = B > 1 ? __ldg(bm + 1) : 0ull;
+            uint64_t b2 = B > 2 ? __ldg(bm + 2) : 0ull, b3 = B > 3 ? __ldg(bm + 3) : 0ull;
+            uint32_t q0 = nw > 0 ? __ldg(sp) : 0u, q1 = nw > 1 ? __ldg(sp + 1) : 0u;
+            uint32_t q2 = nw > 2 ? __ldg(sp + 2) : 0u, q3 = nw > 3 ? __ldg(sp + 3) : 0u;
+            int64_t nq = 4;      // the next sign word to load
+            for (int i = 0; i < B; ++i) {
+                const uint64_t b = b0;
+                b0 = b1;
+                b1 = b2;
+                b2 = b3;
+                b3 = i + 4 < B ? __ldg(bm + i + 4) : 0ull;
+                const uint32_t *xw = xs + i * kXBeatWords;
 #pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const uint32_t v = __shfl_up_sync(~0u, incl, d);
-                    if (lane >= d) incl += v;
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t bh = uint32_t(b >> (32 * h));
+                    const int k = __popc(bh);
+                    if (avail < k) {   // avail <= 31 here, so 32 more bits fit
+                        cur |= uint64_t(q0) << avail;
+                        avail += 32;
+                        q0 = q1;
+                        q1 = q2;
+                        q2 = q3;
+                        q3 = nq < nw ? __ldg(sp + nq) : 0u;
+                        ++nq;
+                    }
+                    const uint32_t n = deposit32(uint32_t(cur), bh, lut);
+                    cur >>= k;
+                    avail -= k;
+                    mac_codes_b(bh & ~n, n, xw + 8 * h, acc);
                 }
-                const uint32_t tot = __shfl_sync(~0u, incl, 31);
-                if (i < E.B) {
-                    // the word's sign bits: k bits from bit `bit` of the row's stream;
-                    // only words holding some of them are read
-                    const uint32_t bit = run + incl - k;
-                    const uint32_t w = bit >> 5, sh = bit & 31u;
-                    const uint32_t w0 = k > 0 ? sgb[w] : 0u;
-                    const uint32_t w1 = sh + k > 32 ? sgb[w + 1] : 0u;
-                    const uint32_t w2 = sh + k > 64 ? sgb[w + 2] : 0u;
-                    const uint64_t lo = (uint64_t(w1) << 32) | w0;
-                    const uint64_t s = sh ? (lo >> sh) | (uint64_t(w2) << (64 - sh)) : lo;
-                    const uint64_t n = deposit64(s, b, lut);
-                    const uint64_t p = b & ~n;
-                    const uint32_t *xw = xs + i * kXBeatWords;
-                    mac_codes_b(uint32_t(p), uint32_t(n), xw, acc);
-                    mac_codes_b(uint32_t(p >> 32), uint32_t(n >> 32), xw + 8, acc);
-                }
-                run += tot;
             }
-            int32_t y = codes_sum(acc);
-#pragma unroll
-            for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(~0u, y, o);
-            y -= xsum;
-            if (lane == 0) {
-                if (E.y_i32) E.y_i32[r] = y;
-                if (E.y_f32) E.y_f32[r] = dequant(y, E.w_scale, xsc);
-            }
-            __syncwarp();   // the slot is read before the next issue overwrites it
-            b0 = c0;
-            b1 = c1;
+            const int32_t y = codes_sum(acc) - xsum;
+            if (E.y_i32) E.y_i32[row] = y;
+            if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, xsc);
         }
-        cp_wait<0>();
-        __syncwarp();
     }
 }
 
@@ -371,11 +315,7 @@ cudaError_t launch_bitcos_many(const BitcosDev *list, int count, cudaStream_t s)
         }
         L.total_cost = cost;
         L.max_beats = maxB;
-        L.bm_bytes = (maxB * 8 + 15) & ~15;
-        // sign words of a row: at most ceil(K/32) <= 2 * maxB
-        L.rowbuf = L.bm_bytes + ((2 * maxB * 4 + 15) & ~15);
-        const size_t smem = size_t(kLutBytes) + size_t(maxB) * kXBeatWords * 4 + kWarpsB * 4 +
-                            size_t(kWarpsB) * 2 * L.rowbuf;
+        const size_t smem = size_t(kLutBytes) + size_t(maxB) * kXBeatWords * 4 + kWarpsB * 4;
         e = cudaFuncSetAttribute(bitcos_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem));
         if (e != cudaSuccess) return e;
