@@ -1,0 +1,56 @@
+"""Host-side logic of bench.py that decides what a benchmark line reports: the
+clock summary (throttle reasons read from nvidia-smi's CSV), the replica
+rates, and the rule that DRAM traffic from a committed profile is reported
+only while the kernel source it was taken on is unchanged."""
+import importlib.util
+import json
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_clock_summary_median_and_reasons(bench):
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 2055, 2070, 1350.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1300.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    out = s.summary()
+    assert out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0 and out["samples"] == 3
+    assert out["reasons"] == ["sw_power_cap"]
+    s.lines = ["0, 1500, 2070, 700, 0x8, Active, Not Active, Active, Not Active"]
+    assert s.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_clock_summary_without_samples(bench):
+    out = bench.ClockSampler(0).summary()
+    assert out == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_replica_rates(bench):
+    gbs, tps = bench.replica_rates(step_bytes=500_000_000, steps=100, total_ms=10.0, world=4)
+    assert gbs == pytest.approx(4 * 500e6 * 100 / 0.01 / 1e9)
+    assert tps == pytest.approx(4 * 100 / 0.01)
+
+
+def test_traffic_only_while_the_source_is_unchanged(bench, monkeypatch):
+    with open(os.path.join(ROOT, "profiles", "select_accumulate_stack30.json")) as f:
+        d = json.load(f)
+    monkeypatch.setattr(bench, "source_hash", lambda paths: d["source_hash"])
+    assert bench.committed_traffic(0) == d["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "source_hash", lambda paths: "0" * 16)
+    assert bench.committed_traffic(0) is None
+
