@@ -657,6 +657,40 @@ def run_prefill(args):
     print(json.dumps(out), flush=True)
 
 
+MMA_CYCLES_M128 = 101.4   # tcgen05.mma cta_group::1 kind::f16, M = 128, N <= 128: measured back to back
+
+
+def batch_floors(M: int, shapes, nbytes: int, peak_gbs: float, sm_count: int, sm_mhz: float) -> dict:
+    """Lower bounds on one batched step over `shapes` ((N, K) per product) with
+    M activation rows, for the path the library takes at that M:
+      hbm: the step's algorithmic bytes at the measured copy peak;
+      dp4a path (2 <= M <= 12, rows in chunks of 8): the code-byte logic (38
+        instructions per weight row and beat, once per chunk) plus 16 dp4a per
+        activation row and beat, at 128 lanes per SM per cycle;
+      tensor path (13 <= M <= 128): four M = 128 MMAs per 128 weight rows and
+        beat at MMA_CYCLES_M128 each, one MMA stream per SM.
+    Returns the floors in ms and which one is larger (the bound)."""
+    f = sm_mhz * 1e6
+    out = {"hbm_floor_ms": nbytes / (peak_gbs * 1e9) * 1e3}
+    row_beats = sum(N * ((K + 63) // 64) for N, K in shapes)
+    if 2 <= M <= 12:
+        chunks = (M + 7) // 8
+        out["path"] = "dp4a"
+        out["alu_floor_ms"] = row_beats * (38 * chunks + 16 * M) / (128 * sm_count * f) * 1e3
+        other = out["alu_floor_ms"]
+    elif 13 <= M <= 128:
+        tiles = sum(((N + 127) // 128) * ((K + 63) // 64) for N, K in shapes)
+        out["path"] = "tensor (weights as the 128-row operand)"
+        out["mma_floor_ms"] = tiles * 4 * MMA_CYCLES_M128 / (sm_count * f) * 1e3
+        other = out["mma_floor_ms"]
+    else:
+        out["path"] = "dp4a (M = 1)" if M == 1 else "tensor (pair tiles)"
+        other = 0.0
+    out["bound"] = "hbm" if out["hbm_floor_ms"] >= other else ("alu" if M <= 12 else "mma")
+    out["floor_ms"] = max(out["hbm_floor_ms"], other)
+    return out
+
+
 def run_batch_sweep(args):
     """Batched decode over the 30-layer stack: M activation rows per projection."""
     import torch
@@ -678,6 +712,8 @@ def run_batch_sweep(args):
     for i, (layer, idx, name, N, K) in enumerate(synth.stack_items(args.layers)):
         st.x[i].copy_(torch.from_numpy(synth.projection_acts(3, layer, idx, Mmax)))
     st.quantize()
+    peak, peak_kind = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     out = {}
     for M in synth.BATCH_SWEEP:
         plist = t.ProjList([(st.planes[i], st.specs[i][4], st.q[i][:M], st.s[i][:M], st.specs[i][2],
@@ -686,11 +722,19 @@ def run_batch_sweep(args):
         ms = _timed(lambda: t.trit_gemm_many(plist, err), max(3, args.steps // M), args.warmup, stream)
         nbytes = sum(t.payload_bytes(N, K) + M * (t.k_pad(K) + 4 + 8 * N)
                      for _, N, K, _, _ in st.specs)
+        fl = batch_floors(M, [(N, K) for _, N, K, _, _ in st.specs], nbytes, peak, sms, 2070.0)
         out[M] = {"ms_per_step": round(ms, 4), "tok_per_s": round(M / (ms * 1e-3), 1),
-                  "GBs": round(nbytes / (ms * 1e-3) / 1e9, 1), "err_flag": int(err.item())}
+                  "GBs": round(nbytes / (ms * 1e-3) / 1e9, 1), "err_flag": int(err.item()),
+                  "path": fl["path"], "bound": fl["bound"],
+                  "hbm_floor_ms": round(fl["hbm_floor_ms"], 4),
+                  "compute_floor_ms": round(fl.get("alu_floor_ms", fl.get("mma_floor_ms", 0.0)), 4),
+                  "frac_of_floor": round(fl["floor_ms"] / ms, 4)}
     print(json.dumps({"metric": "batched ternary decode over the 30-layer stack",
                       "unit": "tok/s", "value": out[Mmax]["tok_per_s"],
-                      "config": {"workload": "bitnet-2b4t-30layer-batch-sweep"}, "by_M": out}),
+                      "config": {"workload": "bitnet-2b4t-30layer-batch-sweep"},
+                      "floors": {"peak_gbs": peak, "peak_kind": peak_kind, "sm_count": sms,
+                                 "sm_mhz": 2070.0, "mma_cycles_m128": MMA_CYCLES_M128},
+                      "by_M": out}),
           flush=True)
 
 

@@ -54,3 +54,21 @@ def test_traffic_only_while_the_source_is_unchanged(bench, monkeypatch):
     monkeypatch.setattr(bench, "source_hash", lambda paths: "0" * 16)
     assert bench.committed_traffic(0) is None
 
+
+
+def test_batch_floors(bench):
+    shapes = [(2560, 2560), (6912, 2560), (2560, 6912)]
+    row_beats = 2560 * 40 + 6912 * 40 + 2560 * 108
+    tiles = 20 * 40 + 54 * 40 + 20 * 108
+    f = 2070e6
+    one = bench.batch_floors(1, shapes, 10**9, 6785.2, 152, 2070.0)
+    assert one["bound"] == "hbm" and one["hbm_floor_ms"] == pytest.approx(1e9 / 6785.2e9 * 1e3)
+    m8 = bench.batch_floors(8, shapes, 10**9, 6785.2, 152, 2070.0)
+    assert m8["path"] == "dp4a"
+    assert m8["alu_floor_ms"] == pytest.approx(row_beats * (38 + 128) / (128 * 152 * f) * 1e3)
+    m12 = bench.batch_floors(12, shapes, 10**9, 6785.2, 152, 2070.0)
+    assert m12["alu_floor_ms"] == pytest.approx(row_beats * (76 + 192) / (128 * 152 * f) * 1e3)
+    m64 = bench.batch_floors(64, shapes, 10**9, 6785.2, 152, 2070.0)
+    assert m64["path"].startswith("tensor") and m64["bound"] in ("hbm", "mma")
+    assert m64["mma_floor_ms"] == pytest.approx(tiles * 4 * 101.4 / (152 * f) * 1e3)
+    assert m64["floor_ms"] == max(m64["hbm_floor_ms"], m64["mma_floor_ms"])
