@@ -418,6 +418,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_layers)
         out["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores(args.cpu_layers)
+        out["cpu_baseline"]["configs"] = cpu_baseline_configs()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -475,6 +476,31 @@ def cpu_baseline(layers):
             "sample": f"layers 0..{layers - 1} of the 30-layer stack ({len(items)} projections, "
                       f"{weights} weights), quantise + product, {passes} passes of "
                       f"{dt:.2f} s each"}
+
+
+def cpu_baseline_configs(seconds: float = 2.0):
+    """The oracle, single-threaded, on the two small workloads: one 2560 x 2560
+    product (P(0) = 0.4219) and one layer (seven products); quantise + product,
+    whole passes for about `seconds` each."""
+    import oracle
+    import synth
+    w0, x0 = synth.config0()
+    cases = {"single_product_2560x2560": [(oracle.pack(w0), float(synth.w_scale(w0)), x0, 2560, 2560)],
+             "one_layer_7_products": [(oracle.pack(w), float(synth.w_scale(w)), x, w.shape[1], w.shape[0])
+                                      for _, w, x in synth.config1()]}
+    out = {}
+    for name, items in cases.items():
+        weights = sum(n * K for _, _, _, K, n in items)
+        passes, t = 0, time.perf_counter()
+        while True:
+            oracle_step(items)
+            passes += 1
+            if time.perf_counter() - t >= seconds:
+                break
+        dt = (time.perf_counter() - t) / passes
+        out[name] = {"weights_per_s": round(weights / dt), "plane_gbs": round(weights / 4 / dt / 1e9, 4),
+                     "cores": 1, "passes": passes, "s_per_pass": round(dt, 4)}
+    return out
 
 
 def _oracle_shard(layers, shard, nshards, seconds, barrier, q):
