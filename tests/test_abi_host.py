@@ -152,3 +152,70 @@ def test_argument_errors_are_rejected_on_the_host(trit):
         assert L.trit_bitcos_gemv_many(ctypes.cast(lst, ctypes.c_void_p), 2, s) == code
     lst = (B * 1)(ok)
     assert L.trit_bitcos_gemv_many(ctypes.cast(lst, ctypes.c_void_p), 0, s) == 1
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="uses fake pointers; only run where no GPU can be reached")
+def test_argument_errors_of_the_other_entry_points(trit):
+    """The entry points the test above leaves out: each case is invalid by
+    construction and must be refused on the host before any CUDA call."""
+    L = trit.lib()
+    p = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10001)
+    null = ctypes.c_void_p(0)
+    s = null
+    nan = float("nan")
+    # trit_unpack(planes, N, K, w, err, stream)
+    assert L.trit_unpack(p, 4, 64, null, p, s) == 1
+    assert L.trit_unpack(odd, 4, 64, p, p, s) == 1
+    assert L.trit_unpack(p, 0, 64, p, p, s) == 2
+    # trit_gemv(planes, w_scale, x, x_scale, N, K, y_i32, y_f32, err, stream)
+    assert L.trit_gemv(p, 1.0, p, p, 8, 64, null, null, p, s) == 1
+    assert L.trit_gemv(p, 1.0, p, p, 8, 0, p, p, p, s) == 2
+    assert L.trit_gemv(p, nan, p, p, 8, 64, p, p, p, s) == 4
+    # trit_quant_act_many(list, count, err, stream)
+    A = trit.TritAct
+    assert L.trit_quant_act_many(null, 1, p, s) == 1
+    acts = (A * 2)(A(p, p, p, 2, 64), A(p, p, p, 2, 0))
+    assert L.trit_quant_act_many(ctypes.cast(acts, ctypes.c_void_p), 2, p, s) == 2
+    acts = (A * 1)(A(p, odd, p, 2, 64))
+    assert L.trit_quant_act_many(ctypes.cast(acts, ctypes.c_void_p), 1, p, s) == 1
+    assert L.trit_quant_act_many(ctypes.cast(acts, ctypes.c_void_p), 0, p, s) == 1
+    # trit_quant_gemv_many(list, count, err, stream)
+    Q = trit.TritQProj
+    good_q = Q(p, p, p, p, p, p, 8, 64, 1.0, 0)
+    for bad, code in [(Q(p, p, p, p, p, p, 8, 64, 1.0, 1), 1),
+                      (Q(p, null, p, p, p, p, 8, 64, 1.0, 0), 1),
+                      (Q(p, p, odd, p, p, p, 8, 64, 1.0, 0), 1),
+                      (Q(p, p, p, p, p, p, 8, trit.MAX_FUSED_K + 1, 1.0, 0), 2),
+                      (Q(p, p, p, p, p, p, 8, 64, 0.0, 0), 4)]:
+        lst = (Q * 2)(good_q, bad)
+        assert L.trit_quant_gemv_many(ctypes.cast(lst, ctypes.c_void_p), 2, p, s) == code
+    # trit_intmlp_gemv_many(list, count, err, stream)
+    Mp = trit.TritMlpProj
+    good_m = Mp(p, p, p, p, 1.0, 1.0, p, p, p, p, 8, 64, 1.0, 0)
+    for bad, code in [(Mp(p, p, p, p, 1.0, 1.0, p, p, p, p, 8, 64, 1.0, 2), 1),
+                      (Mp(p, p, p, p, 1.0, 1.0, odd, p, p, p, 8, 64, 1.0, 0), 1),
+                      (Mp(p, p, p, p, 1.0, 1.0, p, p, null, null, 8, 64, 1.0, 0), 1),
+                      (Mp(p, p, p, p, 1.0, 1.0, p, p, p, p, 8, trit.MAX_FUSED_K + 1, 1.0, 0), 2),
+                      (Mp(p, p, p, p, nan, 1.0, p, p, p, p, 8, 64, 1.0, 0), 4),
+                      (Mp(p, p, p, p, 1.0, -1.0, p, p, p, p, 8, 64, 1.0, 0), 4)]:
+        lst = (Mp * 2)(good_m, bad)
+        assert L.trit_intmlp_gemv_many(ctypes.cast(lst, ctypes.c_void_p), 2, p, s) == code
+    # trit_quant_act_folded(x, gain, M, K, eps, x_i8, x_scale, err, stream)
+    assert L.trit_quant_act_folded(p, null, 2, 64, 1e-6, p, p, p, s) == 1
+    assert L.trit_quant_act_folded(p, p, 2, 0, 1e-6, p, p, p, s) == 2
+    assert L.trit_quant_act_folded(p, p, 2, 64, -1.0, p, p, p, s) == 4
+    # trit_intmlp_quant(a_gate, a_up, M, N, w_gate, w_up, x_scale, h_i8, h_scale, stream)
+    assert L.trit_intmlp_quant(p, p, 1, 64, 1.0, 1.0, p, odd, p, s) == 1
+    assert L.trit_intmlp_quant(p, p, 1, 0, 1.0, 1.0, p, p, p, s) == 2
+    assert L.trit_intmlp_quant(p, p, 1, 64, 1.0, 0.0, p, p, p, s) == 4
+    # trit_gemm_noalloc(planes, w_scale, x, x_scale, M, N, K, y_i32, y_f32, err, stream)
+    assert L.trit_gemm_noalloc(p, 1.0, p, p, 1, 8, 64, p, p, null, s) == 1
+    assert L.trit_gemm_noalloc(p, 1.0, p, p, 1, 8, 0, p, p, p, s) == 2
+    assert L.trit_gemm_noalloc(p, 0.0, p, p, 1, 8, 64, p, p, p, s) == 4
+    # trit_read_probe(buf, bytes, sink, stream), trit_check_div127(mismatches)
+    assert L.trit_read_probe(p, 8, p, s) == 1
+    assert L.trit_read_probe(p, 17, p, s) == 1
+    assert L.trit_read_probe(p, 64, null, s) == 1
+    assert L.trit_check_div127(None) == 1
