@@ -685,6 +685,66 @@ def run_prefill(args):
 
 MMA_CYCLES_M128 = 101.4   # tcgen05.mma cta_group::1 kind::f16, M = 128, N <= 128: measured back to back
 
+# ---- issue rates (trit_issue_probe) -------------------------------------------
+
+ISSUE_KINDS = ("dp4a", "lop3", "prmt", "shf", "imad", "iadd", "shfl", "lds32", "lds128")
+
+
+def issue_rates(rec, threads: int, iters: int) -> dict:
+    """Per-SM completion rates from a trit_issue_probe record ([CTAs, 3] of SM
+    id, start clock, end clock): for every SM, the instructions its CTAs issued
+    (32 * iters per thread) over the span from the earliest start to the latest
+    end (SM clocks).  Returns lanes (thread-instructions) per SM-clock: the
+    median over SMs, and the lowest and highest."""
+    per_sm = {}
+    for smid, t0, t1 in rec:
+        n, lo, hi = per_sm.get(int(smid), (0, None, None))
+        lo = int(t0) if lo is None else min(lo, int(t0))
+        hi = int(t1) if hi is None else max(hi, int(t1))
+        per_sm[int(smid)] = (n + 1, lo, hi)
+    rates = sorted(n * threads * 32 * iters / max(hi - lo, 1) for n, lo, hi in per_sm.values())
+    return {"lanes_per_clk": round(statistics.median(rates), 2), "min": round(rates[0], 2),
+            "max": round(rates[-1], 2), "sms": len(rates)}
+
+
+def measure_issue_rates(dev, iters: int = 2048, threads: int = 256, ctas_per_sm: int = 4) -> dict:
+    """Every probe kind at ctas_per_sm x threads per SM (32 warps), each thread
+    issuing 32 * iters instructions in eight chains."""
+    import torch
+
+    import bit_plane_select_gb300 as t
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {}
+    for kind in ISSUE_KINDS:
+        t.trit_issue_probe(kind, sms * ctas_per_sm, threads, 16, dev)      # warm the kernel
+        rec = t.trit_issue_probe(kind, sms * ctas_per_sm, threads, iters, dev)
+        torch.cuda.synchronize(dev)
+        r = issue_rates(rec.cpu().numpy(), threads, iters)
+        if kind == "lds32":
+            r["bytes_per_clk"] = round(4 * r["lanes_per_clk"], 1)
+        if kind == "lds128":
+            r["bytes_per_clk"] = round(16 * r["lanes_per_clk"], 1)
+        out[kind] = r
+    return out
+
+
+def run_issue(args):
+    """The integer and shared-memory issue rates the decode kernels are built
+    from, in lanes per SM-clock (clock64 spans, so independent of the clock)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    with ClockSampler(0) as clk:
+        rates = measure_issue_rates(dev)
+    print(json.dumps({"metric": "issue rates, lanes per SM-clock", "unit": "lanes/clk/SM",
+                      "value": rates["dp4a"]["lanes_per_clk"], "by_kind": rates,
+                      "config": {"workload": "trit_issue_probe, 4 CTAs x 256 threads per SM, "
+                                             "8 chains per thread"},
+                      "clocks": clk.summary()}), flush=True)
+
 
 def batch_floors(M: int, shapes, nbytes: int, peak_gbs: float, sm_count: int, sm_mhz: float) -> dict:
     """Lower bounds on one batched step over `shapes` ((N, K) per product) with
@@ -928,7 +988,7 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=90.0)
-    ap.add_argument("--workload", choices=["decode", "prefill", "batch", "mlp", "bitcos"],
+    ap.add_argument("--workload", choices=["decode", "prefill", "batch", "mlp", "bitcos", "issue"],
                     default="decode",
                     help="decode (default): the 30-layer batch-1 stack; prefill, batch, mlp and "
                          "bitcos print extra lines for the other configurations")
@@ -945,6 +1005,8 @@ def main():
         run_mlp(args)
     elif args.workload == "bitcos":
         run_bitcos(args)
+    elif args.workload == "issue":
+        run_issue(args)
     else:
         run_ours(args)
 

@@ -29,7 +29,7 @@ __all__ = [
     "trit_quant_gemv_many", "ProjList", "ActList", "QProjList", "TritProj", "TritAct",
     "TritQProj", "MAX_FUSED_K", "trit_gemm_noalloc", "NOALLOC_SCRATCH_BYTES",
     "trit_quant_act_folded", "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
-    "trit_intmlp_gemv_many", "MlpProjList", "TritMlpProj",
+    "trit_intmlp_gemv_many", "MlpProjList", "TritMlpProj", "PROBE_KINDS", "trit_issue_probe",
 ]
 
 ERR_P1 = 1
@@ -116,7 +116,7 @@ def lib():
         L.trit_verify.argtypes = [p, i64, i64, p, p, p]
         L.trit_quant_act.argtypes = [p, i64, i64, p, p, p, p]
         L.trit_quant_act_many.argtypes = [p, i32, p, p]
-        L.trit_gemv.argtypes = [p, f32, p, p, i64, i64, p, p, p, p]
+        L.trit_gemv.argtypes = [p, f32, p, f32, i64, i64, p, p, p, p]
         L.trit_gemm.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         L.trit_gemm_many.argtypes = [p, i32, p, p]
         L.trit_quant_gemv_many.argtypes = [p, i32, p, p]
@@ -126,13 +126,15 @@ def lib():
         L.trit_intmlp_quant.argtypes = [p, p, i64, i64, f32, f32, p, p, p, p]
         L.trit_check_div127.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
         L.trit_read_probe.argtypes = [p, i64, p, p]
+        L.trit_issue_probe.argtypes = [i32, i32, i32, i64, p, p, p]
         L.trit_bitcos_pack.argtypes = [p, i64, i64, p, p, p, p]
         L.trit_bitcos_gemv_many.argtypes = [p, i32, p]
         for name in ("trit_pack", "trit_unpack", "trit_verify", "trit_quant_act",
                      "trit_quant_act_many", "trit_gemv", "trit_gemm", "trit_gemm_many",
                      "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_quant_act_folded",
                      "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
-                     "trit_intmlp_gemv_many", "trit_bitcos_pack", "trit_bitcos_gemv_many"):
+                     "trit_intmlp_gemv_many", "trit_bitcos_pack", "trit_bitcos_gemv_many",
+                     "trit_issue_probe"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -324,6 +326,27 @@ def trit_read_probe(buf: torch.Tensor, sink: torch.Tensor | None = None, stream=
     return sink
 
 
+# instruction kinds of trit_issue_probe (TRIT_PROBE_* in include/trit.h)
+PROBE_KINDS = {"dp4a": 0, "lop3": 1, "prmt": 2, "shf": 3, "imad": 4, "iadd": 5, "shfl": 6,
+               "lds32": 7, "lds128": 8}
+
+
+def trit_issue_probe(kind: str, blocks: int, threads: int, iters: int, device=None,
+                     stream=None) -> torch.Tensor:
+    """Launch the issue-rate probe for one instruction kind; returns the int64
+    [blocks, 3] device tensor of (SM id, start clock, end clock) per CTA (valid
+    once the stream has synchronised).  Every thread issues 32 * iters
+    instructions."""
+    dev = torch.device("cuda") if device is None else device
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    rec = torch.zeros((blocks, 3), dtype=torch.int64, device=dev)
+    _check(lib().trit_issue_probe(PROBE_KINDS[kind], blocks, threads, iters,
+                                  ctypes.c_void_p(sink.data_ptr()), ctypes.c_void_p(rec.data_ptr()),
+                                  _stream(stream)), "trit_issue_probe")
+    rec._probe_sink = sink   # keep the sink alive with the record
+    return rec
+
+
 def trit_check_div127() -> int:
     """Number of float32 bit patterns where the library's division by 127 (used
     by every fp32 dequantisation) differs from the IEEE divide; 0 = identical."""
@@ -332,8 +355,12 @@ def trit_check_div127() -> int:
     return int(n.value)
 
 
-def trit_gemv(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale: torch.Tensor,
+def trit_gemv(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale: float,
               K: int, y_i32=None, y_f32=None, err_flag=None, stream=None):
+    """One activation row, its scale a host float (the C signature's by-value
+    x_scale).  Returns (y_i32 [N], y_f32 [N], err_flag)."""
+    if isinstance(x_scale, torch.Tensor):
+        raise TypeError("trit_gemv takes x_scale as a float; use trit_gemm for a device scale")
     N = planes.shape[0]
     if y_i32 is None:
         y_i32 = torch.empty(N, dtype=torch.int32, device=planes.device)
@@ -341,7 +368,7 @@ def trit_gemv(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale:
         y_f32 = torch.empty(N, dtype=torch.float32, device=planes.device)
     err_flag = _err(err_flag, planes.device)
     _check(lib().trit_gemv(_dev(planes, torch.uint8, "planes"), float(w_scale),
-                           _dev(x_i8, torch.int8, "x_i8"), _dev(x_scale, torch.float32, "x_scale"),
+                           _dev(x_i8, torch.int8, "x_i8"), float(x_scale),
                            N, K, _dev(y_i32, torch.int32, "y_i32", True),
                            _dev(y_f32, torch.float32, "y_f32", True),
                            _dev(err_flag, torch.int32, "err_flag"), _stream(stream)), "trit_gemv")

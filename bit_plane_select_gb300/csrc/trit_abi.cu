@@ -73,7 +73,7 @@ ProjDev to_dev(const trit_proj &p) {
     d.K = int32_t(p.K);
     d.B = int32_t(beats_per_row(p.K));
     d.w_scale = p.w_scale;
-    d.pad_ = 0;
+    d.x_scale_val = 0.0f;
     return d;
 }
 
@@ -159,7 +159,7 @@ ProjDev to_dev(const trit_qproj &p) {
     d.K = int32_t(p.K);
     d.B = int32_t(beats_per_row(p.K));
     d.w_scale = p.w_scale;
-    d.pad_ = 0;
+    d.x_scale_val = 0.0f;
     return d;
 }
 
@@ -197,7 +197,7 @@ TRIT_API const char *trit_status_string(trit_status s) {
 
 TRIT_API const char *trit_last_cuda_error(void) { return g_last_cuda_error; }
 
-TRIT_API int32_t trit_abi_version(void) { return 2; }
+TRIT_API int32_t trit_abi_version(void) { return 3; }
 
 TRIT_API int64_t trit_payload_bytes(int64_t N, int64_t K) {
     if (!rows_ok(N) || !cols_ok(K)) return -1;
@@ -336,7 +336,7 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
             m.down.K = int32_t(p.K);
             m.down.B = int32_t(beats_per_row(p.K));
             m.down.w_scale = p.w_scale;
-            m.down.pad_ = 0;
+            m.down.x_scale_val = 0.0f;
             m.a_gate = p.a_gate;
             m.a_up = p.a_up;
             m.x_scale_in = p.x_scale;
@@ -368,9 +368,32 @@ TRIT_API trit_status trit_gemm(const uint8_t *planes, float w_scale, const int8_
 }
 
 TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_t *x_i8,
-                               const float *x_scale, int64_t N, int64_t K, int32_t *y_i32,
-                               float *y_f32, uint32_t *err_flag, trit_stream_t stream) {
-    return trit_gemm(planes, w_scale, x_i8, x_scale, 1, N, K, y_i32, y_f32, err_flag, stream);
+                               float x_scale, int64_t N, int64_t K, int32_t *y_i32, float *y_f32,
+                               uint32_t *err_flag, trit_stream_t stream) {
+    // validated as trit_gemm validates M = 1, with the scale checked here: the
+    // kernel takes it as a launch parameter instead of reading it from memory
+    trit_proj p;
+    p.planes = planes;
+    p.x_i8 = x_i8;
+    p.x_scale = reinterpret_cast<const float *>(planes);   // any non-NULL aligned stand-in
+    p.y_i32 = y_i32;
+    p.y_f32 = y_f32;
+    p.M = 1;
+    p.N = N;
+    p.K = K;
+    p.w_scale = w_scale;
+    p.reserved = 0;
+    if (!err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
+    trit_status st = check_proj(p);
+    if (st != TRIT_OK) return st;
+    if (!isfinite(x_scale) || x_scale < 0.0f) return TRIT_E_SCALE;
+    st = check_device();
+    if (st != TRIT_OK) return st;
+    ProjDev d = to_dev(p);
+    d.x_scale = nullptr;
+    d.x_scale_val = x_scale;
+    cudaError_t e = launch_gemv_many(&d, 1, err_flag, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
 
 TRIT_API trit_status trit_quant_act_folded(const float *x, const float *gain, int64_t M, int64_t K,
@@ -395,6 +418,20 @@ TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *s
     trit_status st = check_device();
     if (st != TRIT_OK) return st;
     cudaError_t e = launch_read_probe(buf, bytes, sink, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
+}
+
+TRIT_API trit_status trit_issue_probe(int32_t kind, int32_t blocks, int32_t threads, int64_t iters,
+                                      uint32_t *sink, uint64_t *rec, trit_stream_t stream) {
+    if (!sink || !rec || !aligned(sink, 4) || !aligned(rec, 8)) return TRIT_E_ARG;
+    if (kind < TRIT_PROBE_DP4A || kind > TRIT_PROBE_LDS128 || blocks < 1 || threads < 32 ||
+        threads > 512 || threads % 32 || iters < 1)
+        return TRIT_E_ARG;
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    cudaError_t e = launch_issue_probe(kind, blocks, threads, iters, sink,
+                                       reinterpret_cast<unsigned long long *>(rec),
+                                       reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TRIT_OK : cuda_fail(e);
 }
 

@@ -147,6 +147,8 @@ struct List {
     int32_t xs_words;       // shared words per staged activation row
     int64_t total_cost;
     uint32_t *err;
+    float x_scale_val;      // M = 1 entries whose x_scale is NULL take this input scale
+    int32_t pad_;
     MlpDesc mlp[kMaxMlp];
     Entry e[kMaxList];
 };
@@ -882,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
             xsc = stage_x_fp32(E, xs, g0 == 0, L.err, s_xsum);
         } else {
             stage_x<MT>(E, xs, L.xs_words, s_xsum);
-            xsc = E.x_scale[0];
+            xsc = E.x_scale ? E.x_scale[0] : L.x_scale_val;
         }
         __syncthreads();
         const int32_t xsum = MT == 1 ? read_xsum(s_xsum) : 0;
@@ -927,10 +929,12 @@ int occupancy(size_t smem) {
 
 template <int MT>
 cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
-                        const MlpDesc *mlp = nullptr, int nmlp = 0) {
+                        const MlpDesc *mlp = nullptr, int nmlp = 0, float x_scale_val = 0.0f) {
     static thread_local List L;   // host staging for the by-value parameter block
     L.count = n;
     L.err = err;
+    L.x_scale_val = x_scale_val;
+    L.pad_ = 0;
     for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = i < nmlp ? mlp[i] : MlpDesc{};
     int64_t cost = 0, groups = 0;
     int max_iters = 1;
@@ -971,12 +975,13 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
 // product's int32 sums (y_i32, or the y_f32 buffer itself read as int32).
 __global__ void __launch_bounds__(256) segment_epilogue_kernel(const int32_t *acc, float *y_f32,
                                                                int64_t M, int64_t N, float w_scale,
-                                                               const float *x_scale) {
+                                                               const float *x_scale,
+                                                               float x_scale_val) {
     const int64_t total = M * N;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t m = i / N;
-        y_f32[i] = dequant(acc[i], w_scale, x_scale[m]);
+        y_f32[i] = dequant(acc[i], w_scale, x_scale ? x_scale[m] : x_scale_val);
     }
 }
 
@@ -1008,22 +1013,31 @@ Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb
 }
 
 template <int MT>
-cudaError_t launch_entries(const Entry *all, int count, uint32_t *err, cudaStream_t s) {
+cudaError_t launch_entries(const Entry *all, int count, uint32_t *err, cudaStream_t s,
+                           float x_scale_val) {
     for (int base = 0; base < count; base += kMaxList) {
         const int n = count - base < kMaxList ? count - base : kMaxList;
-        cudaError_t e = launch_list<MT>(all + base, n, err, s);
+        cudaError_t e = launch_list<MT>(all + base, n, err, s, nullptr, 0, x_scale_val);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
 // Expand the products into list entries -- activation rows MT at a time, and
-// column segments for rows longer than seg_beats(MT) -- and launch them.
+// column segments for rows longer than seg_beats(MT) -- and launch them.  A
+// product whose x_scale is NULL (M = 1) takes x_scale_val as its input scale;
+// such a product is launched on its own (count == 1).
 template <int MT>
 cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {
     static thread_local Entry buf[kMaxList];
     int n = 0;
     cudaError_t e = cudaSuccess;
+    float xs_val = 0.0f;
+    for (int i = 0; i < count; ++i)
+        if (!list[i].x_scale && !list[i].xf) {
+            if (count != 1 || MT != 1 || list[i].M != 1) return cudaErrorInvalidValue;
+            xs_val = list[i].x_scale_val;
+        }
     // zero the accumulation targets of segmented products first
     for (int i = 0; i < count && e == cudaSuccess; ++i) {
         const ProjDev &p = list[i];
@@ -1044,13 +1058,13 @@ cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaS
                 if (MT > 1) buf[n].groups = (p.N + kRowsPerGroupM - 1) / kRowsPerGroupM;
                 ++n;
                 if (n == kMaxList) {
-                    e = launch_entries<MT>(buf, n, err, s);
+                    e = launch_entries<MT>(buf, n, err, s, xs_val);
                     n = 0;
                 }
             }
         }
     }
-    if (e == cudaSuccess && n) e = launch_entries<MT>(buf, n, err, s);
+    if (e == cudaSuccess && n) e = launch_entries<MT>(buf, n, err, s, xs_val);
     for (int i = 0; i < count && e == cudaSuccess; ++i) {
         const ProjDev &p = list[i];
         if (p.B > seg_beats(MT) && p.y_f32) {
@@ -1060,7 +1074,7 @@ cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaS
             const int64_t cap = int64_t(device_sm_count()) * 8;
             blocks = blocks < cap ? blocks : cap;
             segment_epilogue_kernel<<<int(blocks), 256, 0, s>>>(acc, p.y_f32, p.M, p.N, p.w_scale,
-                                                                p.x_scale);
+                                                                p.x_scale, p.x_scale_val);
             e = cudaGetLastError();
         }
     }

@@ -264,7 +264,7 @@ struct ProjDev {            // one product as a kernel sees it
     int64_t M, N;
     int32_t K, B;
     float w_scale;
-    int32_t pad_;
+    float x_scale_val;      // the input scale when x_scale is NULL (M = 1 integer path only)
 };
 
 // One IntMlp down projection (M = 1): its activation row is formed in the
@@ -319,6 +319,8 @@ cudaError_t fixed_scratch(uint8_t **out);
 cudaError_t launch_quant_folded(const float *x, const float *g, int64_t M, int64_t K, float eps,
                                 int8_t *q, float *x_scale, uint32_t *err, cudaStream_t s);
 cudaError_t launch_read_probe(const void *p, int64_t bytes, uint32_t *sink, cudaStream_t s);
+cudaError_t launch_issue_probe(int kind, int blocks, int threads, int64_t iters, uint32_t *sink,
+                               unsigned long long *rec, cudaStream_t s);
 cudaError_t launch_check_div127(uint64_t lo, uint64_t hi, unsigned long long *mismatches,
                                 cudaStream_t s);
 cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t N,

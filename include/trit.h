@@ -69,7 +69,8 @@ typedef enum trit_status {
     TRIT_OK = 0,
     TRIT_E_ARG = 1,         /* NULL where a pointer is required, count <= 0, misalignment */
     TRIT_E_SHAPE = 2,       /* a size outside the supported range */
-    TRIT_E_SCALE = 4,       /* w_scale not finite or <= 0 ("The .trit format, version 1" -- 2.2) */
+    TRIT_E_SCALE = 4,       /* w_scale not finite or <= 0 ("The .trit format, version 1" -- 2.2);
+                               trit_gemv's by-value x_scale not finite or < 0 */
     TRIT_E_CUDA = 6,        /* a CUDA runtime call or launch failed */
     TRIT_E_DEVICE = 7,      /* the current device is not an sm_103 GPU */
     TRIT_E_SCRATCH = 8,     /* trit_gemm_noalloc: the call needs more than
@@ -174,9 +175,22 @@ TRIT_API trit_status trit_gemm(const uint8_t *planes, float w_scale, const int8_
                                int32_t *y_i32, float *y_f32, uint32_t *err_flag,
                                trit_stream_t stream);
 
-/* trit_gemv -- trit_gemm with M = 1. */
+/*
+ * trit_gemv -- one activation row (M = 1) with its scale passed BY VALUE:
+ *     y_i32[r] = sum_{W[r][c] = +1} x_c - sum_{W[r][c] = -1} x_c,
+ *     y_f32[r] = (((float)y_i32[r] * w_scale) * x_scale) / 127
+ * ("Tritium ..." -- Introduction, Eq. 3; Why exactness, concretely).  The
+ * results are bit-identical to trit_gemm with M = 1 and a device scale holding
+ * the same value; use trit_gemm (M = 1) when the scale lives on the device, as
+ * it does straight after trit_quant_act, to avoid reading it back to the host.
+ *   x_i8      [K_pad] int8, device, 16-byte aligned
+ *   x_scale   host fp32: the row's absmax; must be finite and >= 0
+ *             (TRIT_E_SCALE otherwise; 0 is the scale of an all-zero row)
+ *   w_scale   finite, > 0 (TRIT_E_SCALE)
+ *   y_i32, y_f32, err_flag   as for trit_gemm
+ */
 TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_t *x_i8,
-                               const float *x_scale, int64_t N, int64_t K, int32_t *y_i32,
+                               float x_scale, int64_t N, int64_t K, int32_t *y_i32,
                                float *y_f32, uint32_t *err_flag, trit_stream_t stream);
 
 /* One product of a list: the arguments of trit_gemm, all device pointers. */
@@ -367,6 +381,34 @@ TRIT_API trit_status trit_quant_act_many(const trit_act *list, int32_t count,
  * for null or misaligned pointers or a bad size. */
 TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *sink,
                                      trit_stream_t stream);
+
+/* trit_issue_probe -- measurement aid: the per-SM completion rate of one
+ * instruction that the select-accumulate kernels are built from (their decode
+ * budget -- "Tritium ..." -- On popcount and The hardware core: the ternary
+ * product is integer adds and bit logic, so these rates, not multiplies, bound
+ * it).  Launches `blocks` CTAs of `threads` threads; every thread issues
+ * 32 * iters instructions of kind `kind` in eight independent chains.  Thread 0
+ * of CTA i writes rec[3i] = its SM id, rec[3i+1] / rec[3i+2] = clock64() at
+ * the start / end of the timed loop (after barriers).  Instructions per SM-clock
+ * = (threads * 32 * iters * CTAs on that SM) / (latest end - earliest start on
+ * that SM), all CTAs being resident at once (blocks <= SMs x CTAs per SM).
+ * The shared-memory kinds read 4-byte words / 16-byte vectors at
+ * conflict-free addresses (16 KB of static shared memory per CTA).
+ *   kind     one of TRIT_PROBE_*
+ *   blocks   >= 1;  threads: a multiple of 32 in [32, 512];  iters >= 1
+ *   sink     device u32 (its value is meaningless);  rec: device u64 [3*blocks]
+ * TRIT_E_ARG for a bad kind, size or pointer.  Asynchronous on `stream`. */
+#define TRIT_PROBE_DP4A 0      /* dp4a.s32.s32 */
+#define TRIT_PROBE_LOP3 1      /* lop3.b32 */
+#define TRIT_PROBE_PRMT 2      /* prmt.b32 */
+#define TRIT_PROBE_SHF 3       /* shf.l.wrap.b32 (funnel shift) */
+#define TRIT_PROBE_IMAD 4      /* mad.lo.u32 */
+#define TRIT_PROBE_IADD 5      /* add.u32 */
+#define TRIT_PROBE_SHFL 6      /* shfl.sync.bfly.b32 */
+#define TRIT_PROBE_LDS32 7     /* ld.shared.u32 (+ one xor) */
+#define TRIT_PROBE_LDS128 8    /* ld.shared.v4.u32 (+ xors) */
+TRIT_API trit_status trit_issue_probe(int32_t kind, int32_t blocks, int32_t threads, int64_t iters,
+                                      uint32_t *sink, uint64_t *rec, trit_stream_t stream);
 
 /* trit_check_div127 -- diagnostic: every fp32 dequantisation divides by 127
  * ("Tritium: One Weight Format for Ternary Inference ..." -- Numerics: y_f32 =

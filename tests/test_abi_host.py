@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(trit):
     lib = ctypes.CDLL(trit.library_path())
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert trit.lib().trit_abi_version() == 2
+    assert trit.lib().trit_abi_version() == 3
 
 
 def test_struct_layouts(trit):
@@ -169,10 +169,20 @@ def test_argument_errors_of_the_other_entry_points(trit):
     assert L.trit_unpack(p, 4, 64, null, p, s) == 1
     assert L.trit_unpack(odd, 4, 64, p, p, s) == 1
     assert L.trit_unpack(p, 0, 64, p, p, s) == 2
-    # trit_gemv(planes, w_scale, x, x_scale, N, K, y_i32, y_f32, err, stream)
-    assert L.trit_gemv(p, 1.0, p, p, 8, 64, null, null, p, s) == 1
-    assert L.trit_gemv(p, 1.0, p, p, 8, 0, p, p, p, s) == 2
-    assert L.trit_gemv(p, nan, p, p, 8, 64, p, p, p, s) == 4
+    # trit_gemv(planes, w_scale, x, x_scale BY VALUE, N, K, y_i32, y_f32, err, stream)
+    inf = float("inf")
+    assert L.trit_gemv(p, 1.0, p, 1.0, 8, 64, null, null, p, s) == 1
+    assert L.trit_gemv(p, 1.0, odd, 1.0, 8, 64, p, p, p, s) == 1
+    assert L.trit_gemv(p, 1.0, p, 1.0, 8, 64, p, p, null, s) == 1
+    assert L.trit_gemv(p, 1.0, p, 1.0, 8, 0, p, p, p, s) == 2
+    assert L.trit_gemv(p, 1.0, p, 1.0, 0, 64, p, p, p, s) == 2
+    assert L.trit_gemv(p, nan, p, 1.0, 8, 64, p, p, p, s) == 4
+    for bad_xs in (nan, inf, -1.0):
+        assert L.trit_gemv(p, 1.0, p, bad_xs, 8, 64, p, p, p, s) == 4
+    # valid arguments pass the host checks and stop at the device check
+    # (TRIT_E_CUDA or TRIT_E_DEVICE where no sm_103 GPU can be reached)
+    for good_xs in (0.0, 1.0, 3e38):
+        assert L.trit_gemv(p, 1.0, p, good_xs, 8, 64, p, p, p, s) in (6, 7)
     # trit_quant_act_many(list, count, err, stream)
     A = trit.TritAct
     assert L.trit_quant_act_many(null, 1, p, s) == 1

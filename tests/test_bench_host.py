@@ -72,3 +72,15 @@ def test_batch_floors(bench):
     assert m64["path"].startswith("tensor") and m64["bound"] in ("hbm", "mma")
     assert m64["mma_floor_ms"] == pytest.approx(tiles * 4 * 101.4 / (152 * f) * 1e3)
     assert m64["floor_ms"] == max(m64["hbm_floor_ms"], m64["mma_floor_ms"])
+
+
+def test_issue_rates_from_records(bench):
+    """Two SMs: SM 0 ran two CTAs over 1000 clocks in total, SM 5 one CTA over
+    400 clocks; 64 threads x 32 x 10 instructions per CTA."""
+    import numpy as np
+    rec = np.array([[0, 100, 900], [0, 200, 1100], [5, 50, 450]], dtype=np.int64)
+    r = bench.issue_rates(rec, threads=64, iters=10)
+    per_cta = 64 * 32 * 10
+    assert r["sms"] == 2
+    assert r["min"] == round(2 * per_cta / 1000, 2)
+    assert r["max"] == round(per_cta / 400, 2)

@@ -85,7 +85,7 @@ def test_bitcos_equals_plane_path(t, orc):
     (W, ws, xd, xsd, y, f), _, w, x, xs = product(t, orc, 2560, 6912, 0.42, 9)
     t.trit_bitcos_gemv_many(t.BitcosList([(W, ws, xd, xsd, y, f)]))
     planes, _ = t.trit_pack(torch.from_numpy(w).cuda(), ws)
-    y2, f2, err = t.trit_gemv(planes, ws, xd, xsd, 6912)
+    y2, f2, err = t.trit_gemv(planes, ws, xd, float(np.asarray(xs).reshape(-1)[0]), 6912)
     assert int(host(err)[0]) == 0
     np.testing.assert_array_equal(host(y), host(y2).reshape(-1))
     np.testing.assert_array_equal(host(f).view(np.uint32), host(f2).reshape(-1).view(np.uint32))

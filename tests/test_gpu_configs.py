@@ -80,7 +80,7 @@ def test_config0_single_gemv(t, orc):
     ws = float(synth.w_scale(w))
     planes, err = t.trit_pack(torch.from_numpy(w).cuda(), ws)
     q, s, err = t.trit_quant_act(torch.from_numpy(x).cuda(), err_flag=err)
-    y, f, err = t.trit_gemv(planes, ws, q, s, 2560, err_flag=err)
+    y, f, err = t.trit_gemv(planes, ws, q, float(s.item()), 2560, err_flag=err)
     assert int(host(err)[0]) == 0
     check_projection(orc, w, x, q, s, y[None, :], f[None, :], ws, 2560)
 

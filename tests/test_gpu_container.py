@@ -58,7 +58,7 @@ def test_file_upload_then_gemv_matches_oracle(t, orc, tmp_path):
     # products over the uploaded planes
     x = synth.activations(rng, 1, K)
     q, s, _ = orc.quant(x)
-    y, fy, err = t.trit_gemv(planes, ws, torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), K)
+    y, fy, err = t.trit_gemv(planes, ws, torch.from_numpy(q).cuda(), float(s.reshape(-1)[0]), K)
     ry, rf = orc.gemm(planes_host, ws, q, s, K)[:2]
     torch.cuda.synchronize()
     assert int(err.item()) == 0

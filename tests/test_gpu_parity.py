@@ -212,10 +212,32 @@ def test_gemv_entry_point(t, orc):
     x = padded_x(rng, 1, K)
     xs = np.array([1.5], np.float32)
     planes, _ = t.trit_pack(dev(w), 2.0)
-    y, f, err = t.trit_gemv(planes, 2.0, dev(x), dev(xs), K)
+    y, f, err = t.trit_gemv(planes, 2.0, dev(x), float(xs[0]), K)
     ry, rf, _ = orc.gemm(orc.pack(w), 2.0, x, xs, K)
     np.testing.assert_array_equal(host(y), ry[0])
     assert_f32_close(host(f), rf[0])
+
+
+@pytest.mark.parametrize("N,K,xs", [(515, 2560, 1.5), (77, 6912, 0.0), (9, 73793, 3.25),
+                                    (33, 100, 1e-30)])
+def test_gemv_scale_by_value(t, orc, N, K, xs):
+    """trit_gemv takes the activation scale by value: the same bits as the
+    oracle and as trit_gemm (M = 1) with the scale in device memory -- also for
+    rows longer than one column segment (K > 73,728), whose fp32 outputs come
+    from the separate dequantisation pass, and for a zero scale."""
+    rng = synth.rng_for(107, K)
+    w = synth.ternary(rng, N, K, 0.42)
+    x = padded_x(rng, 1, K)
+    xsa = np.array([xs], np.float32)
+    planes, _ = t.trit_pack(dev(w), 0.75)
+    y, f, err = t.trit_gemv(planes, 0.75, dev(x), xs, K)
+    y2, f2, err2 = t.trit_gemm(planes, 0.75, dev(x), dev(xsa), K)
+    ry, rf, _ = orc.gemm(orc.pack(w), 0.75, x, xsa, K)
+    assert int(host(err)[0]) == 0 and int(host(err2)[0]) == 0
+    np.testing.assert_array_equal(host(y), ry[0])
+    np.testing.assert_array_equal(host(f).view(np.uint32), rf[0].view(np.uint32))
+    np.testing.assert_array_equal(host(y2).reshape(-1), host(y))
+    np.testing.assert_array_equal(host(f2).reshape(-1).view(np.uint32), host(f).view(np.uint32))
 
 
 @pytest.mark.parametrize("K", [64, 6912, 6913])
@@ -564,3 +586,26 @@ def test_skinny_list_of_mixed_m(t, orc):
         np.testing.assert_array_equal(host(y)[:, rows], ry)
         assert_f32_close(host(f)[:, rows], rf)
 
+
+
+def test_issue_probe_rates_are_plausible(t):
+    """The issue-rate probe runs for every kind and reports a rate between one
+    lane per SM-clock and the SM's 128 lanes (4 schedulers x 32 lanes) -- a
+    record that is filled in and self-consistent, not a claim about the
+    numbers themselves."""
+    import importlib.util
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_for_probe", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    for kind in bench.ISSUE_KINDS:
+        rec = t.trit_issue_probe(kind, sms * 2, 256, 64, dev)
+        torch.cuda.synchronize()
+        r = rec.cpu().numpy()
+        assert (r[:, 2] > r[:, 1]).all(), kind
+        assert set(int(v) for v in r[:, 0]) <= set(range(sms)), kind
+        rates = bench.issue_rates(r, 256, 64)
+        assert 1.0 <= rates["lanes_per_clk"] <= 132.0, (kind, rates)

@@ -1,12 +1,18 @@
 """trit_gemm_noalloc, the entry point that allocates nothing, against
-trit_gemm on the same inputs: two calls in a row on one stream (the second
-reusing the fixed scratch the first one wrote) must each give trit_gemm's
-bits.  Also: a product whose activation copy does not fit the fixed buffer is
-refused before anything is enqueued, and a both-bits-set beat is flagged the
-same way.  The file sorts last so that it also runs after everything else."""
+trit_gemm and against the CPU oracle on the same inputs: two calls in a row on
+one stream (the second reusing the fixed scratch the first one wrote) must
+each give trit_gemm's bits, and the oracle's on sampled rows.  The device's
+memory pool must not grow during the calls (trit_gemm on the same product
+does grow it: the control).  Also: a product whose activation copy does not
+fit the fixed buffer is refused before anything is enqueued, and a
+both-bits-set beat is flagged the same way.  The file sorts last so that it
+also runs after everything else."""
+import ctypes
+
 import numpy as np
 import pytest
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -47,7 +53,25 @@ def make_product(t, M, N, K, seed):
     x[:, :K] = rng.integers(-128, 128, size=(M, K)).astype(np.int8)
     xs = rng.uniform(0.05, 8.0, size=M).astype(np.float32)
     return dict(planes=planes, ws=ws, x=torch.from_numpy(x).cuda(),
-                xs=torch.from_numpy(xs).cuda(), M=M, N=N, K=K)
+                xs=torch.from_numpy(xs).cuda(), M=M, N=N, K=K, w=w, xh=x, xsh=xs)
+
+
+def oracle_rows(N, seed):
+    """About 24 output rows to compare with the oracle: the first, the last and
+    a seeded sample between them."""
+    rng = np.random.default_rng(seed)
+    rows = set(int(r) for r in rng.choice(N, size=min(N, 22), replace=False))
+    return np.array(sorted(rows | {0, N - 1}), dtype=np.int64)
+
+
+def matches_oracle(P, got, seed):
+    torch.cuda.synchronize()
+    rows = oracle_rows(P["N"], seed)
+    ry, rf, rerr = oracle.gemm(oracle.pack(P["w"]), P["ws"], P["xh"], P["xsh"], P["K"], rows=rows)
+    assert not rerr.any()
+    y32, yf = got[0].cpu().numpy(), got[1].cpu().numpy()
+    np.testing.assert_array_equal(y32[:, rows], ry)
+    np.testing.assert_array_equal(yf[:, rows].view(np.uint32), rf.view(np.uint32))
 
 
 def outputs(P):
@@ -100,6 +124,54 @@ def test_two_calls_in_a_row_match_trit_gemm(t, first, second):
     same(ra, ea)
     same(rb, eb)
     assert int(ra[2].item()) == 0 and int(rb[2].item()) == 0
+    matches_oracle(A, ra, 11)
+    matches_oracle(B, rb, 12)
+
+
+# ---- the device's default memory pool (driver API, read through libcuda) ----
+# cudaMallocAsync, the allocator trit_gemm's tensor-core paths use, draws from
+# the device's current memory pool -- the default one unless someone replaced
+# it; torch's caching allocator does not use it.  The pool's high-water mark of
+# memory in use is reset to 0 before the calls and read after them.
+CU_MEMPOOL_ATTR_USED_MEM_HIGH = 8
+
+
+def _driver():
+    try:
+        return ctypes.CDLL("libcuda.so.1")
+    except OSError:
+        pytest.skip("libcuda.so.1 not found")
+
+
+def pool_used_high(reset=False):
+    cu = _driver()
+    dev = ctypes.c_int(0)
+    assert cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()) == 0
+    pool = ctypes.c_void_p(0)
+    assert cu.cuDeviceGetDefaultMemPool(ctypes.byref(pool), dev) == 0
+    v = ctypes.c_uint64(0)
+    if reset:
+        assert cu.cuMemPoolSetAttribute(pool, CU_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(v)) == 0
+    assert cu.cuMemPoolGetAttribute(pool, CU_MEMPOOL_ATTR_USED_MEM_HIGH, ctypes.byref(v)) == 0
+    return int(v.value)
+
+
+@pytest.mark.parametrize("first,second", [PAIRS[0], PAIRS[1], PAIRS[5]])
+def test_no_pool_growth(t, first, second):
+    """Two tensor-core products through trit_gemm_noalloc leave the pool's
+    high-water mark at zero; the same two through trit_gemm raise it."""
+    A = make_product(t, *first, seed=7)
+    B = make_product(t, *second, seed=8)
+    torch.cuda.synchronize()
+    assert pool_used_high(reset=True) == 0
+    via_noalloc(t, A)
+    via_noalloc(t, B)
+    torch.cuda.synchronize()
+    assert pool_used_high() == 0, "trit_gemm_noalloc drew memory from the device pool"
+    via_gemm(t, A)
+    via_gemm(t, B)
+    torch.cuda.synchronize()
+    assert pool_used_high() > 0, "control: trit_gemm's tensor-core path allocates on the stream"
 
 
 def test_limit_counts_row_blocks_in_pairs(t):
