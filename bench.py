@@ -687,10 +687,11 @@ MMA_CYCLES_M128 = 101.4   # tcgen05.mma cta_group::1 kind::f16, M = 128, N <= 12
 
 # ---- issue rates (trit_issue_probe) -------------------------------------------
 
-ISSUE_KINDS = ("dp4a", "lop3", "prmt", "shf", "imad", "iadd", "shfl", "lds32", "lds128")
+ISSUE_KINDS = ("dp4a", "dp4a.su", "lop3", "prmt", "shf", "imad", "iadd", "shfl", "lds32",
+               "lds128", "dp4a+lop3")
 
 
-def issue_rates(rec, threads: int, iters: int) -> dict:
+def issue_rates(rec, threads: int, iters: int, per_iter: int = 32) -> dict:
     """Per-SM completion rates from a trit_issue_probe record ([CTAs, 3] of SM
     id, start clock, end clock): for every SM, the instructions its CTAs issued
     (32 * iters per thread) over the span from the earliest start to the latest
@@ -702,7 +703,7 @@ def issue_rates(rec, threads: int, iters: int) -> dict:
         lo = int(t0) if lo is None else min(lo, int(t0))
         hi = int(t1) if hi is None else max(hi, int(t1))
         per_sm[int(smid)] = (n + 1, lo, hi)
-    rates = sorted(n * threads * 32 * iters / max(hi - lo, 1) for n, lo, hi in per_sm.values())
+    rates = sorted(n * threads * per_iter * iters / max(hi - lo, 1) for n, lo, hi in per_sm.values())
     return {"lanes_per_clk": round(statistics.median(rates), 2), "min": round(rates[0], 2),
             "max": round(rates[-1], 2), "sms": len(rates)}
 
@@ -719,7 +720,7 @@ def measure_issue_rates(dev, iters: int = 2048, threads: int = 256, ctas_per_sm:
         t.trit_issue_probe(kind, sms * ctas_per_sm, threads, 16, dev)      # warm the kernel
         rec = t.trit_issue_probe(kind, sms * ctas_per_sm, threads, iters, dev)
         torch.cuda.synchronize(dev)
-        r = issue_rates(rec.cpu().numpy(), threads, iters)
+        r = issue_rates(rec.cpu().numpy(), threads, iters, 64 if kind == "dp4a+lop3" else 32)
         if kind == "lds32":
             r["bytes_per_clk"] = round(4 * r["lanes_per_clk"], 1)
         if kind == "lds128":

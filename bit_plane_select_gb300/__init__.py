@@ -328,7 +328,8 @@ def trit_read_probe(buf: torch.Tensor, sink: torch.Tensor | None = None, stream=
 
 # instruction kinds of trit_issue_probe (TRIT_PROBE_* in include/trit.h)
 PROBE_KINDS = {"dp4a": 0, "lop3": 1, "prmt": 2, "shf": 3, "imad": 4, "iadd": 5, "shfl": 6,
-               "lds32": 7, "lds128": 8}
+               "lds32": 7, "lds128": 8, "dp4a+lop3": 9,
+               "dp4a.su": 10}
 
 
 def trit_issue_probe(kind: str, blocks: int, threads: int, iters: int, device=None,

@@ -424,7 +424,7 @@ TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *s
 TRIT_API trit_status trit_issue_probe(int32_t kind, int32_t blocks, int32_t threads, int64_t iters,
                                       uint32_t *sink, uint64_t *rec, trit_stream_t stream) {
     if (!sink || !rec || !aligned(sink, 4) || !aligned(rec, 8)) return TRIT_E_ARG;
-    if (kind < TRIT_PROBE_DP4A || kind > TRIT_PROBE_LDS128 || blocks < 1 || threads < 32 ||
+    if (kind < TRIT_PROBE_DP4A || kind > TRIT_PROBE_DP4A_SU || blocks < 1 || threads < 32 ||
         threads > 512 || threads % 32 || iters < 1)
         return TRIT_E_ARG;
     trit_status st = check_device();

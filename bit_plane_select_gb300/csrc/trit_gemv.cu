@@ -59,7 +59,14 @@
 // M > 1 (code bytes).  Each beat is expanded once into sixteen words of code
 // bytes c in {0, 1, 2} (the M = 1 code words, then a shift and a mask per word:
 // 38 logic instructions per beat) and reused for every activation row held by
-// the CTA: 16 dp4a per row, then the row's column sum is subtracted.
+// the CTA: 16 dp4a per row, then the row's column sum is subtracted.  A lane
+// holds four weight rows (32-row groups), so every activation word it reads
+// from shared memory serves four rows; the CTA stages its MT activation rows
+// beat-interleaved (all rows of a beat side by side) so every read is an
+// immediate offset from one pointer.  At a group's end the four lanes of a row
+// set reduce-scatter their partial sums, so each lane finishes one row.  The
+// bound is the dp4a rate: 64 lanes per SM-clock on this device, i.e. two
+// SM-clocks per row-beat at M = 8 (the probe in trit_probe.cu measures it).
 #include "trit_internal.cuh"
 
 namespace trit {
@@ -96,6 +103,25 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 #ifndef TRIT_WAVES
 #define TRIT_WAVES 1
 #endif
+#ifndef TRIT_MIN_BLOCKS_M1
+#define TRIT_MIN_BLOCKS_M1 3
+#endif
+// M > 1 path: steps of loads in flight per row of a lane, per staged row count.
+#ifndef TRIT_RING_M2
+#define TRIT_RING_M2 2
+#endif
+#ifndef TRIT_RING_M4
+#define TRIT_RING_M4 2
+#endif
+#ifndef TRIT_RING_M8
+#define TRIT_RING_M8 1
+#endif
+__host__ __device__ constexpr int ring_rows(int mt) {
+    return mt == 8 ? TRIT_RING_M8 : mt == 4 ? TRIT_RING_M4 : TRIT_RING_M2;
+}
+// CTAs per SM the kernel is compiled for (its register budget: 128 per thread
+// for MT > 1)
+__host__ __device__ constexpr int min_blocks(int mt) { return mt == 1 ? TRIT_MIN_BLOCKS_M1 : 2; }
 // Cost units charged ahead of each entry's groups for staging its activations
 // (M = 1 launches; a group step costs 100; 0 disables): a CTA whose share starts
 // an entry gets that much less group work.  Measured on the 30-layer stack (3,000 ... 70,000
@@ -144,7 +170,7 @@ constexpr int kMaxMlp = 8;
 
 struct List {
     int32_t count;
-    int32_t xs_words;       // shared words per staged activation row
+    int32_t xs_words;       // shared words of the staged activations
     int64_t total_cost;
     uint32_t *err;
     float x_scale_val;      // M = 1 entries whose x_scale is NULL take this input scale
@@ -200,17 +226,27 @@ __device__ __forceinline__ int32_t read_xsum_row(const int32_t *s_xsum, int m) {
     return s;
 }
 
-// Code bytes of one 32-column plane word pair: c[j] has byte i = c of column
-// 8i + j (c = 1 + pos - neg in {0, 1, 2}), matching staged activation word j.
-__device__ __forceinline__ void code_bytes(uint32_t P, uint32_t N, uint32_t (&c)[8]) {
+// Two-bit code words of one 32-column plane word pair (P, N): ze holds the
+// codes c = 1 + pos - neg in {0, 1, 2} of the even columns k at bits (k, k+1),
+// zo those of the odd columns at bits (k-1, k), so (ze >> 2j) & 0x03030303 has
+// byte i = c of column 8i + 2j and (zo >> 2j) & 0x03030303 that of column
+// 8i + 2j + 1 -- the columns of staged activation words 2j and 2j + 1.
+__device__ __forceinline__ void code_words(uint32_t P, uint32_t N, uint32_t &ze, uint32_t &zo) {
     const uint32_t nor = ~(P | N);
-    const uint32_t ze = (nor & 0x55555555u) | ((P << 1) & 0xAAAAAAAAu);
-    const uint32_t zo = ((nor >> 1) & 0x55555555u) | (P & 0xAAAAAAAAu);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        c[2 * j] = (ze >> (2 * j)) & 0x03030303u;
-        c[2 * j + 1] = (zo >> (2 * j)) & 0x03030303u;
-    }
+    ze = (nor & 0x55555555u) | ((P << 1) & 0xAAAAAAAAu);
+    zo = ((nor >> 1) & 0x55555555u) | (P & 0xAAAAAAAAu);
+}
+
+// Shared-memory words of one staged beat.  M = 1: the row's beats at a stride
+// of kXBeatWords.  MT > 1: the MT rows' words of a beat side by side (16 words
+// each: the two permuted 32-column halves), beats at a stride of MT * 16 + 4
+// words -- 4 words mod 32 banks, so the four beats a warp reads at once fall on
+// distinct banks -- and every row's words of a beat at a fixed offset from the
+// beat's start, so the product loop addresses them with immediate offsets.
+__host__ __device__ constexpr int beat_words(int mt) { return mt == 1 ? kXBeatWords : mt * 16 + 4; }
+template <int MT>
+__device__ __forceinline__ int xs_word(int m, int beat) {
+    return MT == 1 ? beat * kXBeatWords : beat * beat_words(MT) + m * 16;
 }
 
 // Stage activation rows 0..MT-1 of entry E into shared memory, permuted, zero
@@ -218,8 +254,7 @@ __device__ __forceinline__ void code_bytes(uint32_t P, uint32_t N, uint32_t (&c)
 // staged by warps m*kWarps/MT .. (m+1)*kWarps/MT - 1, each of which publishes
 // its part of the row's column sum in s_xsum[warp].
 template <int MT>
-__device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_words,
-                                        int32_t *s_xsum) {
+__device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int32_t *s_xsum) {
     static_assert(kWarps % MT == 0, "whole warps per staged row");
     constexpr int kWpr = kWarps / MT;
     const int halves = E.iters * kLanesPerRow * 2;
@@ -257,7 +292,7 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int xs_wor
 #pragma unroll
             for (int j = 0; j < 8; ++j) out[j] = 0;
         }
-        uint32_t *dst = xs + m * xs_words + (hb >> 1) * kXBeatWords + (hb & 1) * 8;
+        uint32_t *dst = xs + xs_word<MT>(m, hb >> 1) + (hb & 1) * 8;
         reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
         reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
     }
@@ -489,11 +524,11 @@ __device__ __forceinline__ int32_t row_sum4(int32_t v) {
     return v;
 }
 
-// Process groups [gb, ge) of entry E with one warp.  Returns the OR of pos & neg.
-template <int MT>
-__device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *xs, int xs_words,
-                                               float xsc, int32_t xsum, int64_t gb, int64_t ge,
-                                               int rs, int bs) {
+// M = 1, any row length: process groups [gb, ge) of entry E with one warp.
+// Returns the OR of pos & neg.
+__device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *xs, float xsc,
+                                               int32_t xsum, int64_t gb, int64_t ge, int rs,
+                                               int bs) {
     const int it = E.iters;
     const int steps = int(ge - gb) * it;
     const int64_t N = E.N;
@@ -524,9 +559,9 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
     for (int d = 0; d < kDepth; ++d) ring[d] = next_load();
 
     // ---- compute cursor
-    int acc[MT == 1 ? 8 : MT];
+    int acc[8];
 #pragma unroll
-    for (int i = 0; i < (MT == 1 ? 8 : MT); ++i) acc[i] = 0;
+    for (int i = 0; i < 8; ++i) acc[i] = 0;
     int64_t row = gb * kRowsPerGroup + rs;
     int ct = 0;
     const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
@@ -537,68 +572,24 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
         const uint4 v = slot;
         slot = next_load();
         viol |= (v.x & v.z) | (v.y & v.w);
-        if constexpr (MT == 1) {
-            const uint4 a0 = xs4[xoff], a1 = xs4[xoff + 1], a2 = xs4[xoff + 2], a3 = xs4[xoff + 3];
-            const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
-            mac_codes(v.x, v.z, xl, acc);
-            mac_codes(v.y, v.w, xh, acc);
-        } else {
-            // bytes of w: +1 where pos, -1 (0xFF) where neg, 0 elsewhere
-            uint32_t wl[8], wh[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t nl = prmt(v.z << (7 - j), 0u, 0xBA98u);
-                const uint32_t nh = prmt(v.w << (7 - j), 0u, 0xBA98u);
-                wl[j] = ((v.x >> j) & 0x01010101u) | nl;
-                wh[j] = ((v.y >> j) & 0x01010101u) | nh;
-            }
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const uint4 *X = xs4 + m * (xs_words / 4) + xoff;
-                const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
-                int a = acc[m];
-                a = dp4a_ss(a0.x, wl[0], a); a = dp4a_ss(a0.y, wl[1], a);
-                a = dp4a_ss(a0.z, wl[2], a); a = dp4a_ss(a0.w, wl[3], a);
-                a = dp4a_ss(a1.x, wl[4], a); a = dp4a_ss(a1.y, wl[5], a);
-                a = dp4a_ss(a1.z, wl[6], a); a = dp4a_ss(a1.w, wl[7], a);
-                a = dp4a_ss(a2.x, wh[0], a); a = dp4a_ss(a2.y, wh[1], a);
-                a = dp4a_ss(a2.z, wh[2], a); a = dp4a_ss(a2.w, wh[3], a);
-                a = dp4a_ss(a3.x, wh[4], a); a = dp4a_ss(a3.y, wh[5], a);
-                a = dp4a_ss(a3.z, wh[6], a); a = dp4a_ss(a3.w, wh[7], a);
-                acc[m] = a;
-            }
-        }
+        const uint4 a0 = xs4[xoff], a1 = xs4[xoff + 1], a2 = xs4[xoff + 2], a3 = xs4[xoff + 3];
+        const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+        mac_codes(v.x, v.z, xl, acc);
+        mac_codes(v.y, v.w, xh, acc);
         xoff += kLanesPerRow * kXBeatVec;
         if (++ct == it) {
-            if constexpr (MT == 1) {
-                const int32_t y = row_sum4(codes_total(acc)) - xsum;
-                if (bs == 0 && row < N) {
-                    if (E.acc) {
-                        atomicAdd(E.acc + row, y);
-                    } else {
-                        if (E.y_i32) E.y_i32[row] = y;
-                        if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, xsc);
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = 0;
-            } else {
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const int32_t y = row_sum4(acc[m]);
-                    acc[m] = 0;
-                    if (bs == 0 && row < N && m < rows_of(E)) {
-                        const int64_t o = int64_t(m) * N + row;
-                        if (E.acc) {
-                            atomicAdd(E.acc + o, y);
-                        } else {
-                            if (E.y_i32) E.y_i32[o] = y;
-                            if (E.y_f32) E.y_f32[o] = dequant(y, E.w_scale, E.x_scale[m]);
-                        }
-                    }
+            const int32_t y = row_sum4(codes_total(acc)) - xsum;
+            if (bs == 0 && row < N) {
+                if (E.acc) {
+                    atomicAdd(E.acc + row, y);
+                } else {
+                    if (E.y_i32) E.y_i32[row] = y;
+                    if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, xsc);
                 }
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0;
             ct = 0;
             xoff = xbase;
             row += kRowsPerGroup;
@@ -616,115 +607,171 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
     return viol;
 }
 
-// M > 1: groups of 16 rows.  Lane (rs, bs) takes rows 16g + rs and 16g + 8 + rs
-// at beats bs, bs + 4, ...: each beat is expanded once into code bytes, and
-// every activation word read from shared memory (the dominant
-// shared-memory traffic at M > 1) serves both rows.
-constexpr int kRowsPerGroupM = 16;
+// M > 1: groups of 8 * kRowsPerLane rows.  Lane (rs, bs) takes the rows
+// 32g + rs + 8i (i < kRowsPerLane) at beats bs, bs + 4, ...: each beat is
+// expanded once into code bytes, one 32-column half at a time, and every
+// activation word read from shared memory serves all of the lane's rows.
+// Shared-memory reads of the activations were the bound with fewer rows per
+// lane (each dp4a of a lane consumed 4 / rows-per-lane bytes of them, against
+// 128 bytes per clock per SM).
+constexpr int kRowsPerLane = 4;
+constexpr int kRowsPerGroupM = 8 * kRowsPerLane;
 
+// Reduce-scatter of a lane's kRowsPerLane x MT partial sums over the four lanes
+// of its rows (lanes 4 rs + bs, bs = 0..3): after two butterfly steps lane bs
+// holds the complete sums of its row i = 2 (bs & 1) + (bs >> 1) for every m
+// (so the four lanes finish and store four different rows).
 template <int MT>
-__device__ __forceinline__ uint32_t run_groups2(const Entry &E, const uint32_t *xs, int xs_words,
-                                                const int32_t *s_xsum, int64_t gb, int64_t ge,
-                                                int rs, int bs) {
-    constexpr int D = 2;   // loads in flight per row and lane
+__device__ __forceinline__ void reduce_rows(const int (&acc)[kRowsPerLane][MT], int bs,
+                                            int (&out)[MT]) {
+    constexpr int H = 2 * MT;   // values per half: rows {0, 1} or {2, 3}
+    const bool b0 = bs & 1, b1 = (bs >> 1) & 1;
+    int t[H];
+#pragma unroll
+    for (int v = 0; v < H; ++v) {
+        const int lo = acc[v / MT][v % MT], hi = acc[2 + v / MT][v % MT];
+        const int send = b0 ? lo : hi;
+        t[v] = (b0 ? hi : lo) + __shfl_xor_sync(~0u, send, 1);
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const int send = b1 ? t[m] : t[MT + m];
+        out[m] = (b1 ? t[MT + m] : t[m]) + __shfl_xor_sync(~0u, send, 2);
+    }
+}
+
+// One beat of every row of a lane (M > 1): the two-bit code words of both
+// 32-column halves of the lane's kRowsPerLane rows (v), multiplied by the MT
+// staged activation rows of the beat at xp, added into acc.  The caller may
+// refill v's registers once this returns.
+template <int MT>
+__device__ __forceinline__ void mac_beat_rows(const uint4 (&v)[kRowsPerLane], const uint4 *xp,
+                                              int (&acc)[kRowsPerLane][MT], uint32_t &viol) {
+    constexpr int R = kRowsPerLane;
+    uint32_t zw[2][R][2];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        viol |= (v[i].x & v[i].z) | (v[i].y & v[i].w);
+        code_words(v[i].x, v[i].z, zw[0][i][0], zw[0][i][1]);
+        code_words(v[i].y, v[i].w, zw[1][i][0], zw[1][i][1]);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            // activation words 4q..4q+3 of half h (columns 8i + j, j = 4q..4q+3)
+            // and the code bytes c = 1 + pos - neg of the same columns
+            uint32_t c[R][4];
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                c[i][0] = (zw[h][i][0] >> (4 * q)) & 0x03030303u;
+                c[i][1] = (zw[h][i][1] >> (4 * q)) & 0x03030303u;
+                c[i][2] = (zw[h][i][0] >> (4 * q + 2)) & 0x03030303u;
+                c[i][3] = (zw[h][i][1] >> (4 * q + 2)) & 0x03030303u;
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const uint4 a = xp[4 * m + 2 * h + q];
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    int t = acc[i][m];
+                    t = dp4a_su(a.x, c[i][0], t);
+                    t = dp4a_su(a.y, c[i][1], t);
+                    t = dp4a_su(a.z, c[i][2], t);
+                    t = dp4a_su(a.w, c[i][3], t);
+                    acc[i][m] = t;
+                }
+            }
+        }
+    }
+}
+
+// Output m of row r of entry E from its complete integer sum v (column sum of
+// the activation row already taken off).
+__device__ __forceinline__ void store_out(const Entry &E, int m, int64_t r, int32_t v) {
+    const int64_t o = int64_t(m) * E.N + r;
+    if (E.acc) {
+        atomicAdd(E.acc + o, v);
+    } else {
+        if (E.y_i32) E.y_i32[o] = v;
+        if (E.y_f32) E.y_f32[o] = dequant(v, E.w_scale, E.x_scale[m]);
+    }
+}
+
+// The M > 1 product loop over whole groups [gb, ge) of entry E: loads clamped
+// to the planes (rows past N read row N - 1, beats past the row's end its last
+// beat), D steps of loads in flight per row.
+template <int MT, int D>
+__device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32_t *xs,
+                                                    const int32_t *s_xsum, int64_t gb,
+                                                    int64_t ge, int rs, int bs) {
+    constexpr int R = kRowsPerLane;
+    constexpr int BV = beat_words(MT) / 4;   // uint4 per staged beat
     const int it = E.iters;
     const int steps = int(ge - gb) * it;
     const int64_t N = E.N;
     uint32_t viol = 0;
 
-    // ---- load cursor (rows past the warp's last valid row and beats past the
-    // row's last beat are clamped to valid addresses)
+    // ---- load cursor
     const int last_beat = E.B - 1;
     const int64_t last_row = (ge * kRowsPerGroupM < N ? ge * kRowsPerGroupM : N) - 1;
     int64_t lrow = gb * kRowsPerGroupM + rs;
     auto row_at = [&](int64_t r) { return E.planes + (r < last_row ? r : last_row) * E.bstride; };
-    const uint4 *la = row_at(lrow), *lb = row_at(lrow + 8);
+    const uint4 *lp[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) lp[i] = row_at(lrow + 8 * i);
     int lt = 0, loff = bs;
-    auto next_load = [&](uint4 &va, uint4 &vb) {
+    auto next_load = [&](uint4 (&v)[R]) {
         const int o = loff < last_beat ? loff : last_beat;
-        va = ldg_stream(la + o);
-        vb = ldg_stream(lb + o);
+#pragma unroll
+        for (int i = 0; i < R; ++i) v[i] = ldg_stream(lp[i] + o);
         loff += kLanesPerRow;
         if (++lt == it) {
             lt = 0;
             loff = bs;
             lrow += kRowsPerGroupM;
-            la = row_at(lrow);
-            lb = row_at(lrow + 8);
+#pragma unroll
+            for (int i = 0; i < R; ++i) lp[i] = row_at(lrow + 8 * i);
         }
     };
-    uint4 ra[D], rb[D];
+    uint4 ring[D][R];
 #pragma unroll
-    for (int d = 0; d < D; ++d) next_load(ra[d], rb[d]);
+    for (int d = 0; d < D; ++d) next_load(ring[d]);
 
-    int accA[MT], accB[MT];
+    int acc[R][MT];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) accA[m] = accB[m] = 0;
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[i][m] = 0;
     int64_t row = gb * kRowsPerGroupM + rs;
     int ct = 0;
-    const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
-    const int xbase = bs * kXBeatVec;
-    int xoff = xbase;
-
-    // code bytes c = 1 + pos - neg of the beat's columns
-    auto expand = [](const uint4 &v, uint32_t (&wl)[8], uint32_t (&wh)[8]) {
-        code_bytes(v.x, v.z, wl);
-        code_bytes(v.y, v.w, wh);
-    };
-    auto dot16 = [](const uint4 &a0, const uint4 &a1, const uint4 &a2, const uint4 &a3,
-                    const uint32_t (&wl)[8], const uint32_t (&wh)[8], int a) {
-        a = dp4a_su(a0.x, wl[0], a); a = dp4a_su(a0.y, wl[1], a);
-        a = dp4a_su(a0.z, wl[2], a); a = dp4a_su(a0.w, wl[3], a);
-        a = dp4a_su(a1.x, wl[4], a); a = dp4a_su(a1.y, wl[5], a);
-        a = dp4a_su(a1.z, wl[6], a); a = dp4a_su(a1.w, wl[7], a);
-        a = dp4a_su(a2.x, wh[0], a); a = dp4a_su(a2.y, wh[1], a);
-        a = dp4a_su(a2.z, wh[2], a); a = dp4a_su(a2.w, wh[3], a);
-        a = dp4a_su(a3.x, wh[4], a); a = dp4a_su(a3.y, wh[5], a);
-        a = dp4a_su(a3.z, wh[6], a); a = dp4a_su(a3.w, wh[7], a);
-        return a;
-    };
+    // this lane's staged beats: bs, bs + 4, ...; row m of a beat at 4m uint4
+    const uint4 *xbase = reinterpret_cast<const uint4 *>(xs) + bs * BV;
+    const uint4 *xp = xbase;
 
     auto body = [&](int slot) {
-        const uint4 va = ra[slot], vb = rb[slot];
-        next_load(ra[slot], rb[slot]);
-        viol |= (va.x & va.z) | (va.y & va.w) | (vb.x & vb.z) | (vb.y & vb.w);
-        uint32_t wlA[8], whA[8], wlB[8], whB[8];
-        expand(va, wlA, whA);
-        expand(vb, wlB, whB);
+        uint4 v[R];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const uint4 *X = xs4 + m * (xs_words / 4) + xoff;
-            const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
-            accA[m] = dot16(a0, a1, a2, a3, wlA, whA, accA[m]);
-            accB[m] = dot16(a0, a1, a2, a3, wlB, whB, accB[m]);
-        }
-        xoff += kLanesPerRow * kXBeatVec;
+        for (int i = 0; i < R; ++i) v[i] = ring[slot][i];
+        mac_beat_rows<MT>(v, xp, acc, viol);
+        next_load(ring[slot]);
+        xp += kLanesPerRow * BV;
         if (++ct == it) {
+            // the row sums: each of the four lanes of a row group finishes one row
+            int y[MT];
+            reduce_rows<MT>(acc, bs, y);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const int32_t xsum = read_xsum_row<MT>(s_xsum, m);
-                const int32_t ya = row_sum4(accA[m]) - xsum;
-                const int32_t yb = row_sum4(accB[m]) - xsum;
-                accA[m] = accB[m] = 0;
-                if (bs == 0 && m < rows_of(E)) {
+            for (int i = 0; i < R; ++i)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int64_t r = row + 8 * h;
-                        const int32_t y = h ? yb : ya;
-                        if (r < N) {
-                            const int64_t o = int64_t(m) * N + r;
-                            if (E.acc) {
-                                atomicAdd(E.acc + o, y);
-                            } else {
-                                if (E.y_i32) E.y_i32[o] = y;
-                                if (E.y_f32) E.y_f32[o] = dequant(y, E.w_scale, E.x_scale[m]);
-                            }
-                        }
-                    }
-                }
+                for (int m = 0; m < MT; ++m) acc[i][m] = 0;
+            const int64_t r = row + 8 * (2 * (bs & 1) + (bs >> 1));
+            if (r < N) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    if (m < rows_of(E)) store_out(E, m, r, y[m] - read_xsum_row<MT>(s_xsum, m));
             }
             ct = 0;
-            xoff = xbase;
+            xp = xbase;
             row += kRowsPerGroupM;
         }
     };
@@ -817,11 +864,8 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
     return viol;
 }
 
-#ifndef TRIT_MIN_BLOCKS
-#define TRIT_MIN_BLOCKS 3
-#endif
 template <int MT>
-__global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
+__global__ void __launch_bounds__(kThreads, min_blocks(MT))
     select_accumulate_kernel(const __grid_constant__ List L) {
     extern __shared__ __align__(16) uint32_t xs[];
     __shared__ int32_t s_xsum[kWarps];
@@ -883,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
         } else if (MT == 1 && E.xf) {
             xsc = stage_x_fp32(E, xs, g0 == 0, L.err, s_xsum);
         } else {
-            stage_x<MT>(E, xs, L.xs_words, s_xsum);
+            stage_x<MT>(E, xs, s_xsum);
             xsc = E.x_scale ? E.x_scale[0] : L.x_scale_val;
         }
         __syncthreads();
@@ -891,19 +935,15 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? TRIT_MIN_BLOCKS : 2)
         if (MT == 1 && mlp_of(E)) xsc = s_mlp_scale;
         if (wb < we) {
             if constexpr (MT == 1) {
-                if (path == 1) {
+                if (path == 1)
                     viol |= fixed_run<10, TRIT_RING_40>(E, xs, xsc, xsum, wb, we, rs, bs);
-                    continue;
-                }
-                if (path == 2) {
+                else if (path == 2)
                     viol |= fixed_run<27, TRIT_RING_108>(E, xs, xsc, xsum, wb, we, rs, bs);
-                    continue;
-                }
+                else
+                    viol |= run_groups(E, xs, xsc, xsum, wb, we, rs, bs);
+            } else {
+                viol |= run_groups_rows<MT, ring_rows(MT)>(E, xs, s_xsum, wb, we, rs, bs);
             }
-            if constexpr (MT == 1)
-                viol |= run_groups<MT>(E, xs, L.xs_words, xsc, xsum, wb, we, rs, bs);
-            else
-                viol |= run_groups2<MT>(E, xs, L.xs_words, s_xsum, wb, we, rs, bs);
         }
     }
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
@@ -947,8 +987,8 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
         if (entries[i].iters > max_iters) max_iters = entries[i].iters;
     }
     L.total_cost = cost;
-    L.xs_words = max_iters * kLanesPerRow * kXBeatWords;
-    const size_t smem = size_t(L.xs_words) * 4 * MT;
+    L.xs_words = max_iters * kLanesPerRow * beat_words(MT);
+    const size_t smem = size_t(L.xs_words) * 4;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_accumulate_kernel<MT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1111,14 +1151,38 @@ cudaError_t launch_intmlp_gemv_many(const MlpProjDev *list, int count, uint32_t 
     return cudaSuccess;
 }
 
-// Activation rows are taken 8 at a time (4 or 2 when every product of the list
-// has fewer); each chunk re-reads the planes.
+// Activation rows are taken 8 at a time; a product's remaining r < 8 rows go
+// to the kernel staging 2 (r <= 2), 4 (r <= 4) or 8 rows, so no chunk stages
+// more empty rows than it must.  Every chunk re-reads the planes.
 cudaError_t launch_gemm_dp4a_many(const ProjDev *list, int count, uint32_t *err, cudaStream_t s) {
-    int64_t maxM = 1;
-    for (int i = 0; i < count; ++i) maxM = list[i].M > maxM ? list[i].M : maxM;
-    if (maxM >= 8) return launch_products<8>(list, count, err, s);
-    if (maxM >= 4) return launch_products<4>(list, count, err, s);
-    return launch_products<2>(list, count, err, s);
+    static thread_local ProjDev by8[TRIT_MAX_LIST_PER_LAUNCH], by4[TRIT_MAX_LIST_PER_LAUNCH],
+        by2[TRIT_MAX_LIST_PER_LAUNCH];
+    int n8 = 0, n4 = 0, n2 = 0;
+    for (int i = 0; i < count; ++i) {
+        const ProjDev &p = list[i];
+        const int64_t full = p.M / 8 * 8, r = p.M - full;
+        if (full) {
+            by8[n8] = p;
+            by8[n8++].M = full;
+        }
+        if (r) {
+            ProjDev q = p;
+            const int64_t Kp = int64_t(p.B) * 64;
+            q.x = p.x ? p.x + full * Kp : nullptr;
+            q.x_scale = p.x_scale ? p.x_scale + full : nullptr;
+            q.y_i32 = p.y_i32 ? p.y_i32 + full * p.N : nullptr;
+            q.y_f32 = p.y_f32 ? p.y_f32 + full * p.N : nullptr;
+            q.M = r;
+            if (r <= 2) by2[n2++] = q;
+            else if (r <= 4) by4[n4++] = q;
+            else by8[n8++] = q;
+        }
+    }
+    cudaError_t e = cudaSuccess;
+    if (n8) e = launch_products<8>(by8, n8, err, s);
+    if (e == cudaSuccess && n4) e = launch_products<4>(by4, n4, err, s);
+    if (e == cudaSuccess && n2) e = launch_products<2>(by2, n2, err, s);
+    return e;
 }
 
 }  // namespace trit

@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(256) read_probe_kernel(const uint4 *p, int64_t
 // read conflict-free addresses (lane-contiguous words / 16-byte vectors) and
 // fold what they read into the chains, so no load is dead.
 template <int KIND, int U>
-__device__ __forceinline__ void probe_op(uint32_t (&a)[8], uint32_t b, uint32_t c, uint32_t smb) {
+__device__ __forceinline__ void probe_op(uint32_t (&a)[8], uint32_t b, uint32_t c, uint32_t smb,
+                                         uint32_t zmask) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         if constexpr (KIND == TRIT_PROBE_DP4A) {
@@ -52,20 +53,26 @@ __device__ __forceinline__ void probe_op(uint32_t (&a)[8], uint32_t b, uint32_t 
             asm volatile("add.u32 %0, %0, %1;" : "+r"(a[k]) : "r"(b));
         } else if constexpr (KIND == TRIT_PROBE_SHFL) {
             asm volatile("shfl.sync.bfly.b32 %0, %0, 1, 0x1f, 0xffffffff;" : "+r"(a[k]));
+        } else if constexpr (KIND == TRIT_PROBE_DP4A_SU) {
+            asm volatile("dp4a.s32.u32 %0, %1, %2, %0;" : "+r"(a[k]) : "r"(b), "r"(c));
+        } else if constexpr (KIND == TRIT_PROBE_DP4A_LOP3) {
+            asm volatile("dp4a.s32.s32 %0, %1, %2, %0;" : "+r"(a[k]) : "r"(b), "r"(c));
+            asm volatile("lop3.b32 %0, %0, %1, %2, 0x96;" : "+r"(a[k]) : "r"(b), "r"(c));
         } else {
-            // each load's address carries an opaque zero from its chain, so a
-            // thread has at most eight loads in flight (bounded registers)
-            uint32_t z;
-            asm volatile("and.b32 %0, %1, 0;" : "=r"(z) : "r"(a[k]));
+            // each load's address carries a zero the compiler cannot see (the
+            // chain value and-ed with a mask that is 0 at run time), so no load
+            // can be hoisted out of the loop and a thread has at most eight in
+            // flight
+            const uint32_t z = a[k] & zmask;
             if constexpr (KIND == TRIT_PROBE_LDS32) {
                 // smb = shared base + 4 * lane: word (lane, block 8U + k) of 32 x 32 words
                 uint32_t v;
-                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smb + z + 128u * (8 * U + k)));
+                asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(smb + z + 128u * (8 * U + k)));
                 a[k] ^= v;
             } else {   // TRIT_PROBE_LDS128: smb = shared base + 16 * lane, blocks of 512 bytes
                 asm volatile(
                     "{\n\t.reg .b32 t0, t1, t2, t3;\n\t"
-                    "ld.shared.v4.u32 {t0, t1, t2, t3}, [%1];\n\t"
+                    "ld.volatile.shared.v4.u32 {t0, t1, t2, t3}, [%1];\n\t"
                     "xor.b32 t0, t0, t1;\n\txor.b32 t2, t2, t3;\n\t"
                     "xor.b32 t0, t0, t2;\n\txor.b32 %0, %0, t0;\n\t}"
                     : "+r"(a[k])
@@ -76,7 +83,7 @@ __device__ __forceinline__ void probe_op(uint32_t (&a)[8], uint32_t b, uint32_t 
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(512) issue_probe_kernel(int64_t iters, uint32_t seed,
+__global__ void __launch_bounds__(512) issue_probe_kernel(int64_t iters, uint32_t seed, uint32_t zmask,
                                                            uint32_t *sink, unsigned long long *rec) {
     __shared__ __align__(16) uint32_t sm[4 * 32 * 32];   // 16 KB: 32 blocks of 32 lanes x 16 bytes
     for (int i = threadIdx.x; i < 4 * 32 * 32; i += blockDim.x) sm[i] = seed ^ (uint32_t(i) * 0x9E3779B9u);
@@ -90,10 +97,10 @@ __global__ void __launch_bounds__(512) issue_probe_kernel(int64_t iters, uint32_
     __syncthreads();
     const unsigned long long t0 = clock64();
     for (int64_t it = 0; it < iters; ++it) {
-        probe_op<KIND, 0>(a, b, c, smb);
-        probe_op<KIND, 1>(a, b, c, smb);
-        probe_op<KIND, 2>(a, b, c, smb);
-        probe_op<KIND, 3>(a, b, c, smb);
+        probe_op<KIND, 0>(a, b, c, smb, zmask);
+        probe_op<KIND, 1>(a, b, c, smb, zmask);
+        probe_op<KIND, 2>(a, b, c, smb, zmask);
+        probe_op<KIND, 3>(a, b, c, smb, zmask);
     }
     __syncthreads();
     const unsigned long long t1 = clock64();
@@ -117,7 +124,7 @@ cudaError_t launch_issue_probe(int kind, int blocks, int threads, int64_t iters,
     const uint32_t seed = 0x2545F491u;
     switch (kind) {
 #define TRIT_PROBE_CASE(K) \
-    case K: issue_probe_kernel<K><<<blocks, threads, 0, s>>>(iters, seed, sink, rec); break;
+    case K: issue_probe_kernel<K><<<blocks, threads, 0, s>>>(iters, seed, 0u, sink, rec); break;
         TRIT_PROBE_CASE(TRIT_PROBE_DP4A)
         TRIT_PROBE_CASE(TRIT_PROBE_LOP3)
         TRIT_PROBE_CASE(TRIT_PROBE_PRMT)
@@ -127,6 +134,8 @@ cudaError_t launch_issue_probe(int kind, int blocks, int threads, int64_t iters,
         TRIT_PROBE_CASE(TRIT_PROBE_SHFL)
         TRIT_PROBE_CASE(TRIT_PROBE_LDS32)
         TRIT_PROBE_CASE(TRIT_PROBE_LDS128)
+        TRIT_PROBE_CASE(TRIT_PROBE_DP4A_LOP3)
+        TRIT_PROBE_CASE(TRIT_PROBE_DP4A_SU)
 #undef TRIT_PROBE_CASE
         default: return cudaErrorInvalidValue;
     }

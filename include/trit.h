@@ -387,7 +387,8 @@ TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *s
  * budget -- "Tritium ..." -- On popcount and The hardware core: the ternary
  * product is integer adds and bit logic, so these rates, not multiplies, bound
  * it).  Launches `blocks` CTAs of `threads` threads; every thread issues
- * 32 * iters instructions of kind `kind` in eight independent chains.  Thread 0
+ * 32 * iters instructions of kind `kind` in eight independent chains (64 * iters
+ * for TRIT_PROBE_DP4A_LOP3, whose chains alternate the two).  Thread 0
  * of CTA i writes rec[3i] = its SM id, rec[3i+1] / rec[3i+2] = clock64() at
  * the start / end of the timed loop (after barriers).  Instructions per SM-clock
  * = (threads * 32 * iters * CTAs on that SM) / (latest end - earliest start on
@@ -407,6 +408,8 @@ TRIT_API trit_status trit_read_probe(const void *buf, int64_t bytes, uint32_t *s
 #define TRIT_PROBE_SHFL 6      /* shfl.sync.bfly.b32 */
 #define TRIT_PROBE_LDS32 7     /* ld.shared.u32 (+ one xor) */
 #define TRIT_PROBE_LDS128 8    /* ld.shared.v4.u32 (+ xors) */
+#define TRIT_PROBE_DP4A_LOP3 9 /* dp4a then lop3 on each chain: both count */
+#define TRIT_PROBE_DP4A_SU 10  /* dp4a.s32.u32 (signed by unsigned bytes) */
 TRIT_API trit_status trit_issue_probe(int32_t kind, int32_t blocks, int32_t threads, int64_t iters,
                                       uint32_t *sink, uint64_t *rec, trit_stream_t stream);
 

@@ -173,6 +173,11 @@ GEMM_CASES = [
     (1, 1, 1), (1, 3, 63), (1, 4, 64), (1, 5, 65), (1, 33, 200), (1, 257, 2560), (1, 1000, 6912),
     (1, 127, 1000), (2, 37, 130), (3, 64, 2560), (4, 33, 6912), (5, 100, 65), (7, 17, 640),
     (8, 260, 2560), (9, 45, 300), (12, 77, 1000), (13, 70, 2560), (16, 70, 2560), (17, 31, 191), (33, 9, 6912),
+    # M > 1 with many 32-row groups per CTA (warp shares cut groups at step
+    # boundaries), the 8 + 2 and 8 + 4 row chunkings, ragged N, and rows long
+    # enough to be cut into column segments at 8 and at 2 rows
+    (2, 6912, 2560), (3, 2560, 6912), (6, 2048, 2560), (10, 1000, 6912), (11, 2049, 2560),
+    (12, 640, 2560), (9, 50, 20000), (4, 96, 18500),
 ]
 
 
@@ -607,5 +612,5 @@ def test_issue_probe_rates_are_plausible(t):
         r = rec.cpu().numpy()
         assert (r[:, 2] > r[:, 1]).all(), kind
         assert set(int(v) for v in r[:, 0]) <= set(range(sms)), kind
-        rates = bench.issue_rates(r, 256, 64)
+        rates = bench.issue_rates(r, 256, 64, 64 if kind == "dp4a+lop3" else 32)
         assert 1.0 <= rates["lanes_per_clk"] <= 132.0, (kind, rates)
