@@ -57,21 +57,35 @@ def test_traffic_only_while_the_source_is_unchanged(bench, monkeypatch):
 
 
 def test_batch_floors(bench):
+    """The floors of the path each M takes: the HBM bytes at the copy peak; for
+    the dp4a path the largest of the dp4a, logic, shared-memory and issue
+    bounds at the given rates (rows in chunks of 8, the remainder staged as 2,
+    4 or 8 rows); for the small-M tensor path the MMA bound; no compute floor
+    without a sampled clock."""
     shapes = [(2560, 2560), (6912, 2560), (2560, 6912)]
     row_beats = 2560 * 40 + 6912 * 40 + 2560 * 108
     tiles = 20 * 40 + 54 * 40 + 20 * 108
-    f = 2070e6
-    one = bench.batch_floors(1, shapes, 10**9, 6785.2, 152, 2070.0)
+    f = 2070e6 * 152
+    rates = {"dp4a": {"lanes_per_clk": 64.0}, "lop3": {"lanes_per_clk": 64.0},
+             "lds128": {"bytes_per_clk": 128.0}}
+    one = bench.batch_floors(1, shapes, 10**9, 6785.2, 152, 2070.0, rates)
     assert one["bound"] == "hbm" and one["hbm_floor_ms"] == pytest.approx(1e9 / 6785.2e9 * 1e3)
-    m8 = bench.batch_floors(8, shapes, 10**9, 6785.2, 152, 2070.0)
-    assert m8["path"] == "dp4a"
-    assert m8["alu_floor_ms"] == pytest.approx(row_beats * (38 + 128) / (128 * 152 * f) * 1e3)
-    m12 = bench.batch_floors(12, shapes, 10**9, 6785.2, 152, 2070.0)
-    assert m12["alu_floor_ms"] == pytest.approx(row_beats * (76 + 192) / (128 * 152 * f) * 1e3)
-    m64 = bench.batch_floors(64, shapes, 10**9, 6785.2, 152, 2070.0)
+    m8 = bench.batch_floors(8, shapes, 10**9, 6785.2, 152, 2070.0, rates)
+    assert m8["path"] == "dp4a" and m8["chunks"] == [8]
+    assert m8["alu_floors_ms"]["dp4a"] == pytest.approx(row_beats * 128 / 64 / f * 1e3, rel=1e-3)
+    assert m8["alu_floors_ms"]["logic"] == pytest.approx(row_beats * 38 / 64 / f * 1e3, rel=1e-3)
+    assert m8["alu_floor_ms"] == m8["alu_floors_ms"]["dp4a"]
+    m12 = bench.batch_floors(12, shapes, 10**9, 6785.2, 152, 2070.0, rates)
+    assert m12["chunks"] == [8, 4]
+    assert m12["alu_floors_ms"]["dp4a"] == pytest.approx(row_beats * 192 / 64 / f * 1e3, rel=1e-3)
+    m3 = bench.batch_floors(3, shapes, 10**9, 6785.2, 152, 2070.0, rates)
+    assert m3["chunks"] == [4]
+    m64 = bench.batch_floors(64, shapes, 10**9, 6785.2, 152, 2070.0, rates)
     assert m64["path"].startswith("tensor") and m64["bound"] in ("hbm", "mma")
-    assert m64["mma_floor_ms"] == pytest.approx(tiles * 4 * 101.4 / (152 * f) * 1e3)
+    assert m64["mma_floor_ms"] == pytest.approx(tiles * 4 * 101.4 / f * 1e3)
     assert m64["floor_ms"] == max(m64["hbm_floor_ms"], m64["mma_floor_ms"])
+    unsampled = bench.batch_floors(8, shapes, 10**9, 6785.2, 152, None, rates)
+    assert "alu_floor_ms" not in unsampled and unsampled["floor_ms"] == unsampled["hbm_floor_ms"]
 
 
 def test_issue_rates_from_records(bench):
