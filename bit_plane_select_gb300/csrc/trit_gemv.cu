@@ -56,10 +56,12 @@
 // reads activations or writes outputs -- the prefetch of the next token's
 // planes overlaps the tail of the current one.
 //
-// M > 1 (code bytes).  Each beat is expanded once into sixteen words of code
-// bytes c in {0, 1, 2} (the M = 1 code words, then a shift and a mask per word:
-// 38 logic instructions per beat) and reused for every activation row held by
-// the CTA: 16 dp4a per row, then the row's column sum is subtracted.  A lane
+// M > 1 (masked code words).  Each beat's code words are formed once (the M = 1
+// code words) and masked into sixteen words of bytes 4^k c, c in {0, 1, 2},
+// reused for every activation row held by the CTA: 16 dp4a per row into one of
+// NJ accumulators per weight class k (NJ = 4: 16 AND per beat, no shift; NJ = 1:
+// code bytes of weight 1, 28 logic instructions per beat), folded exactly at
+// the row's end, then the row's column sum is subtracted.  A lane
 // holds four weight rows (32-row groups), so every activation word it reads
 // from shared memory serves four rows; the CTA stages its MT activation rows
 // beat-interleaved (all rows of a beat side by side) so every read is an
@@ -119,6 +121,24 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 __host__ __device__ constexpr int ring_rows(int mt) {
     return mt == 8 ? TRIT_RING_M8 : mt == 4 ? TRIT_RING_M4 : TRIT_RING_M2;
 }
+// M > 1 path: accumulators per (weight row, activation row) -- the number of
+// weight classes 4^j the code words are masked into (4: every mask is an AND of
+// the code word, no shift; 2: one shift per code word; 1: code bytes of weight
+// 1, three shifts per code word) -- per staged row count.  Measured on the
+// 30-layer stack: M = 2 129.9 us with 1 class, 123.6 with 2, 121.5 with 4; M = 4
+// unchanged by 2 classes (4 spill); M = 8 spills with 2 (351 against 322 us).
+#ifndef TRIT_NJ_M2
+#define TRIT_NJ_M2 4
+#endif
+#ifndef TRIT_NJ_M4
+#define TRIT_NJ_M4 2
+#endif
+#ifndef TRIT_NJ_M8
+#define TRIT_NJ_M8 1
+#endif
+__host__ __device__ constexpr int acc_classes(int mt) {
+    return mt == 8 ? TRIT_NJ_M8 : mt == 4 ? TRIT_NJ_M4 : TRIT_NJ_M2;
+}
 // CTAs per SM the kernel is compiled for (its register budget: 128 per thread
 // for MT > 1)
 __host__ __device__ constexpr int min_blocks(int mt) { return mt == 1 ? TRIT_MIN_BLOCKS_M1 : 2; }
@@ -130,6 +150,19 @@ __host__ __device__ constexpr int min_blocks(int mt) { return mt == 1 ? TRIT_MIN
 #define TRIT_STAGE_COST 30000
 #endif
 constexpr int64_t kStageCost = TRIT_STAGE_COST;
+// The same charge for launches staging MT > 1 rows (a group step there is a
+// 32-row group's step; 0 disables).  Measured on the 30-layer stack: 8,000
+// takes M = 8 from 322.9 to 312.7 us and M = 4 from 191.0 to 188.1 us, and costs
+// M = 2 three microseconds, so two-row launches take none.
+#ifndef TRIT_STAGE_COST_M2
+#define TRIT_STAGE_COST_M2 0
+#endif
+#ifndef TRIT_STAGE_COST_MT
+#define TRIT_STAGE_COST_MT 8000
+#endif
+__host__ __device__ constexpr int64_t stage_cost(int mt) {
+    return mt == 1 ? kStageCost : mt == 2 ? int64_t(TRIT_STAGE_COST_M2) : int64_t(TRIT_STAGE_COST_MT);
+}
 constexpr int kL2Ahead = TRIT_L2_AHEAD;
 
 // Beats per column segment for MT staged rows: MT * seg_beats * 80 bytes of
@@ -642,11 +675,16 @@ __device__ __forceinline__ void reduce_rows(const int (&acc)[kRowsPerLane][MT], 
 
 // One beat of every row of a lane (M > 1): the two-bit code words of both
 // 32-column halves of the lane's kRowsPerLane rows (v), multiplied by the MT
-// staged activation rows of the beat at xp, added into acc.  The caller may
-// refill v's registers once this returns.
-template <int MT>
+// staged activation rows of the beat at xp, added into acc.  With NJ weight
+// classes the byte codes reach dp4a as (code word >> s) & (0x03030303 << 2k),
+// byte value 4^k c, into accumulator k of NJ: NJ = 4 needs no shift (s = 0, k = j),
+// NJ = 2 one shift by 4 for the upper two j (k = j & 1), NJ = 1 the shift by
+// 2j (k = 0).  Accumulator k holds a multiple of 4^k; fold_classes divides it
+// out exactly.  The caller may refill v's registers once this returns.
+template <int MT, int NJ>
 __device__ __forceinline__ void mac_beat_rows(const uint4 (&v)[kRowsPerLane], const uint4 *xp,
-                                              int (&acc)[kRowsPerLane][MT], uint32_t &viol) {
+                                              int (&acc)[kRowsPerLane][MT][NJ], uint32_t &viol) {
+    static_assert(NJ == 1 || NJ == 2 || NJ == 4, "weight classes");
     constexpr int R = kRowsPerLane;
     uint32_t zw[2][R][2];
 #pragma unroll
@@ -659,31 +697,65 @@ __device__ __forceinline__ void mac_beat_rows(const uint4 (&v)[kRowsPerLane], co
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            // activation words 4q..4q+3 of half h (columns 8i + j, j = 4q..4q+3)
-            // and the code bytes c = 1 + pos - neg of the same columns
+            // activation words 4q..4q+3 of half h hold columns 8i + 4q + {0,1,2,3};
+            // their codes are j = 2q (words 4q, 4q+1: even, odd code word) and
+            // j = 2q + 1 (words 4q+2, 4q+3)
+            constexpr uint32_t M0 = 0x03030303u;
             uint32_t c[R][4];
+            int k0 = 0, k1 = 0;   // accumulator of the j = 2q / j = 2q + 1 codes
 #pragma unroll
             for (int i = 0; i < R; ++i) {
-                c[i][0] = (zw[h][i][0] >> (4 * q)) & 0x03030303u;
-                c[i][1] = (zw[h][i][1] >> (4 * q)) & 0x03030303u;
-                c[i][2] = (zw[h][i][0] >> (4 * q + 2)) & 0x03030303u;
-                c[i][3] = (zw[h][i][1] >> (4 * q + 2)) & 0x03030303u;
+                const uint32_t ze = zw[h][i][0], zo = zw[h][i][1];
+                if (NJ == 4) {
+                    c[i][0] = ze & (M0 << (4 * q));
+                    c[i][1] = zo & (M0 << (4 * q));
+                    c[i][2] = ze & (M0 << (4 * q + 2));
+                    c[i][3] = zo & (M0 << (4 * q + 2));
+                    k0 = 2 * q;
+                    k1 = 2 * q + 1;
+                } else if (NJ == 2) {
+                    const uint32_t se = ze >> (4 * q), so = zo >> (4 * q);
+                    c[i][0] = se & M0;
+                    c[i][1] = so & M0;
+                    c[i][2] = se & (M0 << 2);
+                    c[i][3] = so & (M0 << 2);
+                    k0 = 0;
+                    k1 = 1;
+                } else {
+                    c[i][0] = (ze >> (4 * q)) & M0;
+                    c[i][1] = (zo >> (4 * q)) & M0;
+                    c[i][2] = (ze >> (4 * q + 2)) & M0;
+                    c[i][3] = (zo >> (4 * q + 2)) & M0;
+                    k0 = 0;
+                    k1 = 0;
+                }
             }
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 const uint4 a = xp[4 * m + 2 * h + q];
 #pragma unroll
                 for (int i = 0; i < R; ++i) {
-                    int t = acc[i][m];
-                    t = dp4a_su(a.x, c[i][0], t);
-                    t = dp4a_su(a.y, c[i][1], t);
-                    t = dp4a_su(a.z, c[i][2], t);
-                    t = dp4a_su(a.w, c[i][3], t);
-                    acc[i][m] = t;
+                    int t0 = acc[i][m][k0];
+                    t0 = dp4a_su(a.x, c[i][0], t0);
+                    t0 = dp4a_su(a.y, c[i][1], t0);
+                    acc[i][m][k0] = t0;
+                    int t1 = acc[i][m][k1];
+                    t1 = dp4a_su(a.z, c[i][2], t1);
+                    t1 = dp4a_su(a.w, c[i][3], t1);
+                    acc[i][m][k1] = t1;
                 }
             }
         }
     }
+}
+
+// sum_k acc[k] / 4^k, exact (accumulator k is a multiple of 4^k).
+template <int NJ>
+__device__ __forceinline__ int fold_classes(const int (&a)[NJ]) {
+    int t = a[0];
+#pragma unroll
+    for (int k = 1; k < NJ; ++k) t += a[k] >> (2 * k);
+    return t;
 }
 
 // Output m of row r of entry E from its complete integer sum v (column sum of
@@ -701,7 +773,7 @@ __device__ __forceinline__ void store_out(const Entry &E, int m, int64_t r, int3
 // The M > 1 product loop over whole groups [gb, ge) of entry E: loads clamped
 // to the planes (rows past N read row N - 1, beats past the row's end its last
 // beat), D steps of loads in flight per row.
-template <int MT, int D>
+template <int MT, int D, int NJ>
 __device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32_t *xs,
                                                     const int32_t *s_xsum, int64_t gb,
                                                     int64_t ge, int rs, int bs) {
@@ -738,11 +810,13 @@ __device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32
 #pragma unroll
     for (int d = 0; d < D; ++d) next_load(ring[d]);
 
-    int acc[R][MT];
+    int acc[R][MT][NJ];
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[i][m] = 0;
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int k = 0; k < NJ; ++k) acc[i][m][k] = 0;
     int64_t row = gb * kRowsPerGroupM + rs;
     int ct = 0;
     // this lane's staged beats: bs, bs + 4, ...; row m of a beat at 4m uint4
@@ -753,17 +827,22 @@ __device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32
         uint4 v[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) v[i] = ring[slot][i];
-        mac_beat_rows<MT>(v, xp, acc, viol);
+        mac_beat_rows<MT, NJ>(v, xp, acc, viol);
         next_load(ring[slot]);
         xp += kLanesPerRow * BV;
         if (++ct == it) {
             // the row sums: each of the four lanes of a row group finishes one row
-            int y[MT];
-            reduce_rows<MT>(acc, bs, y);
+            int tot[R][MT];
 #pragma unroll
             for (int i = 0; i < R; ++i)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[i][m] = 0;
+                for (int m = 0; m < MT; ++m) {
+                    tot[i][m] = fold_classes<NJ>(acc[i][m]);
+#pragma unroll
+                    for (int k = 0; k < NJ; ++k) acc[i][m][k] = 0;
+                }
+            int y[MT];
+            reduce_rows<MT>(tot, bs, y);
             const int64_t r = row + 8 * (2 * (bs & 1) + (bs >> 1));
             if (r < N) {
 #pragma unroll
@@ -942,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
                 else
                     viol |= run_groups(E, xs, xsc, xsum, wb, we, rs, bs);
             } else {
-                viol |= run_groups_rows<MT, ring_rows(MT)>(E, xs, s_xsum, wb, we, rs, bs);
+                viol |= run_groups_rows<MT, ring_rows(MT), acc_classes(MT)>(E, xs, s_xsum, wb, we, rs, bs);
             }
         }
     }
@@ -980,7 +1059,7 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
     int max_iters = 1;
     for (int i = 0; i < n; ++i) {
         L.e[i] = entries[i];
-        if (MT == 1) cost += kStageCost;   // staging the entry's row, charged to whoever starts it
+        cost += stage_cost(MT);   // staging the entry's rows, charged to whoever starts it
         L.e[i].cost_begin = cost;
         cost += entries[i].groups * entries[i].gcost;
         groups += entries[i].groups;
