@@ -1219,6 +1219,60 @@ def run_mlp(args):
     print(json.dumps(out), flush=True)
 
 
+def run_decode_ordered(args):
+    """The dependency-ordered decode of one token over the 30-layer stack: per
+    layer qkv -> o -> gate/up -> IntMlp + down, each launch reading what the one
+    before it wrote (the per-matvec ordering of "Tritium ..." -- Why it does not
+    scale), timed as a CUDA graph of one token replayed (120 launches per token
+    with programmatic serialisation)."""
+    import torch
+
+    import __graft_entry__
+    import synth
+    from bit_plane_select_gb300.stack import LayerChain
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    names = [p[0] for p in synth.PROJECTIONS]
+    weights = []
+    for layer in range(args.layers):
+        lw = {}
+        for i, n in enumerate(names):
+            w = synth.stack_weights(SEED, layer, i)
+            lw[n] = (torch.from_numpy(w), float(synth.w_scale(w)))
+        weights.append(lw)
+    chain = LayerChain(weights, dev)
+    for layer in range(args.layers):
+        chain.x[layer].copy_(torch.from_numpy(synth.projection_acts(SEED, layer, 0, 1)[0]))
+    del weights
+    for _ in range(3):
+        chain.step()
+    torch.cuda.synchronize()
+    # the 120 launches of one token captured in a CUDA graph and replayed
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain.step()
+    steps = max(50, min(args.steps, 2000))
+    with ClockSampler(0) as clk:
+        ms = _timed(g.replay, steps, args.warmup, stream)
+    eager = _timed(chain.step, max(20, steps // 10), args.warmup, stream)
+    nbytes = chain.step_bytes()
+    peak, peak_kind = peaks()
+    out = {"metric": "dependency-ordered batch-1 decode over the 30-layer stack", "unit": "tok/s",
+           "value": round(1e3 / ms, 1), "us_per_token": round(ms * 1e3, 2),
+           "GBs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm_peak": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "peak": peak,
+           "peak_kind": peak_kind, "launches_per_token": chain.launches_per_step,
+           "us_per_launch": round(ms * 1e3 / chain.launches_per_step, 3),
+           "algorithmic_bytes_per_token": nbytes, "eager_us_per_token": round(eager * 1e3, 2),
+           "timing": f"CUDA graph of one token replayed {steps} times", "err_flag": int(chain.err.item()),
+           "clocks": clk.summary(),
+           "config": {"workload": "bitnet-2b4t-30layer-decode-ordered-batch1", "layers": args.layers,
+                      "order": "per layer: [q,k,v] <- x; [o] <- q; [gate,up] <- o; IntMlp+[down] <- gate,up"}}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1233,7 +1287,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip configs 0, 1, 3 and 4 in the default run")
     ap.add_argument("--reference-budget", type=float, default=90.0)
-    ap.add_argument("--workload", choices=["decode", "prefill", "batch", "mlp", "bitcos", "issue"],
+    ap.add_argument("--workload", choices=["decode", "prefill", "batch", "mlp", "bitcos", "issue",
+                                           "decode-ordered"],
                     default="decode",
                     help="decode (default): the 30-layer batch-1 stack; prefill, batch, mlp and "
                          "bitcos print extra lines for the other configurations")
@@ -1252,6 +1307,8 @@ def main():
         run_bitcos(args)
     elif args.workload == "issue":
         run_issue(args)
+    elif args.workload == "decode-ordered":
+        run_decode_ordered(args)
     else:
         run_ours(args)
 

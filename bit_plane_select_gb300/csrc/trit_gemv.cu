@@ -491,7 +491,6 @@ __device__ __forceinline__ void stage_x_intmlp(const Entry &E, const MlpDesc &D,
             lo = s_max[1][i];
         }
     const IntMlpRow R = intmlp_row(hi, lo);
-    const bool fast = R.small && !R.zero;
     const int64_t Kp = beats_per_row(K) * 64;
     int32_t xsum = 0;
     for (int hb = threadIdx.x; hb < halves; hb += kThreads) {
@@ -524,7 +523,7 @@ __device__ __forceinline__ void stage_x_intmlp(const Entry &E, const MlpDesc &D,
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int c = 4 * w + j;
-                    v[j] = fast ? intmlp_code_small(g[c], u[c], R) : intmlp_code(g[c], u[c], R);
+                    v[j] = intmlp_code_est(g[c], u[c], R);
                 }
                 in[2 * h8 + w] = pack4(v[0], v[1], v[2], v[3]);
                 xsum = dp4a_ss(in[2 * h8 + w], 0x01010101u, xsum);

@@ -110,7 +110,8 @@ __device__ __forceinline__ trit_u128 intmlp_abs_t(int32_t ag, int32_t au, bool &
 struct IntMlpRow {
     trit_u128 A;
     bool small, zero;
-    float k;
+    float k;    // 127 / A in fp32 when A < 2^56 (the 64-bit path), else 0
+    float kf;   // 127 / fl(A) in fp32 for any A > 0 (the estimate of intmlp_code_est)
 };
 __device__ __forceinline__ IntMlpRow intmlp_row(uint64_t hi, uint64_t lo) {
     IntMlpRow R;
@@ -118,6 +119,8 @@ __device__ __forceinline__ IntMlpRow intmlp_row(uint64_t hi, uint64_t lo) {
     R.zero = hi == 0 && lo == 0;
     R.small = hi == 0 && lo < (uint64_t(1) << 56);
     R.k = R.small && !R.zero ? __fdiv_rn(127.0f, __ull2float_rn(lo)) : 0.0f;
+    const float af = __fadd_rn(__fmul_rn(__ull2float_rn(hi), 0x1p64f), __ull2float_rn(lo));
+    R.kf = R.zero ? 0.0f : __fdiv_rn(127.0f, af);
     return R;
 }
 
@@ -171,6 +174,30 @@ __device__ __forceinline__ int intmlp_code_small(int32_t ag, int32_t au, const I
     const uint64_t t = uint64_t(ag) * uint64_t(ag) * uu;
     const int v = round_127_ratio_small(t, uint64_t(R.A), R.k);
     return au < 0 ? -v : v;
+}
+
+// The signed code of one column, any row: an fp32 estimate first, the exact
+// integer rounding only near a tie.  The estimate p = fl(fl(fl(g)^2) * fl(|u|)) * kf
+// of 127 |t| / A carries at most ten fp32 roundings of relative size 2^-24
+// (g twice through g^2, g^2, u, the product, A's two halves and their sum,
+// 127 / fl(A), the last product), so |p - 127 |t| / A| <= 127 * 10 * 2^-24
+// (1 + 2^-20) < 7.6e-5.  Where
+// p's distance from the nearest half-integer exceeds 1.5e-4 the exact quotient
+// lies on the same side of it and rounds to the same integer as p; otherwise
+// the exact path decides.
+__device__ __forceinline__ int intmlp_code_est(int32_t ag, int32_t au, const IntMlpRow &R) {
+    if (R.zero || ag <= 0 || au == 0) return 0;
+    const float g = __int2float_rn(ag);
+    const float tf = __fmul_rn(__fmul_rn(g, g), fabsf(__int2float_rn(au)));
+    const float p = __fmul_rn(tf, R.kf);
+    const float fl = floorf(p);
+    const float fr = __fsub_rn(p, fl);   // exact: p < 2^8 and fl is p's integer part
+    if (fabsf(__fsub_rn(fr, 0.5f)) > 1.5e-4f) {
+        int q = int(fl) + (fr > 0.5f ? 1 : 0);
+        q = q > 127 ? 127 : q;
+        return au < 0 ? -q : q;
+    }
+    return R.small ? intmlp_code_small(ag, au, R) : intmlp_code(ag, au, R);
 }
 
 // max|t| (hi:lo) * ((S_g * S_g) * S_u), S = w * x_scale / 127, in double, rounded once.

@@ -135,8 +135,7 @@ __global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *
             }
         const IntMlpRow R = intmlp_row(hi, lo);
         int8_t *qr = q + m * ldq;
-        const bool fast = R.small && !R.zero;
-        for (int64_t base = 0; base < ldq; base += 8 * kNThreads) {
+            for (int64_t base = 0; base < ldq; base += 8 * kNThreads) {
             int32_t g[8], u[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -148,7 +147,7 @@ __global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *
             for (int r = 0; r < 8; ++r) {
                 const int64_t c = base + r * kNThreads + threadIdx.x;
                 if (c < ldq)
-                    qr[c] = int8_t(fast ? intmlp_code_small(g[r], u[r], R) : intmlp_code(g[r], u[r], R));
+                    qr[c] = int8_t(intmlp_code_est(g[r], u[r], R));
             }
         }
         if (threadIdx.x == 0) h_scale[m] = intmlp_scale(hi, lo, w_g, w_u, x_scale[m]);

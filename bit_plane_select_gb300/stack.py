@@ -144,3 +144,94 @@ class TernaryStack:
     def quant_bytes(self) -> int:
         """fp32 activations read, int8 codes (K_pad per row) and scales written."""
         return sum(M * (4 * K + k_pad(K) + 4) for _, N, K, M, _ in self.specs)
+
+
+class LayerChain:
+    """The dependency-ordered decode of one token through ternary layers: per
+    layer four launches, each reading what the one before wrote --
+      1. q, k, v from the layer's input row (quantiser fused),
+      2. o from q's fp32 output (the attention output's stand-in: attention
+         itself is not a ternary product),
+      3. gate and up from o's fp32 output (gate also writes the input scale),
+      4. the IntMlp codes of relu(a_gate)^2 a_up and the down product.
+    This is the per-matvec ordering of a real token ("Tritium ..." -- Why it
+    does not scale): every launch waits for the grid before it (programmatic
+    stream serialisation) before it reads its input.  Each layer's input row is
+    its own buffer (x[layer]); the residual stream and the norms are not part
+    of the ternary path.
+
+    weights: per layer, a dict name -> (int8 [N, K] tensor, w_scale) for the
+    seven projections q, k, v, o, gate, up, down."""
+
+    NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+    def __init__(self, weights, device="cuda"):
+        from . import MlpProjList
+        self.device = torch.device(device)
+        dev = self.device
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.layers = []
+        self.plane_bytes = 0
+        for lw in weights:
+            P, S, shape = {}, {}, {}
+            for name in self.NAMES:
+                w, ws = lw[name]
+                planes, err = trit_pack(w.to(dev), ws)
+                if int(err.item()) != 0:
+                    raise ValueError(f"{name}: non-ternary weights")
+                P[name], S[name], shape[name] = planes, float(ws), tuple(w.shape)
+                self.plane_bytes += planes.numel()
+            Nq, K = shape["q"]
+            Nk, Nv = shape["k"][0], shape["v"][0]
+            No, Ko = shape["o"]
+            Nf, Kg = shape["gate"]
+            Nd, Kd = shape["down"]
+            if Ko != Nq or Kg != No or Kd != Nf or shape["up"] != shape["gate"]:
+                raise ValueError("layer shapes do not chain")
+            L = {"P": P, "S": S}
+            L["x"] = torch.zeros(K, dtype=torch.float32, device=dev)
+            for name, n in (("q", Nq), ("k", Nk), ("v", Nv), ("o", No), ("down", Nd)):
+                L["y_" + name] = torch.zeros(n, dtype=torch.int32, device=dev)
+                L["f_" + name] = torch.zeros(n, dtype=torch.float32, device=dev)
+            L["a_gate"] = torch.zeros(Nf, dtype=torch.int32, device=dev)
+            L["a_up"] = torch.zeros(Nf, dtype=torch.int32, device=dev)
+            L["s_gu"] = torch.zeros(1, dtype=torch.float32, device=dev)
+            L["qkv"] = QProjList([(P[n], S[n], L["x"], None, None, L["y_" + n], L["f_" + n])
+                                  for n in ("q", "k", "v")])
+            L["o"] = QProjList([(P["o"], S["o"], L["f_q"], None, None, L["y_o"], L["f_o"])])
+            L["gu"] = QProjList([(P["gate"], S["gate"], L["f_o"], None, L["s_gu"], L["a_gate"], None),
+                                 (P["up"], S["up"], L["f_o"], None, None, L["a_up"], None)])
+            L["down"] = MlpProjList([(P["down"], S["down"], L["a_gate"], L["a_up"], L["s_gu"],
+                                      S["gate"], S["up"], None, None, L["y_down"], L["f_down"])])
+            self.layers.append(L)
+
+    @property
+    def x(self):
+        return [L["x"] for L in self.layers]
+
+    def step(self, stream=None):
+        """One token through every layer: 4 launches per layer."""
+        from . import trit_intmlp_gemv_many
+        for L in self.layers:
+            trit_quant_gemv_many(L["qkv"], self.err, stream)
+            trit_quant_gemv_many(L["o"], self.err, stream)
+            trit_quant_gemv_many(L["gu"], self.err, stream)
+            trit_intmlp_gemv_many(L["down"], self.err, stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 4 * len(self.layers)
+
+    def step_bytes(self) -> int:
+        """Algorithmic bytes of one token: every plane byte read once; per
+        launch its fp32 (or int32) inputs read and int32 + fp32 outputs written."""
+        b = self.plane_bytes
+        for L in self.layers:
+            K = L["x"].numel()
+            nq, nk, nv = (L["y_" + n].numel() for n in ("q", "k", "v"))
+            no, nf, nd = L["y_o"].numel(), L["a_gate"].numel(), L["y_down"].numel()
+            b += 4 * K + 8 * (nq + nk + nv)          # qkv: x read, y + f written
+            b += 4 * nq + 8 * no                     # o: q's f read
+            b += 4 * no + 4 + 8 * nf                 # gate/up: o's f read, scale, a_gate + a_up
+            b += 8 * nf + 4 + 8 * nd                 # down: a_gate + a_up read, scale
+        return b

@@ -229,3 +229,4 @@ def test_argument_errors_of_the_other_entry_points(trit):
     assert L.trit_read_probe(p, 17, p, s) == 1
     assert L.trit_read_probe(p, 64, null, s) == 1
     assert L.trit_check_div127(None) == 1
+
