@@ -1,9 +1,11 @@
 """Full-size parity on the five workloads, through the same calls the benchmark
 times (one quantise launch and one product launch over the whole list).
 
-Outputs the oracle can afford are compared one by one: every row for the
-single GEMV and the single layer, sampled rows (first, last and seeded random
-ones) for the 30-layer stack, the batch sweep and the prefill GEMMs.  Every
+Outputs are compared one by one with the oracle: every row of every
+projection for the single GEMV, the single layer, the 30-layer stack and the
+batch sweep at M = 1, 2, 4, 8; sampled rows (first, last and seeded random
+ones) of every projection at M = 16, 32, 64, and of every seventh prefill
+GEMM (a different seventh for each M) with sampled activation rows.  Every
 output row is also covered at full size by an invariant that holds at any
 size: sum_r y[m, r] = sum_c x[m, c] * (sum_r W[r, c]), the column sums taken
 from the drawn int8 weights in numpy int64."""
@@ -112,7 +114,7 @@ def test_config1_one_layer(t, orc):
         check_projection(orc, w, x, st.q[i], st.s[i], st.y[i], st.f[i], wss[i], K)
 
 
-def test_config2_stack_sampled(t, orc):
+def test_config2_stack_every_row(t, orc):
     st, items, wss = build_stack(t, synth.LAYERS, 2, 1)
     assert st.fusable
     st.step_two_launch()       # quantise, then multiply: two launches
@@ -125,30 +127,61 @@ def test_config2_stack_sampled(t, orc):
     # the fused launch and the two-launch path agree bit for bit on every output
     assert torch.equal(st.y_arena, y2) and torch.equal(st.q_arena, q2)
     assert torch.equal(st.f_arena.view(torch.int32), f2.view(torch.int32))
+    # every row of every projection against the oracle (2.08e9 weights)
     for i, (layer, idx, name, N, K) in enumerate(items):
         w = synth.stack_weights(2, layer, idx)
         x = synth.projection_acts(2, layer, idx, 1)
-        check_projection(orc, w, x, st.q[i], st.s[i], st.y[i], st.f[i], wss[i], K,
-                         rows=sample_rows(N, (2, layer, idx)))
+        check_projection(orc, w, x, st.q[i], st.s[i], st.y[i], st.f[i], wss[i], K)
 
 
 def test_config3_batch_sweep_and_corruption(t, orc):
     Mmax = max(synth.BATCH_SWEEP)
     st, items, wss = build_stack(t, synth.LAYERS, 3, Mmax)
     st.quantize()
+    FULL = (1, 2, 4, 8)        # every row of every projection, against the oracle
+    got, sampled, colsums = {}, {}, {}
     for M in synth.BATCH_SWEEP:
         plist = t.ProjList([(st.planes[i], wss[i], st.q[i][:M], st.s[i][:M], items[i][4],
                              st.y[i][:M], st.f[i][:M]) for i in range(len(items))])
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         t.trit_gemm_many(plist, err)
         assert int(host(err)[0]) == 0, M
-        mrows = np.arange(M)
-        for i in range(0, len(items), 1 if M in (1, 64) else 13):
-            layer, idx, name, N, K = items[i]
-            w = synth.stack_weights(3, layer, idx)
-            x = synth.projection_acts(3, layer, idx, Mmax)
-            check_projection(orc, w, x, st.q[i], st.s[i], st.y[i][:M], st.f[i][:M], wss[i], K,
-                             rows=sample_rows(N, (3, layer, idx, M)), mrows=mrows)
+        for i, (layer, idx, name, N, K) in enumerate(items):
+            y, f = st.y[i][:M], st.f[i][:M]
+            colsums[M, i] = host(y.to(torch.int64).sum(dim=1))
+            if M in FULL:
+                got[M, i] = (host(y).copy(), host(f).copy())
+            else:
+                rows = sample_rows(N, (3, layer, idx, M))
+                ri = torch.from_numpy(rows).cuda()
+                sampled[M, i] = (rows, host(y[:, ri]), host(f[:, ri]))
+    # one pass over the projections: the activation rows of every M are the
+    # first M of the 64, so one oracle product of eight rows checks every row
+    # of M = 1, 2, 4, 8; M = 16, 32, 64 (tensor cores) are checked on sampled
+    # rows, and every M by the column-sum invariant over all rows
+    m8 = max(FULL)
+    for i, (layer, idx, name, N, K) in enumerate(items):
+        w = synth.stack_weights(3, layer, idx)
+        q_ref, s_ref, e_ref = orc.quant(synth.projection_acts(3, layer, idx, Mmax))
+        assert not e_ref.any()
+        np.testing.assert_array_equal(host(st.q[i]), q_ref)
+        ry, rf, rerr = orc.gemm(orc.pack(w), wss[i], q_ref[:m8], s_ref[:m8], K)
+        assert not rerr.any()
+        for M in FULL:
+            y, f = got[M, i]
+            np.testing.assert_array_equal(y, ry[:M])
+            assert_f32_close(f, rf[:M])
+        colsum = w.astype(np.int64).sum(axis=0)
+        for M in synth.BATCH_SWEEP:
+            np.testing.assert_array_equal(colsums[M, i], q_ref[:M, :K].astype(np.int64) @ colsum)
+            if M in FULL:
+                continue
+            rows, ys, fs = sampled[M, i]
+            sy, sf, serr = orc.gemm(orc.pack(w[rows]), wss[i], q_ref[:M], s_ref[:M], K)
+            assert not serr.any()
+            np.testing.assert_array_equal(ys, sy)
+            assert_f32_close(fs, sf)
+    del got, sampled
 
     # 0.1% of the beats of every projection get both bits set at one position
     corrupted_rows = {}
@@ -199,14 +232,16 @@ def test_config4_prefill_sampled(t, orc):
             y = torch.empty((M, N), dtype=torch.int32, device="cuda")
             f = torch.empty((M, N), dtype=torch.float32, device="cuda")
             entries.append((planes[i], wss[i], q, s, K, y, f))
-            if i % 7 == 0 or i == len(items) - 1:
+            if i % 7 == M % 7 or i == len(items) - 1:
                 xs_host[i] = x
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         t.trit_gemm_many(t.ProjList(entries), err)
         assert int(host(err)[0]) == 0
         rng = synth.rng_for(501, M)
+        # every 7th projection, a different seventh for each M (the two M
+        # together cover different gate / up / down weights), and the last
         for i, (layer, idx, name, N, K) in enumerate(items):
-            if i % 7 and i != len(items) - 1:
+            if i % 7 != M % 7 and i != len(items) - 1:
                 continue
             w = synth.projection_weights(4, layer, idx)
             rows = sample_rows(N, (5, layer, idx, M))
