@@ -76,8 +76,22 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+// Lanes per weight row: M > 1 paths 4; M = 1 TRIT_M1_LANES (4: a warp load
+// covers 8 rows x 64 bytes; 8: 4 rows x 128 bytes).  A plain read probe of the
+// stack's rows streams 3-5% faster with 4 x 128 bytes, but the kernel is
+// slower with it: 100.2 against 95.8 us per 30-layer token (ring depth 2, 7
+// and 14 for the 108-beat rows, two or four groups prefetched: all slower).
+#ifndef TRIT_M1_LANES
+#define TRIT_M1_LANES 4
+#endif
 constexpr int kLanesPerRow = 4;
-constexpr int kRowsPerGroup = 32 / kLanesPerRow;
+constexpr int kLanes1 = TRIT_M1_LANES;
+static_assert(kLanes1 == 4 || kLanes1 == 8, "lanes per row at M = 1");
+constexpr int kRowsPerGroup = 32 / kLanes1;   // rows of an M = 1 group
+__host__ __device__ constexpr int lanes_of(int mt) { return mt == 1 ? kLanes1 : kLanesPerRow; }
+// The unrolled M = 1 paths: rows of 40 and 108 beats (K = 2560, 6912).
+constexpr int kIt40 = 40 / kLanes1;
+constexpr int kIt108 = (108 + kLanes1 - 1) / kLanes1;
 constexpr int kDepth = 4;                   // 16-byte loads in flight per lane
 constexpr int kMaxList = TRIT_MAX_LIST_PER_LAUNCH;
 constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
@@ -94,10 +108,10 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 #define TRIT_RING_40 5
 #endif
 #ifndef TRIT_RING_108
-#define TRIT_RING_108 3
+#define TRIT_RING_108 (TRIT_M1_LANES == 8 ? 7 : 3)
 #endif
 #ifndef TRIT_PREFETCH_FIRST
-#define TRIT_PREFETCH_FIRST 2
+#define TRIT_PREFETCH_FIRST (TRIT_M1_LANES == 8 ? 4 : 2)
 #endif
 #ifndef TRIT_COST_108
 #define TRIT_COST_108 100
@@ -183,7 +197,7 @@ struct Entry {
     int64_t groups;         // ceil(N / 8)
     int64_t cost_begin;     // prefix sum of groups * gcost over the list
     int32_t xld;            // activation row stride (K_pad)
-    int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / 4)
+    int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / lanes)
     int32_t bstride;        // beats per full row of the planes
     int32_t mrows;          // bits 0-7: activation rows of this entry (<= MT); bits 8-15:
                             // 1 + index of its IntMlp descriptor (0: none)
@@ -290,7 +304,7 @@ template <int MT>
 __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int32_t *s_xsum) {
     static_assert(kWarps % MT == 0, "whole warps per staged row");
     constexpr int kWpr = kWarps / MT;
-    const int halves = E.iters * kLanesPerRow * 2;
+    const int halves = E.iters * lanes_of(MT) * 2;
     const int m = (threadIdx.x >> 5) / kWpr;
     int32_t xsum = 0;
     for (int hb = ((threadIdx.x >> 5) % kWpr) * 32 + (threadIdx.x & 31); hb < halves;
@@ -342,7 +356,7 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
     __shared__ uint32_t s_red[2][kWarps];
     const int K = E.K;
     const int nhb = (K + 31) / 32;                   // half-blocks that hold columns
-    const int halves = E.iters * kLanesPerRow * 2;   // half-blocks staged (>= nhb)
+    const int halves = E.iters * kLanes1 * 2;   // half-blocks staged (>= nhb)
     const float *x = E.xf;
     const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
     auto load4 = [&](int c) -> float4 {   // columns c..c+3, zero past K
@@ -423,7 +437,7 @@ __device__ __forceinline__ void stage_x_intmlp(const Entry &E, const MlpDesc &D,
                                                bool owner, int32_t *s_xsum, float *s_scale) {
     __shared__ uint64_t s_max[2][kWarps];
     const int K = E.K;
-    const int halves = E.iters * kLanesPerRow * 2;
+    const int halves = E.iters * kLanes1 * 2;
     // 16-byte loads when the rows allow them (K % 4 == 0, 16-byte aligned)
     const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(D.a_gate) & 15) == 0) &&
                      ((reinterpret_cast<uintptr_t>(D.a_up) & 15) == 0);
@@ -550,9 +564,10 @@ __device__ __forceinline__ void stage_x_intmlp(const Entry &E, const MlpDesc &D,
     }
 }
 
-__device__ __forceinline__ int32_t row_sum4(int32_t v) {
+__device__ __forceinline__ int32_t row_sum1(int32_t v) {
     v += __shfl_xor_sync(~0u, v, 1);
     v += __shfl_xor_sync(~0u, v, 2);
+    if (kLanes1 == 8) v += __shfl_xor_sync(~0u, v, 4);
     return v;
 }
 
@@ -576,7 +591,7 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
     int lt = 0, loff = bs;
     auto next_load = [&]() -> uint4 {
         const uint4 v = ldg_stream(lrow + (loff < last_beat ? loff : last_beat));
-        loff += kLanesPerRow;
+        loff += kLanes1;
         if (++lt == it) {
             lt = 0;
             loff = bs;
@@ -609,9 +624,9 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
         const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
         mac_codes(v.x, v.z, xl, acc);
         mac_codes(v.y, v.w, xh, acc);
-        xoff += kLanesPerRow * kXBeatVec;
+        xoff += kLanes1 * kXBeatVec;
         if (++ct == it) {
-            const int32_t y = row_sum4(codes_total(acc)) - xsum;
+            const int32_t y = row_sum1(codes_total(acc)) - xsum;
             if (bs == 0 && row < N) {
                 if (E.acc) {
                     atomicAdd(E.acc + row, y);
@@ -874,9 +889,9 @@ __device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32
 
 template <int IT>
 __device__ __forceinline__ const uint4 *fixed_row_ptr(const Entry &E, int64_t g, int64_t last_row,
-                                                      int rs, int bs) {
+                                                      int rs) {
     const int64_t r = g * kRowsPerGroup + rs;
-    return E.planes + (r < last_row ? r : last_row) * int64_t(E.bstride) + bs;
+    return E.planes + (r < last_row ? r : last_row) * int64_t(E.bstride);
 }
 
 __device__ __forceinline__ int64_t fixed_last_row(const Entry &E, int64_t ge) {
@@ -894,13 +909,18 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
     const float w_scale = E.w_scale;
     const int64_t last_row = fixed_last_row(E, ge);
     const uint4 *xb = reinterpret_cast<const uint4 *>(xs) + bs * kXBeatVec;
+    // beat of step t: bs + kLanes1 t; only the last step can pass the row's end
+    // (kLanes1 (IT - 1) < B <= kLanes1 IT), and there it is clamped to the row's
+    // last beat, whose staged activations past B are zero
+    const int last_off = bs + kLanes1 * (IT - 1) < E.B ? bs + kLanes1 * (IT - 1) : E.B - 1;
+    auto off = [&](int t) { return t == IT - 1 ? last_off : bs + kLanes1 * t; };
 
     uint32_t viol = 0;
-    const uint4 *rp = fixed_row_ptr<IT>(E, gb, last_row, rs, bs);
-    const uint4 *rpn = fixed_row_ptr<IT>(E, gb + 1, last_row, rs, bs);
+    const uint4 *rp = fixed_row_ptr<IT>(E, gb, last_row, rs);
+    const uint4 *rpn = fixed_row_ptr<IT>(E, gb + 1, last_row, rs);
     uint4 ring[D];
 #pragma unroll
-    for (int d = 0; d < D; ++d) ring[d] = ldg_stream(rp + d * kLanesPerRow);
+    for (int d = 0; d < D; ++d) ring[d] = ldg_stream(rp + off(d));
     int64_t row = gb * kRowsPerGroup + rs;
     const bool pf = kL2Ahead > 0 && rs == 0 && bs == 0 && E.B == E.bstride;
     for (int64_t g = gb; g < ge; ++g) {
@@ -916,17 +936,17 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
 #pragma unroll
         for (int t = 0; t < IT; ++t) {
             const uint4 v = ring[t % D];
-            ring[t % D] = (t + D < IT) ? ldg_stream(rp + (t + D) * kLanesPerRow)
-                                       : ldg_stream(rpn + (t + D - IT) * kLanesPerRow);
+            ring[t % D] = (t + D < IT) ? ldg_stream(rp + off(t + D))
+                                       : ldg_stream(rpn + off(t + D - IT));
             viol |= (v.x & v.z) | (v.y & v.w);
-            const uint4 *X = xb + t * (kLanesPerRow * kXBeatVec);
+            const uint4 *X = xb + t * (kLanes1 * kXBeatVec);
             const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
             const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
             mac_codes(v.x, v.z, xl, acc);
             mac_codes(v.y, v.w, xh, acc);
         }
-        const int32_t y = row_sum4(codes_total(acc)) - xsum;
+        const int32_t y = row_sum1(codes_total(acc)) - xsum;
         if (bs == 0 && row < N) {
             if (acc_out) {
                 atomicAdd(acc_out + row, y);
@@ -937,7 +957,7 @@ __device__ __forceinline__ uint32_t fixed_run(const Entry &E, const uint32_t *xs
         }
         row += kRowsPerGroup;
         rp = rpn;
-        rpn = fixed_row_ptr<IT>(E, g + 2, last_row, rs, bs);
+        rpn = fixed_row_ptr<IT>(E, g + 2, last_row, rs);
     }
     return viol;
 }
@@ -949,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
     __shared__ int32_t s_xsum[kWarps];
     __shared__ float s_mlp_scale;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rs = lane / kLanesPerRow, bs = lane % kLanesPerRow;
+    const int rs = lane / lanes_of(MT), bs = lane % lanes_of(MT);
     const int64_t lo = int64_t(blockIdx.x) * L.total_cost / gridDim.x;
     const int64_t hi = (int64_t(blockIdx.x) + 1) * L.total_cost / gridDim.x;
     uint32_t viol = 0;
@@ -982,8 +1002,8 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
         const int64_t n = g1 - g0;
         const int64_t wb = g0 + n * warp / kWarps, we = g0 + n * (warp + 1) / kWarps;
         // 1: rows of 40 beats, 2: rows of 108 beats (unrolled paths), 0: generic
-        const int path = (MT == 1 && E.B == 40 && E.iters == 10) ? 1
-                       : (MT == 1 && E.B == 108 && E.iters == 27) ? 2 : 0;
+        const int path = (MT == 1 && E.B == 40 && E.iters == kIt40) ? 1
+                       : (MT == 1 && E.B == 108 && E.iters == kIt108) ? 2 : 0;
         // start this warp's first groups streaming into L2 before the barrier
         constexpr int kRows = MT == 1 ? kRowsPerGroup : kRowsPerGroupM;
         if (TRIT_PREFETCH_FIRST && lane == 0 && wb < we && E.B == E.bstride) {
@@ -1014,9 +1034,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
         if (wb < we) {
             if constexpr (MT == 1) {
                 if (path == 1)
-                    viol |= fixed_run<10, TRIT_RING_40>(E, xs, xsc, xsum, wb, we, rs, bs);
+                    viol |= fixed_run<kIt40, TRIT_RING_40>(E, xs, xsc, xsum, wb, we, rs, bs);
                 else if (path == 2)
-                    viol |= fixed_run<27, TRIT_RING_108>(E, xs, xsc, xsum, wb, we, rs, bs);
+                    viol |= fixed_run<kIt108, TRIT_RING_108>(E, xs, xsc, xsum, wb, we, rs, bs);
                 else
                     viol |= run_groups(E, xs, xsc, xsum, wb, we, rs, bs);
             } else {
@@ -1065,7 +1085,7 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
         if (entries[i].iters > max_iters) max_iters = entries[i].iters;
     }
     L.total_cost = cost;
-    L.xs_words = max_iters * kLanesPerRow * beat_words(MT);
+    L.xs_words = max_iters * lanes_of(MT) * beat_words(MT);
     const size_t smem = size_t(L.xs_words) * 4;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(select_accumulate_kernel<MT>,
@@ -1104,7 +1124,8 @@ __global__ void __launch_bounds__(256) segment_epilogue_kernel(const int32_t *ac
 }
 
 // One list entry: activation rows [m0, m0 + mrows) and beats [b0, b0 + nb) of p.
-Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb, int32_t *acc) {
+Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb, int32_t *acc,
+                 int lanes) {
     Entry E;
     const int64_t Kp = int64_t(p.B) * 64;
     E.planes = p.planes + b0;
@@ -1122,7 +1143,7 @@ Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb
     const int64_t kseg = int64_t(p.K) - b0 * 64;
     E.K = int32_t(kseg < nb * 64 ? kseg : nb * 64);
     E.B = int32_t(nb);
-    E.iters = int32_t((nb + kLanesPerRow - 1) / kLanesPerRow);
+    E.iters = int32_t((nb + lanes - 1) / lanes);
     E.bstride = p.B;
     E.mrows = mrows;
     E.gcost = E.iters * (nb == 108 ? TRIT_COST_108 : 100);
@@ -1172,7 +1193,7 @@ cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaS
             const int rows = int(p.M - m0 < MT ? p.M - m0 : MT);
             for (int64_t b0 = 0; b0 < p.B && e == cudaSuccess; b0 += seg_beats(MT)) {
                 const int64_t nb = p.B - b0 < seg_beats(MT) ? p.B - b0 : seg_beats(MT);
-                buf[n] = make_entry(p, m0, rows, b0, nb, acc);
+                buf[n] = make_entry(p, m0, rows, b0, nb, acc, lanes_of(MT));
                 if (MT > 1) buf[n].groups = (p.N + kRowsPerGroupM - 1) / kRowsPerGroupM;
                 ++n;
                 if (n == kMaxList) {
@@ -1215,7 +1236,7 @@ cudaError_t launch_intmlp_gemv_many(const MlpProjDev *list, int count, uint32_t 
         const int n = count - base < kMaxMlp ? count - base : kMaxMlp;
         for (int i = 0; i < n; ++i) {
             const MlpProjDev &m = list[base + i];
-            buf[i] = make_entry(m.down, 0, 1, 0, m.down.B, nullptr);
+            buf[i] = make_entry(m.down, 0, 1, 0, m.down.B, nullptr, kLanes1);
             buf[i].mrows |= (i + 1) << 8;
             desc[i].a_gate = m.a_gate;
             desc[i].a_up = m.a_up;
