@@ -62,11 +62,12 @@
 // NJ accumulators per weight class k (NJ = 4: 16 AND per beat, no shift; NJ = 1:
 // code bytes of weight 1, 28 logic instructions per beat), folded exactly at
 // the row's end, then the row's column sum is subtracted.  A lane
-// holds four weight rows (32-row groups), so every activation word it reads
-// from shared memory serves four rows; the CTA stages its MT activation rows
+// holds two weight rows (16-row groups), so every activation word it reads
+// from shared memory serves two rows; the CTA stages its MT activation rows
 // beat-interleaved (all rows of a beat side by side) so every read is an
 // immediate offset from one pointer.  At a group's end the four lanes of a row
-// set reduce-scatter their partial sums, so each lane finishes one row.  The
+// set reduce-scatter their partial sums, so every row is finished by two of
+// them and stored by one.  The
 // bound is the dp4a rate: 64 lanes per SM-clock on this device, i.e. two
 // SM-clocks per row-beat at M = 8 (the probe in trit_probe.cu measures it).
 #include "trit_internal.cuh"
@@ -124,13 +125,13 @@ constexpr int kXBeatVec = kXBeatWords / 4;  // uint4 per staged beat
 #endif
 // M > 1 path: steps of loads in flight per row of a lane, per staged row count.
 #ifndef TRIT_RING_M2
-#define TRIT_RING_M2 2
+#define TRIT_RING_M2 4
 #endif
 #ifndef TRIT_RING_M4
-#define TRIT_RING_M4 2
+#define TRIT_RING_M4 4
 #endif
 #ifndef TRIT_RING_M8
-#define TRIT_RING_M8 1
+#define TRIT_RING_M8 2
 #endif
 __host__ __device__ constexpr int ring_rows(int mt) {
     return mt == 8 ? TRIT_RING_M8 : mt == 4 ? TRIT_RING_M4 : TRIT_RING_M2;
@@ -139,8 +140,10 @@ __host__ __device__ constexpr int ring_rows(int mt) {
 // weight classes 4^j the code words are masked into (4: every mask is an AND of
 // the code word, no shift; 2: one shift per code word; 1: code bytes of weight
 // 1, three shifts per code word) -- per staged row count.  Measured on the
-// 30-layer stack: M = 2 129.9 us with 1 class, 123.6 with 2, 121.5 with 4; M = 4
-// unchanged by 2 classes (4 spill); M = 8 spills with 2 (351 against 322 us).
+// 30-layer stack with four weight rows per lane: M = 2 129.9 us with 1 class,
+// 123.6 with 2, 121.5 with 4; M = 4 unchanged by 2 classes (4 spill); M = 8
+// spilled with 2 (351 against 322 us).  With two rows per lane (below) M = 8
+// takes 2 classes without spilling.
 #ifndef TRIT_NJ_M2
 #define TRIT_NJ_M2 4
 #endif
@@ -148,14 +151,19 @@ __host__ __device__ constexpr int ring_rows(int mt) {
 #define TRIT_NJ_M4 2
 #endif
 #ifndef TRIT_NJ_M8
-#define TRIT_NJ_M8 1
+#define TRIT_NJ_M8 2
 #endif
 __host__ __device__ constexpr int acc_classes(int mt) {
     return mt == 8 ? TRIT_NJ_M8 : mt == 4 ? TRIT_NJ_M4 : TRIT_NJ_M2;
 }
 // CTAs per SM the kernel is compiled for (its register budget: 128 per thread
 // for MT > 1)
-__host__ __device__ constexpr int min_blocks(int mt) { return mt == 1 ? TRIT_MIN_BLOCKS_M1 : 2; }
+#ifndef TRIT_MIN_BLOCKS_M2
+#define TRIT_MIN_BLOCKS_M2 2
+#endif
+__host__ __device__ constexpr int min_blocks(int mt) {
+    return mt == 1 ? TRIT_MIN_BLOCKS_M1 : mt == 2 ? TRIT_MIN_BLOCKS_M2 : 2;
+}
 // Cost units charged ahead of each entry's groups for staging its activations
 // (M = 1 launches; a group step costs 100; 0 disables): a CTA whose share starts
 // an entry gets that much less group work.  Measured on the 30-layer stack (3,000 ... 70,000
@@ -654,25 +662,50 @@ __device__ __forceinline__ uint32_t run_groups(const Entry &E, const uint32_t *x
     return viol;
 }
 
-// M > 1: groups of 8 * kRowsPerLane rows.  Lane (rs, bs) takes the rows
-// 32g + rs + 8i (i < kRowsPerLane) at beats bs, bs + 4, ...: each beat is
-// expanded once into code bytes, one 32-column half at a time, and every
-// activation word read from shared memory serves all of the lane's rows.
-// Shared-memory reads of the activations were the bound with fewer rows per
-// lane (each dp4a of a lane consumed 4 / rows-per-lane bytes of them, against
-// 128 bytes per clock per SM).
-constexpr int kRowsPerLane = 4;
-constexpr int kRowsPerGroupM = 8 * kRowsPerLane;
+// M > 1: groups of 8 R rows, R = rows_per_lane(MT).  Lane (rs, bs) takes the
+// rows 8R g + rs + 8i (i < R) at beats bs, bs + 4, ...: each beat's code words
+// are formed once per row and every activation word read from shared memory
+// serves all R of the lane's rows.  Shared-memory reads of the activations
+// were the bound with one row per lane (each dp4a of a lane consumed 4 / R
+// bytes of them, against 128 bytes per clock per SM); two rows per lane with
+// a deeper load ring measured faster than four.
+// Weight rows per lane (2 or 4) per staged row count.  Measured on the 30-layer
+// stack (ring depth per row in brackets): M = 2 121.1 us with four rows [2],
+// 115.4 with two [4] (118.8 [3], 117.7 [5], 119.9 [6], 133.0 [8]; two rows at
+// three CTAs per SM 127.6); M = 4 187.5 -> 183.6 (two rows [4], 2 classes);
+// M = 8 311.6 -> 307.7 (two rows [2], 2 classes; [3] 325.2).
+#ifndef TRIT_RPL_M2
+#define TRIT_RPL_M2 2
+#endif
+#ifndef TRIT_RPL_M4
+#define TRIT_RPL_M4 2
+#endif
+#ifndef TRIT_RPL_M8
+#define TRIT_RPL_M8 2
+#endif
+__host__ __device__ constexpr int rows_per_lane(int mt) {
+    return mt == 2 ? TRIT_RPL_M2 : mt == 4 ? TRIT_RPL_M4 : TRIT_RPL_M8;
+}
+__host__ __device__ constexpr int rows_per_group(int mt) { return 8 * rows_per_lane(mt); }
 
-// Reduce-scatter of a lane's kRowsPerLane x MT partial sums over the four lanes
-// of its rows (lanes 4 rs + bs, bs = 0..3): after two butterfly steps lane bs
+// Reduce-scatter of a lane's R x MT partial sums over the four lanes of its
+// rows (lanes 4 rs + bs, bs = 0..3).  R = 4: after two butterfly steps lane bs
 // holds the complete sums of its row i = 2 (bs & 1) + (bs >> 1) for every m
-// (so the four lanes finish and store four different rows).
-template <int MT>
-__device__ __forceinline__ void reduce_rows(const int (&acc)[kRowsPerLane][MT], int bs,
-                                            int (&out)[MT]) {
-    constexpr int H = 2 * MT;   // values per half: rows {0, 1} or {2, 3}
+// (so the four lanes finish and store four different rows).  R = 2: lane bs
+// holds those of row i = bs & 1 (lanes bs and bs ^ 2 hold the same row).
+template <int MT, int R>
+__device__ __forceinline__ void reduce_rows(const int (&acc)[R][MT], int bs, int (&out)[MT]) {
     const bool b0 = bs & 1, b1 = (bs >> 1) & 1;
+    if constexpr (R == 2) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            const int send = b0 ? acc[0][m] : acc[1][m];
+            const int t = (b0 ? acc[1][m] : acc[0][m]) + __shfl_xor_sync(~0u, send, 1);
+            out[m] = t + __shfl_xor_sync(~0u, t, 2);
+        }
+        return;
+    }
+    constexpr int H = 2 * MT;   // values per half: rows {0, 1} or {2, 3}
     int t[H];
 #pragma unroll
     for (int v = 0; v < H; ++v) {
@@ -695,11 +728,10 @@ __device__ __forceinline__ void reduce_rows(const int (&acc)[kRowsPerLane][MT], 
 // NJ = 2 one shift by 4 for the upper two j (k = j & 1), NJ = 1 the shift by
 // 2j (k = 0).  Accumulator k holds a multiple of 4^k; fold_classes divides it
 // out exactly.  The caller may refill v's registers once this returns.
-template <int MT, int NJ>
-__device__ __forceinline__ void mac_beat_rows(const uint4 (&v)[kRowsPerLane], const uint4 *xp,
-                                              int (&acc)[kRowsPerLane][MT][NJ], uint32_t &viol) {
+template <int MT, int NJ, int R>
+__device__ __forceinline__ void mac_beat_rows(const uint4 (&v)[R], const uint4 *xp,
+                                              int (&acc)[R][MT][NJ], uint32_t &viol) {
     static_assert(NJ == 1 || NJ == 2 || NJ == 4, "weight classes");
-    constexpr int R = kRowsPerLane;
     uint32_t zw[2][R][2];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -791,7 +823,8 @@ template <int MT, int D, int NJ>
 __device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32_t *xs,
                                                     const int32_t *s_xsum, int64_t gb,
                                                     int64_t ge, int rs, int bs) {
-    constexpr int R = kRowsPerLane;
+    constexpr int R = rows_per_lane(MT);
+    constexpr int kRowsPerGroupM = rows_per_group(MT);
     constexpr int BV = beat_words(MT) / 4;   // uint4 per staged beat
     const int it = E.iters;
     const int steps = int(ge - gb) * it;
@@ -841,7 +874,7 @@ __device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32
         uint4 v[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) v[i] = ring[slot][i];
-        mac_beat_rows<MT, NJ>(v, xp, acc, viol);
+        mac_beat_rows<MT, NJ, R>(v, xp, acc, viol);
         next_load(ring[slot]);
         xp += kLanesPerRow * BV;
         if (++ct == it) {
@@ -856,9 +889,9 @@ __device__ __forceinline__ uint32_t run_groups_rows(const Entry &E, const uint32
                     for (int k = 0; k < NJ; ++k) acc[i][m][k] = 0;
                 }
             int y[MT];
-            reduce_rows<MT>(tot, bs, y);
-            const int64_t r = row + 8 * (2 * (bs & 1) + (bs >> 1));
-            if (r < N) {
+            reduce_rows<MT, R>(tot, bs, y);
+            const int64_t r = row + 8 * (R == 4 ? 2 * (bs & 1) + (bs >> 1) : (bs & 1));
+            if (r < N && (R == 4 || (bs >> 1) == 0)) {
 #pragma unroll
                 for (int m = 0; m < MT; ++m)
                     if (m < rows_of(E)) store_out(E, m, r, y[m] - read_xsum_row<MT>(s_xsum, m));
@@ -1005,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
         const int path = (MT == 1 && E.B == 40 && E.iters == kIt40) ? 1
                        : (MT == 1 && E.B == 108 && E.iters == kIt108) ? 2 : 0;
         // start this warp's first groups streaming into L2 before the barrier
-        constexpr int kRows = MT == 1 ? kRowsPerGroup : kRowsPerGroupM;
+        constexpr int kRows = MT == 1 ? kRowsPerGroup : rows_per_group(MT);
         if (TRIT_PREFETCH_FIRST && lane == 0 && wb < we && E.B == E.bstride) {
             const int64_t r0 = wb * kRows;
             const int64_t ahead = TRIT_PREFETCH_FIRST;
@@ -1194,7 +1227,7 @@ cudaError_t launch_products(const ProjDev *list, int count, uint32_t *err, cudaS
             for (int64_t b0 = 0; b0 < p.B && e == cudaSuccess; b0 += seg_beats(MT)) {
                 const int64_t nb = p.B - b0 < seg_beats(MT) ? p.B - b0 : seg_beats(MT);
                 buf[n] = make_entry(p, m0, rows, b0, nb, acc, lanes_of(MT));
-                if (MT > 1) buf[n].groups = (p.N + kRowsPerGroupM - 1) / kRowsPerGroupM;
+                if (MT > 1) buf[n].groups = (p.N + rows_per_group(MT) - 1) / rows_per_group(MT);
                 ++n;
                 if (n == kMaxList) {
                     e = launch_entries<MT>(buf, n, err, s, xs_val);
