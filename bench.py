@@ -870,6 +870,16 @@ def run_issue(args):
                       "clocks": clk.summary()}), flush=True)
 
 
+# Per (weight row, beat) instruction counts of the dp4a path for a chunk of mt
+# staged activation rows, as the kernel is built: the code words (10 logic),
+# the P1 check (3) and the masks into weight classes (16 / 20 / 28 logic for
+# 4 / 2 / 1 classes: classes 4, 2, 2 at 2, 4, 8 staged rows), 16 dp4a per
+# activation row, and the staged activations read from shared memory -- 64
+# bytes per activation row and beat, shared by the lane's two weight rows.
+DP4A_LOGIC = {2: 10 + 3 + 16, 4: 10 + 3 + 20, 8: 10 + 3 + 20}
+DP4A_ROWS_PER_LANE = 2
+
+
 def batch_floors(M: int, shapes, nbytes: int, peak_gbs: float, sm_count: int, sm_mhz,
                  rates: dict | None = None) -> dict:
     """Lower bounds on one batched step over `shapes` ((N, K) per product) with
@@ -877,11 +887,11 @@ def batch_floors(M: int, shapes, nbytes: int, peak_gbs: float, sm_count: int, sm
       hbm: the step's algorithmic bytes at the measured copy peak;
       dp4a path (2 <= M <= 12): rows in chunks of 8, the remainder staged as 2,
         4 or 8 rows; per weight row-beat and chunk of mt staged rows: 16 mt dp4a
-        (the dp4a pipe), 38 logic instructions forming the code bytes (the
-        logic pipe), 16 mt bytes of staged activations (four rows per lane
-        share each read; shared memory), 16 mt + 42 instructions issued; each
-        at the rate `rates` gives (trit_issue_probe, lanes per SM-clock), the
-        bound being the largest;
+        (the dp4a pipe), DP4A_LOGIC[mt] logic instructions (the logic pipe),
+        64 mt / DP4A_ROWS_PER_LANE bytes of staged activations (shared memory),
+        16 mt + DP4A_LOGIC[mt] + 2 mt instructions issued; each at the rate
+        `rates` gives (trit_issue_probe, lanes per SM-clock), the bound being
+        the largest;
       tensor path (13 <= M <= 128): four M = 128 MMAs per 128 weight rows and
         beat at MMA_CYCLES_M128 each, one MMA stream per SM.
     With no sampled clock (sm_mhz None) the compute floors are None."""
@@ -900,9 +910,9 @@ def batch_floors(M: int, shapes, nbytes: int, peak_gbs: float, sm_count: int, sm
         if sm_mhz:
             f = sm_mhz * 1e6 * sm_count
             per = {"dp4a": sum(16 * mt for mt in chunks) / dp4a,
-                   "logic": 38 * len(chunks) / lop,
-                   "shared": sum(16 * mt for mt in chunks) / lds,
-                   "issue": sum(16 * mt + 42 for mt in chunks) / 128.0}
+                   "logic": sum(DP4A_LOGIC[mt] for mt in chunks) / lop,
+                   "shared": sum(64 * mt / DP4A_ROWS_PER_LANE for mt in chunks) / lds,
+                   "issue": sum(16 * mt + DP4A_LOGIC[mt] + 2 * mt for mt in chunks) / 128.0}
             out["alu_floors_ms"] = {k: row_beats * v / f * 1e3 for k, v in per.items()}
             out["alu_floor_ms"] = max(out["alu_floors_ms"].values())
             other = out["alu_floor_ms"]

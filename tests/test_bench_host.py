@@ -73,8 +73,13 @@ def test_batch_floors(bench):
     m8 = bench.batch_floors(8, shapes, 10**9, 6785.2, 152, 2070.0, rates)
     assert m8["path"] == "dp4a" and m8["chunks"] == [8]
     assert m8["alu_floors_ms"]["dp4a"] == pytest.approx(row_beats * 128 / 64 / f * 1e3, rel=1e-3)
-    assert m8["alu_floors_ms"]["logic"] == pytest.approx(row_beats * 38 / 64 / f * 1e3, rel=1e-3)
+    assert m8["alu_floors_ms"]["logic"] == pytest.approx(row_beats * 33 / 64 / f * 1e3, rel=1e-3)
+    assert m8["alu_floors_ms"]["shared"] == pytest.approx(row_beats * 256 / 128 / f * 1e3, rel=1e-3)
     assert m8["alu_floor_ms"] == m8["alu_floors_ms"]["dp4a"]
+    m2 = bench.batch_floors(2, shapes, 10**9, 6785.2, 152, 2070.0, rates)
+    assert m2["alu_floors_ms"]["logic"] == pytest.approx(row_beats * 29 / 64 / f * 1e3, rel=1e-3)
+    assert m2["alu_floors_ms"]["issue"] == pytest.approx(row_beats * (32 + 29 + 4) / 128 / f * 1e3,
+                                                         rel=1e-3)
     m12 = bench.batch_floors(12, shapes, 10**9, 6785.2, 152, 2070.0, rates)
     assert m12["chunks"] == [8, 4]
     assert m12["alu_floors_ms"]["dp4a"] == pytest.approx(row_beats * 192 / 64 / f * 1e3, rel=1e-3)
