@@ -22,6 +22,11 @@ namespace {
 
 constexpr int kNThreads = 256;
 constexpr int kNWarps = kNThreads / 32;
+// IntMlp rows when there are no more rows than SMs (decode): one CTA per row
+#ifndef TRIT_INTMLP_THREADS_FEW
+#define TRIT_INTMLP_THREADS_FEW 1024
+#endif
+constexpr int kIntMlpThreadsFew = TRIT_INTMLP_THREADS_FEW;
 
 __device__ __forceinline__ double block_sum_f64(double v, double *red) {
 #pragma unroll
@@ -88,11 +93,16 @@ __global__ void __launch_bounds__(kNThreads) quant_folded_kernel(const float *x,
 
 // ---- IntMlp ----------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *ag, const int32_t *au,
-                                                                 int64_t M, int64_t N, int64_t ldq,
-                                                                 float w_g, float w_u,
-                                                                 const float *x_scale, int8_t *q,
-                                                                 float *h_scale) {
+// NT threads per row (one CTA per row): a decode row (M = 1, N = 6,912) is
+// latency-bound, so more threads mean fewer dependent rounds per pass.
+template <int NT>
+__global__ void __launch_bounds__(NT) intmlp_quant_kernel(const int32_t *ag, const int32_t *au,
+                                                          int64_t M, int64_t N, int64_t ldq,
+                                                          float w_g, float w_u,
+                                                          const float *x_scale, int8_t *q,
+                                                          float *h_scale) {
+    constexpr int kNThreads = NT;
+    constexpr int kNWarps = NT / 32;
     __shared__ uint64_t red[2][kNWarps];
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const int32_t *gr = ag + m * N, *ur = au + m * N;
@@ -135,7 +145,7 @@ __global__ void __launch_bounds__(kNThreads) intmlp_quant_kernel(const int32_t *
             }
         const IntMlpRow R = intmlp_row(hi, lo);
         int8_t *qr = q + m * ldq;
-            for (int64_t base = 0; base < ldq; base += 8 * kNThreads) {
+        for (int64_t base = 0; base < ldq; base += 8 * kNThreads) {
             int32_t g[8], u[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -197,8 +207,12 @@ cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M,
                                 float w_g, float w_u, const float *x_scale, int8_t *q,
                                 float *h_scale, cudaStream_t s) {
     const int64_t ldq = beats_per_row(N) * 64;
-    intmlp_quant_kernel<<<rows_grid(M), kNThreads, 0, s>>>(ag, au, M, N, ldq, w_g, w_u, x_scale, q,
-                                                            h_scale);
+    if (M <= int64_t(device_sm_count()))
+        intmlp_quant_kernel<kIntMlpThreadsFew><<<int(M), kIntMlpThreadsFew, 0, s>>>(
+            ag, au, M, N, ldq, w_g, w_u, x_scale, q, h_scale);
+    else
+        intmlp_quant_kernel<kNThreads><<<rows_grid(M), kNThreads, 0, s>>>(ag, au, M, N, ldq, w_g, w_u,
+                                                                           x_scale, q, h_scale);
     return cudaGetLastError();
 }
 

@@ -161,12 +161,17 @@ class LayerChain:
     of the ternary path.
 
     weights: per layer, a dict name -> (int8 [N, K] tensor, w_scale) for the
-    seven projections q, k, v, o, gate, up, down."""
+    seven projections q, k, v, o, gate, up, down.
+
+    fused_mlp: True runs stage 4 as one launch (every CTA of the down product
+    forms the IntMlp codes it needs); False as two (trit_intmlp_quant forms the
+    codes once, then the down product reads them) -- the same bits either way."""
 
     NAMES = ("q", "k", "v", "o", "gate", "up", "down")
 
-    def __init__(self, weights, device="cuda"):
+    def __init__(self, weights, device="cuda", fused_mlp: bool = False):
         from . import MlpProjList
+        self.fused_mlp = fused_mlp
         self.device = torch.device(device)
         dev = self.device
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -203,6 +208,10 @@ class LayerChain:
                                  (P["up"], S["up"], L["f_o"], None, None, L["a_up"], None)])
             L["down"] = MlpProjList([(P["down"], S["down"], L["a_gate"], L["a_up"], L["s_gu"],
                                       S["gate"], S["up"], None, None, L["y_down"], L["f_down"])])
+            L["h"] = torch.zeros(k_pad(Kd), dtype=torch.int8, device=dev)
+            L["s_h"] = torch.zeros(1, dtype=torch.float32, device=dev)
+            L["down_i8"] = ProjList([(P["down"], S["down"], L["h"], L["s_h"], Kd, L["y_down"],
+                                      L["f_down"])])
             self.layers.append(L)
 
     @property
@@ -210,17 +219,27 @@ class LayerChain:
         return [L["x"] for L in self.layers]
 
     def step(self, stream=None):
-        """One token through every layer: 4 launches per layer."""
-        from . import trit_intmlp_gemv_many
+        """One token through every layer: 4 (fused_mlp) or 5 launches per layer."""
+        from . import trit_intmlp_gemv_many, trit_intmlp_quant
         for L in self.layers:
             trit_quant_gemv_many(L["qkv"], self.err, stream)
             trit_quant_gemv_many(L["o"], self.err, stream)
             trit_quant_gemv_many(L["gu"], self.err, stream)
-            trit_intmlp_gemv_many(L["down"], self.err, stream)
+            if self.fused_mlp:
+                trit_intmlp_gemv_many(L["down"], self.err, stream)
+            else:
+                S = L["S"]
+                trit_intmlp_quant(L["a_gate"][None, :], L["a_up"][None, :], S["gate"], S["up"],
+                                  L["s_gu"], L["h"][None, :], L["s_h"], stream)
+                trit_gemm_many(L["down_i8"], self.err, stream)
+
+    @property
+    def stages_per_step(self) -> int:
+        return 4 * len(self.layers)
 
     @property
     def launches_per_step(self) -> int:
-        return 4 * len(self.layers)
+        return (4 if self.fused_mlp else 5) * len(self.layers)
 
     def step_bytes(self) -> int:
         """Algorithmic bytes of one token: every plane byte read once; per
