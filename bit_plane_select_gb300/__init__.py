@@ -55,14 +55,14 @@ class TritProj(ctypes.Structure):
     _fields_ = [("planes", ctypes.c_void_p), ("x_i8", ctypes.c_void_p),
                 ("x_scale", ctypes.c_void_p), ("y_i32", ctypes.c_void_p),
                 ("y_f32", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
-                ("K", ctypes.c_int64), ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+                ("K", ctypes.c_int64), ("w_scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
 
 
 class TritQProj(ctypes.Structure):
     _fields_ = [("planes", ctypes.c_void_p), ("x", ctypes.c_void_p), ("x_i8", ctypes.c_void_p),
                 ("x_scale", ctypes.c_void_p), ("y_i32", ctypes.c_void_p),
                 ("y_f32", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+                ("w_scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
 
 
 class TritMlpProj(ctypes.Structure):
@@ -376,14 +376,21 @@ def trit_gemv(planes: torch.Tensor, w_scale: float, x_i8: torch.Tensor, x_scale:
     return y_i32, y_f32, err_flag
 
 
+# trit_proj / trit_qproj flags: the planes were complete before the kernel
+# preceding the call on its stream was launched (packed, then synchronised)
+PLANES_READY = 1
+
+
 class ProjList:
     """A prepared host array of trit_proj entries (tensors are kept alive).
 
     entries: iterables of (planes, w_scale, x_i8, x_scale, K, y_i32, y_f32);
-    M is x_i8's row count, N the planes' row count.
+    M is x_i8's row count, N the planes' row count.  planes_ready sets
+    PLANES_READY on every entry.
     """
 
-    def __init__(self, entries):
+    def __init__(self, entries, planes_ready: bool = False):
+        flags = PLANES_READY if planes_ready else 0
         self._keep = []
         items = []
         for planes, w_scale, x_i8, x_scale, K, y_i32, y_f32 in entries:
@@ -392,7 +399,7 @@ class ProjList:
                 _dev(planes, torch.uint8, "planes"), _dev(x_i8, torch.int8, "x_i8"),
                 _dev(x_scale, torch.float32, "x_scale"),
                 _dev(y_i32, torch.int32, "y_i32", True), _dev(y_f32, torch.float32, "y_f32", True),
-                M, planes.shape[0], K, float(w_scale), 0))
+                M, planes.shape[0], K, float(w_scale), flags))
             self._keep.append((planes, x_i8, x_scale, y_i32, y_f32))
         self.count = len(items)
         self.array = (TritProj * self.count)(*items)
@@ -401,9 +408,11 @@ class ProjList:
 class QProjList:
     """A prepared host array of trit_qproj entries (fused quantise-and-multiply,
     M = 1): (planes, w_scale, x fp32 [K] or [1, K], x_i8 out or None,
-    x_scale out or None, y_i32, y_f32)."""
+    x_scale out or None, y_i32, y_f32).  planes_ready sets PLANES_READY on
+    every entry."""
 
-    def __init__(self, entries):
+    def __init__(self, entries, planes_ready: bool = False):
+        flags = PLANES_READY if planes_ready else 0
         self._keep = []
         items = []
         for planes, w_scale, x, x_i8, x_scale, y_i32, y_f32 in entries:
@@ -412,7 +421,7 @@ class QProjList:
                 _dev(planes, torch.uint8, "planes"), _dev(x, torch.float32, "x"),
                 _dev(x_i8, torch.int8, "x_i8", True), _dev(x_scale, torch.float32, "x_scale", True),
                 _dev(y_i32, torch.int32, "y_i32", True), _dev(y_f32, torch.float32, "y_f32", True),
-                planes.shape[0], K, float(w_scale), 0))
+                planes.shape[0], K, float(w_scale), flags))
             self._keep.append((planes, x, x_i8, x_scale, y_i32, y_f32))
         self.count = len(items)
         self.array = (TritQProj * self.count)(*items)

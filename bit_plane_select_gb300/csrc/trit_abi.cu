@@ -49,7 +49,8 @@ trit_status check_device() {
 }
 
 trit_status check_proj(const trit_proj &p) {
-    if (!p.planes || !p.x_i8 || !p.x_scale || (!p.y_i32 && !p.y_f32) || p.reserved != 0)
+    if (!p.planes || !p.x_i8 || !p.x_scale || (!p.y_i32 && !p.y_f32) ||
+        (p.flags & ~TRIT_PROJ_PLANES_READY) != 0)
         return TRIT_E_ARG;
     if (!aligned(p.planes, 16) || !aligned(p.x_i8, 16) || !aligned(p.x_scale, 4) ||
         !aligned(p.y_i32, 4) || !aligned(p.y_f32, 4))
@@ -74,6 +75,7 @@ ProjDev to_dev(const trit_proj &p) {
     d.B = int32_t(beats_per_row(p.K));
     d.w_scale = p.w_scale;
     d.x_scale_val = 0.0f;
+    d.planes_ready = (p.flags & TRIT_PROJ_PLANES_READY) != 0;
     return d;
 }
 
@@ -136,7 +138,8 @@ trit_status run_many(const trit_proj *list, int32_t count, uint32_t *err_flag, c
 }
 
 trit_status check_qproj(const trit_qproj &p) {
-    if (!p.planes || !p.x || (!p.y_i32 && !p.y_f32) || p.reserved != 0) return TRIT_E_ARG;
+    if (!p.planes || !p.x || (!p.y_i32 && !p.y_f32) || (p.flags & ~TRIT_PROJ_PLANES_READY) != 0)
+        return TRIT_E_ARG;
     if (!aligned(p.planes, 16) || !aligned(p.x, 4) || !aligned(p.x_i8, 16) ||
         !aligned(p.x_scale, 4) || !aligned(p.y_i32, 4) || !aligned(p.y_f32, 4))
         return TRIT_E_ARG;
@@ -160,6 +163,7 @@ ProjDev to_dev(const trit_qproj &p) {
     d.B = int32_t(beats_per_row(p.K));
     d.w_scale = p.w_scale;
     d.x_scale_val = 0.0f;
+    d.planes_ready = (p.flags & TRIT_PROJ_PLANES_READY) != 0;
     return d;
 }
 
@@ -197,7 +201,7 @@ TRIT_API const char *trit_status_string(trit_status s) {
 
 TRIT_API const char *trit_last_cuda_error(void) { return g_last_cuda_error; }
 
-TRIT_API int32_t trit_abi_version(void) { return 3; }
+TRIT_API int32_t trit_abi_version(void) { return 4; }
 
 TRIT_API int64_t trit_payload_bytes(int64_t N, int64_t K) {
     if (!rows_ok(N) || !cols_ok(K)) return -1;
@@ -337,6 +341,7 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
             m.down.B = int32_t(beats_per_row(p.K));
             m.down.w_scale = p.w_scale;
             m.down.x_scale_val = 0.0f;
+            m.down.planes_ready = false;
             m.a_gate = p.a_gate;
             m.a_up = p.a_up;
             m.x_scale_in = p.x_scale;
@@ -363,7 +368,7 @@ TRIT_API trit_status trit_gemm(const uint8_t *planes, float w_scale, const int8_
     p.N = N;
     p.K = K;
     p.w_scale = w_scale;
-    p.reserved = 0;
+    p.flags = 0;
     return run_many(&p, 1, err_flag, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -382,7 +387,7 @@ TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_
     p.N = N;
     p.K = K;
     p.w_scale = w_scale;
-    p.reserved = 0;
+    p.flags = 0;
     if (!err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
     trit_status st = check_proj(p);
     if (st != TRIT_OK) return st;
@@ -485,7 +490,7 @@ TRIT_API trit_status trit_gemm_noalloc(const uint8_t *planes, float w_scale, con
     p.N = N;
     p.K = K;
     p.w_scale = w_scale;
-    p.reserved = 0;
+    p.flags = 0;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
     trit_status st = check_proj(p);

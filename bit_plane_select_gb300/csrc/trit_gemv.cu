@@ -208,7 +208,8 @@ struct Entry {
     int32_t K, B, iters;    // columns and beats of this entry's segment; iters = ceil(B / lanes)
     int32_t bstride;        // beats per full row of the planes
     int32_t mrows;          // bits 0-7: activation rows of this entry (<= MT); bits 8-15:
-                            // 1 + index of its IntMlp descriptor (0: none)
+                            // 1 + index of its IntMlp descriptor (0: none); bit 16:
+                            // kPlanesReady
     int32_t gcost;          // cost units of one group: iters x a per-step weight
     float w_scale;
 };
@@ -229,7 +230,7 @@ struct List {
     int64_t total_cost;
     uint32_t *err;
     float x_scale_val;      // M = 1 entries whose x_scale is NULL take this input scale
-    int32_t pad_;
+    int32_t flags;          // pre-loading launches: 1 = copy the planes before the grid dependency
     MlpDesc mlp[kMaxMlp];
     Entry e[kMaxList];
 };
@@ -237,6 +238,8 @@ static_assert(sizeof(List) <= 32764, "kernel parameter space");
 
 __host__ __device__ __forceinline__ int rows_of(const Entry &E) { return E.mrows & 0xff; }
 __host__ __device__ __forceinline__ int mlp_of(const Entry &E) { return (E.mrows >> 8) & 0xff; }
+// Entry.mrows bit: the planes may be read before the grid dependency resolves
+constexpr int32_t kPlanesReady = 1 << 16;
 
 // Code-word multiply-accumulate of one 32-column plane word pair (M = 1).
 __device__ __forceinline__ void mac_codes(uint32_t P, uint32_t N, const uint32_t (&x)[8],
@@ -356,18 +359,23 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int32_t *s
 
 // Fused path: quantise the fp32 row of entry E (K <= seg_beats(1)*64 columns)
 // straight into the permuted shared-memory layout, with the arithmetic of
-// trit_quant_act.  Each thread owns 32-column half-blocks; the second pass
-// re-reads its half-blocks (from L1).  The owner CTA also writes the
-// natural-layout codes (zero tail to K_pad) and the scale.  Returns the scale.
+// trit_quant_act.  Each thread owns 4-column quads q = tid, tid + 256, ...;
+// the first kHoldQ of them stay in registers between the absmax pass and the
+// code pass (the rest are re-read, from L1).  A quad's four codes land in four
+// permuted words of its 32-column half-block (column 8i + j -> word j, byte i).
+// The owner CTA also writes the natural-layout codes (zero tail to K_pad) and
+// the scale.  Returns the scale.
+constexpr int kHoldQ = 4;
 __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool owner,
                                               uint32_t *err, int32_t *s_xsum) {
     __shared__ uint32_t s_red[2][kWarps];
     const int K = E.K;
-    const int nhb = (K + 31) / 32;                   // half-blocks that hold columns
-    const int halves = E.iters * kLanes1 * 2;   // half-blocks staged (>= nhb)
+    const int nq = (K + 3) / 4;                  // quads that hold columns
+    const int sq = E.iters * kLanes1 * 16;       // quads staged (>= nq)
     const float *x = E.xf;
     const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
-    auto load4 = [&](int c) -> float4 {   // columns c..c+3, zero past K
+    auto load4 = [&](int q) -> float4 {   // columns 4q..4q+3, zero past K
+        const int c = 4 * q;
         if (vec && c + 4 <= K) return *reinterpret_cast<const float4 *>(x + c);
         float4 f;
         f.x = c + 0 < K ? x[c + 0] : 0.0f;
@@ -377,15 +385,20 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
         return f;
     };
     uint32_t amax = 0, bad = 0;
-    for (int hb = threadIdx.x; hb < nhb; hb += kThreads) {
+    auto scan = [&](const float4 &f) {
+        bad |= !isfinite(f.x) | !isfinite(f.y) | !isfinite(f.z) | !isfinite(f.w);
+        amax = max(amax, max(max(quant_abs_bits(f.x), quant_abs_bits(f.y)),
+                             max(quant_abs_bits(f.z), quant_abs_bits(f.w))));
+    };
+    float4 held[kHoldQ];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 f = load4(hb * 32 + 4 * q);
-            bad |= !isfinite(f.x) | !isfinite(f.y) | !isfinite(f.z) | !isfinite(f.w);
-            amax = max(amax, max(max(quant_abs_bits(f.x), quant_abs_bits(f.y)),
-                                 max(quant_abs_bits(f.z), quant_abs_bits(f.w))));
-        }
+    for (int r = 0; r < kHoldQ; ++r) {
+        const int q = int(threadIdx.x) + r * kThreads;
+        held[r] = q < nq ? load4(q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int r = 0; r < kHoldQ; ++r) scan(held[r]);
+    for (int q = int(threadIdx.x) + kHoldQ * kThreads; q < nq; q += kThreads) scan(load4(q));
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
         amax = max(amax, __shfl_xor_sync(~0u, amax, o));
@@ -406,26 +419,27 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
     const QuantScale qs = quant_scale(amax, bad != 0);
     const int64_t Kp = beats_per_row(K) * 64;
     int32_t xsum = 0;
-    for (int hb = threadIdx.x; hb < halves; hb += kThreads) {
-        uint32_t in[8];
+    auto emit = [&](int q, const float4 &f) {
+        const uint32_t w = pack4(quant_code(f.x, qs), quant_code(f.y, qs), quant_code(f.z, qs),
+                                 quant_code(f.w, qs));
+        xsum = dp4a_ss(w, 0x01010101u, xsum);
+        if (owner && E.x_i8_out && int64_t(q) * 4 < Kp)
+            *reinterpret_cast<uint32_t *>(E.x_i8_out + int64_t(q) * 4) = w;
+        const int hb = q >> 3, k = q & 7;
+        uint8_t *dst = reinterpret_cast<uint8_t *>(xs + (hb >> 1) * kXBeatWords + (hb & 1) * 8 +
+                                                   4 * (k & 1)) + (k >> 1);
+        dst[0] = uint8_t(w);
+        dst[4] = uint8_t(w >> 8);
+        dst[8] = uint8_t(w >> 16);
+        dst[12] = uint8_t(w >> 24);
+    };
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 f = hb < nhb ? load4(hb * 32 + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
-            in[q] = pack4(quant_code(f.x, qs), quant_code(f.y, qs), quant_code(f.z, qs),
-                          quant_code(f.w, qs));
-            xsum = dp4a_ss(in[q], 0x01010101u, xsum);
-        }
-        if (owner && E.x_i8_out && int64_t(hb) * 32 < Kp) {
-            uint4 *o = reinterpret_cast<uint4 *>(E.x_i8_out + int64_t(hb) * 32);
-            o[0] = make_uint4(in[0], in[1], in[2], in[3]);
-            o[1] = make_uint4(in[4], in[5], in[6], in[7]);
-        }
-        uint32_t out[8];
-        permute_block(in, out);
-        uint32_t *dst = xs + (hb >> 1) * kXBeatWords + (hb & 1) * 8;
-        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    for (int r = 0; r < kHoldQ; ++r) {
+        const int q = int(threadIdx.x) + r * kThreads;
+        if (q < sq) emit(q, held[r]);
     }
+    for (int q = int(threadIdx.x) + kHoldQ * kThreads; q < sq; q += kThreads)
+        emit(q, q < nq ? load4(q) : make_float4(0.f, 0.f, 0.f, 0.f));
     publish_xsum(xsum, s_xsum);
     if (owner && threadIdx.x == 0) {
         if (E.x_scale) *const_cast<float *>(E.x_scale) = qs.a;
@@ -1080,6 +1094,190 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
 }
 
+// 16-byte asynchronous copy global -> shared (cached in L2 only); completes at
+// the issuing thread's cpa_wait_all, visible to that thread.
+__device__ __forceinline__ void cpa16(void *smem, const void *gmem) {
+    const uint32_t sa = uint32_t(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Small M = 1 launches, every warp one group at most (the per-matvec launches
+// of a dependency-ordered token).  Each lane copies all of its group's beats
+// into shared memory at once (cp.async), so the product waits for one memory
+// round trip, not one per ring refill.  Where every entry's planes are marked
+// ready (complete before the preceding kernel was launched) the copies start as
+// soon as the CTA is resident -- under programmatic serialisation while the
+// preceding grid still runs -- and after griddepcontrol.wait only the staging
+// of the activations and the products out of shared memory remain; otherwise
+// they start after the wait.  Groups are
+// numbered across the list (Entry.cost_begin: the entry's first group; the
+// list's total_cost: all groups); warp w of CTA b takes group 8b + w.  Shared
+// memory: the staged activations (xs_words), then per warp iters x 32 lanes x
+// 16 bytes of planes, lane-interleaved so each step's reads are contiguous.
+__global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(const __grid_constant__ List L) {
+    extern __shared__ __align__(16) uint32_t xs[];
+    __shared__ int32_t s_xsum[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rs = lane / kLanes1, bs = lane % kLanes1;
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int max_iters = L.xs_words / (kLanes1 * kXBeatWords);
+    uint4 *pl = reinterpret_cast<uint4 *>(xs + L.xs_words) + (warp * max_iters) * 32 + lane;
+    const int64_t G = L.total_cost;
+    const int64_t cta0 = int64_t(blockIdx.x) * kWarps;
+    auto entry_of = [&](int64_t gw) {   // last entry whose first group is <= gw
+        int a = 0, b = L.count - 1;
+        while (a < b) {
+            const int mid = (a + b + 1) >> 1;
+            if (L.e[mid].cost_begin <= gw) a = mid;
+            else b = mid - 1;
+        }
+        return a;
+    };
+    const int64_t gw = cta0 + warp;
+    const int we = gw < G ? entry_of(gw) : -1;
+    auto copy_planes = [&]() {
+        if (we < 0) return;
+        const Entry &E = L.e[we];
+        const int64_t r = (gw - E.cost_begin) * kRowsPerGroup + rs;
+        const uint4 *rp = E.planes + (r < E.N ? r : E.N - 1) * int64_t(E.bstride);
+        // beat of step t: bs + 4t, clamped to the row's last beat (the staged
+        // activations past the row's end are zero)
+        for (int t = 0; t < E.iters; ++t) {
+            const int beat = bs + kLanes1 * t;
+            cpa16(pl + t * 32, rp + (beat < E.B ? beat : E.B - 1));
+        }
+        cpa_commit();
+    };
+    // planes written by the preceding kernel are visible only after the wait
+    const bool early = L.flags & 1;
+    if (early) copy_planes();
+    const int64_t last = cta0 + kWarps - 1 < G ? cta0 + kWarps - 1 : G - 1;
+    const int e0 = entry_of(cta0), e1 = entry_of(last);
+    uint32_t viol = 0;
+    for (int e = e0; e <= e1; ++e) {
+        const Entry &E = L.e[e];
+        if (e == e0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (!early) copy_planes();
+        } else {
+            __syncthreads();   // the previous entry's readers are done with xs
+        }
+        const bool owner = E.cost_begin >= cta0;   // this CTA holds the entry's group 0
+        float xsc;
+        if (E.xf) {
+            xsc = stage_x_fp32(E, xs, owner, L.err, s_xsum);
+        } else {
+            stage_x<1>(E, xs, s_xsum);
+            xsc = E.x_scale ? E.x_scale[0] : L.x_scale_val;
+        }
+        __syncthreads();
+        const int32_t xsum = read_xsum(s_xsum);
+        if (we != e) continue;
+        cpa_wait_all();
+        const uint4 *xb = reinterpret_cast<const uint4 *>(xs) + bs * kXBeatVec;
+        int acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0;
+#pragma unroll 2
+        for (int t = 0; t < E.iters; ++t) {
+            const uint4 v = pl[t * 32];
+            viol |= (v.x & v.z) | (v.y & v.w);
+            const uint4 *X = xb + t * (kLanes1 * kXBeatVec);
+            const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
+            const uint32_t xl[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t xh[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+            mac_codes(v.x, v.z, xl, acc);
+            mac_codes(v.y, v.w, xh, acc);
+        }
+        const int32_t y = row_sum1(codes_total(acc)) - xsum;
+        const int64_t row = (gw - E.cost_begin) * kRowsPerGroup + rs;
+        if (bs == 0 && row < E.N) {
+            if (E.acc) {
+                atomicAdd(E.acc + row, y);
+            } else {
+                if (E.y_i32) E.y_i32[row] = y;
+                if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, xsc);
+            }
+        }
+    }
+    if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
+}
+
+// Shared memory a pre-loading launch may take (the staged activations and
+// every warp's planes); larger lists take the streaming kernel.
+#ifndef TRIT_PRE_SMEM_MAX
+#define TRIT_PRE_SMEM_MAX (200 * 1024)
+#endif
+
+// Launch entries[0..n) (M = 1, no IntMlp rows) on the pre-loading kernel when
+// every entry holds whole rows and the list's groups fit one resident wave with
+// one group per warp.  Returns false (nothing launched) otherwise.
+bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
+                     float x_scale_val, cudaError_t &status) {
+#if TRIT_PRE_SMEM_MAX <= 0
+    return false;
+#else
+    int64_t groups = 0;
+    int max_iters = 1;
+    bool early = true;
+    for (int i = 0; i < n; ++i) {
+        if (entries[i].B != entries[i].bstride || rows_of(entries[i]) != 1) return false;
+        early = early && (entries[i].mrows & kPlanesReady) != 0;
+        groups += entries[i].groups;
+        if (entries[i].iters > max_iters) max_iters = entries[i].iters;
+    }
+    const int xs_words = max_iters * kLanes1 * kXBeatWords;
+    const size_t smem = size_t(xs_words) * 4 + size_t(kWarps) * max_iters * 32 * 16;
+    if (smem > size_t(TRIT_PRE_SMEM_MAX)) return false;
+    const int64_t grid = (groups + kWarps - 1) / kWarps;
+    static thread_local size_t last_smem = ~size_t(0);
+    static thread_local int last_dev = -1, last_occ = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (smem != last_smem || dev != last_dev) {
+        status = cudaFuncSetAttribute(select_accumulate_pre_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (status != cudaSuccess) return true;
+        int occ = 0;
+        status = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_accumulate_pre_kernel,
+                                                               kThreads, smem);
+        if (status != cudaSuccess) return true;
+        last_occ = occ;
+        last_smem = smem;
+        last_dev = dev;
+    }
+    if (grid > int64_t(last_occ) * device_sm_count()) return false;
+    static thread_local List L;
+    L.count = n;
+    L.err = err;
+    L.x_scale_val = x_scale_val;
+    L.flags = early ? 1 : 0;
+    for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = MlpDesc{};
+    int64_t g = 0;
+    for (int i = 0; i < n; ++i) {
+        L.e[i] = entries[i];
+        L.e[i].cost_begin = g;
+        g += entries[i].groups;
+    }
+    L.total_cost = groups;
+    L.xs_words = xs_words;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    status = cudaLaunchKernelEx(&cfg, select_accumulate_pre_kernel, L);
+    return true;
+#endif
+}
+
 template <int MT>
 int occupancy(size_t smem) {
     // cached per (shared-memory size, device); sizes repeat from call to call
@@ -1101,11 +1299,15 @@ int occupancy(size_t smem) {
 template <int MT>
 cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
                         const MlpDesc *mlp = nullptr, int nmlp = 0, float x_scale_val = 0.0f) {
+    if (MT == 1 && nmlp == 0) {
+        cudaError_t st = cudaSuccess;
+        if (launch_list_pre(entries, n, err, s, x_scale_val, st)) return st;
+    }
     static thread_local List L;   // host staging for the by-value parameter block
     L.count = n;
     L.err = err;
     L.x_scale_val = x_scale_val;
-    L.pad_ = 0;
+    L.flags = 0;
     for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = i < nmlp ? mlp[i] : MlpDesc{};
     int64_t cost = 0, groups = 0;
     int max_iters = 1;
@@ -1178,7 +1380,7 @@ Entry make_entry(const ProjDev &p, int64_t m0, int mrows, int64_t b0, int64_t nb
     E.B = int32_t(nb);
     E.iters = int32_t((nb + lanes - 1) / lanes);
     E.bstride = p.B;
-    E.mrows = mrows;
+    E.mrows = mrows | (p.planes_ready ? kPlanesReady : 0);
     E.gcost = E.iters * (nb == 108 ? TRIT_COST_108 : 100);
     E.w_scale = p.w_scale;
     return E;

@@ -292,6 +292,7 @@ struct ProjDev {            // one product as a kernel sees it
     int32_t K, B;
     float w_scale;
     float x_scale_val;      // the input scale when x_scale is NULL (M = 1 integer path only)
+    bool planes_ready;      // TRIT_PROJ_PLANES_READY: planes may be read before the grid dependency
 };
 
 // One IntMlp down projection (M = 1): its activation row is formed in the

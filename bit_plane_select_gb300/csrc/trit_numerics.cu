@@ -104,6 +104,10 @@ __global__ void __launch_bounds__(NT) intmlp_quant_kernel(const int32_t *ag, con
     constexpr int kNThreads = NT;
     constexpr int kNWarps = NT / 32;
     __shared__ uint64_t red[2][kNWarps];
+    // launched with programmatic serialisation: the next launch may start its
+    // own set-up now; the gate and up outputs are read after the preceding grid
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const int32_t *gr = ag + m * N, *ur = au + m * N;
         trit_u128 amax = 0;
@@ -207,13 +211,21 @@ cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M,
                                 float w_g, float w_u, const float *x_scale, int8_t *q,
                                 float *h_scale, cudaStream_t s) {
     const int64_t ldq = beats_per_row(N) * 64;
-    if (M <= int64_t(device_sm_count()))
-        intmlp_quant_kernel<kIntMlpThreadsFew><<<int(M), kIntMlpThreadsFew, 0, s>>>(
-            ag, au, M, N, ldq, w_g, w_u, x_scale, q, h_scale);
-    else
-        intmlp_quant_kernel<kNThreads><<<rows_grid(M), kNThreads, 0, s>>>(ag, au, M, N, ldq, w_g, w_u,
-                                                                           x_scale, q, h_scale);
-    return cudaGetLastError();
+    const bool few = M <= int64_t(device_sm_count());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(few ? int(M) : rows_grid(M)));
+    cfg.blockDim = dim3(few ? kIntMlpThreadsFew : kNThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (few)
+        return cudaLaunchKernelEx(&cfg, intmlp_quant_kernel<kIntMlpThreadsFew>, ag, au, M, N, ldq,
+                                  w_g, w_u, x_scale, q, h_scale);
+    return cudaLaunchKernelEx(&cfg, intmlp_quant_kernel<kNThreads>, ag, au, M, N, ldq, w_g, w_u,
+                              x_scale, q, h_scale);
 }
 
 }  // namespace trit

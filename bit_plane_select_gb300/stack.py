@@ -201,17 +201,21 @@ class LayerChain:
             L["a_gate"] = torch.zeros(Nf, dtype=torch.int32, device=dev)
             L["a_up"] = torch.zeros(Nf, dtype=torch.int32, device=dev)
             L["s_gu"] = torch.zeros(1, dtype=torch.float32, device=dev)
+            # the planes are packed (and the stream synchronised) here, before any
+            # launch of the chain: every list may read them ahead of its grid dependency
             L["qkv"] = QProjList([(P[n], S[n], L["x"], None, None, L["y_" + n], L["f_" + n])
-                                  for n in ("q", "k", "v")])
-            L["o"] = QProjList([(P["o"], S["o"], L["f_q"], None, None, L["y_o"], L["f_o"])])
+                                  for n in ("q", "k", "v")], planes_ready=True)
+            L["o"] = QProjList([(P["o"], S["o"], L["f_q"], None, None, L["y_o"], L["f_o"])],
+                               planes_ready=True)
             L["gu"] = QProjList([(P["gate"], S["gate"], L["f_o"], None, L["s_gu"], L["a_gate"], None),
-                                 (P["up"], S["up"], L["f_o"], None, None, L["a_up"], None)])
+                                 (P["up"], S["up"], L["f_o"], None, None, L["a_up"], None)],
+                                planes_ready=True)
             L["down"] = MlpProjList([(P["down"], S["down"], L["a_gate"], L["a_up"], L["s_gu"],
                                       S["gate"], S["up"], None, None, L["y_down"], L["f_down"])])
             L["h"] = torch.zeros(k_pad(Kd), dtype=torch.int8, device=dev)
             L["s_h"] = torch.zeros(1, dtype=torch.float32, device=dev)
             L["down_i8"] = ProjList([(P["down"], S["down"], L["h"], L["s_h"], Kd, L["y_down"],
-                                      L["f_down"])])
+                                      L["f_down"])], planes_ready=True)
             self.layers.append(L)
 
     @property

@@ -193,6 +193,19 @@ TRIT_API trit_status trit_gemv(const uint8_t *planes, float w_scale, const int8_
                                float x_scale, int64_t N, int64_t K, int32_t *y_i32,
                                float *y_f32, uint32_t *err_flag, trit_stream_t stream);
 
+/*
+ * Bits of trit_proj.flags and trit_qproj.flags (any other bit: TRIT_E_ARG).
+ *
+ * TRIT_PROJ_PLANES_READY: the entry's planes were complete before the kernel
+ * that precedes this call on `stream` was launched (for instance packed, then
+ * the stream synchronised), and nothing writes them while the call runs.  A
+ * list whose every entry sets it may be launched with programmatic dependent
+ * launch reading its planes into shared memory while the preceding kernel
+ * still runs; the activations are read, and anything is written, only after
+ * that kernel has completed.  Results are identical with or without the bit.
+ */
+#define TRIT_PROJ_PLANES_READY 1u
+
 /* One product of a list: the arguments of trit_gemm, all device pointers. */
 typedef struct trit_proj {
     const uint8_t *planes;
@@ -202,7 +215,7 @@ typedef struct trit_proj {
     float *y_f32;        /* may be NULL (not both) */
     int64_t M, N, K;
     float w_scale;
-    uint32_t reserved;   /* must be 0 */
+    uint32_t flags;      /* 0 or TRIT_PROJ_PLANES_READY */
 } trit_proj;
 
 /*
@@ -227,7 +240,7 @@ typedef struct trit_qproj {
     float *y_f32;        /* may be NULL (not both) */
     int64_t N, K;
     float w_scale;
-    uint32_t reserved;   /* must be 0 */
+    uint32_t flags;      /* 0 or TRIT_PROJ_PLANES_READY */
 } trit_qproj;
 
 /*

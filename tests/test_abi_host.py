@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(trit):
     lib = ctypes.CDLL(trit.library_path())
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert trit.lib().trit_abi_version() == 3
+    assert trit.lib().trit_abi_version() == 4
 
 
 def test_struct_layouts(trit):
@@ -128,7 +128,7 @@ def test_argument_errors_are_rejected_on_the_host(trit):
     assert L.trit_gemm_many(null, 1, p, s) == 1
     lst = (trit.TritProj * 2)(trit.TritProj(p, p, p, p, p, 1, 8, 64, 1.0, 0),
                               trit.TritProj(p, p, p, p, p, 1, 8, 64, 1.0, 7))
-    assert L.trit_gemm_many(ctypes.cast(lst, ctypes.c_void_p), 2, p, s) == 1   # reserved != 0
+    assert L.trit_gemm_many(ctypes.cast(lst, ctypes.c_void_p), 2, p, s) == 1   # unknown flag bits
     assert L.trit_gemm_many(ctypes.cast(lst, ctypes.c_void_p), 0, p, s) == 1
     # trit_quant_act(x, M, K, x_i8, x_scale, err, stream)
     assert L.trit_quant_act(p, 2, 0, p, p, p, s) == 2
@@ -194,7 +194,7 @@ def test_argument_errors_of_the_other_entry_points(trit):
     # trit_quant_gemv_many(list, count, err, stream)
     Q = trit.TritQProj
     good_q = Q(p, p, p, p, p, p, 8, 64, 1.0, 0)
-    for bad, code in [(Q(p, p, p, p, p, p, 8, 64, 1.0, 1), 1),
+    for bad, code in [(Q(p, p, p, p, p, p, 8, 64, 1.0, 2), 1),   # unknown flag bit
                       (Q(p, null, p, p, p, p, 8, 64, 1.0, 0), 1),
                       (Q(p, p, odd, p, p, p, 8, 64, 1.0, 0), 1),
                       (Q(p, p, p, p, p, p, 8, trit.MAX_FUSED_K + 1, 1.0, 0), 2),

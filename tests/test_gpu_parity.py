@@ -373,6 +373,78 @@ def test_gemm_many_mixed_list(t, orc):
         assert_f32_close(host(f), rf)
 
 
+# ---- small lists: every warp one group, planes copied to shared memory -------
+
+def _m1_list(t, orc, rng, shapes, ready, fused):
+    """M = 1 products of the given (N, K) shapes in one list call, against the
+    oracle; fused: fp32 rows through trit_quant_gemv_many, else int8 rows
+    through trit_gemm_many."""
+    entries, refs = [], []
+    for N, K in shapes:
+        w = synth.ternary(rng, N, K, float(rng.uniform(0.385, 0.508)))
+        ws = float(synth.w_scale(w))
+        planes, _ = t.trit_pack(dev(w), ws)
+        y = torch.empty(N, dtype=torch.int32, device="cuda")
+        f = torch.empty(N, dtype=torch.float32, device="cuda")
+        if fused:
+            x = rng.standard_normal(K).astype(np.float32)
+            q = torch.full((((K + 63) // 64) * 64,), 55, dtype=torch.int8, device="cuda")
+            s = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+            entries.append((planes, ws, dev(x), q, s, y, f))
+            q_ref, s_ref, _ = orc.quant(x[None, :])
+            ry, rf, _ = orc.gemm(orc.pack(w), ws, q_ref, s_ref, K)
+            refs.append((q_ref[0], s_ref, ry[0], rf[0]))
+        else:
+            x = padded_x(rng, 1, K)
+            xs = (rng.random(1) + 0.5).astype(np.float32)
+            entries.append((planes, ws, dev(x), dev(xs), K, y, f))
+            ry, rf, _ = orc.gemm(orc.pack(w), ws, x, xs, K)
+            refs.append((None, None, ry[0], rf[0]))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if ready:
+        torch.cuda.synchronize()
+    if fused:
+        t.trit_quant_gemv_many(t.QProjList(entries, planes_ready=ready), err)
+    else:
+        t.trit_gemm_many(t.ProjList(entries, planes_ready=ready), err)
+    assert int(host(err)[0]) == 0
+    for e, (q_ref, s_ref, ry, rf) in zip(entries, refs):
+        y, f = e[5], e[6]
+        if fused:
+            np.testing.assert_array_equal(host(e[3]), q_ref)
+            np.testing.assert_array_equal(host(e[4]), s_ref)
+        np.testing.assert_array_equal(host(y), ry)
+        np.testing.assert_array_equal(host(f).view(np.uint32), rf.view(np.uint32))
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("ready", [False, True])
+def test_small_list_entry_boundaries(t, orc, ready, fused):
+    """Entries of 1-3 groups, so that CTAs of eight warps hold the ends of
+    several entries (staging each in turn), ragged rows and tails."""
+    rng = synth.rng_for(130, int(ready), int(fused))
+    shapes = [(3, 2560), (9, 2560), (17, 2560), (1, 2560), (8, 2560), (23, 2560), (5, 2560),
+              (64, 2560), (2, 2560)]
+    _m1_list(t, orc, rng, shapes, ready, fused)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("K", [1, 100, 6912, 11000, 12800])
+def test_small_list_row_lengths(t, orc, K, fused):
+    """Rows from one column to past the shared-memory limit of the
+    pre-loading launch (11,000 columns take it, 12,800 the streaming kernel)."""
+    rng = synth.rng_for(131, K, int(fused))
+    _m1_list(t, orc, rng, [(77, K), (1, K), (130, K)], True, fused)
+
+
+@pytest.mark.parametrize("N", [19456, 19464])
+def test_small_list_one_wave_boundary(t, orc, N):
+    """2,432 groups of 2,560 columns fill two CTAs on each of 152 SMs (the
+    pre-loading launch); 2,433 do not and take the streaming kernel."""
+    rng = synth.rng_for(132, N)
+    _m1_list(t, orc, rng, [(N, 2560)], True, True)
+
+
 def test_error_status_raises(t):
     x = torch.zeros((1, 64), dtype=torch.int8, device="cuda")
     planes = torch.zeros((4, 1, 16), dtype=torch.uint8, device="cuda")
@@ -390,10 +462,12 @@ def test_error_status_raises(t):
 FUSED_K = [1, 65, 200, 2560, 6912, 6913, 40000, 73728]
 
 
+@pytest.mark.parametrize("ready", [False, True])
 @pytest.mark.parametrize("K", FUSED_K)
-def test_quant_gemv_many_matches_oracle(t, orc, K):
+def test_quant_gemv_many_matches_oracle(t, orc, K, ready):
     """One launch quantises each fp32 row and multiplies it: codes, scale and
-    products equal the oracle's quantiser followed by its product."""
+    products equal the oracle's quantiser followed by its product -- with the
+    planes read after the grid dependency, or (marked ready) before it."""
     rng = synth.rng_for(120, K)
     rows = quant_cases(rng, K)          # normal, zero, denormal, ties, huge, NaN, Inf rows
     Ns = [37, 8, 5, 64, 129, 3, 250, 17]
@@ -412,7 +486,9 @@ def test_quant_gemv_many_matches_oracle(t, orc, K):
         ry, rf, _ = orc.gemm(orc.pack(w), ws, q_ref, s_ref, K)
         refs.append((q_ref[0], s_ref, ry[0], rf[0], e_ref[0]))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    t.trit_quant_gemv_many(t.QProjList(entries), err)
+    if ready:
+        torch.cuda.synchronize()   # the planes are complete before any preceding kernel
+    t.trit_quant_gemv_many(t.QProjList(entries, planes_ready=ready), err)
     any_bad = any(r[4] for r in refs)
     assert int(host(err)[0]) == (t.ERR_NONFINITE if any_bad else 0)
     for (_, _, _, q, s, y, f), (q_ref, s_ref, ry, rf, _) in zip(entries, refs):
