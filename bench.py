@@ -1144,11 +1144,15 @@ def run_bitcos(args):
 
 
 def run_mlp(args):
-    """The MLP blocks of the 30-layer stack at batch 1 (row f1): per layer, gate
-    and up from one fp32 activation row with the quantiser fused (one launch),
-    then the IntMlp codes of relu(a_gate)^2 a_up and the down product (one
-    launch) -- against the same chain with the standalone IntMlp quantiser
-    between (three launches).  Each step is one token through every layer."""
+    """The MLP blocks of the 30-layer stack at batch 1 (row f1), one token
+    through every layer, three ways with the same bits: "paired" -- gate and
+    up in one launch that also publishes the max|t| partials, then the down
+    product forming the IntMlp codes from them (trit_mlp_gate_up,
+    trit_mlp_down: two launches per layer); "fused" -- gate/up, then every CTA
+    of the down launch forming the codes with its own max|t| pass (two); and
+    "three_launch" -- gate/up, the standalone IntMlp quantiser, the down product
+    of its int8 codes.  Beside them the same 90 products with no dependency:
+    all gate/up in one launch, all down products (int8 codes) in another."""
     import torch
 
     import __graft_entry__
@@ -1162,7 +1166,8 @@ def run_mlp(args):
     ig, iu, idn = names.index("gate"), names.index("up"), names.index("down")
     K, N = synth.PROJECTIONS[ig][2], synth.PROJECTIONS[ig][1]      # 2560, 6912
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    fused, three, keep = [], [], []
+    paired, fused, three, keep = [], [], [], []
+    indep_gu, indep_dn = [], []
     plane_bytes = 0
     for layer in range(args.layers):
         pl, ws = [], []
@@ -1179,12 +1184,26 @@ def run_mlp(args):
         hs = torch.empty(1, dtype=torch.float32, device=dev)
         y = torch.empty(K, dtype=torch.int32, device=dev)
         yf = torch.empty(K, dtype=torch.float32, device=dev)
-        gu = t.QProjList([(pl[0], ws[0], x, None, xs, a_g, None), (pl[1], ws[1], x, None, None, a_u, None)])
+        tmax = torch.empty(t.trit_mlp_tmax_bytes(N), dtype=torch.uint8, device=dev)
+        gu_e = [(pl[0], ws[0], x, None, xs, a_g, None), (pl[1], ws[1], x, None, None, a_u, None)]
+        gu = t.QProjList(gu_e, planes_ready=True)
         dn = t.MlpProjList([(pl[2], ws[2], a_g, a_u, xs, ws[0], ws[1], None, None, y, yf)])
-        dn3 = t.ProjList([(pl[2], ws[2], h, hs, N, y, yf)])
+        dn3_e = [(pl[2], ws[2], h, hs, N, y, yf)]
+        dn3 = t.ProjList(dn3_e, planes_ready=True)
+        paired.append(t.MlpBlockList([(pl[0], pl[1], pl[2], ws[0], ws[1], ws[2], x, xs, a_g, a_u,
+                                       tmax, None, None, y, yf)], planes_ready=True))
         fused.append((gu, dn))
         three.append((gu, a_g, a_u, ws[0], ws[1], xs, h, hs, dn3))
-        keep.append((pl, x, a_g, a_u, xs, h, hs, y, yf))
+        indep_gu += gu_e
+        indep_dn += dn3_e
+        keep.append((pl, x, a_g, a_u, xs, h, hs, y, yf, tmax))
+    torch.cuda.synchronize(dev)   # the planes are complete before any launch below
+    indep = (t.QProjList(indep_gu, planes_ready=True), t.ProjList(indep_dn, planes_ready=True))
+
+    def step_paired():
+        for bl in paired:
+            t.trit_mlp_gate_up(bl, err)
+            t.trit_mlp_down(bl, err)
 
     def step_fused():
         for gu, dn in fused:
@@ -1197,9 +1216,14 @@ def run_mlp(args):
             t.trit_intmlp_quant(a_g, a_u, wg, wu, xs, h, hs)
             t.trit_gemm_many(dn3, err)
 
+    def step_indep():
+        t.trit_quant_gemv_many(indep[0], err)
+        t.trit_gemm_many(indep[1], err)
+
     steps = max(20, args.steps // 100)
-    eager_f = _timed(step_fused, steps, args.warmup, stream)
-    eager_3 = _timed(step_three, steps, args.warmup, stream)
+    eager = {name: _timed(fn, steps, args.warmup, stream)
+             for name, fn in (("paired", step_paired), ("fused", step_fused),
+                              ("three_launch", step_three))}
 
     # the launches of one step captured in a CUDA graph: replay time is device
     # time, free of the per-call host work of the eager loop above
@@ -1212,17 +1236,25 @@ def run_mlp(args):
             fn()
         return _timed(g.replay, steps, args.warmup, stream)
 
-    ms_f = graph_ms(step_fused)
-    ms_3 = graph_ms(step_three)
+    ms = {"paired": graph_ms(step_paired), "fused": graph_ms(step_fused),
+          "three_launch": graph_ms(step_three)}
+    ms_i = graph_ms(step_indep)
+    launches = {"paired": 2, "fused": 2, "three_launch": 3}
     act_bytes = args.layers * (K * 4 + 4 + 2 * N * 4 * 2 + K * 8)
     nbytes = plane_bytes + act_bytes
-    out = {"metric": "MLP blocks of the 30-layer stack, batch 1 (gate+up fused quantise; IntMlp + down)",
-           "unit": "tok/s", "value": round(1e3 / ms_f, 1),
-           "ms_per_step": round(ms_f, 4), "GBs": round(nbytes / (ms_f * 1e-3) / 1e9, 1),
+    ms_p = ms["paired"]
+    out = {"metric": "MLP blocks of the 30-layer stack, batch 1 (gate+up with max|t| partials; "
+                     "IntMlp codes + down)",
+           "unit": "tok/s", "value": round(1e3 / ms_p, 1),
+           "ms_per_step": round(ms_p, 4), "GBs": round(nbytes / (ms_p * 1e-3) / 1e9, 1),
            "launches_per_step": 2 * args.layers, "timing": "CUDA graph of one step, replayed",
-           "three_launch_path": {"ms_per_step": round(ms_3, 4), "tok_per_s": round(1e3 / ms_3, 1),
-                                 "launches_per_step": 3 * args.layers},
-           "eager_ms_per_step": {"fused": round(eager_f, 4), "three_launch": round(eager_3, 4)},
+           "forms": {k: {"ms_per_step": round(v, 4), "tok_per_s": round(1e3 / v, 1),
+                         "launches_per_step": launches[k] * args.layers,
+                         "eager_ms_per_step": round(eager[k], 4)} for k, v in ms.items()},
+           "independent_products": {"ms_per_step": round(ms_i, 4), "launches_per_step": 2,
+                                    "what": "the same 60 gate/up and 30 down products with no "
+                                            "dependency between them: two launches"},
+           "chain_over_independent": round(ms_p / ms_i, 2),
            "algorithmic_bytes_per_step": nbytes, "err_flag": int(err.item()),
            "config": {"workload": "bitnet-2b4t-30layer-mlp-batch1", "layers": args.layers,
                       "gate_up": [N, K], "down": [K, N]}}
@@ -1258,11 +1290,13 @@ def run_decode_ordered(args):
     del weights
     steps = max(50, min(args.steps, 2000))
     forms = {}
-    # both forms of the MLP stage on the same chain: the IntMlp quantiser as a
-    # launch of its own (five launches per layer), or inside the down product (four)
+    # the three forms of the MLP stage on the same chain: gate/up publishing the
+    # max|t| partials, then the down product forming the codes ("paired", four
+    # launches per layer); the IntMlp quantiser as a launch of its own ("split",
+    # five); every down CTA forming the codes, max|t| pass included ("fused", four)
     with ClockSampler(0) as clk:
-        for fused in (False, True):
-            chain.fused_mlp = fused
+        for form in LayerChain.MLP_FORMS:
+            chain.mlp_form = form
             for _ in range(3):
                 chain.step()
             torch.cuda.synchronize()
@@ -1272,7 +1306,7 @@ def run_decode_ordered(args):
                 chain.step()
             ms = _timed(g.replay, steps, args.warmup, stream)
             eager = _timed(chain.step, max(20, steps // 10), args.warmup, stream)
-            forms["fused" if fused else "split"] = {
+            forms[form] = {
                 "us_per_token": round(ms * 1e3, 2), "launches_per_token": chain.launches_per_step,
                 "us_per_launch": round(ms * 1e3 / chain.launches_per_step, 3),
                 "eager_us_per_token": round(eager * 1e3, 2)}
@@ -1292,8 +1326,9 @@ def run_decode_ordered(args):
            "timing": f"CUDA graph of one token replayed {steps} times", "err_flag": int(chain.err.item()),
            "clocks": clk.summary(),
            "config": {"workload": "bitnet-2b4t-30layer-decode-ordered-batch1", "layers": args.layers,
-                      "order": "per layer: [q,k,v] <- x; [o] <- q; [gate,up] <- o; "
-                               "IntMlp quantiser -> [down] (split) or IntMlp+[down] (fused)"}}
+                      "order": "per layer: [q,k,v] <- x; [o] <- q; [gate,up] <- o; IntMlp + [down] "
+                               "<- gate,up (paired: max|t| partials from the gate/up launch; split: "
+                               "a quantiser launch between; fused: max|t| in every down CTA)"}}
     print(json.dumps(out), flush=True)
 
 

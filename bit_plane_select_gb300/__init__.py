@@ -30,6 +30,8 @@ __all__ = [
     "TritQProj", "MAX_FUSED_K", "trit_gemm_noalloc", "NOALLOC_SCRATCH_BYTES",
     "trit_quant_act_folded", "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
     "trit_intmlp_gemv_many", "MlpProjList", "TritMlpProj", "PROBE_KINDS", "trit_issue_probe",
+    "PLANES_READY", "TritMlpBlock", "MlpBlockList", "trit_mlp_tmax_bytes", "trit_mlp_gate_up",
+    "trit_mlp_down",
 ]
 
 ERR_P1 = 1
@@ -71,6 +73,16 @@ class TritMlpProj(ctypes.Structure):
                 ("h_i8", ctypes.c_void_p), ("h_scale", ctypes.c_void_p),
                 ("y_i32", ctypes.c_void_p), ("y_f32", ctypes.c_void_p), ("N", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("w_scale", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+
+
+class TritMlpBlock(ctypes.Structure):
+    _fields_ = [("gate_planes", ctypes.c_void_p), ("up_planes", ctypes.c_void_p),
+                ("down_planes", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("x_scale", ctypes.c_void_p), ("a_gate", ctypes.c_void_p), ("a_up", ctypes.c_void_p),
+                ("tmax", ctypes.c_void_p), ("h_i8", ctypes.c_void_p), ("h_scale", ctypes.c_void_p),
+                ("y_i32", ctypes.c_void_p), ("y_f32", ctypes.c_void_p), ("K", ctypes.c_int64),
+                ("F", ctypes.c_int64), ("N", ctypes.c_int64), ("w_gate", ctypes.c_float),
+                ("w_up", ctypes.c_float), ("w_down", ctypes.c_float), ("flags", ctypes.c_uint32)]
 
 
 class TritBitcosProj(ctypes.Structure):
@@ -121,6 +133,10 @@ def lib():
         L.trit_gemm_many.argtypes = [p, i32, p, p]
         L.trit_quant_gemv_many.argtypes = [p, i32, p, p]
         L.trit_intmlp_gemv_many.argtypes = [p, i32, p, p]
+        L.trit_mlp_tmax_bytes.restype = i64
+        L.trit_mlp_tmax_bytes.argtypes = [i64]
+        L.trit_mlp_gate_up.argtypes = [p, i32, p, p]
+        L.trit_mlp_down.argtypes = [p, i32, p, p]
         L.trit_gemm_noalloc.argtypes = [p, f32, p, p, i64, i64, i64, p, p, p, p]
         L.trit_quant_act_folded.argtypes = [p, p, i64, i64, f32, p, p, p, p]
         L.trit_intmlp_quant.argtypes = [p, p, i64, i64, f32, f32, p, p, p, p]
@@ -134,7 +150,7 @@ def lib():
                      "trit_quant_gemv_many", "trit_gemm_noalloc", "trit_quant_act_folded",
                      "trit_intmlp_quant", "trit_check_div127", "trit_read_probe",
                      "trit_intmlp_gemv_many", "trit_bitcos_pack", "trit_bitcos_gemv_many",
-                     "trit_issue_probe"):
+                     "trit_issue_probe", "trit_mlp_gate_up", "trit_mlp_down"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -480,6 +496,55 @@ def trit_intmlp_gemv_many(mlist: MlpProjList, err_flag: torch.Tensor, stream=Non
     _check(lib().trit_intmlp_gemv_many(ctypes.cast(mlist.array, ctypes.c_void_p), mlist.count,
                                        _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
            "trit_intmlp_gemv_many")
+
+
+def trit_mlp_tmax_bytes(F: int) -> int:
+    return int(lib().trit_mlp_tmax_bytes(F))
+
+
+class MlpBlockList:
+    """A prepared host array of trit_mlp_block entries: batch-1 MLP blocks in
+    two launches (trit_mlp_gate_up, then trit_mlp_down).  entries: (gate
+    planes, up planes, down planes, w_gate, w_up, w_down, x fp32 [K], x_scale
+    out [1], a_gate out int32 [F], a_up out int32 [F], tmax workspace (uint8,
+    trit_mlp_tmax_bytes(F)), h_i8 out or None, h_scale out or None, y_i32 or
+    None, y_f32 or None).  planes_ready sets PLANES_READY on every block."""
+
+    def __init__(self, entries, planes_ready: bool = False):
+        flags = PLANES_READY if planes_ready else 0
+        self._keep = []
+        items = []
+        for (gp, upl, dp, w_gate, w_up, w_down, x, x_scale, a_gate, a_up, tmax, h_i8, h_scale,
+             y_i32, y_f32) in entries:
+            F, Kp = gp.shape[0], gp.shape[1]
+            N = dp.shape[0]
+            K = x.shape[-1]
+            if upl.shape[0] != F or k_pad(K) // 64 != Kp or dp.shape[1] != k_pad(F) // 64:
+                raise ValueError("gate, up and down planes do not chain")
+            items.append(TritMlpBlock(
+                _dev(gp, torch.uint8, "gate_planes"), _dev(upl, torch.uint8, "up_planes"),
+                _dev(dp, torch.uint8, "down_planes"), _dev(x, torch.float32, "x"),
+                _dev(x_scale, torch.float32, "x_scale"), _dev(a_gate, torch.int32, "a_gate"),
+                _dev(a_up, torch.int32, "a_up"), _dev(tmax, torch.uint8, "tmax"),
+                _dev(h_i8, torch.int8, "h_i8", True), _dev(h_scale, torch.float32, "h_scale", True),
+                _dev(y_i32, torch.int32, "y_i32", True), _dev(y_f32, torch.float32, "y_f32", True),
+                K, F, N, float(w_gate), float(w_up), float(w_down), flags))
+            self._keep.append((gp, upl, dp, x, x_scale, a_gate, a_up, tmax, h_i8, h_scale,
+                               y_i32, y_f32))
+        self.count = len(items)
+        self.array = (TritMlpBlock * self.count)(*items)
+
+
+def trit_mlp_gate_up(blist: MlpBlockList, err_flag: torch.Tensor, stream=None):
+    _check(lib().trit_mlp_gate_up(ctypes.cast(blist.array, ctypes.c_void_p), blist.count,
+                                  _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_mlp_gate_up")
+
+
+def trit_mlp_down(blist: MlpBlockList, err_flag: torch.Tensor, stream=None):
+    _check(lib().trit_mlp_down(ctypes.cast(blist.array, ctypes.c_void_p), blist.count,
+                               _dev(err_flag, torch.int32, "err_flag"), _stream(stream)),
+           "trit_mlp_down")
 
 
 def trit_quant_act_many(alist: ActList, err_flag: torch.Tensor, stream=None):

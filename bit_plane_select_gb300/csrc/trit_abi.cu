@@ -178,6 +178,87 @@ int device_sm_count() {
     return sms > 0 ? sms : 1;
 }
 
+// ---- MLP blocks in two launches ----------------------------------------------------
+
+namespace {
+trit_status check_mlp_block(const trit_mlp_block &b) {
+    if (!b.gate_planes || !b.up_planes || !b.down_planes || !b.x || !b.x_scale || !b.a_gate ||
+        !b.a_up || !b.tmax || (!b.y_i32 && !b.y_f32) || (b.flags & ~TRIT_PROJ_PLANES_READY) != 0)
+        return TRIT_E_ARG;
+    if (!aligned(b.gate_planes, 16) || !aligned(b.up_planes, 16) || !aligned(b.down_planes, 16) ||
+        !aligned(b.x, 4) || !aligned(b.x_scale, 4) || !aligned(b.a_gate, 16) ||
+        !aligned(b.a_up, 16) || !aligned(b.tmax, 16) || !aligned(b.h_i8, 16) ||
+        !aligned(b.h_scale, 4) || !aligned(b.y_i32, 4) || !aligned(b.y_f32, 4))
+        return TRIT_E_ARG;
+    if (!cols_ok(b.K) || !rows_ok(b.F) || !cols_ok(b.F) || !rows_ok(b.N) ||
+        b.K > TRIT_MAX_FUSED_K || b.F > TRIT_MAX_FUSED_K)
+        return TRIT_E_SHAPE;
+    for (float w : {b.w_gate, b.w_up, b.w_down})
+        if (!isfinite(w) || !(w > 0.0f)) return TRIT_E_SCALE;
+    return TRIT_OK;
+}
+
+MlpBlockDev mlp_to_dev(const trit_mlp_block &b) {
+    const bool ready = (b.flags & TRIT_PROJ_PLANES_READY) != 0;
+    auto proj = [&](const uint8_t *planes, int64_t N, int64_t K, float w) {
+        ProjDev d;
+        d.planes = reinterpret_cast<const uint4 *>(planes);
+        d.x = nullptr;
+        d.xf = nullptr;
+        d.x_i8_out = nullptr;
+        d.x_scale = nullptr;
+        d.y_i32 = nullptr;
+        d.y_f32 = nullptr;
+        d.M = 1;
+        d.N = N;
+        d.K = int32_t(K);
+        d.B = int32_t(beats_per_row(K));
+        d.w_scale = w;
+        d.x_scale_val = 0.0f;
+        d.planes_ready = ready;
+        return d;
+    };
+    MlpBlockDev m;
+    m.gate = proj(b.gate_planes, b.F, b.K, b.w_gate);
+    m.gate.xf = b.x;
+    m.gate.x_scale = b.x_scale;
+    m.gate.y_i32 = b.a_gate;
+    m.up = proj(b.up_planes, b.F, b.K, b.w_up);
+    m.up.xf = b.x;
+    m.up.y_i32 = b.a_up;
+    m.down = proj(b.down_planes, b.N, b.F, b.w_down);
+    m.down.x_i8_out = b.h_i8;
+    m.down.x_scale = b.h_scale;
+    m.down.y_i32 = b.y_i32;
+    m.down.y_f32 = b.y_f32;
+    m.w_gate = b.w_gate;
+    m.w_up = b.w_up;
+    m.tmax = static_cast<uint64_t *>(b.tmax);
+    return m;
+}
+
+template <typename Launch>
+trit_status run_mlp_blocks(const trit_mlp_block *list, int32_t count, uint32_t *err_flag,
+                           trit_stream_t stream, Launch launch) {
+    if (!list || count <= 0 || !err_flag || !aligned(err_flag, 4)) return TRIT_E_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        const trit_status st = check_mlp_block(list[i]);
+        if (st != TRIT_OK) return st;
+    }
+    trit_status st = check_device();
+    if (st != TRIT_OK) return st;
+    static thread_local MlpBlockDev buf[TRIT_MAX_LIST_PER_LAUNCH];
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int32_t base = 0; base < count; base += TRIT_MAX_LIST_PER_LAUNCH) {
+        const int n = count - base < TRIT_MAX_LIST_PER_LAUNCH ? count - base : TRIT_MAX_LIST_PER_LAUNCH;
+        for (int i = 0; i < n; ++i) buf[i] = mlp_to_dev(list[base + i]);
+        const cudaError_t e = launch(buf, n, err_flag, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return TRIT_OK;
+}
+}  // namespace
+
 }  // namespace trit
 
 using namespace trit;
@@ -301,6 +382,19 @@ TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count,
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return TRIT_OK;
+}
+
+
+TRIT_API int64_t trit_mlp_tmax_bytes(int64_t F) { return F < 1 ? 0 : 16 * mlp_tmax_parts(F); }
+
+TRIT_API trit_status trit_mlp_gate_up(const trit_mlp_block *list, int32_t count,
+                                      uint32_t *err_flag, trit_stream_t stream) {
+    return run_mlp_blocks(list, count, err_flag, stream, launch_mlp_gate_up);
+}
+
+TRIT_API trit_status trit_mlp_down(const trit_mlp_block *list, int32_t count,
+                                   uint32_t *err_flag, trit_stream_t stream) {
+    return run_mlp_blocks(list, count, err_flag, stream, launch_mlp_down);
 }
 
 TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t count,

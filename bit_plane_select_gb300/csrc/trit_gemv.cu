@@ -221,6 +221,11 @@ struct MlpDesc {
     const int32_t *a_gate, *a_up;   // [K] each
     const float *x_scale;           // the gate/up input's activation scale
     float w_gate, w_up;
+    // pre-loading launches: the per-CTA max|t| partials (hi, lo word pairs) a
+    // paired gate/up launch writes and the down launch reduces
+    uint64_t *tmax;
+    int32_t ntmax;
+    int32_t pad_;
 };
 constexpr int kMaxMlp = 8;
 
@@ -366,6 +371,19 @@ __device__ __forceinline__ void stage_x(const Entry &E, uint32_t *xs, int32_t *s
 // The owner CTA also writes the natural-layout codes (zero tail to K_pad) and
 // the scale.  Returns the scale.
 constexpr int kHoldQ = 4;
+// The four codes w (bytes: columns 4q..4q+3) into the permuted layout: column
+// 8i + j of a 32-column half-block goes to word j, byte i.  (Byte stores: a
+// variant gathering whole words with four warp shuffles per lane measured
+// slower.)
+__device__ __forceinline__ void put_quad(uint32_t *xs, int q, uint32_t w) {
+    const int hb = q >> 3, k = q & 7;
+    uint8_t *dst = reinterpret_cast<uint8_t *>(xs + (hb >> 1) * kXBeatWords + (hb & 1) * 8 +
+                                               4 * (k & 1)) + (k >> 1);
+    dst[0] = uint8_t(w);
+    dst[4] = uint8_t(w >> 8);
+    dst[8] = uint8_t(w >> 16);
+    dst[12] = uint8_t(w >> 24);
+}
 __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool owner,
                                               uint32_t *err, int32_t *s_xsum) {
     __shared__ uint32_t s_red[2][kWarps];
@@ -425,13 +443,7 @@ __device__ __forceinline__ float stage_x_fp32(const Entry &E, uint32_t *xs, bool
         xsum = dp4a_ss(w, 0x01010101u, xsum);
         if (owner && E.x_i8_out && int64_t(q) * 4 < Kp)
             *reinterpret_cast<uint32_t *>(E.x_i8_out + int64_t(q) * 4) = w;
-        const int hb = q >> 3, k = q & 7;
-        uint8_t *dst = reinterpret_cast<uint8_t *>(xs + (hb >> 1) * kXBeatWords + (hb & 1) * 8 +
-                                                   4 * (k & 1)) + (k >> 1);
-        dst[0] = uint8_t(w);
-        dst[4] = uint8_t(w >> 8);
-        dst[8] = uint8_t(w >> 16);
-        dst[12] = uint8_t(w >> 24);
+        put_quad(xs, q, w);
     };
 #pragma unroll
     for (int r = 0; r < kHoldQ; ++r) {
@@ -581,6 +593,97 @@ __device__ __forceinline__ void stage_x_intmlp(const Entry &E, const MlpDesc &D,
     // others read it after the staging barrier
     if (threadIdx.x == 0) {
         const float scale = intmlp_scale(hi, lo, D.w_gate, D.w_up, *D.x_scale);
+        *s_scale = scale;
+        if (owner && E.x_scale) *const_cast<float *>(E.x_scale) = scale;
+    }
+}
+
+// 16-byte asynchronous copy global -> shared (cached in L2 only); completes at
+// the issuing thread's cpa_wait_all, visible to that thread.
+__device__ __forceinline__ void cpa16(void *smem, const void *gmem) {
+    const uint32_t sa = uint32_t(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// IntMlp input of a pre-loading launch (M = 1): as stage_x_intmlp, but max|t|
+// is reduced from the D.ntmax per-CTA partials the paired gate/up launch
+// published, so the row is read once: a_gate and a_up are copied into shared
+// memory (rows: iters x 256 int32 each) with every copy in flight together
+// with the partials' loads, and the codes follow the reduction.  The last
+// thread forms the scale (its double-precision factor first); the scale goes
+// to *s_scale, readable after the staging barrier.  The owner CTA also writes
+// the natural-layout codes (zero tail to K_pad) and the scale.
+__device__ __forceinline__ void stage_x_intmlp_parts(const Entry &E, const MlpDesc &D, uint32_t *xs,
+                                                     int32_t *rows, bool owner, int32_t *s_xsum,
+                                                     float *s_scale) {
+    __shared__ uint64_t s_m[2][kWarps];
+    const int K = E.K;
+    const int nq = (K + 3) / 4, sq = E.iters * kLanes1 * 16;
+    int32_t *sg = rows, *su = rows + 4 * sq;
+    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(D.a_gate) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(D.a_up) & 15) == 0);
+    if (vec) {
+        for (int q = threadIdx.x; q < nq; q += kThreads) {
+            cpa16(sg + 4 * q, D.a_gate + 4 * q);
+            cpa16(su + 4 * q, D.a_up + 4 * q);
+        }
+        cpa_commit();
+    } else {
+        for (int c = threadIdx.x; c < K; c += kThreads) {
+            sg[c] = D.a_gate[c];
+            su[c] = D.a_up[c];
+        }
+    }
+    const bool scaler = threadIdx.x == kThreads - 1;
+    uint64_t hi = 0, lo = 0;
+    auto umax = [&](uint64_t h2, uint64_t l2) {
+        if (h2 > hi || (h2 == hi && l2 > lo)) {
+            hi = h2;
+            lo = l2;
+        }
+    };
+    for (int i = threadIdx.x; i < D.ntmax; i += kThreads) umax(D.tmax[2 * i], D.tmax[2 * i + 1]);
+    // the scale's factor while the partials' loads are in flight
+    double kfac = 0.0;
+    if (scaler) kfac = intmlp_scale_factor(D.w_gate, D.w_up, *D.x_scale);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) umax(__shfl_xor_sync(~0u, hi, o), __shfl_xor_sync(~0u, lo, o));
+    if ((threadIdx.x & 31) == 0) {
+        s_m[0][threadIdx.x >> 5] = hi;
+        s_m[1][threadIdx.x >> 5] = lo;
+    }
+    cpa_wait_all();
+    __syncthreads();   // the partials' maxima and every copied row word
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) umax(s_m[0][i], s_m[1][i]);
+    const IntMlpRow R = intmlp_row(hi, lo);
+    const int64_t Kp = beats_per_row(K) * 64;
+    int32_t xsum = 0;
+    for (int q = threadIdx.x; q < sq; q += kThreads) {
+        int4 g = make_int4(0, 0, 0, 0), u = make_int4(0, 0, 0, 0);
+        if (q < nq) {
+            const int c = 4 * q;
+            if (c + 4 <= K) {
+                g = *reinterpret_cast<const int4 *>(sg + c);
+                u = *reinterpret_cast<const int4 *>(su + c);
+            } else {
+                g.x = sg[c];
+                u.x = su[c];
+                if (c + 1 < K) { g.y = sg[c + 1]; u.y = su[c + 1]; }
+                if (c + 2 < K) { g.z = sg[c + 2]; u.z = su[c + 2]; }
+            }
+        }
+        const uint32_t w = intmlp_codes4(g, u, R);
+        xsum = dp4a_ss(w, 0x01010101u, xsum);
+        if (owner && E.x_i8_out && int64_t(q) * 4 < Kp)
+            *reinterpret_cast<uint32_t *>(E.x_i8_out + int64_t(q) * 4) = w;
+        put_quad(xs, q, w);
+    }
+    publish_xsum(xsum, s_xsum);
+    if (scaler) {
+        const float scale = intmlp_scale_apply(hi, lo, kfac);
         *s_scale = scale;
         if (owner && E.x_scale) *const_cast<float *>(E.x_scale) = scale;
     }
@@ -1094,14 +1197,6 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);
 }
 
-// 16-byte asynchronous copy global -> shared (cached in L2 only); completes at
-// the issuing thread's cpa_wait_all, visible to that thread.
-__device__ __forceinline__ void cpa16(void *smem, const void *gmem) {
-    const uint32_t sa = uint32_t(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Small M = 1 launches, every warp one group at most (the per-matvec launches
 // of a dependency-ordered token).  Each lane copies all of its group's beats
@@ -1111,14 +1206,28 @@ __device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_all
 // soon as the CTA is resident -- under programmatic serialisation while the
 // preceding grid still runs -- and after griddepcontrol.wait only the staging
 // of the activations and the products out of shared memory remain; otherwise
-// they start after the wait.  Groups are
-// numbered across the list (Entry.cost_begin: the entry's first group; the
-// list's total_cost: all groups); warp w of CTA b takes group 8b + w.  Shared
-// memory: the staged activations (xs_words), then per warp iters x 32 lanes x
-// 16 bytes of planes, lane-interleaved so each step's reads are contiguous.
+// they start after the wait.
+//
+// Groups are numbered across the list (Entry.cost_begin: the entry's first
+// group; the list's total_cost: all groups); warp w of CTA b takes group
+// 8b + w.  Shared memory: the staged activations (xs_words), then per warp
+// iters x 32 lanes x 16 bytes of planes, lane-interleaved so each step's reads
+// are contiguous.
+//
+// Paired lists (flags bit 1: the gate and up projections of IntMlp blocks,
+// entries 2p and 2p + 1, one input row): the c-th CTA of pair p stages the row
+// once, its warps 0-3 take gate groups 4c..4c+3 and warps 4-7 the same up
+// groups, and after the products warp 0 forms t = relu(a_gate)^2 a_up of the
+// CTA's 32 rows and publishes their max |t| as partial c of the pair's
+// descriptor ("Tritium ..." -- Numerics, IntMlp).  An entry with an IntMlp
+// descriptor in an unpaired list stages its row from those partials
+// (stage_x_intmlp_parts).
 __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(const __grid_constant__ List L) {
+    static_assert(kWarps == 8, "paired lists split the CTA into two halves of four warps");
     extern __shared__ __align__(16) uint32_t xs[];
     __shared__ int32_t s_xsum[kWarps];
+    __shared__ float s_mlp_scale;
+    __shared__ int32_t s_pair[2][4][kRowsPerGroup];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rs = lane / kLanes1, bs = lane % kLanes1;
     asm volatile("griddepcontrol.launch_dependents;");
@@ -1126,6 +1235,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
     uint4 *pl = reinterpret_cast<uint4 *>(xs + L.xs_words) + (warp * max_iters) * 32 + lane;
     const int64_t G = L.total_cost;
     const int64_t cta0 = int64_t(blockIdx.x) * kWarps;
+    const bool paired = (L.flags & 2) != 0;
     auto entry_of = [&](int64_t gw) {   // last entry whose first group is <= gw
         int a = 0, b = L.count - 1;
         while (a < b) {
@@ -1135,12 +1245,30 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         }
         return a;
     };
-    const int64_t gw = cta0 + warp;
-    const int we = gw < G ? entry_of(gw) : -1;
+    // this warp's entry (-1: none) and group, and the entries the CTA stages
+    int we = -1, e0, e1;
+    int64_t g = 0, pc = 0;
+    if (paired) {   // gate and up share cost_begin, so the search lands on up
+        const int eu = entry_of(cta0), eg = eu - 1;
+        pc = int64_t(blockIdx.x) - L.e[eg].cost_begin / kWarps;
+        g = 4 * pc + (warp & 3);
+        const int ew = warp < 4 ? eg : eu;
+        we = g < L.e[ew].groups ? ew : -1;
+        e0 = e1 = eg;
+    } else {
+        const int64_t gw = cta0 + warp;
+        if (gw < G) {
+            we = entry_of(gw);
+            g = gw - L.e[we].cost_begin;
+        }
+        const int64_t last = cta0 + kWarps - 1 < G ? cta0 + kWarps - 1 : G - 1;
+        e0 = entry_of(cta0);
+        e1 = entry_of(last);
+    }
     auto copy_planes = [&]() {
         if (we < 0) return;
         const Entry &E = L.e[we];
-        const int64_t r = (gw - E.cost_begin) * kRowsPerGroup + rs;
+        const int64_t r = g * kRowsPerGroup + rs;
         const uint4 *rp = E.planes + (r < E.N ? r : E.N - 1) * int64_t(E.bstride);
         // beat of step t: bs + 4t, clamped to the row's last beat (the staged
         // activations past the row's end are zero)
@@ -1151,11 +1279,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         cpa_commit();
     };
     // planes written by the preceding kernel are visible only after the wait
-    const bool early = L.flags & 1;
+    const bool early = (L.flags & 1) != 0;
     if (early) copy_planes();
-    const int64_t last = cta0 + kWarps - 1 < G ? cta0 + kWarps - 1 : G - 1;
-    const int e0 = entry_of(cta0), e1 = entry_of(last);
     uint32_t viol = 0;
+    int32_t my_y = 0;   // paired lists: this lane's row sum (0 where there is none)
     for (int e = e0; e <= e1; ++e) {
         const Entry &E = L.e[e];
         if (e == e0) {
@@ -1164,9 +1291,17 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         } else {
             __syncthreads();   // the previous entry's readers are done with xs
         }
-        const bool owner = E.cost_begin >= cta0;   // this CTA holds the entry's group 0
+        // the CTA that holds the entry's group 0 writes its codes and scale
+        const bool owner = paired ? pc == 0 : E.cost_begin >= cta0;
+        const bool intmlp = !paired && mlp_of(E) != 0;
         float xsc;
-        if (E.xf) {
+        if (intmlp) {
+            stage_x_intmlp_parts(E, L.mlp[mlp_of(E) - 1], xs,
+                                 reinterpret_cast<int32_t *>(xs + L.xs_words) +
+                                     kWarps * max_iters * 128,
+                                 owner, s_xsum, &s_mlp_scale);
+            xsc = 0.0f;   // read from s_mlp_scale after the barrier
+        } else if (E.xf) {
             xsc = stage_x_fp32(E, xs, owner, L.err, s_xsum);
         } else {
             stage_x<1>(E, xs, s_xsum);
@@ -1174,14 +1309,16 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         }
         __syncthreads();
         const int32_t xsum = read_xsum(s_xsum);
-        if (we != e) continue;
+        if (intmlp) xsc = s_mlp_scale;
+        if (we < 0 || (!paired && we != e)) continue;
+        const Entry &W = L.e[we];   // paired: the up warps' entry is not the staged one
         cpa_wait_all();
         const uint4 *xb = reinterpret_cast<const uint4 *>(xs) + bs * kXBeatVec;
         int acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0;
 #pragma unroll 2
-        for (int t = 0; t < E.iters; ++t) {
+        for (int t = 0; t < W.iters; ++t) {
             const uint4 v = pl[t * 32];
             viol |= (v.x & v.z) | (v.y & v.w);
             const uint4 *X = xb + t * (kLanes1 * kXBeatVec);
@@ -1192,13 +1329,37 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
             mac_codes(v.y, v.w, xh, acc);
         }
         const int32_t y = row_sum1(codes_total(acc)) - xsum;
-        const int64_t row = (gw - E.cost_begin) * kRowsPerGroup + rs;
-        if (bs == 0 && row < E.N) {
-            if (E.acc) {
-                atomicAdd(E.acc + row, y);
+        const int64_t row = g * kRowsPerGroup + rs;
+        if (row < W.N) my_y = y;
+        if (bs == 0 && row < W.N) {
+            if (W.acc) {
+                atomicAdd(W.acc + row, y);
             } else {
-                if (E.y_i32) E.y_i32[row] = y;
-                if (E.y_f32) E.y_f32[row] = dequant(y, E.w_scale, xsc);
+                if (W.y_i32) W.y_i32[row] = y;
+                if (W.y_f32) W.y_f32[row] = dequant(y, W.w_scale, xsc);
+            }
+        }
+    }
+    if (paired) {
+        if (bs == 0) s_pair[warp >> 2][warp & 3][rs] = my_y;
+        __syncthreads();
+        if (warp == 0) {
+            bool neg;
+            const trit_u128 t = intmlp_abs_t(s_pair[0][lane >> 3][lane & 7],
+                                             s_pair[1][lane >> 3][lane & 7], neg);
+            uint64_t hi = uint64_t(t >> 64), lo = uint64_t(t);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const uint64_t h2 = __shfl_xor_sync(~0u, hi, o), l2 = __shfl_xor_sync(~0u, lo, o);
+                if (h2 > hi || (h2 == hi && l2 > lo)) {
+                    hi = h2;
+                    lo = l2;
+                }
+            }
+            if (lane == 0) {
+                uint64_t *tm = L.mlp[mlp_of(L.e[e0]) - 1].tmax + 2 * pc;
+                tm[0] = hi;
+                tm[1] = lo;
             }
         }
     }
@@ -1206,22 +1367,36 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
 }
 
 // Shared memory a pre-loading launch may take (the staged activations and
-// every warp's planes); larger lists take the streaming kernel.
-#ifndef TRIT_PRE_SMEM_MAX
-#define TRIT_PRE_SMEM_MAX (200 * 1024)
+// every warp's planes); larger lists take the streaming kernel.  TRIT_PRE_LOAD
+// 0 keeps small lists on the streaming kernel (the MLP block calls still use
+// the pre-loading one).
+constexpr size_t kPreSmemMax = 225 * 1024;
+#ifndef TRIT_PRE_LOAD
+#define TRIT_PRE_LOAD 1
 #endif
 
-// Launch entries[0..n) (M = 1, no IntMlp rows) on the pre-loading kernel when
-// every entry holds whole rows and the list's groups fit one resident wave with
-// one group per warp.  Returns false (nothing launched) otherwise.
+__host__ __device__ constexpr int64_t pre_iters(int64_t K) { return ((K + 63) / 64 + kLanes1 - 1) / kLanes1; }
+// Shared memory of a pre-loading launch whose longest row has `iters` steps:
+// the staged activations, every warp's planes and, with IntMlp rows, their
+// gate and up outputs (iters x 256 int32 each).
+size_t pre_smem(int64_t iters, bool intmlp = false) {
+    return size_t(iters) * kLanes1 * kXBeatWords * 4 + size_t(kWarps) * iters * 32 * 16 +
+           (intmlp ? size_t(iters) * 2 * 256 * 4 : 0);
+}
+
+// Launch entries[0..n) (M = 1) on the pre-loading kernel when every entry
+// holds whole rows and, unless forced, the list's groups fit one resident wave
+// with one group per warp.  Returns false (nothing launched) otherwise; true
+// with the launch's status in `status`.  Paired lists: entries 2p, 2p + 1 are
+// the gate and up products of IntMlp block p (mlp[p] receives the partials).
 bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
-                     float x_scale_val, cudaError_t &status) {
-#if TRIT_PRE_SMEM_MAX <= 0
-    return false;
-#else
-    int64_t groups = 0;
+                     float x_scale_val, cudaError_t &status, const MlpDesc *mlp = nullptr,
+                     int nmlp = 0, bool paired = false, bool force = false) {
+    if (!force && !TRIT_PRE_LOAD) return false;
+    int64_t groups = 0, grid = 0;
     int max_iters = 1;
     bool early = true;
+    if (paired && n % 2) return false;
     for (int i = 0; i < n; ++i) {
         if (entries[i].B != entries[i].bstride || rows_of(entries[i]) != 1) return false;
         early = early && (entries[i].mrows & kPlanesReady) != 0;
@@ -1229,9 +1404,25 @@ bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
         if (entries[i].iters > max_iters) max_iters = entries[i].iters;
     }
     const int xs_words = max_iters * kLanes1 * kXBeatWords;
-    const size_t smem = size_t(xs_words) * 4 + size_t(kWarps) * max_iters * 32 * 16;
-    if (smem > size_t(TRIT_PRE_SMEM_MAX)) return false;
-    const int64_t grid = (groups + kWarps - 1) / kWarps;
+    const size_t smem = pre_smem(max_iters, nmlp > 0 && !paired);
+    if (smem > kPreSmemMax) return false;
+    static thread_local List L;
+    if (paired) {
+        for (int p = 0; p < n / 2; ++p) {
+            L.e[2 * p] = entries[2 * p];
+            L.e[2 * p + 1] = entries[2 * p + 1];
+            L.e[2 * p].cost_begin = L.e[2 * p + 1].cost_begin = grid * kWarps;
+            grid += (entries[2 * p].groups + 3) / 4;
+        }
+    } else {
+        int64_t g = 0;
+        for (int i = 0; i < n; ++i) {
+            L.e[i] = entries[i];
+            L.e[i].cost_begin = g;
+            g += entries[i].groups;
+        }
+        grid = (groups + kWarps - 1) / kWarps;
+    }
     static thread_local size_t last_smem = ~size_t(0);
     static thread_local int last_dev = -1, last_occ = 0;
     int dev = 0;
@@ -1239,6 +1430,13 @@ bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
     if (smem != last_smem || dev != last_dev) {
         status = cudaFuncSetAttribute(select_accumulate_pre_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (status != cudaSuccess) return true;
+        // one shared-memory carve-out for every launch of this kernel, so that
+        // the CTAs of a launch can become resident beside those of the one
+        // before it (a carve-out change waits for the SM to drain)
+        status = cudaFuncSetAttribute(select_accumulate_pre_kernel,
+                                      cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      int(cudaSharedmemCarveoutMaxShared));
         if (status != cudaSuccess) return true;
         int occ = 0;
         status = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_accumulate_pre_kernel,
@@ -1248,20 +1446,13 @@ bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
         last_smem = smem;
         last_dev = dev;
     }
-    if (grid > int64_t(last_occ) * device_sm_count()) return false;
-    static thread_local List L;
+    if (!force && grid > int64_t(last_occ) * device_sm_count()) return false;
     L.count = n;
     L.err = err;
     L.x_scale_val = x_scale_val;
-    L.flags = early ? 1 : 0;
-    for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = MlpDesc{};
-    int64_t g = 0;
-    for (int i = 0; i < n; ++i) {
-        L.e[i] = entries[i];
-        L.e[i].cost_begin = g;
-        g += entries[i].groups;
-    }
-    L.total_cost = groups;
+    L.flags = (early ? 1 : 0) | (paired ? 2 : 0);
+    for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = i < nmlp ? mlp[i] : MlpDesc{};
+    L.total_cost = paired ? grid * kWarps : groups;
     L.xs_words = xs_words;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
@@ -1275,7 +1466,6 @@ bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
     cfg.numAttrs = 1;
     status = cudaLaunchKernelEx(&cfg, select_accumulate_pre_kernel, L);
     return true;
-#endif
 }
 
 template <int MT>
@@ -1478,11 +1668,110 @@ cudaError_t launch_intmlp_gemv_many(const MlpProjDev *list, int count, uint32_t 
             desc[i].x_scale = m.x_scale_in;
             desc[i].w_gate = m.w_gate;
             desc[i].w_up = m.w_up;
+            desc[i].tmax = nullptr;
+            desc[i].ntmax = 0;
+            desc[i].pad_ = 0;
         }
         cudaError_t e = launch_list<1>(buf, n, err, s, desc, n);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// ---- batch-1 MLP blocks in two launches ------------------------------------------
+
+int64_t mlp_tmax_parts(int64_t F) { return ((F + kRowsPerGroup - 1) / kRowsPerGroup + 3) / 4; }
+
+bool mlp_pairs_supported(int64_t K, int64_t F) {
+    return pre_smem(pre_iters(K)) <= kPreSmemMax && pre_smem(pre_iters(F), true) <= kPreSmemMax;
+}
+
+// Gate and up of each block: blocks that the pre-loading kernel takes go as
+// paired lists (publishing the max|t| partials), the others as fused
+// quantise-and-multiply products (their down launch reduces max|t| itself).
+cudaError_t launch_mlp_gate_up(const MlpBlockDev *list, int count, uint32_t *err, cudaStream_t s) {
+    static thread_local Entry buf[2 * kMaxMlp];
+    static thread_local MlpDesc desc[kMaxMlp];
+    static thread_local ProjDev rest[TRIT_MAX_LIST_PER_LAUNCH];
+    int n = 0, nr = 0;
+    cudaError_t e = cudaSuccess;
+    auto flush = [&]() {
+        if (n && e == cudaSuccess &&
+            !launch_list_pre(buf, 2 * n, err, s, 0.0f, e, desc, n, true, true))
+            e = cudaErrorInvalidValue;
+        n = 0;
+    };
+    auto flush_rest = [&]() {
+        if (nr && e == cudaSuccess) e = launch_gemv_many(rest, nr, err, s);
+        nr = 0;
+    };
+    for (int i = 0; i < count && e == cudaSuccess; ++i) {
+        const MlpBlockDev &b = list[i];
+        if (mlp_pairs_supported(b.gate.K, b.gate.N)) {
+            buf[2 * n] = make_entry(b.gate, 0, 1, 0, b.gate.B, nullptr, kLanes1);
+            buf[2 * n].mrows |= (n + 1) << 8;
+            buf[2 * n + 1] = make_entry(b.up, 0, 1, 0, b.up.B, nullptr, kLanes1);
+            desc[n] = MlpDesc{};
+            desc[n].tmax = b.tmax;
+            desc[n].ntmax = int32_t(mlp_tmax_parts(b.gate.N));
+            if (++n == kMaxMlp) flush();
+        } else {
+            rest[nr++] = b.gate;
+            rest[nr++] = b.up;
+            if (nr + 2 > TRIT_MAX_LIST_PER_LAUNCH) flush_rest();
+        }
+    }
+    flush();
+    flush_rest();
+    return e;
+}
+
+// The down projection of each block, its row formed from the gate and up
+// outputs: from the published partials on the pre-loading kernel, else by the
+// streaming kernel's own max|t| pass.
+cudaError_t launch_mlp_down(const MlpBlockDev *list, int count, uint32_t *err, cudaStream_t s) {
+    static thread_local Entry buf[kMaxMlp];
+    static thread_local MlpDesc desc[kMaxMlp];
+    static thread_local MlpProjDev rest[kMaxMlp];
+    int n = 0, nr = 0;
+    cudaError_t e = cudaSuccess;
+    auto flush = [&]() {
+        if (n && e == cudaSuccess && !launch_list_pre(buf, n, err, s, 0.0f, e, desc, n, false, true))
+            e = cudaErrorInvalidValue;
+        n = 0;
+    };
+    auto flush_rest = [&]() {
+        if (nr && e == cudaSuccess) e = launch_intmlp_gemv_many(rest, nr, err, s);
+        nr = 0;
+    };
+    for (int i = 0; i < count && e == cudaSuccess; ++i) {
+        const MlpBlockDev &b = list[i];
+        if (mlp_pairs_supported(b.gate.K, b.gate.N)) {
+            buf[n] = make_entry(b.down, 0, 1, 0, b.down.B, nullptr, kLanes1);
+            buf[n].mrows |= (n + 1) << 8;
+            desc[n].a_gate = b.gate.y_i32;
+            desc[n].a_up = b.up.y_i32;
+            desc[n].x_scale = b.gate.x_scale;
+            desc[n].w_gate = b.w_gate;
+            desc[n].w_up = b.w_up;
+            desc[n].tmax = b.tmax;
+            desc[n].ntmax = int32_t(mlp_tmax_parts(b.gate.N));
+            desc[n].pad_ = 0;
+            if (++n == kMaxMlp) flush();
+        } else {
+            MlpProjDev &m = rest[nr++];
+            m.down = b.down;
+            m.a_gate = b.gate.y_i32;
+            m.a_up = b.up.y_i32;
+            m.x_scale_in = b.gate.x_scale;
+            m.w_gate = b.w_gate;
+            m.w_up = b.w_up;
+            if (nr == kMaxMlp) flush_rest();
+        }
+    }
+    flush();
+    flush_rest();
+    return e;
 }
 
 // Activation rows are taken 8 at a time; a product's remaining r < 8 rows go

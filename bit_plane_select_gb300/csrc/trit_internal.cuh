@@ -181,35 +181,84 @@ __device__ __forceinline__ int intmlp_code_small(int32_t ag, int32_t au, const I
 // of 127 |t| / A carries at most ten fp32 roundings of relative size 2^-24
 // (g twice through g^2, g^2, u, the product, A's two halves and their sum,
 // 127 / fl(A), the last product), so |p - 127 |t| / A| <= 127 * 10 * 2^-24
-// (1 + 2^-20) < 7.6e-5.  Where
-// p's distance from the nearest half-integer exceeds 1.5e-4 the exact quotient
-// lies on the same side of it and rounds to the same integer as p; otherwise
-// the exact path decides.
-__device__ __forceinline__ int intmlp_code_est(int32_t ag, int32_t au, const IntMlpRow &R) {
-    if (R.zero || ag <= 0 || au == 0) return 0;
-    const float g = __int2float_rn(ag);
+// (1 + 2^-20) < 7.6e-5.  Where p's distance from the nearest half-integer
+// exceeds 1.5e-4 the exact quotient lies on the same side of it and rounds to
+// the same integer as p; otherwise the exact path decides.
+//
+// intmlp_code_fast has no branch: relu and the zero cases fall out of the
+// arithmetic (g = 0 for a_g <= 0 gives p = 0; kf = 0 for a zero row), and p
+// (0 <= p < 2^8) is rounded to an integer by adding and subtracting 1.5 * 2^23
+// (fp32 round-to-nearest-even at unit spacing); fr = p - that integer is exact,
+// and |fr| < 0.5 - 1.5e-4 is the "far from a tie" test.  Four columns then
+// run as independent chains (intmlp_codes4) instead of four branchy calls.
+// The exact path, kept out of line so that the unrolled column loops around
+// it stay small.  R travels as scalars (by value, in registers).
+static __device__ __noinline__ int intmlp_code_exact(int32_t ag, int32_t au, uint64_t a_hi,
+                                                     uint64_t a_lo, float k, bool small) {
+    IntMlpRow R;
+    R.A = (trit_u128(a_hi) << 64) | trit_u128(a_lo);
+    R.small = small;
+    R.zero = false;
+    R.k = k;
+    R.kf = 0.0f;
+    return small ? intmlp_code_small(ag, au, R) : intmlp_code(ag, au, R);
+}
+
+__device__ __forceinline__ int intmlp_code_fast(int32_t ag, int32_t au, const IntMlpRow &R,
+                                                bool &near) {
+    const float g = __int2float_rn(ag > 0 ? ag : 0);
     const float tf = __fmul_rn(__fmul_rn(g, g), fabsf(__int2float_rn(au)));
     const float p = __fmul_rn(tf, R.kf);
-    const float fl = floorf(p);
-    const float fr = __fsub_rn(p, fl);   // exact: p < 2^8 and fl is p's integer part
-    if (fabsf(__fsub_rn(fr, 0.5f)) > 1.5e-4f) {
-        int q = int(fl) + (fr > 0.5f ? 1 : 0);
-        q = q > 127 ? 127 : q;
-        return au < 0 ? -q : q;
+    const float big = __fadd_rn(p, 12582912.0f);
+    const float fr = __fsub_rn(p, __fsub_rn(big, 12582912.0f));
+    near = fabsf(fr) >= 0.49985f;
+    int q = __float_as_int(big) - 0x4B400000;
+    q = q > 127 ? 127 : q;
+    return au < 0 ? -q : q;
+}
+
+__device__ __forceinline__ int intmlp_code_est(int32_t ag, int32_t au, const IntMlpRow &R) {
+    bool near;
+    const int q = intmlp_code_fast(ag, au, R, near);
+    if (!near) return q;
+    return intmlp_code_exact(ag, au, uint64_t(R.A >> 64), uint64_t(R.A), R.k, R.small);
+}
+
+// Four columns' codes packed as bytes (column c in byte c).
+__device__ __forceinline__ uint32_t intmlp_codes4(int4 g, int4 u, const IntMlpRow &R) {
+    bool n0, n1, n2, n3;
+    int c0 = intmlp_code_fast(g.x, u.x, R, n0);
+    int c1 = intmlp_code_fast(g.y, u.y, R, n1);
+    int c2 = intmlp_code_fast(g.z, u.z, R, n2);
+    int c3 = intmlp_code_fast(g.w, u.w, R, n3);
+    if (n0 | n1 | n2 | n3) {   // rare: a column within 1.5e-4 of a tie
+        const uint64_t hi = uint64_t(R.A >> 64), lo = uint64_t(R.A);
+        if (n0) c0 = intmlp_code_exact(g.x, u.x, hi, lo, R.k, R.small);
+        if (n1) c1 = intmlp_code_exact(g.y, u.y, hi, lo, R.k, R.small);
+        if (n2) c2 = intmlp_code_exact(g.z, u.z, hi, lo, R.k, R.small);
+        if (n3) c3 = intmlp_code_exact(g.w, u.w, hi, lo, R.k, R.small);
     }
-    return R.small ? intmlp_code_small(ag, au, R) : intmlp_code(ag, au, R);
+    return (uint32_t(c0) & 0xffu) | ((uint32_t(c1) & 0xffu) << 8) | ((uint32_t(c2) & 0xffu) << 16) |
+           (uint32_t(c3) << 24);
 }
 
 // max|t| (hi:lo) * ((S_g * S_g) * S_u), S = w * x_scale / 127, in double, rounded once.
-__device__ __forceinline__ float intmlp_scale(uint64_t hi, uint64_t lo, float w_g, float w_u,
-                                              float x_scale) {
+// Split in two so that the factor, which does not depend on max|t|, can be
+// formed while max|t| is still being reduced.
+__device__ __forceinline__ double intmlp_scale_factor(float w_g, float w_u, float x_scale) {
     const double s = double(x_scale);
     const double sg = __ddiv_rn(__dmul_rn(double(w_g), s), 127.0);
     const double su = __ddiv_rn(__dmul_rn(double(w_u), s), 127.0);
-    const double k = __dmul_rn(__dmul_rn(sg, sg), su);
+    return __dmul_rn(__dmul_rn(sg, sg), su);
+}
+__device__ __forceinline__ float intmlp_scale_apply(uint64_t hi, uint64_t lo, double k) {
     const double a = __dadd_rn(__dmul_rn(__ull2double_rn(hi), 18446744073709551616.0),
                                __ull2double_rn(lo));
     return __double2float_rn(__dmul_rn(a, k));
+}
+__device__ __forceinline__ float intmlp_scale(uint64_t hi, uint64_t lo, float w_g, float w_u,
+                                              float x_scale) {
+    return intmlp_scale_apply(hi, lo, intmlp_scale_factor(w_g, w_u, x_scale));
 }
 
 // The fp32 dequantisation of one output, one rounding per step, never contracted.
@@ -307,6 +356,20 @@ struct MlpProjDev {
 };
 cudaError_t launch_intmlp_gemv_many(const MlpProjDev *list, int count, uint32_t *err,
                                     cudaStream_t s);
+
+// One batch-1 MLP block for the two-launch path: gate and up (fp32 input,
+// fused quantiser; y_i32 = a_gate / a_up, gate's x_scale = the input scale),
+// the down projection (x_i8_out / x_scale = the optional h_i8 / h_scale
+// outputs) and the per-CTA max|t| partials the gate/up launch publishes.
+struct MlpBlockDev {
+    ProjDev gate, up, down;
+    float w_gate, w_up;
+    uint64_t *tmax;   // 2 words (hi, lo) per partial
+};
+int64_t mlp_tmax_parts(int64_t F);
+bool mlp_pairs_supported(int64_t K, int64_t F);
+cudaError_t launch_mlp_gate_up(const MlpBlockDev *list, int count, uint32_t *err, cudaStream_t s);
+cudaError_t launch_mlp_down(const MlpBlockDev *list, int count, uint32_t *err, cudaStream_t s);
 
 cudaError_t launch_pack(const int8_t *w, int64_t N, int64_t K, float w_scale, uint8_t *planes,
                         float *scale_out, uint32_t *err, cudaStream_t s);

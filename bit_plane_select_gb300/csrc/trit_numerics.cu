@@ -94,78 +94,104 @@ __global__ void __launch_bounds__(kNThreads) quant_folded_kernel(const float *x,
 // ---- IntMlp ----------------------------------------------------------------------
 
 // NT threads per row (one CTA per row): a decode row (M = 1, N = 6,912) is
-// latency-bound, so more threads mean fewer dependent rounds per pass.
+// latency-bound, so the row's first kHoldI * (NT - 32) columns are loaded once,
+// held in registers through both passes, and the block maximum is reduced by
+// one warp and broadcast.  The last warp takes no columns: it forms the
+// scale, whose double arithmetic is slow on this device -- the factor
+// S_g^2 S_u while the others reduce max|t|, the product with max|t| while they
+// form the codes.
+constexpr int kHoldI = 8;
 template <int NT>
 __global__ void __launch_bounds__(NT) intmlp_quant_kernel(const int32_t *ag, const int32_t *au,
                                                           int64_t M, int64_t N, int64_t ldq,
                                                           float w_g, float w_u,
                                                           const float *x_scale, int8_t *q,
                                                           float *h_scale) {
-    constexpr int kNThreads = NT;
-    constexpr int kNWarps = NT / 32;
-    __shared__ uint64_t red[2][kNWarps];
+    constexpr int kW = NT / 32;
+    constexpr int kC = NT - 32;   // threads that take columns
+    static_assert(kW <= 32 && kW >= 2, "one warp reduces the warps' maxima");
+    __shared__ uint64_t red[2][kW];
+    __shared__ uint64_t fin[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // launched with programmatic serialisation: the next launch may start its
     // own set-up now; the gate and up outputs are read after the preceding grid
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    auto umax = [](uint64_t &hi, uint64_t &lo, uint64_t h2, uint64_t l2) {
+        if (h2 > hi || (h2 == hi && l2 > lo)) {
+            hi = h2;
+            lo = l2;
+        }
+    };
+    auto warp_max = [&](uint64_t &hi, uint64_t &lo) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            umax(hi, lo, __shfl_xor_sync(~0u, hi, o), __shfl_xor_sync(~0u, lo, o));
+    };
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const int32_t *gr = ag + m * N, *ur = au + m * N;
+        const bool scaler = warp == kW - 1;
+        // the scaler warp's columns lie past every row (t = 0, code 0)
+        const int64_t c0 = scaler ? INT64_MAX / 2 : int64_t(threadIdx.x);
+        double kfac = 0.0;
+        if (scaler && lane == 0) kfac = intmlp_scale_factor(w_g, w_u, x_scale[m]);
+        int32_t g[kHoldI], u[kHoldI];
+#pragma unroll
+        for (int r = 0; r < kHoldI; ++r) {
+            const int64_t c = int64_t(r) * kC + c0;
+            g[r] = c < N ? gr[c] : 0;   // past N: t = 0, code 0
+            u[r] = c < N ? ur[c] : 0;
+        }
         trit_u128 amax = 0;
-        for (int64_t base = 0; base < N; base += 8 * kNThreads) {   // 8 predicated loads per array
-            int32_t g[8], u[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int64_t c = base + r * kNThreads + threadIdx.x;
-                g[r] = c < N ? gr[c] : 0;
-                u[r] = c < N ? ur[c] : 0;
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                bool neg;
-                const trit_u128 t = intmlp_abs_t(g[r], u[r], neg);
-                amax = t > amax ? t : amax;
-            }
+        for (int r = 0; r < kHoldI; ++r) {
+            bool neg;
+            const trit_u128 t = intmlp_abs_t(g[r], u[r], neg);
+            amax = t > amax ? t : amax;
+        }
+        for (int64_t c = int64_t(kHoldI) * kC + c0; c < N; c += kC) {
+            bool neg;
+            const trit_u128 t = intmlp_abs_t(gr[c], ur[c], neg);
+            amax = t > amax ? t : amax;
         }
         uint64_t hi = uint64_t(amax >> 64), lo = uint64_t(amax);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const uint64_t h2 = __shfl_xor_sync(~0u, hi, o), l2 = __shfl_xor_sync(~0u, lo, o);
-            if (h2 > hi || (h2 == hi && l2 > lo)) {
-                hi = h2;
-                lo = l2;
-            }
-        }
-        if ((threadIdx.x & 31) == 0) {
-            red[0][threadIdx.x >> 5] = hi;
-            red[1][threadIdx.x >> 5] = lo;
+        warp_max(hi, lo);
+        if (lane == 0) {
+            red[0][warp] = hi;
+            red[1][warp] = lo;
         }
         __syncthreads();
-        hi = red[0][0];
-        lo = red[1][0];
-        for (int i = 1; i < kNWarps; ++i)
-            if (red[0][i] > hi || (red[0][i] == hi && red[1][i] > lo)) {
-                hi = red[0][i];
-                lo = red[1][i];
-            }
-        const IntMlpRow R = intmlp_row(hi, lo);
-        int8_t *qr = q + m * ldq;
-        for (int64_t base = 0; base < ldq; base += 8 * kNThreads) {
-            int32_t g[8], u[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int64_t c = base + r * kNThreads + threadIdx.x;
-                g[r] = c < N ? gr[c] : 0;   // past N: code 0
-                u[r] = c < N ? ur[c] : 0;
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int64_t c = base + r * kNThreads + threadIdx.x;
-                if (c < ldq)
-                    qr[c] = int8_t(intmlp_code_est(g[r], u[r], R));
+        if (warp == 0) {
+            hi = lane < kW ? red[0][lane] : 0;
+            lo = lane < kW ? red[1][lane] : 0;
+            warp_max(hi, lo);
+            if (lane == 0) {
+                fin[0] = hi;
+                fin[1] = lo;
             }
         }
-        if (threadIdx.x == 0) h_scale[m] = intmlp_scale(hi, lo, w_g, w_u, x_scale[m]);
-        __syncthreads();   // red reused by the next row
+        __syncthreads();
+        hi = fin[0];
+        lo = fin[1];
+        if (scaler) {
+            if (lane == 0) h_scale[m] = intmlp_scale_apply(hi, lo, kfac);
+        } else {
+            const IntMlpRow R = intmlp_row(hi, lo);
+            int8_t *qr = q + m * ldq;
+#pragma unroll
+            for (int r = 0; r < kHoldI; r += 4) {
+                const uint32_t w = intmlp_codes4(make_int4(g[r], g[r + 1], g[r + 2], g[r + 3]),
+                                                 make_int4(u[r], u[r + 1], u[r + 2], u[r + 3]), R);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t c = int64_t(r + j) * kC + c0;
+                    if (c < ldq) qr[c] = int8_t(w >> (8 * j));
+                }
+            }
+            for (int64_t c = int64_t(kHoldI) * kC + c0; c < ldq; c += kC)
+                qr[c] = c < N ? int8_t(intmlp_code_est(gr[c], ur[c], R)) : int8_t(0);
+        }
+        __syncthreads();   // red and fin reused by the next row
     }
 }
 

@@ -163,15 +163,22 @@ class LayerChain:
     weights: per layer, a dict name -> (int8 [N, K] tensor, w_scale) for the
     seven projections q, k, v, o, gate, up, down.
 
-    fused_mlp: True runs stage 4 as one launch (every CTA of the down product
-    forms the IntMlp codes it needs); False as two (trit_intmlp_quant forms the
-    codes once, then the down product reads them) -- the same bits either way."""
+    mlp_form -- the same bits every way:
+      "paired": gate/up as one launch that also publishes max|t| partials
+        (trit_mlp_gate_up), then the down product forming the IntMlp codes from
+        them while it stages its row (trit_mlp_down): 4 launches per layer;
+      "split": gate/up, trit_intmlp_quant, the down product of its int8 codes: 5;
+      "fused": gate/up, then every CTA of the down product forms the codes it
+        needs, max|t| pass included (trit_intmlp_gemv_many): 4."""
 
     NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+    MLP_FORMS = ("paired", "split", "fused")
 
-    def __init__(self, weights, device="cuda", fused_mlp: bool = False):
-        from . import MlpProjList
-        self.fused_mlp = fused_mlp
+    def __init__(self, weights, device="cuda", mlp_form: str = "paired"):
+        from . import MlpBlockList, MlpProjList, trit_mlp_tmax_bytes
+        if mlp_form not in self.MLP_FORMS:
+            raise ValueError(f"mlp_form must be one of {self.MLP_FORMS}")
+        self.mlp_form = mlp_form
         self.device = torch.device(device)
         dev = self.device
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -216,6 +223,10 @@ class LayerChain:
             L["s_h"] = torch.zeros(1, dtype=torch.float32, device=dev)
             L["down_i8"] = ProjList([(P["down"], S["down"], L["h"], L["s_h"], Kd, L["y_down"],
                                       L["f_down"])], planes_ready=True)
+            L["tmax"] = torch.zeros(trit_mlp_tmax_bytes(Nf), dtype=torch.uint8, device=dev)
+            L["mlp"] = MlpBlockList([(P["gate"], P["up"], P["down"], S["gate"], S["up"], S["down"],
+                                      L["f_o"], L["s_gu"], L["a_gate"], L["a_up"], L["tmax"], None,
+                                      None, L["y_down"], L["f_down"])], planes_ready=True)
             self.layers.append(L)
 
     @property
@@ -223,13 +234,17 @@ class LayerChain:
         return [L["x"] for L in self.layers]
 
     def step(self, stream=None):
-        """One token through every layer: 4 (fused_mlp) or 5 launches per layer."""
-        from . import trit_intmlp_gemv_many, trit_intmlp_quant
+        """One token through every layer: 4 launches per layer (5 for "split")."""
+        from . import trit_intmlp_gemv_many, trit_intmlp_quant, trit_mlp_down, trit_mlp_gate_up
         for L in self.layers:
             trit_quant_gemv_many(L["qkv"], self.err, stream)
             trit_quant_gemv_many(L["o"], self.err, stream)
+            if self.mlp_form == "paired":
+                trit_mlp_gate_up(L["mlp"], self.err, stream)
+                trit_mlp_down(L["mlp"], self.err, stream)
+                continue
             trit_quant_gemv_many(L["gu"], self.err, stream)
-            if self.fused_mlp:
+            if self.mlp_form == "fused":
                 trit_intmlp_gemv_many(L["down"], self.err, stream)
             else:
                 S = L["S"]
@@ -243,7 +258,7 @@ class LayerChain:
 
     @property
     def launches_per_step(self) -> int:
-        return (4 if self.fused_mlp else 5) * len(self.layers)
+        return (5 if self.mlp_form == "split" else 4) * len(self.layers)
 
     def step_bytes(self) -> int:
         """Algorithmic bytes of one token: every plane byte read once; per

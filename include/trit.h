@@ -291,6 +291,60 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
                                            uint32_t *err_flag, trit_stream_t stream);
 
 /*
+ * One batch-1 MLP block in two launches ("Tritium ..." -- Numerics, IntMlp):
+ *   trit_mlp_gate_up: the fp32 row x (K values) quantised as trit_quant_act
+ *     does (x_scale out) and multiplied by the gate and up planes (F x K each)
+ *     into a_gate and a_up (int32, F values each); each CTA of the launch also
+ *     forms t = relu(a_gate)^2 * a_up of the rows it computed and stores their
+ *     max |t| in `tmax`.
+ *   trit_mlp_down: the down projection (N x F) of the codes of t --
+ *     round-half-even(127 t / max|t|), exact, max|t| reduced from `tmax` --
+ *     with scale max|t| * S_g^2 * S_u (S = w * x_scale / 127): y_i32 / y_f32
+ *     and, when asked for, h_i8 and h_scale.
+ * Results are bit-identical to trit_quant_gemv_many([gate, up]) followed by
+ * trit_intmlp_quant and trit_gemm of the down projection; a_gate, a_up and
+ * x_scale are the first call's outputs.  trit_mlp_down reads what
+ * trit_mlp_gate_up of the same blocks wrote: call it after that call on the
+ * same stream, with x_scale, a_gate, a_up and tmax untouched in between.
+ * Blocks whose rows exceed the pre-loading kernel's shared memory (K above
+ * 13,312 or F above 8,960 columns) take the fused paths instead (tmax
+ * unused), with the same results.  K and F are limited to TRIT_MAX_FUSED_K (TRIT_E_SHAPE);
+ * w_gate, w_up and w_down must be finite and > 0 (TRIT_E_SCALE).
+ *   x          [K] fp32, device, 4-byte aligned
+ *   x_scale    [1] fp32 out
+ *   a_gate, a_up  [F] int32 out, 16-byte aligned
+ *   tmax       workspace of trit_mlp_tmax_bytes(F) bytes, 16-byte aligned
+ *   h_i8       out, may be NULL: [F_pad] int8, zero tail, 16-byte aligned
+ *   h_scale    out, may be NULL: [1] fp32
+ *   y_i32, y_f32  [N] outputs, either may be NULL (not both)
+ * `list` is a host array; up to 8 blocks share one launch.
+ */
+typedef struct trit_mlp_block {
+    const uint8_t *gate_planes;
+    const uint8_t *up_planes;
+    const uint8_t *down_planes;
+    const float *x;
+    float *x_scale;
+    int32_t *a_gate;
+    int32_t *a_up;
+    void *tmax;
+    int8_t *h_i8;
+    float *h_scale;
+    int32_t *y_i32;
+    float *y_f32;
+    int64_t K, F, N;
+    float w_gate, w_up, w_down;
+    uint32_t flags;           /* 0 or TRIT_PROJ_PLANES_READY (all three planes) */
+} trit_mlp_block;
+
+/* Bytes of the tmax workspace of a block with F gate/up rows (16 per 32 rows). */
+TRIT_API int64_t trit_mlp_tmax_bytes(int64_t F);
+TRIT_API trit_status trit_mlp_gate_up(const trit_mlp_block *list, int32_t count,
+                                      uint32_t *err_flag, trit_stream_t stream);
+TRIT_API trit_status trit_mlp_down(const trit_mlp_block *list, int32_t count,
+                                   uint32_t *err_flag, trit_stream_t stream);
+
+/*
  * trit_quant_act_folded -- quantise the normalised activations of a layer
  * without dividing by the rms ("Tritium ..." -- Numerics, Folded).  For each
  * row m of x (M x K fp32, row-major) and the norm gains g (K fp32):

@@ -50,6 +50,7 @@ def test_struct_layouts(trit):
     assert ctypes.sizeof(trit.TritQProj) == 72 and trit.TritQProj.w_scale.offset == 64
     assert ctypes.sizeof(trit.TritMlpProj) == 96
     assert ctypes.sizeof(trit.TritBitcosProj) == 88
+    assert ctypes.sizeof(trit.TritMlpBlock) == 136
 
 
 def test_struct_layouts_match_the_c_compiler(trit, tmp_path):
@@ -62,7 +63,7 @@ def test_struct_layouts_match_the_c_compiler(trit, tmp_path):
         pytest.skip("no C compiler")
     structs = {"trit_proj": trit.TritProj, "trit_qproj": trit.TritQProj,
                "trit_act": trit.TritAct, "trit_mlpproj": trit.TritMlpProj,
-               "trit_bitcos_proj": trit.TritBitcosProj}
+               "trit_bitcos_proj": trit.TritBitcosProj, "trit_mlp_block": trit.TritMlpBlock}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "trit.h"', "int main(void) {"]
     for cname, cls in structs.items():
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -84,6 +85,36 @@ def test_struct_layouts_match_the_c_compiler(trit, tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(cls), cname
         for fname, _ in cls._fields_:
             assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
+
+
+def test_mlp_block_validation(trit):
+    """trit_mlp_gate_up / trit_mlp_down reject bad blocks before touching a
+    device; the partials workspace is 16 bytes per 32 gate/up rows."""
+    L = trit.lib()
+    assert L.trit_mlp_tmax_bytes(6912) == 16 * 216
+    assert L.trit_mlp_tmax_bytes(1) == 16 and L.trit_mlp_tmax_bytes(33) == 32
+    assert L.trit_mlp_tmax_bytes(0) == 0
+    p, null, odd = ctypes.c_void_p(1 << 16), None, ctypes.c_void_p((1 << 16) + 4)
+    s = ctypes.c_void_p(None)
+    B = trit.TritMlpBlock
+
+    def blk(**kw):
+        a = dict(gate_planes=p, up_planes=p, down_planes=p, x=p, x_scale=p, a_gate=p, a_up=p,
+                 tmax=p, h_i8=null, h_scale=null, y_i32=p, y_f32=p, K=2560, F=6912, N=2560,
+                 w_gate=1.0, w_up=1.0, w_down=1.0, flags=0)
+        a.update(kw)
+        return B(**a)
+
+    for bad, code in [(blk(tmax=null), 1), (blk(a_gate=odd), 1), (blk(y_i32=null, y_f32=null), 1),
+                      (blk(flags=2), 1), (blk(x=null), 1), (blk(F=0), 2), (blk(K=trit.MAX_FUSED_K + 1), 2),
+                      (blk(F=trit.MAX_FUSED_K + 1), 2), (blk(N=0), 2), (blk(w_up=0.0), 4),
+                      (blk(w_down=float("nan")), 4)]:
+        lst = (B * 2)(blk(), bad)
+        for fn in (L.trit_mlp_gate_up, L.trit_mlp_down):
+            assert fn(ctypes.cast(lst, ctypes.c_void_p), 2, p, s) == code
+    lst = (B * 1)(blk())
+    assert L.trit_mlp_gate_up(ctypes.cast(lst, ctypes.c_void_p), 0, p, s) == 1
+    assert L.trit_mlp_down(ctypes.cast(lst, ctypes.c_void_p), 1, null, s) == 1
 
 
 def test_payload_bytes(trit):

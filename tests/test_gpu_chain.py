@@ -1,6 +1,6 @@
 """The dependency-ordered decode (LayerChain): two layers of the BitNet-shaped
 stack, four launches per layer (five with the IntMlp quantiser as a launch of
-its own) each reading the previous launch's outputs,
+its own), each reading the previous launch's outputs,
 against the oracle's chain -- quantiser, product, quantiser of the product's
 fp32 output, ..., IntMlp quantiser, down product -- every int32 output
 bit-exact and every fp32 output bit-identical at every stage (so the chain
@@ -31,16 +31,16 @@ def host(x):
     return x.cpu().numpy()
 
 
-@pytest.mark.parametrize("fused_mlp", [True, False])
-def test_layer_chain_matches_oracle_chain(t, orc, fused_mlp):
+@pytest.mark.parametrize("mlp_form", ["paired", "split", "fused"])
+def test_layer_chain_matches_oracle_chain(t, orc, mlp_form):
     from bit_plane_select_gb300.stack import LayerChain
     seed, layers = 9, 2
     names = [p[0] for p in synth.PROJECTIONS]
     W = [{n: synth.stack_weights(seed, layer, i) for i, n in enumerate(names)} for layer in range(layers)]
     ws = [{n: float(synth.w_scale(W[l][n])) for n in names} for l in range(layers)]
     chain = LayerChain([{n: (torch.from_numpy(W[l][n]), ws[l][n]) for n in names} for l in range(layers)],
-                       fused_mlp=fused_mlp)
-    assert chain.launches_per_step == (4 if fused_mlp else 5) * layers
+                       mlp_form=mlp_form)
+    assert chain.launches_per_step == (5 if mlp_form == "split" else 4) * layers
     xs = [synth.projection_acts(seed, l, 0, 1)[0] for l in range(layers)]
     for l in range(layers):
         chain.x[l].copy_(torch.from_numpy(xs[l]))
@@ -80,7 +80,7 @@ def check_chain_against_oracle(orc, chain, W, ws, xs, layers):
         np.testing.assert_array_equal(host(L["a_gate"]), outs["gate"][0])
         np.testing.assert_array_equal(host(L["a_up"]), outs["up"][0])
         np.testing.assert_array_equal(host(L["s_gu"]).view(np.uint32), s_gu.view(np.uint32))
-        if not chain.fused_mlp:   # the IntMlp codes and scale the down product read
+        if chain.mlp_form == "split":   # the IntMlp codes and scale the down product read
             np.testing.assert_array_equal(host(L["h"])[:h.shape[1]], h[0])
             np.testing.assert_array_equal(host(L["s_h"]).view(np.uint32), hs.view(np.uint32))
         np.testing.assert_array_equal(host(L["y_down"]), yd[0])

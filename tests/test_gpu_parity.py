@@ -429,10 +429,10 @@ def test_small_list_entry_boundaries(t, orc, ready, fused):
 
 
 @pytest.mark.parametrize("fused", [False, True])
-@pytest.mark.parametrize("K", [1, 100, 6912, 11000, 12800])
+@pytest.mark.parametrize("K", [1, 100, 6912, 13312, 13376])
 def test_small_list_row_lengths(t, orc, K, fused):
     """Rows from one column to past the shared-memory limit of the
-    pre-loading launch (11,000 columns take it, 12,800 the streaming kernel)."""
+    pre-loading launch (13,312 columns take it, 13,376 the streaming kernel)."""
     rng = synth.rng_for(131, K, int(fused))
     _m1_list(t, orc, rng, [(77, K), (1, K), (130, K)], True, fused)
 
