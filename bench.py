@@ -370,6 +370,11 @@ def run_ours(args):
         torch.cuda.empty_cache()
         configs["config4"] = gpu_config4(dev, stream, args.layers, max(5, min(20, K)), 3)
         torch.cuda.empty_cache()
+        # config 2's token in dependency order (beside this line's independent step)
+        forms, _, oerr = decode_ordered(dev, stream, args.layers, 500, 5, ("paired",))
+        configs["config2_ordered"] = dict(forms["paired"], err_flag=oerr, mlp_form="paired",
+                                          timing="CUDA graph of one token replayed 500 times")
+        torch.cuda.empty_cache()
     timed_clk = clk.summary()
     clocks = dict(sus["clocks"])
     clocks["sampled_during"] = (f"the sustained pass: {sus['launches']} back-to-back launches of this "
@@ -1261,59 +1266,64 @@ def run_mlp(args):
     print(json.dumps(out), flush=True)
 
 
-def run_decode_ordered(args):
-    """The dependency-ordered decode of one token over the 30-layer stack: per
-    layer qkv -> o -> gate/up -> IntMlp + down, each launch reading what the one
+def decode_ordered(dev, stream, layers, steps, warmup, forms=None):
+    """The dependency-ordered decode of one token over the stack: per layer
+    qkv -> o -> gate/up -> IntMlp + down, each launch reading what the one
     before it wrote (the per-matvec ordering of "Tritium ..." -- Why it does not
-    scale), timed as a CUDA graph of one token replayed (120 launches per token
-    with programmatic serialisation)."""
+    scale), timed as a CUDA graph of one token replayed, for each MLP form."""
     import torch
 
-    import __graft_entry__
     import synth
     from bit_plane_select_gb300.stack import LayerChain
-    __graft_entry__.build()
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    stream = torch.cuda.current_stream(dev)
     names = [p[0] for p in synth.PROJECTIONS]
     weights = []
-    for layer in range(args.layers):
+    for layer in range(layers):
         lw = {}
         for i, n in enumerate(names):
             w = synth.stack_weights(SEED, layer, i)
             lw[n] = (torch.from_numpy(w), float(synth.w_scale(w)))
         weights.append(lw)
     chain = LayerChain(weights, dev)
-    for layer in range(args.layers):
+    for layer in range(layers):
         chain.x[layer].copy_(torch.from_numpy(synth.projection_acts(SEED, layer, 0, 1)[0]))
     del weights
+    out = {}
+    for form in forms or LayerChain.MLP_FORMS:
+        chain.mlp_form = form
+        for _ in range(3):
+            chain.step()
+        torch.cuda.synchronize()
+        # the launches of one token captured in a CUDA graph and replayed
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chain.step()
+        ms = _timed(g.replay, steps, warmup, stream)
+        eager = _timed(chain.step, max(20, steps // 10), warmup, stream)
+        out[form] = {"us_per_token": round(ms * 1e3, 2), "tok_per_s": round(1e3 / ms, 1),
+                     "launches_per_token": chain.launches_per_step,
+                     "us_per_launch": round(ms * 1e3 / chain.launches_per_step, 3),
+                     "eager_us_per_token": round(eager * 1e3, 2)}
+        del g
+    return out, chain.step_bytes(), int(chain.err.item())
+
+
+def run_decode_ordered(args):
+    """The dependency-ordered decode of one token over the 30-layer stack in
+    its three MLP forms (paired: gate/up publishing max|t| partials, then the
+    down product forming the IntMlp codes from them, 4 launches per layer;
+    split: a quantiser launch between, 5; fused: max|t| in every down CTA, 4)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
     steps = max(50, min(args.steps, 2000))
-    forms = {}
-    # the three forms of the MLP stage on the same chain: gate/up publishing the
-    # max|t| partials, then the down product forming the codes ("paired", four
-    # launches per layer); the IntMlp quantiser as a launch of its own ("split",
-    # five); every down CTA forming the codes, max|t| pass included ("fused", four)
     with ClockSampler(0) as clk:
-        for form in LayerChain.MLP_FORMS:
-            chain.mlp_form = form
-            for _ in range(3):
-                chain.step()
-            torch.cuda.synchronize()
-            # the launches of one token captured in a CUDA graph and replayed
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                chain.step()
-            ms = _timed(g.replay, steps, args.warmup, stream)
-            eager = _timed(chain.step, max(20, steps // 10), args.warmup, stream)
-            forms[form] = {
-                "us_per_token": round(ms * 1e3, 2), "launches_per_token": chain.launches_per_step,
-                "us_per_launch": round(ms * 1e3 / chain.launches_per_step, 3),
-                "eager_us_per_token": round(eager * 1e3, 2)}
-            del g
+        forms, nbytes, err = decode_ordered(dev, stream, args.layers, steps, args.warmup)
     best = min(forms, key=lambda k: forms[k]["us_per_token"])
     ms = forms[best]["us_per_token"] * 1e-3
-    nbytes = chain.step_bytes()
     peak, peak_kind = peaks()
     out = {"metric": "dependency-ordered batch-1 decode over the 30-layer stack", "unit": "tok/s",
            "value": round(1e3 / ms, 1), "us_per_token": round(ms * 1e3, 2),
@@ -1323,7 +1333,7 @@ def run_decode_ordered(args):
            "launches_per_token": forms[best]["launches_per_token"],
            "us_per_launch": forms[best]["us_per_launch"],
            "algorithmic_bytes_per_token": nbytes,
-           "timing": f"CUDA graph of one token replayed {steps} times", "err_flag": int(chain.err.item()),
+           "timing": f"CUDA graph of one token replayed {steps} times", "err_flag": err,
            "clocks": clk.summary(),
            "config": {"workload": "bitnet-2b4t-30layer-decode-ordered-batch1", "layers": args.layers,
                       "order": "per layer: [q,k,v] <- x; [o] <- q; [gate,up] <- o; IntMlp + [down] "

@@ -50,6 +50,9 @@ def test_bench_records_meet_the_resource_gates():
         c4 = b.get("configs", {}).get("config4", {}).get("by_M", {}).get("2048")
         if c4:
             assert c4["frac_of_sustained_peak"] >= 0.58, name               # R5
+        co = b.get("configs", {}).get("config2_ordered")
+        if isinstance(co, dict):
+            assert co["us_per_token"] <= 700.0 and co["err_flag"] == 0, name  # R7
         clk = b.get("clocks", {})
         bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
         assert not bad & set(clk.get("reasons") or []), name                # R6
