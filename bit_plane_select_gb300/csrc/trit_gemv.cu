@@ -235,7 +235,10 @@ struct List {
     int64_t total_cost;
     uint32_t *err;
     float x_scale_val;      // M = 1 entries whose x_scale is NULL take this input scale
-    int32_t flags;          // pre-loading launches: 1 = copy the planes before the grid dependency
+    int32_t flags;          // pre-loading launches: 1 = copy the planes before the grid
+                            // dependency, 2 = paired gate/up list, 4 = two warps per group
+    int32_t plane_steps;    // pre-loading launches: 16-byte plane slots per lane
+    int32_t pad_;
     MlpDesc mlp[kMaxMlp];
     Entry e[kMaxList];
 };
@@ -1210,7 +1213,9 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
 //
 // Groups are numbered across the list (Entry.cost_begin: the entry's first
 // group; the list's total_cost: all groups); warp w of CTA b takes group
-// 8b + w.  Shared memory: the staged activations (xs_words), then per warp
+// 8b + w, or (split lists, flags bit 2, when twice the CTAs fit one wave)
+// warps w and w + 4 take group 4b + w, one half of its steps each, the second
+// half's code sums joining the first's through shared memory.  Shared memory: the staged activations (xs_words), then per warp
 // iters x 32 lanes x 16 bytes of planes, lane-interleaved so each step's reads
 // are contiguous.
 //
@@ -1223,7 +1228,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
 // descriptor in an unpaired list stages its row from those partials
 // (stage_x_intmlp_parts).
 __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(const __grid_constant__ List L) {
-    static_assert(kWarps == 8, "paired lists split the CTA into two halves of four warps");
+    static_assert(kWarps == 8, "paired and split lists divide the CTA into two halves of four warps");
     extern __shared__ __align__(16) uint32_t xs[];
     __shared__ int32_t s_xsum[kWarps];
     __shared__ float s_mlp_scale;
@@ -1231,11 +1236,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rs = lane / kLanes1, bs = lane % kLanes1;
     asm volatile("griddepcontrol.launch_dependents;");
-    const int max_iters = L.xs_words / (kLanes1 * kXBeatWords);
-    uint4 *pl = reinterpret_cast<uint4 *>(xs + L.xs_words) + (warp * max_iters) * 32 + lane;
+    uint4 *pl = reinterpret_cast<uint4 *>(xs + L.xs_words) + (warp * L.plane_steps) * 32 + lane;
     const int64_t G = L.total_cost;
-    const int64_t cta0 = int64_t(blockIdx.x) * kWarps;
     const bool paired = (L.flags & 2) != 0;
+    const bool split = (L.flags & 4) != 0;   // two warps per group, one per half of the row
+    const int half = split ? warp >> 2 : 0;
+    const int64_t cta0 = int64_t(blockIdx.x) * (split ? 4 : kWarps);
     auto entry_of = [&](int64_t gw) {   // last entry whose first group is <= gw
         int a = 0, b = L.count - 1;
         while (a < b) {
@@ -1256,14 +1262,22 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         we = g < L.e[ew].groups ? ew : -1;
         e0 = e1 = eg;
     } else {
-        const int64_t gw = cta0 + warp;
+        const int span = split ? 4 : kWarps;
+        const int64_t gw = cta0 + (split ? (warp & 3) : warp);
         if (gw < G) {
             we = entry_of(gw);
             g = gw - L.e[we].cost_begin;
         }
-        const int64_t last = cta0 + kWarps - 1 < G ? cta0 + kWarps - 1 : G - 1;
+        const int64_t last = cta0 + span - 1 < G ? cta0 + span - 1 : G - 1;
         e0 = entry_of(cta0);
         e1 = entry_of(last);
+    }
+    // this warp's steps [t0, t1) of its group's rows (split: one half each)
+    int t0 = 0, t1 = 0;
+    if (we >= 0) {
+        const int it = L.e[we].iters, ith = (it + 1) / 2;
+        t0 = split ? half * ith : 0;
+        t1 = split ? (t0 + ith < it ? t0 + ith : it) : it;
     }
     auto copy_planes = [&]() {
         if (we < 0) return;
@@ -1272,9 +1286,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         const uint4 *rp = E.planes + (r < E.N ? r : E.N - 1) * int64_t(E.bstride);
         // beat of step t: bs + 4t, clamped to the row's last beat (the staged
         // activations past the row's end are zero)
-        for (int t = 0; t < E.iters; ++t) {
+        for (int t = t0; t < t1; ++t) {
             const int beat = bs + kLanes1 * t;
-            cpa16(pl + t * 32, rp + (beat < E.B ? beat : E.B - 1));
+            cpa16(pl + (t - t0) * 32, rp + (beat < E.B ? beat : E.B - 1));
         }
         cpa_commit();
     };
@@ -1282,7 +1296,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
     const bool early = (L.flags & 1) != 0;
     if (early) copy_planes();
     uint32_t viol = 0;
-    int32_t my_y = 0;   // paired lists: this lane's row sum (0 where there is none)
+    int32_t my_part = 0, my_xsum = 0;   // this lane's row code sum and the staged row's column sum
+    float my_xsc = 0.0f;
     for (int e = e0; e <= e1; ++e) {
         const Entry &E = L.e[e];
         if (e == e0) {
@@ -1298,7 +1313,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         if (intmlp) {
             stage_x_intmlp_parts(E, L.mlp[mlp_of(E) - 1], xs,
                                  reinterpret_cast<int32_t *>(xs + L.xs_words) +
-                                     kWarps * max_iters * 128,
+                                     kWarps * L.plane_steps * 128,
                                  owner, s_xsum, &s_mlp_scale);
             xsc = 0.0f;   // read from s_mlp_scale after the barrier
         } else if (E.xf) {
@@ -1311,15 +1326,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
         const int32_t xsum = read_xsum(s_xsum);
         if (intmlp) xsc = s_mlp_scale;
         if (we < 0 || (!paired && we != e)) continue;
-        const Entry &W = L.e[we];   // paired: the up warps' entry is not the staged one
         cpa_wait_all();
         const uint4 *xb = reinterpret_cast<const uint4 *>(xs) + bs * kXBeatVec;
         int acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0;
 #pragma unroll 2
-        for (int t = 0; t < W.iters; ++t) {
-            const uint4 v = pl[t * 32];
+        for (int t = t0; t < t1; ++t) {
+            const uint4 v = pl[(t - t0) * 32];
             viol |= (v.x & v.z) | (v.y & v.w);
             const uint4 *X = xb + t * (kLanes1 * kXBeatVec);
             const uint4 a0 = X[0], a1 = X[1], a2 = X[2], a3 = X[3];
@@ -1328,20 +1342,29 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
             mac_codes(v.x, v.z, xl, acc);
             mac_codes(v.y, v.w, xh, acc);
         }
-        const int32_t y = row_sum1(codes_total(acc)) - xsum;
-        const int64_t row = g * kRowsPerGroup + rs;
-        if (row < W.N) my_y = y;
-        if (bs == 0 && row < W.N) {
-            if (W.acc) {
-                atomicAdd(W.acc + row, y);
-            } else {
-                if (W.y_i32) W.y_i32[row] = y;
-                if (W.y_f32) W.y_f32[row] = dequant(y, W.w_scale, xsc);
-            }
+        my_part = row_sum1(codes_total(acc));
+        my_xsum = xsum;
+        my_xsc = xsc;
+    }
+    int32_t y = my_part - my_xsum;
+    if (split) {   // the second half's code sums join the first half's (same rows)
+        if (half == 1 && bs == 0) s_pair[0][warp & 3][rs] = my_part;
+        __syncthreads();
+        y += s_pair[0][warp & 3][rs];
+    }
+    const int64_t row = g * kRowsPerGroup + rs;
+    const bool mine = we >= 0 && half == 0 && row < L.e[we].N;
+    if (mine && bs == 0) {
+        const Entry &W = L.e[we];   // paired: the up warps' entry is not the staged one
+        if (W.acc) {
+            atomicAdd(W.acc + row, y);
+        } else {
+            if (W.y_i32) W.y_i32[row] = y;
+            if (W.y_f32) W.y_f32[row] = dequant(y, W.w_scale, my_xsc);
         }
     }
     if (paired) {
-        if (bs == 0) s_pair[warp >> 2][warp & 3][rs] = my_y;
+        if (bs == 0) s_pair[warp >> 2][warp & 3][rs] = mine ? y : 0;
         __syncthreads();
         if (warp == 0) {
             bool neg;
@@ -1374,6 +1397,9 @@ constexpr size_t kPreSmemMax = 225 * 1024;
 #ifndef TRIT_PRE_LOAD
 #define TRIT_PRE_LOAD 1
 #endif
+#ifndef TRIT_PRE_SPLIT
+#define TRIT_PRE_SPLIT 1
+#endif
 
 __host__ __device__ constexpr int64_t pre_iters(int64_t K) { return ((K + 63) / 64 + kLanes1 - 1) / kLanes1; }
 // Shared memory of a pre-loading launch whose longest row has `iters` steps:
@@ -1389,6 +1415,50 @@ size_t pre_smem(int64_t iters, bool intmlp = false) {
 // with one group per warp.  Returns false (nothing launched) otherwise; true
 // with the launch's status in `status`.  Paired lists: entries 2p, 2p + 1 are
 // the gate and up products of IntMlp block p (mlp[p] receives the partials).
+// Resident CTAs per SM of the pre-loading kernel with `smem` bytes of dynamic
+// shared memory (a few sizes recur: cached).  The first call on a device sets
+// the kernel's shared-memory limit and carve-out.
+cudaError_t pre_occupancy(size_t smem, int &occ) {
+    struct Slot { int dev; size_t smem; int occ; };
+    static thread_local Slot cache[8];
+    static thread_local int used = 0, next = 0, ready_dev = -1;
+    int dev = 0;
+    cudaError_t st = cudaGetDevice(&dev);
+    if (st != cudaSuccess) return st;
+    for (int i = 0; i < used; ++i)
+        if (cache[i].dev == dev && cache[i].smem == smem) {
+            occ = cache[i].occ;
+            return cudaSuccess;
+        }
+    if (ready_dev != dev) {
+        st = cudaFuncSetAttribute(select_accumulate_pre_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(kPreSmemMax));
+        if (st != cudaSuccess) return st;
+        // one shared-memory carve-out for every launch of this kernel, so that
+        // the CTAs of a launch can become resident beside those of the one
+        // before it (a carve-out change waits for the SM to drain)
+        st = cudaFuncSetAttribute(select_accumulate_pre_kernel,
+                                  cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  int(cudaSharedmemCarveoutMaxShared));
+        if (st != cudaSuccess) return st;
+        ready_dev = dev;
+    }
+    st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_accumulate_pre_kernel, kThreads,
+                                                       smem);
+    if (st != cudaSuccess) return st;
+    cache[next] = Slot{dev, smem, occ};
+    next = (next + 1) % 8;
+    if (used < 8) ++used;
+    return cudaSuccess;
+}
+
+// Launch entries[0..n) (M = 1) on the pre-loading kernel when every entry
+// holds whole rows and, unless forced, the list's groups fit one resident wave
+// with one group per warp.  Returns false (nothing launched) otherwise; true
+// with the launch's status in `status`.  Paired lists: entries 2p, 2p + 1 are
+// the gate and up products of IntMlp block p (mlp[p] receives the partials).
+// Unpaired lists take two warps per group (split) when twice the CTAs, each
+// holding half the steps' planes, still fit one wave.
 bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
                      float x_scale_val, cudaError_t &status, const MlpDesc *mlp = nullptr,
                      int nmlp = 0, bool paired = false, bool force = false) {
@@ -1404,8 +1474,29 @@ bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
         if (entries[i].iters > max_iters) max_iters = entries[i].iters;
     }
     const int xs_words = max_iters * kLanes1 * kXBeatWords;
-    const size_t smem = pre_smem(max_iters, nmlp > 0 && !paired);
+    const bool rows = nmlp > 0 && !paired;   // IntMlp rows staged through shared memory
+    auto smem_of = [&](int steps) {
+        return size_t(xs_words) * 4 + size_t(kWarps) * steps * 32 * 16 +
+               (rows ? size_t(max_iters) * 2 * 256 * 4 : 0);
+    };
+    const int64_t sms = device_sm_count();
+    int steps = max_iters, occ = 0;
+    bool split = false;
+    if (!paired && TRIT_PRE_SPLIT && smem_of((max_iters + 1) / 2) <= kPreSmemMax) {
+        status = pre_occupancy(smem_of((max_iters + 1) / 2), occ);
+        if (status != cudaSuccess) return true;
+        if ((groups + 3) / 4 <= int64_t(occ) * sms) {
+            split = true;
+            steps = (max_iters + 1) / 2;
+            grid = (groups + 3) / 4;
+        }
+    }
+    const size_t smem = smem_of(steps);
     if (smem > kPreSmemMax) return false;
+    if (!split) {
+        status = pre_occupancy(smem, occ);
+        if (status != cudaSuccess) return true;
+    }
     static thread_local List L;
     if (paired) {
         for (int p = 0; p < n / 2; ++p) {
@@ -1421,36 +1512,14 @@ bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
             L.e[i].cost_begin = g;
             g += entries[i].groups;
         }
-        grid = (groups + kWarps - 1) / kWarps;
+        if (!split) grid = (groups + kWarps - 1) / kWarps;
     }
-    static thread_local size_t last_smem = ~size_t(0);
-    static thread_local int last_dev = -1, last_occ = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (smem != last_smem || dev != last_dev) {
-        status = cudaFuncSetAttribute(select_accumulate_pre_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (status != cudaSuccess) return true;
-        // one shared-memory carve-out for every launch of this kernel, so that
-        // the CTAs of a launch can become resident beside those of the one
-        // before it (a carve-out change waits for the SM to drain)
-        status = cudaFuncSetAttribute(select_accumulate_pre_kernel,
-                                      cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      int(cudaSharedmemCarveoutMaxShared));
-        if (status != cudaSuccess) return true;
-        int occ = 0;
-        status = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_accumulate_pre_kernel,
-                                                               kThreads, smem);
-        if (status != cudaSuccess) return true;
-        last_occ = occ;
-        last_smem = smem;
-        last_dev = dev;
-    }
-    if (!force && grid > int64_t(last_occ) * device_sm_count()) return false;
+    if (!force && grid > int64_t(occ) * sms) return false;
     L.count = n;
     L.err = err;
     L.x_scale_val = x_scale_val;
-    L.flags = (early ? 1 : 0) | (paired ? 2 : 0);
+    L.flags = (early ? 1 : 0) | (paired ? 2 : 0) | (split ? 4 : 0);
+    L.plane_steps = steps;
     for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = i < nmlp ? mlp[i] : MlpDesc{};
     L.total_cost = paired ? grid * kWarps : groups;
     L.xs_words = xs_words;
@@ -1498,6 +1567,8 @@ cudaError_t launch_list(const Entry *entries, int n, uint32_t *err, cudaStream_t
     L.err = err;
     L.x_scale_val = x_scale_val;
     L.flags = 0;
+    L.plane_steps = 0;
+    L.pad_ = 0;
     for (int i = 0; i < kMaxMlp; ++i) L.mlp[i] = i < nmlp ? mlp[i] : MlpDesc{};
     int64_t cost = 0, groups = 0;
     int max_iters = 1;
