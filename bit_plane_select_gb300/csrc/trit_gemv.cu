@@ -227,7 +227,7 @@ struct MlpDesc {
     int32_t ntmax;
     int32_t pad_;
 };
-constexpr int kMaxMlp = 8;
+constexpr int kMaxMlp = 32;   // IntMlp descriptors per launch (the list fits 32 KB of parameters)
 
 struct List {
     int32_t count;

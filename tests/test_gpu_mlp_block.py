@@ -108,12 +108,13 @@ def test_mlp_block_matches_oracle(t, orc, K, F, N, ready):
 
 
 def test_mlp_blocks_in_one_call(t, orc):
-    """Nine blocks in one call (two launches of at most eight pairs each),
+    """Thirty-four blocks in one call (two launches of at most 32 pairs each),
     mixed shapes, one past the pre-loading limit, some without h outputs;
     repeated so the partials of a second token overwrite the first."""
     rng = synth.rng_for(141)
     shapes = [(2560, 6912, 2560), (2560, 2560, 640), (128, 200, 300), (13376, 64, 16),
               (640, 96, 8), (200, 33, 65), (2560, 6912, 2560), (64, 64, 64), (320, 1111, 77)]
+    shapes += [(64 + 64 * (i % 3), 40 + i, 24) for i in range(25)]
     blocks = [make_block(t, rng, K, F, N, outs=(i % 3 != 1)) for i, (K, F, N) in enumerate(shapes)]
     for rep in range(2):
         if rep:
