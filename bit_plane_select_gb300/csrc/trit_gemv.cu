@@ -227,7 +227,7 @@ struct MlpDesc {
     int32_t ntmax;
     int32_t pad_;
 };
-constexpr int kMaxMlp = 32;   // IntMlp descriptors per launch (the list fits 32 KB of parameters)
+constexpr int kMaxMlp = 8;   // IntMlp descriptors per launch (each adds 48 bytes to every launch's parameters)
 
 struct List {
     int32_t count;
@@ -1497,6 +1497,10 @@ bool launch_list_pre(const Entry *entries, int n, uint32_t *err, cudaStream_t s,
         status = pre_occupancy(smem, occ);
         if (status != cudaSuccess) return true;
     }
+    // lists longer than a wave go to the streaming kernel: decided before any
+    // copying (a decode step's list takes this exit on every launch)
+    if (!force && !paired && !split && (groups + kWarps - 1) / kWarps > int64_t(occ) * sms)
+        return false;
     static thread_local List L;
     if (paired) {
         for (int p = 0; p < n / 2; ++p) {

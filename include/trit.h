@@ -282,7 +282,7 @@ typedef struct trit_mlpproj {
  * outputs followed by trit_gemv of the codes: y_i32, y_f32 and, when asked for,
  * h_i8 and h_scale are bit-identical to that two-call path.  Every CTA of the
  * launch forms the codes it needs while staging the row, so the int8 codes
- * make no round trip through memory; up to 32 entries share one launch (longer
+ * make no round trip through memory; up to 8 entries share one launch (longer
  * lists take several).  K is limited to TRIT_MAX_FUSED_K (TRIT_E_SHAPE beyond);
  * w_gate, w_up and w_scale must be finite and > 0 (TRIT_E_SCALE).  `list` is a
  * host array; asynchronous on `stream`.
@@ -317,7 +317,7 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
  *   h_i8       out, may be NULL: [F_pad] int8, zero tail, 16-byte aligned
  *   h_scale    out, may be NULL: [1] fp32
  *   y_i32, y_f32  [N] outputs, either may be NULL (not both)
- * `list` is a host array; up to 32 blocks share one launch.
+ * `list` is a host array; up to 8 blocks share one launch.
  */
 typedef struct trit_mlp_block {
     const uint8_t *gate_planes;

@@ -108,7 +108,7 @@ def test_mlp_block_matches_oracle(t, orc, K, F, N, ready):
 
 
 def test_mlp_blocks_in_one_call(t, orc):
-    """Thirty-four blocks in one call (two launches of at most 32 pairs each),
+    """Thirty-four blocks in one call (five launches of at most eight pairs each),
     mixed shapes, one past the pre-loading limit, some without h outputs;
     repeated so the partials of a second token overwrite the first."""
     rng = synth.rng_for(141)
