@@ -1215,9 +1215,10 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
 // group; the list's total_cost: all groups); warp w of CTA b takes group
 // 8b + w, or (split lists, flags bit 2, when twice the CTAs fit one wave)
 // warps w and w + 4 take group 4b + w, one half of its steps each, the second
-// half's code sums joining the first's through shared memory.  Shared memory: the staged activations (xs_words), then per warp
-// iters x 32 lanes x 16 bytes of planes, lane-interleaved so each step's reads
-// are contiguous.
+// half's code sums joining the first's through shared memory.  Shared memory:
+// the staged activations (xs_words), then per warp plane_steps x 32 lanes x
+// 16 bytes of planes, lane-interleaved so each step's reads are contiguous,
+// then (IntMlp rows) the gate and up outputs.
 //
 // Paired lists (flags bit 1: the gate and up projections of IntMlp blocks,
 // entries 2p and 2p + 1, one input row): the c-th CTA of pair p stages the row
