@@ -1762,15 +1762,52 @@ bool mlp_pairs_supported(int64_t K, int64_t F) {
     return pre_smem(pre_iters(K)) <= kPreSmemMax && pre_smem(pre_iters(F), true) <= kPreSmemMax;
 }
 
-// Gate and up of each block: blocks that the pre-loading kernel takes go as
-// paired lists (publishing the max|t| partials), the others as fused
-// quantise-and-multiply products (their down launch reduces max|t| itself).
+// Gate and up of each block.  Blocks that the pre-loading kernel takes go as
+// paired lists (publishing the max|t| partials) when all their 32-row tiles
+// fit one resident wave -- the batch-1 chain of one block per call; longer
+// lists go as fused quantise-and-multiply products on the streaming kernel,
+// followed by one launch forming the same partials from a_gate and a_up.
+// Blocks the pre-loading kernel does not take need no partials (their down
+// launch reduces max|t| itself).
 cudaError_t launch_mlp_gate_up(const MlpBlockDev *list, int count, uint32_t *err, cudaStream_t s) {
     static thread_local Entry buf[2 * kMaxMlp];
     static thread_local MlpDesc desc[kMaxMlp];
     static thread_local ProjDev rest[TRIT_MAX_LIST_PER_LAUNCH];
-    int n = 0, nr = 0;
+    static thread_local MlpTmaxJob jobs[TRIT_MAX_LIST_PER_LAUNCH];
+    int n = 0, nr = 0, nj = 0;
     cudaError_t e = cudaSuccess;
+    int64_t tiles = 0;
+    int iters = 1;
+    for (int i = 0; i < count; ++i)
+        if (mlp_pairs_supported(list[i].gate.K, list[i].gate.N)) {
+            tiles += mlp_tmax_parts(list[i].gate.N);
+            const int it = int(pre_iters(list[i].gate.K));
+            iters = it > iters ? it : iters;
+        }
+    bool paired = true;
+    if (tiles) {
+        int occ = 0;
+        e = pre_occupancy(pre_smem(iters), occ);
+        if (e != cudaSuccess) return e;
+        paired = tiles <= int64_t(occ) * device_sm_count();
+    }
+    if (!paired) {
+        for (int i = 0; i < count && e == cudaSuccess; ++i) {
+            const MlpBlockDev &b = list[i];
+            rest[nr++] = b.gate;
+            rest[nr++] = b.up;
+            if (mlp_pairs_supported(b.gate.K, b.gate.N))
+                jobs[nj++] = MlpTmaxJob{b.gate.y_i32, b.up.y_i32, b.gate.N, b.tmax};
+            if (nr + 2 > TRIT_MAX_LIST_PER_LAUNCH) {
+                e = launch_gemv_many(rest, nr, err, s);
+                if (e == cudaSuccess && nj) e = launch_mlp_tmax(jobs, nj, s);
+                nr = nj = 0;
+            }
+        }
+        if (e == cudaSuccess && nr) e = launch_gemv_many(rest, nr, err, s);
+        if (e == cudaSuccess && nj) e = launch_mlp_tmax(jobs, nj, s);
+        return e;
+    }
     auto flush = [&]() {
         if (n && e == cudaSuccess &&
             !launch_list_pre(buf, 2 * n, err, s, 0.0f, e, desc, n, true, true))

@@ -414,6 +414,15 @@ cudaError_t launch_issue_probe(int kind, int blocks, int threads, int64_t iters,
                                unsigned long long *rec, cudaStream_t s);
 cudaError_t launch_check_div127(uint64_t lo, uint64_t hi, unsigned long long *mismatches,
                                 cudaStream_t s);
+// max|t| partials of IntMlp blocks from their gate and up outputs: partial k of
+// a block is max |relu(a_gate[c])^2 a_up[c]| over c in [32k, 32k + 32), the
+// format the paired gate/up launch publishes (hi, lo words).
+struct MlpTmaxJob {
+    const int32_t *a_gate, *a_up;
+    int64_t F;
+    uint64_t *tmax;
+};
+cudaError_t launch_mlp_tmax(const MlpTmaxJob *jobs, int n, cudaStream_t s);
 cudaError_t launch_intmlp_quant(const int32_t *ag, const int32_t *au, int64_t M, int64_t N,
                                 float w_g, float w_u, const float *x_scale, int8_t *q,
                                 float *h_scale, cudaStream_t s);

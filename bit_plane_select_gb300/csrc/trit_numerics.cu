@@ -218,7 +218,72 @@ int rows_grid(int64_t M) {
     return int(M < cap ? M : cap);
 }
 
+// ---- max|t| partials ---------------------------------------------------------------
+
+constexpr int kMaxTmaxJobs = 32;
+struct TmaxJobs {
+    MlpTmaxJob job[kMaxTmaxJobs];
+    int64_t warp_begin[kMaxTmaxJobs + 1];   // prefix sums of ceil(F / 32)
+    int32_t count;
+};
+
+// One warp per partial: lane l takes column 32k + l of its block.  Launched
+// with programmatic serialisation: the gate and up outputs are read after the
+// preceding grid.
+__global__ void __launch_bounds__(256) mlp_tmax_kernel(const __grid_constant__ TmaxJobs J) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t gw = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= J.warp_begin[J.count]) return;   // whole warps only: no block barrier follows
+    int j = 0;
+    while (j + 1 < J.count && J.warp_begin[j + 1] <= gw) ++j;
+    const MlpTmaxJob &B = J.job[j];
+    const int64_t k = gw - J.warp_begin[j];
+    const int64_t c = 32 * k + lane;
+    bool neg;
+    const trit_u128 t = c < B.F ? intmlp_abs_t(B.a_gate[c], B.a_up[c], neg) : trit_u128(0);
+    uint64_t hi = uint64_t(t >> 64), lo = uint64_t(t);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const uint64_t h2 = __shfl_xor_sync(~0u, hi, o), l2 = __shfl_xor_sync(~0u, lo, o);
+        if (h2 > hi || (h2 == hi && l2 > lo)) {
+            hi = h2;
+            lo = l2;
+        }
+    }
+    if (lane == 0) {
+        B.tmax[2 * k] = hi;
+        B.tmax[2 * k + 1] = lo;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_mlp_tmax(const MlpTmaxJob *jobs, int n, cudaStream_t s) {
+    static thread_local TmaxJobs J;
+    for (int base = 0; base < n; base += kMaxTmaxJobs) {
+        const int m = n - base < kMaxTmaxJobs ? n - base : kMaxTmaxJobs;
+        J.count = m;
+        J.warp_begin[0] = 0;
+        for (int i = 0; i < m; ++i) {
+            J.job[i] = jobs[base + i];
+            J.warp_begin[i + 1] = J.warp_begin[i] + (jobs[base + i].F + 31) / 32;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned((J.warp_begin[m] + 7) / 8));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, mlp_tmax_kernel, J);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 cudaError_t launch_quant_folded(const float *x, const float *g, int64_t M, int64_t K, float eps,
                                 int8_t *q, float *x_scale, uint32_t *err, cudaStream_t s) {
