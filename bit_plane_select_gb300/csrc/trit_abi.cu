@@ -385,7 +385,7 @@ TRIT_API trit_status trit_quant_gemv_many(const trit_qproj *list, int32_t count,
 }
 
 
-TRIT_API int64_t trit_mlp_tmax_bytes(int64_t F) { return F < 1 ? 0 : 16 * mlp_tmax_parts(F); }
+TRIT_API int64_t trit_mlp_tmax_bytes(int64_t F) { return F < 1 ? 0 : mlp_tmax_bytes(F); }
 
 TRIT_API trit_status trit_mlp_gate_up(const trit_mlp_block *list, int32_t count,
                                       uint32_t *err_flag, trit_stream_t stream) {

@@ -611,34 +611,27 @@ __device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_gro
 __device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // IntMlp input of a pre-loading launch (M = 1): as stage_x_intmlp, but max|t|
-// is reduced from the D.ntmax per-CTA partials the paired gate/up launch
-// published, so the row is read once: a_gate and a_up are copied into shared
-// memory (rows: iters x 256 int32 each) with every copy in flight together
-// with the partials' loads, and the codes follow the reduction.  The last
-// thread forms the scale (its double-precision factor first); the scale goes
-// to *s_scale, readable after the staging barrier.  The owner CTA also writes
-// the natural-layout codes (zero tail to K_pad) and the scale.
+// is reduced from the D.ntmax per-CTA partials the gate/up launch published,
+// and each column's code starts from the signed fp32 product it published
+// beside them (intmlp_tf), so the row is read once and as 4 bytes a column:
+// the products are copied into shared memory (rows: iters x 256 fp32) with
+// every copy in flight together with the partials' loads, and the codes follow
+// the reduction; a column near a tie reads its a_gate and a_up for the exact
+// path.  The last thread forms the scale (its double-precision factor while
+// the loads are in flight); the scale goes to *s_scale, readable after the
+// staging barrier.  The owner CTA also writes the natural-layout codes (zero
+// tail to K_pad) and the scale.
 __device__ __forceinline__ void stage_x_intmlp_parts(const Entry &E, const MlpDesc &D, uint32_t *xs,
                                                      int32_t *rows, bool owner, int32_t *s_xsum,
                                                      float *s_scale) {
     __shared__ uint64_t s_m[2][kWarps];
     const int K = E.K;
     const int nq = (K + 3) / 4, sq = E.iters * kLanes1 * 16;
-    int32_t *sg = rows, *su = rows + 4 * sq;
-    const bool vec = (K % 4 == 0) && ((reinterpret_cast<uintptr_t>(D.a_gate) & 15) == 0) &&
-                     ((reinterpret_cast<uintptr_t>(D.a_up) & 15) == 0);
-    if (vec) {
-        for (int q = threadIdx.x; q < nq; q += kThreads) {
-            cpa16(sg + 4 * q, D.a_gate + 4 * q);
-            cpa16(su + 4 * q, D.a_up + 4 * q);
-        }
-        cpa_commit();
-    } else {
-        for (int c = threadIdx.x; c < K; c += kThreads) {
-            sg[c] = D.a_gate[c];
-            su[c] = D.a_up[c];
-        }
-    }
+    float *st = reinterpret_cast<float *>(rows);
+    // the products buffer holds 32 values per partial (zero past K): whole quads
+    const float *tfg = mlp_tf_of(D.tmax, D.ntmax);
+    for (int q = threadIdx.x; q < nq; q += kThreads) cpa16(st + 4 * q, tfg + 4 * q);
+    cpa_commit();
     const bool scaler = threadIdx.x == kThreads - 1;
     uint64_t hi = 0, lo = 0;
     auto umax = [&](uint64_t h2, uint64_t l2) {
@@ -658,27 +651,27 @@ __device__ __forceinline__ void stage_x_intmlp_parts(const Entry &E, const MlpDe
         s_m[1][threadIdx.x >> 5] = lo;
     }
     cpa_wait_all();
-    __syncthreads();   // the partials' maxima and every copied row word
+    __syncthreads();   // the partials' maxima and every copied product
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) umax(s_m[0][i], s_m[1][i]);
     const IntMlpRow R = intmlp_row(hi, lo);
     const int64_t Kp = beats_per_row(K) * 64;
     int32_t xsum = 0;
     for (int q = threadIdx.x; q < sq; q += kThreads) {
-        int4 g = make_int4(0, 0, 0, 0), u = make_int4(0, 0, 0, 0);
-        if (q < nq) {
+        const float4 f = q < nq ? *reinterpret_cast<const float4 *>(st + 4 * q)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        bool n0, n1, n2, n3;
+        int c0 = intmlp_code_tf(f.x, R, n0), c1 = intmlp_code_tf(f.y, R, n1);
+        int c2 = intmlp_code_tf(f.z, R, n2), c3 = intmlp_code_tf(f.w, R, n3);
+        if (n0 | n1 | n2 | n3) {   // rare: a column within 1.5e-4 of a tie (never past K)
             const int c = 4 * q;
-            if (c + 4 <= K) {
-                g = *reinterpret_cast<const int4 *>(sg + c);
-                u = *reinterpret_cast<const int4 *>(su + c);
-            } else {
-                g.x = sg[c];
-                u.x = su[c];
-                if (c + 1 < K) { g.y = sg[c + 1]; u.y = su[c + 1]; }
-                if (c + 2 < K) { g.z = sg[c + 2]; u.z = su[c + 2]; }
-            }
+            const uint64_t ah = uint64_t(R.A >> 64), al = uint64_t(R.A);
+            if (n0) c0 = intmlp_code_exact(D.a_gate[c], D.a_up[c], ah, al, R.k, R.small);
+            if (n1) c1 = intmlp_code_exact(D.a_gate[c + 1], D.a_up[c + 1], ah, al, R.k, R.small);
+            if (n2) c2 = intmlp_code_exact(D.a_gate[c + 2], D.a_up[c + 2], ah, al, R.k, R.small);
+            if (n3) c3 = intmlp_code_exact(D.a_gate[c + 3], D.a_up[c + 3], ah, al, R.k, R.small);
         }
-        const uint32_t w = intmlp_codes4(g, u, R);
+        const uint32_t w = pack4(c0, c1, c2, c3);
         xsum = dp4a_ss(w, 0x01010101u, xsum);
         if (owner && E.x_i8_out && int64_t(q) * 4 < Kp)
             *reinterpret_cast<uint32_t *>(E.x_i8_out + int64_t(q) * 4) = w;
@@ -1380,11 +1373,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_accumulate_pre_kernel(cons
                     lo = l2;
                 }
             }
+            const MlpDesc &D = L.mlp[mlp_of(L.e[e0]) - 1];
             if (lane == 0) {
-                uint64_t *tm = L.mlp[mlp_of(L.e[e0]) - 1].tmax + 2 * pc;
-                tm[0] = hi;
-                tm[1] = lo;
+                D.tmax[2 * pc] = hi;
+                D.tmax[2 * pc + 1] = lo;
             }
+            // each row's signed fp32 product, for the down launch's codes
+            mlp_tf_of(D.tmax, D.ntmax)[32 * pc + lane] =
+                intmlp_tf(s_pair[0][lane >> 3][lane & 7], s_pair[1][lane >> 3][lane & 7]);
         }
     }
     if (__any_sync(~0u, viol != 0) && lane == 0) atomicOr(L.err, TRIT_ERR_P1);

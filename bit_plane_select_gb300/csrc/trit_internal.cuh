@@ -224,6 +224,24 @@ __device__ __forceinline__ int intmlp_code_est(int32_t ag, int32_t au, const Int
     return intmlp_code_exact(ag, au, uint64_t(R.A >> 64), uint64_t(R.A), R.k, R.small);
 }
 
+// The same estimate from the column's signed fp32 product tf = fl(fl(g)^2) *
+// fl(|u|) with u's sign (g = relu(a_g); 0 where the code is 0), formed by the
+// producer with exactly intmlp_code_fast's operations, so p is the same.
+__device__ __forceinline__ float intmlp_tf(int32_t ag, int32_t au) {
+    const float g = __int2float_rn(ag > 0 ? ag : 0);
+    const float tf = __fmul_rn(__fmul_rn(g, g), fabsf(__int2float_rn(au)));
+    return au < 0 ? -tf : tf;
+}
+__device__ __forceinline__ int intmlp_code_tf(float tfs, const IntMlpRow &R, bool &near) {
+    const float p = __fmul_rn(fabsf(tfs), R.kf);
+    const float big = __fadd_rn(p, 12582912.0f);
+    const float fr = __fsub_rn(p, __fsub_rn(big, 12582912.0f));
+    near = fabsf(fr) >= 0.49985f;
+    int q = __float_as_int(big) - 0x4B400000;
+    q = q > 127 ? 127 : q;
+    return tfs < 0.0f ? -q : q;
+}
+
 // Four columns' codes packed as bytes (column c in byte c).
 __device__ __forceinline__ uint32_t intmlp_codes4(int4 g, int4 u, const IntMlpRow &R) {
     bool n0, n1, n2, n3;
@@ -367,6 +385,13 @@ struct MlpBlockDev {
     uint64_t *tmax;   // 2 words (hi, lo) per partial
 };
 int64_t mlp_tmax_parts(int64_t F);
+// The workspace of a block: mlp_tmax_parts(F) partials (hi, lo words), then
+// 32 fp32 per partial: the signed products intmlp_tf of the partial's columns
+// (0 past F).
+inline int64_t mlp_tmax_bytes(int64_t F) { return mlp_tmax_parts(F) * (16 + 32 * 4); }
+__host__ __device__ inline float *mlp_tf_of(uint64_t *tmax, int64_t parts) {
+    return reinterpret_cast<float *>(tmax + 2 * parts);
+}
 bool mlp_pairs_supported(int64_t K, int64_t F);
 cudaError_t launch_mlp_gate_up(const MlpBlockDev *list, int count, uint32_t *err, cudaStream_t s);
 cudaError_t launch_mlp_down(const MlpBlockDev *list, int count, uint32_t *err, cudaStream_t s);

@@ -227,7 +227,8 @@ struct TmaxJobs {
     int32_t count;
 };
 
-// One warp per partial: lane l takes column 32k + l of its block.  Launched
+// One warp per partial: lane l takes column 32k + l of its block and also
+// stores its signed fp32 product (the workspace layout of mlp_tmax_bytes).  Launched
 // with programmatic serialisation: the gate and up outputs are read after the
 // preceding grid.
 __global__ void __launch_bounds__(256) mlp_tmax_kernel(const __grid_constant__ TmaxJobs J) {
@@ -256,6 +257,8 @@ __global__ void __launch_bounds__(256) mlp_tmax_kernel(const __grid_constant__ T
         B.tmax[2 * k] = hi;
         B.tmax[2 * k + 1] = lo;
     }
+    // the column's signed fp32 product, for the down launch's codes (0 past F)
+    mlp_tf_of(B.tmax, (B.F + 31) / 32)[c] = c < B.F ? intmlp_tf(B.a_gate[c], B.a_up[c]) : 0.0f;
 }
 
 }  // namespace

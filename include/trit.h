@@ -296,7 +296,7 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
  *     does (x_scale out) and multiplied by the gate and up planes (F x K each)
  *     into a_gate and a_up (int32, F values each); each CTA of the launch also
  *     forms t = relu(a_gate)^2 * a_up of the rows it computed and stores their
- *     max |t| in `tmax`.
+ *     max |t| and, per column, a signed fp32 form of t in `tmax`.
  *   trit_mlp_down: the down projection (N x F) of the codes of t --
  *     round-half-even(127 t / max|t|), exact, max|t| reduced from `tmax` --
  *     with scale max|t| * S_g^2 * S_u (S = w * x_scale / 127): y_i32 / y_f32
@@ -337,7 +337,7 @@ typedef struct trit_mlp_block {
     uint32_t flags;           /* 0 or TRIT_PROJ_PLANES_READY (all three planes) */
 } trit_mlp_block;
 
-/* Bytes of the tmax workspace of a block with F gate/up rows (16 per 32 rows). */
+/* Bytes of the tmax workspace of a block with F gate/up rows (144 per 32 rows). */
 TRIT_API int64_t trit_mlp_tmax_bytes(int64_t F);
 TRIT_API trit_status trit_mlp_gate_up(const trit_mlp_block *list, int32_t count,
                                       uint32_t *err_flag, trit_stream_t stream);

@@ -89,10 +89,10 @@ def test_struct_layouts_match_the_c_compiler(trit, tmp_path):
 
 def test_mlp_block_validation(trit):
     """trit_mlp_gate_up / trit_mlp_down reject bad blocks before touching a
-    device; the partials workspace is 16 bytes per 32 gate/up rows."""
+    device; the partials workspace is 144 bytes per 32 gate/up rows."""
     L = trit.lib()
-    assert L.trit_mlp_tmax_bytes(6912) == 16 * 216
-    assert L.trit_mlp_tmax_bytes(1) == 16 and L.trit_mlp_tmax_bytes(33) == 32
+    assert L.trit_mlp_tmax_bytes(6912) == 144 * 216
+    assert L.trit_mlp_tmax_bytes(1) == 144 and L.trit_mlp_tmax_bytes(33) == 288
     assert L.trit_mlp_tmax_bytes(0) == 0
     p, null, odd = ctypes.c_void_p(1 << 16), None, ctypes.c_void_p((1 << 16) + 4)
     s = ctypes.c_void_p(None)
