@@ -1211,7 +1211,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks(MT))
 // half's code sums joining the first's through shared memory.  Shared memory:
 // the staged activations (xs_words), then per warp plane_steps x 32 lanes x
 // 16 bytes of planes, lane-interleaved so each step's reads are contiguous,
-// then (IntMlp rows) the gate and up outputs.
+// then (IntMlp rows) the row's signed fp32 products.
 //
 // Paired lists (flags bit 1: the gate and up projections of IntMlp blocks,
 // entries 2p and 2p + 1, one input row): the c-th CTA of pair p stages the row
@@ -1400,8 +1400,10 @@ constexpr size_t kPreSmemMax = 225 * 1024;
 
 __host__ __device__ constexpr int64_t pre_iters(int64_t K) { return ((K + 63) / 64 + kLanes1 - 1) / kLanes1; }
 // Shared memory of a pre-loading launch whose longest row has `iters` steps:
-// the staged activations, every warp's planes and, with IntMlp rows, their
-// gate and up outputs (iters x 256 int32 each).
+// the staged activations, every warp's planes and, with IntMlp rows, two
+// arrays of iters x 256 words: the staging uses one (the signed fp32
+// products); the size also keeps one such CTA per SM (measured: two sharing
+// an SM made the ordered token 7% slower).
 size_t pre_smem(int64_t iters, bool intmlp = false) {
     return size_t(iters) * kLanes1 * kXBeatWords * 4 + size_t(kWarps) * iters * 32 * 16 +
            (intmlp ? size_t(iters) * 2 * 256 * 4 : 0);
