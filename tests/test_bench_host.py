@@ -55,6 +55,19 @@ def test_traffic_only_while_the_source_is_unchanged(bench, monkeypatch):
     assert bench.committed_traffic(0) is None
 
 
+def test_source_hash_sees_code_not_comments(bench, monkeypatch, tmp_path):
+    """The traffic record is keyed on the kernel sources' code: a comment or a
+    blank line does not change the hash, a changed statement does."""
+    src = tmp_path / "k.cu"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    src.write_text("int f(int x) {\n    return x + 1;   // one\n}\n")
+    h0 = bench.source_hash(["k.cu"])
+    src.write_text("// a new header\n/* a block\n   comment */\nint f(int x) {\n\n    return x + 1;   // two\n}\n")
+    assert bench.source_hash(["k.cu"]) == h0
+    src.write_text("int f(int x) {\n    return x + 2;\n}\n")
+    assert bench.source_hash(["k.cu"]) != h0
+
+
 
 def test_batch_floors(bench):
     """The floors of the path each M takes: the HBM bytes at the copy peak; for
