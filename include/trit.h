@@ -291,12 +291,15 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
                                            uint32_t *err_flag, trit_stream_t stream);
 
 /*
- * One batch-1 MLP block in two launches ("Tritium ..." -- Numerics, IntMlp):
+ * Batch-1 MLP blocks in two calls ("Tritium ..." -- Numerics, IntMlp):
  *   trit_mlp_gate_up: the fp32 row x (K values) quantised as trit_quant_act
  *     does (x_scale out) and multiplied by the gate and up planes (F x K each)
- *     into a_gate and a_up (int32, F values each); each CTA of the launch also
- *     forms t = relu(a_gate)^2 * a_up of the rows it computed and stores their
- *     max |t| and, per column, a signed fp32 form of t in `tmax`.
+ *     into a_gate and a_up (int32, F values each); the maxima of
+ *     |t| = |relu(a_gate)^2 * a_up| over each 32 columns and, per column, a
+ *     signed fp32 form of t go to `tmax`.  One block per call is one launch
+ *     whose CTAs form them from the rows they computed; lists whose rows do
+ *     not fit one resident wave take the products on the streaming kernel and
+ *     one more launch forming them.
  *   trit_mlp_down: the down projection (N x F) of the codes of t --
  *     round-half-even(127 t / max|t|), exact, max|t| reduced from `tmax` --
  *     with scale max|t| * S_g^2 * S_u (S = w * x_scale / 127): y_i32 / y_f32
@@ -308,8 +311,9 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
  * same stream, with x_scale, a_gate, a_up and tmax untouched in between.
  * Blocks whose rows exceed the pre-loading kernel's shared memory (K above
  * 13,312 or F above 8,960 columns) take the fused paths instead (tmax
- * unused), with the same results.  K and F are limited to TRIT_MAX_FUSED_K (TRIT_E_SHAPE);
- * w_gate, w_up and w_down must be finite and > 0 (TRIT_E_SCALE).
+ * unused), with the same results.  K and F are limited to TRIT_MAX_FUSED_K
+ * (TRIT_E_SHAPE); w_gate, w_up and w_down must be finite and > 0
+ * (TRIT_E_SCALE).
  *   x          [K] fp32, device, 4-byte aligned
  *   x_scale    [1] fp32 out
  *   a_gate, a_up  [F] int32 out, 16-byte aligned
@@ -317,7 +321,7 @@ TRIT_API trit_status trit_intmlp_gemv_many(const trit_mlpproj *list, int32_t cou
  *   h_i8       out, may be NULL: [F_pad] int8, zero tail, 16-byte aligned
  *   h_scale    out, may be NULL: [1] fp32
  *   y_i32, y_f32  [N] outputs, either may be NULL (not both)
- * `list` is a host array; up to 8 blocks share one launch.
+ * `list` is a host array; up to 8 blocks share one launch of trit_mlp_down.
  */
 typedef struct trit_mlp_block {
     const uint8_t *gate_planes;
